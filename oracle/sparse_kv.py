@@ -1,0 +1,295 @@
+"""Plain CPU restatement of one sparse-KV decode layer -- TEST INFRASTRUCTURE ONLY.
+
+Arrays of bf16 values are passed as their uint16 bit patterns.  Floating-point
+stages compute in fp64 unless a stage produces a quantised value (the bf16
+landmark), where the decision is taken in the precision the stage defines
+(fp32 accumulation, then round-to-nearest-even to bf16).
+
+Notation (from the pages, with the readings where they are silent):
+  B requests, Hq query heads, Hkv KV heads, G = Hq/Hkv (query head h reads KV
+  head floor(h/G)), d head dimension, L context tokens, cs tokens per chunk,
+  C = L/cs chunks, k chunks selected per (request, query, KV head), n_q
+  queries per request (j = 0 the real query, j >= 1 speculative ones).
+
+Parity pins: every function below is pinned by ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "bf16_decode", "bf16_encode", "build_landmarks", "score_landmarks", "select_topk",
+    "resolve_union", "gather_kv", "sparse_attn_decode", "step", "kv_footprint_bytes",
+    "max_batch", "per_step_budget_bytes", "union_of_query_selections",
+]
+
+
+# ---------------------------------------------------------------------------
+# bf16 encoding (IEEE bfloat16: the top 16 bits of an fp32)
+# ---------------------------------------------------------------------------
+
+def _bf16_to_f32(u: np.ndarray) -> np.ndarray:
+    return (np.asarray(u, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def bf16_decode(u: np.ndarray) -> np.ndarray:
+    """bf16 bits -> fp64 values (exact)."""
+    return _bf16_to_f32(u).astype(np.float64)
+
+
+def bf16_encode(x: np.ndarray) -> np.ndarray:
+    """fp32 values -> bf16 bits, rounding to nearest, ties to even (finite inputs)."""
+    bits = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (bits >> np.uint64(16)) & np.uint64(1)
+    return ((bits + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# a0: chunk landmarks
+# ---------------------------------------------------------------------------
+
+def build_landmarks(K: np.ndarray, cs: int) -> np.ndarray:
+    """Chunk-mean key landmarks, bf16 bits [B, Hkv, C, d].
+
+    DualDecoder §2.2: adjacent KV entries are grouped into chunks and each
+    chunk keeps one compact landmark used to rank chunks for a query; §4.1:
+    the landmarks are produced before decoding and stay fixed.  The landmark
+    is the mean key of the chunk.  Reading: the sum runs in fp32 over the
+    chunk's tokens in order t = 0..cs-1, is divided by cs in fp32 and rounded
+    to bf16 (the KV dtype, as the "1/16 of the KV cache" summary size in the
+    OasisKV Methodology implies).
+    """
+    B, H, L, d = K.shape
+    if L % cs:
+        raise ValueError("L must be a multiple of the chunk size")
+    C = L // cs
+    k32 = _bf16_to_f32(K).reshape(B, H, C, cs, d)
+    acc = np.zeros((B, H, C, d), dtype=np.float32)
+    for t in range(cs):
+        acc = acc + k32[:, :, :, t, :]
+    return bf16_encode(acc / np.float32(cs))
+
+
+# ---------------------------------------------------------------------------
+# a1: landmark scores for all queries of a request
+# ---------------------------------------------------------------------------
+
+def score_landmarks(q: np.ndarray, lm: np.ndarray) -> np.ndarray:
+    """s[b, j, g, c] = sum over the q-heads h of KV head g of q[b,j,h,:] . lm[b,g,c,:] (fp64).
+
+    DualDecoder §4.1: the retrieval index is computed from the token being
+    decoded and the landmarks; the speculative token is scored against the
+    same landmarks (§5.2 runs both tokens in one pass).  OasisKV Methodology:
+    blocks are ranked independently for every KV head.  Reading: the per-KV-
+    head score sums the group's query-head dot products; the 1/sqrt(d) scale
+    is left out because it does not change the ranking.
+    """
+    B, n_q, Hq, d = q.shape
+    _, Hkv, C, _ = lm.shape
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    G = Hq // Hkv
+    qf = bf16_decode(q)
+    lf = bf16_decode(lm)
+    s = np.zeros((B, n_q, Hkv, C), dtype=np.float64)
+    for g in range(Hkv):
+        for h in range(g * G, (g + 1) * G):
+            s[:, :, g, :] += np.einsum("bji,bci->bjc", qf[:, :, h, :], lf[:, g, :, :])
+    return s
+
+
+# ---------------------------------------------------------------------------
+# a2: top-k chunks per (request, query, KV head)
+# ---------------------------------------------------------------------------
+
+def select_topk(s: np.ndarray, k: int) -> np.ndarray:
+    """The k chunks with the largest scores per row, returned in ascending chunk order.
+
+    OasisKV Methodology: top-K blocks per KV head.  Reading: rows are ordered
+    by (score descending, chunk index ascending), so among exactly equal
+    scores the lower chunk index is selected first; the chosen set is then
+    listed in ascending chunk index.
+    """
+    *lead, C = s.shape
+    if not 1 <= k <= C:
+        raise ValueError("need 1 <= k <= C")
+    rows = np.asarray(s, dtype=np.float64).reshape(-1, C)
+    out = np.empty((rows.shape[0], k), dtype=np.int32)
+    chunk = np.arange(C)
+    for r in range(rows.shape[0]):
+        order = np.lexsort((chunk, -rows[r]))   # last key is primary
+        out[r] = np.sort(order[:k])
+    return out.reshape(*lead, k)
+
+
+# ---------------------------------------------------------------------------
+# a3: union across queries, residency, miss ordinals
+# ---------------------------------------------------------------------------
+
+def union_of_query_selections(sel: np.ndarray, b: int, g: int) -> list:
+    """Ascending union of the selections of all queries of request b, KV head g."""
+    n_q = sel.shape[1]
+    u = set()
+    for j in range(n_q):
+        u |= set(int(c) for c in sel[b, j, g])
+    return sorted(u)
+
+
+def resolve_union(sel: np.ndarray, resident_slot: np.ndarray) -> dict:
+    """Resolve the union of the queries' selections against the HBM pool.
+
+    Adaptive DHiSparse Fig. 3: the selections of the several queries of a
+    request and KV source are handled together, so each distinct missing row
+    is copied from host once, while each query still attends over its own
+    selection.  Fig. 2: a selected row is looked up in the HBM tiers first
+    and copied from host DRAM only when it is found in none of them.
+
+    Readings: per (b, g) the union U lists chunks in ascending order; a chunk
+    is resident when ``resident_slot[b,g,c] >= 0`` (its slot in the hot pool)
+    and missing otherwise; missing chunks take dense ordinals m = 0..M-1 in
+    (b, g, c) lexicographic order and are addressed as staging slot m,
+    encoded -(m+1).  ``miss_list[m] = (b*Hkv + g)*C + c``.  ``union_qmask``
+    has bit j set when query j selected the chunk.  ``attn_slot[b,j,g,r]`` is
+    the encoded slot of the r-th chunk of query j's selection.
+    Entries of the union arrays past ``union_cnt`` are padding (-1 / 0).
+    """
+    B, n_q, Hkv, k = sel.shape
+    C = resident_slot.shape[2]
+    umax = min(C, n_q * k)
+    union_idx = np.full((B, Hkv, umax), -1, dtype=np.int32)
+    union_slot = np.full((B, Hkv, umax), -1, dtype=np.int32)
+    union_qmask = np.zeros((B, Hkv, umax), dtype=np.uint8)
+    union_cnt = np.zeros((B, Hkv), dtype=np.int32)
+    attn_slot = np.empty((B, n_q, Hkv, k), dtype=np.int32)
+    miss_list = []
+    for b in range(B):
+        for g in range(Hkv):
+            per_query = [set(int(c) for c in sel[b, j, g]) for j in range(n_q)]
+            U = union_of_query_selections(sel, b, g)
+            union_cnt[b, g] = len(U)
+            slot_of = {}
+            for u, c in enumerate(U):
+                rs = int(resident_slot[b, g, c])
+                if rs >= 0:
+                    slot_of[c] = rs
+                else:
+                    m = len(miss_list)
+                    miss_list.append((b * Hkv + g) * C + c)
+                    slot_of[c] = -(m + 1)
+                union_idx[b, g, u] = c
+                union_slot[b, g, u] = slot_of[c]
+                union_qmask[b, g, u] = sum(1 << j for j in range(n_q) if c in per_query[j])
+            for j in range(n_q):
+                for r in range(k):
+                    attn_slot[b, j, g, r] = slot_of[int(sel[b, j, g, r])]
+    return {
+        "union_idx": union_idx, "union_cnt": union_cnt, "union_slot": union_slot,
+        "union_qmask": union_qmask, "miss_list": np.asarray(miss_list, dtype=np.int32),
+        "miss_count": len(miss_list), "attn_slot": attn_slot,
+    }
+
+
+# ---------------------------------------------------------------------------
+# a4: gather of missing chunks into the staging buffer
+# ---------------------------------------------------------------------------
+
+def gather_kv(Kh: np.ndarray, Vh: np.ndarray, miss_list: np.ndarray, cs: int):
+    """Copy chunk ``miss_list[m]`` of the host K and V into staging slot m.
+
+    DualDecoder §5.4 (GPU-side sparse KV assembly): selected KV blocks are
+    moved from host memory into a GPU staging region and placed in the
+    attention layout there.  Reading: staging slot m holds the cs rows of
+    the m-th missing chunk, K and V in separate arrays [M, cs, d].
+    """
+    B, H, L, d = Kh.shape
+    C = L // cs
+    M = len(miss_list)
+    Kst = np.empty((M, cs, d), dtype=Kh.dtype)
+    Vst = np.empty((M, cs, d), dtype=Vh.dtype)
+    for m, packed in enumerate(np.asarray(miss_list).tolist()):
+        unit, c = divmod(int(packed), C)
+        b, g = divmod(unit, H)
+        Kst[m] = Kh[b, g, c * cs:(c + 1) * cs]
+        Vst[m] = Vh[b, g, c * cs:(c + 1) * cs]
+    return Kst, Vst
+
+
+# ---------------------------------------------------------------------------
+# a5: attention of every query over its own selected rows
+# ---------------------------------------------------------------------------
+
+def _rows(pool_hot, pool_stage, slot: int):
+    return pool_hot[slot] if slot >= 0 else pool_stage[-slot - 1]
+
+
+def sparse_attn_decode(q, Khot, Vhot, Kst, Vst, attn_slot, cs: int, scale: float | None = None):
+    """o[b,j,h,:] = sum over the selected rows t of softmax_t(scale * q . K_t) * V_t (fp64).
+
+    DualDecoder §5.2: the output and speculative tokens attend in one pass;
+    OasisKV Methodology: normal and draft queries attend together over one
+    resident working set; Adaptive DHiSparse Fig. 3: each query attends over
+    its own selection.  Readings: scale = 1/sqrt(d); query head h uses KV
+    head floor(h/G); the rows of query j are those of the k chunks in
+    ``attn_slot[b,j,g,:]``; the current step's own new tokens are not part
+    of the path.
+    """
+    B, n_q, Hq, d = q.shape
+    Hkv = attn_slot.shape[2]
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    qf = bf16_decode(q)
+    out = np.zeros((B, n_q, Hq, d), dtype=np.float64)
+    for b in range(B):
+        for j in range(n_q):
+            for g in range(Hkv):
+                slots = [int(s) for s in attn_slot[b, j, g]]
+                Kr = bf16_decode(np.concatenate([_rows(Khot, Kst, s) for s in slots], axis=0))
+                Vr = bf16_decode(np.concatenate([_rows(Vhot, Vst, s) for s in slots], axis=0))
+                for h in range(g * G, (g + 1) * G):
+                    z = (Kr @ qf[b, j, h]) * scale
+                    p = np.exp(z - z.max())
+                    p /= p.sum()
+                    out[b, j, h] = p @ Vr
+    return out
+
+
+# ---------------------------------------------------------------------------
+# a6: one layer's step
+# ---------------------------------------------------------------------------
+
+def step(q, lm, Kh, Vh, resident_slot, Khot, Vhot, k: int, cs: int, scale=None) -> dict:
+    """Score -> top-k -> union/resolve -> gather -> attention for one layer.
+
+    DualDecoder Fig. 8 / §5.1-§5.4: retrieval index from the query and the
+    landmarks, missing entries fetched from host into the layer's staging
+    buffer, then sparse attention over the selected entries.
+    """
+    s = score_landmarks(q, lm)
+    sel = select_topk(s, k)
+    res = resolve_union(sel, resident_slot)
+    Kst, Vst = gather_kv(Kh, Vh, res["miss_list"], cs)
+    out = sparse_attn_decode(q, Khot, Vhot, Kst, Vst, res["attn_slot"], cs, scale)
+    res.update(scores=s, sel=sel, Kst=Kst, Vst=Vst, out=out)
+    return res
+
+
+# ---------------------------------------------------------------------------
+# OasisKV eqs. (1)-(3)
+# ---------------------------------------------------------------------------
+
+def kv_footprint_bytes(B: int, L: int, n_layer: int, n_kv: int, d_h: int, s: int) -> int:
+    """OasisKV eq. (1): M_KV = B * L * N_layer * 2 * N_kv * d_h * s."""
+    return B * L * n_layer * 2 * n_kv * d_h * s
+
+
+def max_batch(m_hbm: int, L: int, n_layer: int, n_kv: int, d_h: int, s: int) -> int:
+    """OasisKV eq. (2): B_max = floor(M_HBM / (L * N_layer * 2 * N_kv * d_h * s))."""
+    return m_hbm // (L * n_layer * 2 * n_kv * d_h * s)
+
+
+def per_step_budget_bytes(b_link: float, t_decode: float) -> float:
+    """OasisKV eq. (3): C_token = B_link * T_decode (bytes the link can move in one step)."""
+    return b_link * t_decode

@@ -1,0 +1,317 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+Each test ties one oracle function to a closed form, a library routine on a
+special case, brute force on a tiny input, an invariant, or a number printed
+on the pages, so that a dropped term, a wrong index or sign, or a transposed
+operand in the oracle fails at least one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_kv_offload_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def enc(x):
+    """fp32 -> bf16 bits through the generator module's encoder (not the oracle's)."""
+    return synth.f32_to_bf16(np.asarray(x, dtype=np.float32))
+
+
+# ---------------------------------------------------------------- eqs. (1)-(3)
+
+def test_eq1_eq2_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "oasiskv_footprint.json")))
+    per_token = oracle.kv_footprint_bytes(1, 1, g["n_layer"], g["n_kv"], g["d_h"], g["s_bytes"])
+    assert per_token == g["bytes_per_token"] == 256 * 1024
+    one_request = oracle.kv_footprint_bytes(1, g["context_tokens"], g["n_layer"], g["n_kv"], g["d_h"], g["s_bytes"])
+    assert round(one_request / 1e9, 1) == g["request_gb_approx"]
+    assert oracle.max_batch(g["hbm_gb"] * 10**9, g["context_tokens"], g["n_layer"], g["n_kv"], g["d_h"],
+                            g["s_bytes"]) == g["max_batch"]
+    # linear in B and L
+    assert oracle.kv_footprint_bytes(3, 10, 2, 8, 128, 2) == 3 * 10 * oracle.kv_footprint_bytes(1, 1, 2, 8, 128, 2)
+
+
+def test_eq3_step_budget():
+    g = json.load(open(os.path.join(GOLDEN, "oasiskv_step_budget.json")))
+    c = oracle.per_step_budget_bytes(g["b_link_bytes_per_s"], g["t_decode_s"])
+    assert c == pytest.approx(1.088e9)
+    m = g["qwen3_8b"]
+    per_tok = oracle.kv_footprint_bytes(1, 1, m["n_layer"], m["n_kv"], m["d_h"], m["s_bytes"])
+    implied_batch = c / per_tok / g["tokens_per_request"]
+    assert 55 < implied_batch < 70
+
+
+# ---------------------------------------------------------------- landmarks
+
+def test_landmark_of_constant_chunk_is_the_key():
+    rng = np.random.default_rng(0)
+    B, H, cs, C, d = 2, 3, 16, 5, 128
+    v = enc(rng.standard_normal((B, H, C, 1, d)))
+    K = np.broadcast_to(v, (B, H, C, cs, d)).reshape(B, H, C * cs, d).copy()
+    lm = oracle.build_landmarks(K, cs)
+    assert np.array_equal(lm, v[:, :, :, 0, :])
+
+
+def test_landmark_chunk_boundaries_and_heads():
+    # K[b,g,t,i] = sign(b,g,i) * t: chunk c's mean is sign * (c*cs + (cs-1)/2), exact in bf16
+    # (the largest mean, 119.5, still fits bf16's 8 significant bits)
+    B, H, L, d, cs = 2, 4, 128, 128, 16
+    t = np.arange(L, dtype=np.float32)
+    sign = np.where((np.arange(B)[:, None, None] + np.arange(H)[None, :, None] + np.arange(d)[None, None, :]) % 2,
+                    -1.0, 1.0).astype(np.float32)
+    K = enc(sign[:, :, None, :] * t[None, None, :, None])
+    lm = oracle.build_landmarks(K, cs)
+    C = L // cs
+    want = sign[:, :, None, :] * (np.arange(C, dtype=np.float32) * cs + (cs - 1) / 2)[None, None, :, None]
+    assert np.array_equal(oracle.bf16_decode(lm), want.astype(np.float64))
+
+
+@pytest.mark.parametrize("cs", [1, 4, 16, 64])
+def test_landmark_equals_exact_mean_when_sums_are_exact(cs):
+    # values on a 2^-7 grid within +-4: every fp32 partial sum is exact, so the
+    # landmark is the bf16 rounding of the exact mean (numpy fp64 mean)
+    rng = np.random.default_rng(cs)
+    B, H, C, d = 1, 2, 7, 128
+    x = np.clip(np.round(rng.standard_normal((B, H, C * cs, d)) * 128) / 128, -3.99, 3.99)
+    K = enc(x)
+    xf = synth.bf16_to_f32(K).astype(np.float64)
+    mean = xf.reshape(B, H, C, cs, d).mean(axis=3)
+    assert np.array_equal(oracle.build_landmarks(K, cs), enc(mean.astype(np.float32)))
+
+
+# ---------------------------------------------------------------- scores
+
+def test_score_one_hot_picks_the_right_head_and_coordinate():
+    B, n_q, Hq, Hkv, C, d = 2, 2, 8, 2, 6, 128
+    G = Hq // Hkv
+    q = np.zeros((B, n_q, Hq, d), np.float32)
+    lm = np.zeros((B, Hkv, C, d), np.float32)
+    b, j, h, i = 1, 1, 6, 37          # head 6 belongs to KV head 1
+    q[b, j, h, i] = 2.0
+    lm[b, h // G, :, i] = np.arange(1, C + 1)
+    lm[b, 0, :, i] = 100.0            # must not leak into KV head 1
+    lm[b, h // G, :, i + 1] = 50.0    # other coordinate must not leak
+    s = oracle.score_landmarks(enc(q), enc(lm))
+    want = np.zeros((B, n_q, Hkv, C))
+    want[b, j, h // G] = 2.0 * np.arange(1, C + 1)
+    assert np.array_equal(s, want)
+
+
+def test_score_with_constant_landmark_is_group_sum_of_query():
+    rng = np.random.default_rng(3)
+    B, n_q, Hq, Hkv, C, d = 2, 3, 12, 3, 5, 128
+    G = Hq // Hkv
+    q = enc(rng.standard_normal((B, n_q, Hq, d)))
+    beta = np.array([1.0, -2.0, 0.5, 4.0, 0.0], np.float32)
+    lm = enc(np.broadcast_to(beta[None, None, :, None], (B, Hkv, C, d)))
+    s = oracle.score_landmarks(q, lm)
+    qf = synth.bf16_to_f32(q).astype(np.float64)
+    gsum = qf.reshape(B, n_q, Hkv, G, d).sum(axis=(3, 4))
+    np.testing.assert_allclose(s, gsum[..., None] * beta[None, None, None, :], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- top-k
+
+def _brute_topk(row, k):
+    C = len(row)
+    hits = []
+    for S in itertools.combinations(range(C), k):
+        inside = set(S)
+        ok = all((row[a] > row[o]) or (row[a] == row[o] and a < o)
+                 for a in inside for o in range(C) if o not in inside)
+        if ok:
+            hits.append(list(S))
+    assert len(hits) == 1
+    return hits[0]
+
+
+@pytest.mark.parametrize("C,k", [(5, 1), (7, 3), (8, 4), (9, 8), (6, 6)])
+def test_topk_brute_force(C, k):
+    rng = np.random.default_rng(C * 10 + k)
+    for trial in range(20):
+        row = np.round(rng.standard_normal(C) * 2) / 2   # frequent exact ties
+        got = oracle.select_topk(row[None, :], k)[0]
+        assert list(got) == _brute_topk(row, k)
+
+
+def test_topk_ties_take_lowest_index_and_output_is_ascending():
+    s = np.array([[1.0, 2.0, 2.0, 2.0, 0.0, 2.0]])
+    assert oracle.select_topk(s, 2).tolist() == [[1, 2]]
+    assert oracle.select_topk(np.zeros((1, 9)), 4).tolist() == [[0, 1, 2, 3]]
+    assert oracle.select_topk(np.array([[0.0, -0.0, 0.0]]), 1).tolist() == [[0]]
+    s = np.array([[3.0, 9.0, 1.0, 7.0]])
+    assert oracle.select_topk(s, 2).tolist() == [[1, 3]]
+    assert oracle.select_topk(s, 4).tolist() == [[0, 1, 2, 3]]
+
+
+# ---------------------------------------------------------------- union / residency
+
+def test_union_worked_example_dedups_shared_rows():
+    # Adaptive DHiSparse Fig. 3: K=4 queries, k=3; row a selected by three
+    # queries, row b by two -- each distinct missing row is copied once.
+    a, b_, C = 5, 9, 16
+    sel = np.array([[[[a, b_, 1]], [[a, 2, 3]], [[a, b_, 4]], [[6, 7, 8]]]], dtype=np.int32)
+    sel = np.sort(sel, axis=-1)
+    res = oracle.resolve_union(sel, np.full((1, 1, C), -1, np.int32))
+    U = [1, 2, 3, 4, a, 6, 7, 8, b_]
+    assert res["union_cnt"][0, 0] == len(U) == res["miss_count"]
+    assert res["union_idx"][0, 0, :len(U)].tolist() == sorted(U)
+    assert sorted(res["miss_list"].tolist()) == sorted(U)
+    qm = dict(zip(res["union_idx"][0, 0, :len(U)].tolist(), res["union_qmask"][0, 0, :len(U)].tolist()))
+    assert bin(qm[a]).count("1") == 3 and bin(qm[b_]).count("1") == 2
+
+
+def _check_union_invariants(sel, slot, res):
+    B, n_q, Hkv, k = sel.shape
+    C = slot.shape[2]
+    expect_m = 0
+    for b in range(B):
+        for g in range(Hkv):
+            sets = [set(sel[b, j, g].tolist()) for j in range(n_q)]
+            U = sorted(set.union(*sets))
+            n = res["union_cnt"][b, g]
+            assert n == len(U) and k <= n <= min(C, n_q * k)
+            assert res["union_idx"][b, g, :n].tolist() == U
+            n_res = 0
+            for u, c in enumerate(U):
+                assert res["union_qmask"][b, g, u] == sum(1 << j for j in range(n_q) if c in sets[j])
+                sl = res["union_slot"][b, g, u]
+                if slot[b, g, c] >= 0:
+                    assert sl == slot[b, g, c]
+                    n_res += 1
+                else:
+                    assert sl == -(expect_m + 1)                      # dense, (b,g,c) order
+                    assert res["miss_list"][expect_m] == (b * Hkv + g) * C + c
+                    expect_m += 1
+            for j in range(n_q):
+                for r in range(k):
+                    c = sel[b, j, g, r]
+                    assert res["attn_slot"][b, j, g, r] == res["union_slot"][b, g, U.index(c)]
+    assert res["miss_count"] == expect_m == len(res["miss_list"])
+
+
+@pytest.mark.parametrize("n_q,overlap,res_frac", [(2, 0.7, 0.0), (2, 0.3, 0.5), (5, 0.5, 0.2), (1, 1.0, 0.9)])
+def test_union_invariants(n_q, overlap, res_frac):
+    B, Hkv, C, k = 3, 2, 40, 6
+    sel = synth.random_selection(77 + n_q, B, n_q, Hkv, C, k, overlap)
+    slot = synth.uniform_residency(5, B, Hkv, C, res_frac)
+    res = oracle.resolve_union(sel, slot)
+    _check_union_invariants(sel, slot, res)
+
+
+# ---------------------------------------------------------------- gather
+
+def test_gather_copies_exact_bytes():
+    rng = np.random.default_rng(9)
+    B, H, L, d, cs = 2, 3, 64, 128, 16
+    C = L // cs
+    Kh = rng.integers(0, 65535, (B, H, L, d), dtype=np.uint16)
+    Vh = rng.integers(0, 65535, (B, H, L, d), dtype=np.uint16)
+    miss = np.array([(1 * H + 2) * C + 3, 0, (0 * H + 1) * C + 2], np.int32)
+    Kst, Vst = oracle.gather_kv(Kh, Vh, miss, cs)
+    assert np.array_equal(Kst[0], Kh[1, 2, 48:64]) and np.array_equal(Vst[0], Vh[1, 2, 48:64])
+    assert np.array_equal(Kst[1], Kh[0, 0, 0:16]) and np.array_equal(Vst[2], Vh[0, 1, 32:48])
+    e = oracle.gather_kv(Kh, Vh, np.zeros(0, np.int32), cs)
+    assert e[0].shape == (0, cs, d)
+
+
+# ---------------------------------------------------------------- attention
+
+def _sdpa(qf, Kf, Vf, scale):
+    t = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(qf)[None, None, None, :], torch.from_numpy(Kf)[None, None],
+        torch.from_numpy(Vf)[None, None], scale=scale)
+    return t[0, 0, 0].numpy()
+
+
+def test_attention_all_chunks_equals_dense_sdpa():
+    rng = np.random.default_rng(11)
+    B, n_q, Hq, Hkv, L, d, cs = 2, 2, 4, 2, 64, 128, 16
+    C = L // cs
+    q = enc(rng.standard_normal((B, n_q, Hq, d)))
+    Kh = enc(rng.standard_normal((B, Hkv, L, d)))
+    Vh = enc(rng.standard_normal((B, Hkv, L, d)))
+    sel = np.broadcast_to(np.arange(C, dtype=np.int32), (B, n_q, Hkv, C)).copy()
+    res = oracle.resolve_union(sel, np.full((B, Hkv, C), -1, np.int32))
+    Kst, Vst = oracle.gather_kv(Kh, Vh, res["miss_list"], cs)
+    empty = np.zeros((0, cs, d), np.uint16)
+    out = oracle.sparse_attn_decode(q, empty, empty, Kst, Vst, res["attn_slot"], cs)
+    qf, Kf, Vf = (synth.bf16_to_f32(x).astype(np.float64) for x in (q, Kh, Vh))
+    G = Hq // Hkv
+    for b in range(B):
+        for j in range(n_q):
+            for h in range(Hq):
+                want = _sdpa(qf[b, j, h], Kf[b, h // G], Vf[b, h // G], 1 / math.sqrt(d))
+                np.testing.assert_allclose(out[b, j, h], want, rtol=1e-10, atol=1e-12)
+
+
+def test_attention_single_row_and_uniform_weights():
+    rng = np.random.default_rng(12)
+    d = 128
+    Vh = enc(rng.standard_normal((1, 1, 8, d)))
+    Kh = enc(rng.standard_normal((1, 1, 8, d)))
+    q = enc(rng.standard_normal((1, 1, 1, d)))
+    # cs = 1, k = 1: the output is the selected V row
+    sel = np.array([[[[5]]]], np.int32)
+    res = oracle.resolve_union(sel, np.full((1, 1, 8), -1, np.int32))
+    Kst, Vst = oracle.gather_kv(Kh, Vh, res["miss_list"], 1)
+    out = oracle.sparse_attn_decode(q, Kst[:0], Vst[:0], Kst, Vst, res["attn_slot"], 1)
+    assert np.array_equal(out[0, 0, 0], synth.bf16_to_f32(Vh[0, 0, 5]).astype(np.float64))
+    # q = 0: equal logits, the output is the mean of the selected V rows
+    sel = np.array([[[[1, 4, 6]]]], np.int32)
+    res = oracle.resolve_union(sel, np.full((1, 1, 8), -1, np.int32))
+    Kst, Vst = oracle.gather_kv(Kh, Vh, res["miss_list"], 1)
+    out = oracle.sparse_attn_decode(np.zeros_like(q), Kst[:0], Vst[:0], Kst, Vst, res["attn_slot"], 1)
+    want = synth.bf16_to_f32(Vh[0, 0, [1, 4, 6]]).astype(np.float64).mean(axis=0)
+    np.testing.assert_allclose(out[0, 0, 0], want, rtol=1e-12, atol=1e-14)
+
+
+def test_attention_uses_floor_h_over_G_and_is_order_invariant():
+    rng = np.random.default_rng(13)
+    B, n_q, Hq, Hkv, d, cs, S = 1, 1, 6, 3, 128, 4, 10
+    Khot = enc(rng.standard_normal((S, cs, d)))
+    # V of the chunks of KV head g is the constant g+1, so a zero query gives g+1
+    Vhot = enc(np.repeat(np.arange(S, dtype=np.float32)[:, None, None], cs, 1) * np.ones((1, 1, d), np.float32))
+    slots = np.array([[[[0, 1], [3, 4], [7, 8]]]], np.int32)       # [B,n_q,Hkv,k]
+    zero = np.zeros((B, n_q, Hq, d), np.uint16)
+    out = oracle.sparse_attn_decode(zero, Khot, Vhot, Khot[:0], Vhot[:0], slots, cs)
+    for h in range(Hq):
+        g = h // (Hq // Hkv)
+        assert np.all(out[0, 0, h] == slots[0, 0, g].mean())
+    q = enc(rng.standard_normal((B, n_q, Hq, d)))
+    Vhot = enc(rng.standard_normal((S, cs, d)))
+    a = oracle.sparse_attn_decode(q, Khot, Vhot, Khot[:0], Vhot[:0], slots, cs)
+    b = oracle.sparse_attn_decode(q, Khot, Vhot, Khot[:0], Vhot[:0], slots[..., ::-1].copy(), cs)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- whole step
+
+@pytest.mark.parametrize("resident_frac", [0.0, 0.5])
+def test_step_with_all_chunks_equals_dense_attention(resident_frac):
+    w = dict(B=1, n_q=2, Hq=4, Hkv=2, L=128, d=128, cs=16)
+    C = w["L"] // w["cs"]
+    rng = np.random.default_rng(21)
+    q = enc(rng.standard_normal((w["B"], w["n_q"], w["Hq"], w["d"])))
+    Kh = enc(rng.standard_normal((w["B"], w["Hkv"], w["L"], w["d"])))
+    Vh = enc(rng.standard_normal((w["B"], w["Hkv"], w["L"], w["d"])))
+    lm = oracle.build_landmarks(Kh, w["cs"])
+    slot = synth.uniform_residency(3, w["B"], w["Hkv"], C, resident_frac)
+    Khot = synth.hot_pool_from(Kh, slot, w["cs"]) if resident_frac else np.zeros((0, w["cs"], w["d"]), np.uint16)
+    Vhot = synth.hot_pool_from(Vh, slot, w["cs"]) if resident_frac else np.zeros((0, w["cs"], w["d"]), np.uint16)
+    r = oracle.step(q, lm, Kh, Vh, slot, Khot, Vhot, C, w["cs"])
+    assert r["miss_count"] == int((slot < 0).sum())
+    qf, Kf, Vf = (synth.bf16_to_f32(x).astype(np.float64) for x in (q, Kh, Vh))
+    G = w["Hq"] // w["Hkv"]
+    for j in range(w["n_q"]):
+        for h in range(w["Hq"]):
+            want = _sdpa(qf[0, j, h], Kf[0, h // G], Vf[0, h // G], 1 / math.sqrt(w["d"]))
+            np.testing.assert_allclose(r["out"][0, j, h], want, rtol=1e-10, atol=1e-12)
