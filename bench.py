@@ -1,0 +1,459 @@
+#!/usr/bin/env python3
+"""Benchmark of one layer of the sparse-KV decode step on GB300.
+
+A step is one ``dd_step`` over one layer of the Llama-3-8B-shaped workload
+(16 requests, 32 query / 8 KV heads, head dim 128, 32K context in chunks of
+16, top-64 chunks per KV head, one real + one speculative query, all KV in
+pinned host memory): score -> top-k -> union/resolve -> gather -> attention.
+Four layers of independent data are cycled so that no step finds its inputs
+in L2.  Prints one JSON line (see the keys below).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--mode zerocopy|memcpy]
+
+``--impl reference`` times the CPU oracle instead (a bounded sample of the
+same workload per step).  Under torchrun every rank runs its own independent
+batch (weak scaling, no collective on the data path); the time is the max over
+ranks.
+"""
+from __future__ import annotations
+
+import os
+
+# the CPU oracle runs single-threaded: its BLAS calls must not spread over cores
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import json
+import math
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_kv_offload_gb300 import synth                      # noqa: E402
+from sparse_kv_offload_gb300.workloads import BY_NAME, LLAMA8B_32K  # noqa: E402
+
+METRIC = "sparse decode steps/s per layer; HBM GB/s and host-gather GB/s vs roofline"
+UNIT = "steps/s"
+N_LAYERS = 4
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            import torch
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", uuid, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+                for n, v in zip(names, r[3:7]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
+class OracleSample:
+    """The oracle's step over single (request, KV head) units of the workload.
+
+    Units are independent through every stage, so one unit is 1/(B*Hkv) of a
+    step: steps/s = units / (B * Hkv * seconds).  The sample is request 0's
+    Hkv units, built from the host generator (the same definition the GPU
+    path's inputs come from)."""
+
+    def __init__(self, w):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        q = synth.queries(w.seed, 1, w.n_q, w.Hq, w.d, w.spec_scale)
+        bias = u_hat = None
+        if w.key_bias == "hot":
+            bias = synth.hot_chunk_bias(w.seed, 1, w.Hkv, w.C, w.hot_frac, w.bias_sigma)
+            u_hat = synth.query_direction(q, w.Hkv)
+        elif w.key_bias == "zipf":
+            bias = synth.zipf_chunk_bias(w.seed, 1, w.Hkv, w.C, w.zipf_alpha, w.bias_sigma)
+            u_hat = synth.query_direction(q, w.Hkv)
+        self.units = []
+        for g in range(w.Hkv):
+            u = np.array([g])
+            K = synth.kv_rows(w.seed, synth.TID_K, 1, w.Hkv, w.L, w.d, w.cs, u, np.zeros(1, np.int64), w.L,
+                              bias, u_hat).reshape(1, 1, w.L, w.d)
+            V = synth.kv_rows(w.seed, synth.TID_V, 1, w.Hkv, w.L, w.d, w.cs, u, np.zeros(1, np.int64),
+                              w.L).reshape(1, 1, w.L, w.d)
+            qg = np.ascontiguousarray(q[:, :, g * w.G:(g + 1) * w.G])
+            self.units.append((qg, oracle.build_landmarks(K, w.cs), K, V))
+        self.slot = np.full((1, 1, w.C), -1, np.int32)
+        self.empty = np.zeros((0, w.cs, w.d), np.uint16)
+        self.next = 0
+
+    def run_units(self, n: int) -> float:
+        t0 = time.perf_counter()
+        for _ in range(n):
+            qg, lm, K, V = self.units[self.next % len(self.units)]
+            self.next += 1
+            self.oracle.step(qg, lm, K, V, self.slot, self.empty, self.empty, self.w.k, self.w.cs)
+        return time.perf_counter() - t0
+
+    def describe(self, n_units):
+        w = self.w
+        return (f"oracle (numpy fp64, one thread) on {n_units} (request, KV head) units of request 0 per "
+                f"timing, each 1/{w.B * w.Hkv} of a step; steps/s = units / ({w.B * w.Hkv} x seconds)")
+
+
+def cpu_baseline(w, budget_s=12.0):
+    s = OracleSample(w)
+    s.run_units(1)
+    done, spent = 0, 0.0
+    while spent < budget_s:
+        spent += s.run_units(1)
+        done += 1
+    return {"value": done / (w.units * spent), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": s.describe(done) + f"; {done} units in {spent:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    w = BY_NAME[args.workload]
+    s = OracleSample(w)
+    t_unit = s.run_units(1)
+    # size each step's sample so that the whole run stays near two minutes
+    per_step = min(2.0, 120.0 / (args.steps + args.warmup))
+    n = int(max(1, min(w.Hkv, per_step // max(t_unit, 1e-6))))
+    for _ in range(args.warmup):
+        s.run_units(n)
+    spent = sum(s.run_units(n) for _ in range(args.steps))
+    value = args.steps * n / (w.units * spent)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, "oracle"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": s.describe(n)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, gather_mode, world=1):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "L": w.L, "cs": w.cs, "k": w.k,
+            "n_q": w.n_q, "residency": w.residency, "gather": gather_mode,
+            "l2": f"inputs larger than L2 ({N_LAYERS} layers of landmarks and host KV cycled)",
+            "parallelism": f"independent batch per GPU x{world}"}
+
+
+# ------------------------------------------------------------------ GPU arm
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank decodes its own batch: a distinct seed per rank."""
+    return seed + 7919 * rank
+
+
+class LayerData:
+    def __init__(self, dd, shape, w, layer, rank):
+        import torch
+        seed = rank_seed(w.seed, rank)
+        self.q = torch.empty(w.B * w.n_q * w.Hq * w.d, dtype=torch.bfloat16, device="cuda")
+        dd.synth_queries(shape, seed, layer, w.spec_scale, self.q)
+        bias = u_hat = None
+        if w.key_bias == "hot":
+            qh = synth.queries(seed, w.B, w.n_q, w.Hq, w.d, w.spec_scale, layer)
+            bias = torch.from_numpy(synth.hot_chunk_bias(seed, w.B, w.Hkv, w.C, w.hot_frac, w.bias_sigma,
+                                                         layer)).cuda()
+            u_hat = torch.from_numpy(synth.query_direction(qh, w.Hkv)).cuda()
+        elif w.key_bias == "zipf":
+            qh = synth.queries(seed, w.B, w.n_q, w.Hq, w.d, w.spec_scale, layer)
+            bias = torch.from_numpy(synth.zipf_chunk_bias(seed, w.B, w.Hkv, w.C, w.zipf_alpha, w.bias_sigma,
+                                                          layer)).cuda()
+            u_hat = torch.from_numpy(synth.query_direction(qh, w.Hkv)).cuda()
+        n = w.B * w.Hkv * w.L * w.d
+        self.Kh = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+        self.Vh = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+        dd.synth_kv(shape, seed, synth.tensor_id(synth.TID_K, layer), self.Kh, bias, u_hat)
+        dd.synth_kv(shape, seed, synth.tensor_id(synth.TID_V, layer), self.Vh)
+        self.lm = torch.empty(w.B * w.Hkv * w.C * w.d, dtype=torch.bfloat16, device="cuda")
+        self.q_host = torch.empty(self.q.numel(), dtype=torch.bfloat16, pin_memory=True)
+        torch.cuda.synchronize()
+        self.q_host.copy_(self.q)
+
+
+def host_link_peaks(dd, shape):
+    """Pinned H2D copy peak (best of 10 x 1 GiB cudaMemcpyAsync) and the
+    zero-copy gather kernel reading 1 GiB of consecutive chunks."""
+    import torch
+    n = 1 << 29                                   # 1 GiB of bf16
+    src = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    src.fill_(1.0)
+    dst = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    best = 0.0
+    for _ in range(10):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        b.synchronize()
+        best = max(best, (2 * n) / (a.elapsed_time(b) * 1e-3) / 1e9)
+    # zero-copy: the gather kernel over every chunk of a 512 MiB K half and a
+    # 512 MiB V half, in order (8 heads x 16384 chunks)
+    from sparse_kv_offload_gb300.dd import Context, Shape
+    units, C = 8, 16384
+    sh = Shape(1, units, units, shape.d, C * shape.cs, shape.cs, 1, 1)
+    m = units * C
+    need = m * shape.cs * shape.d
+    zc = None
+    if 2 * need <= n:
+        with Context(sh, max_misses=m) as ctx:
+            miss = torch.arange(m, dtype=torch.int32, device="cuda")
+            cnt = torch.tensor([m], dtype=torch.int32, device="cuda")
+            Kh, Vh = src[:need], src[need:2 * need]
+            Kst, Vst = dst[:need], dst[need:2 * need]
+            zc = 0.0
+            for _ in range(6):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                ctx.gather_kv(Kh, Vh, miss, cnt, Kst, Vst)
+                b.record()
+                b.synchronize()
+                zc = max(zc, (4 * need) / (a.elapsed_time(b) * 1e-3) / 1e9)
+            if ctx.status() != 0:
+                zc = None
+    del src, dst
+    return best, zc
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    torch.cuda.set_device(local)
+    from sparse_kv_offload_gb300 import build
+    build.build()
+    from sparse_kv_offload_gb300 import dd
+    w = BY_NAME[args.workload]
+    shape = dd.Shape(w.B, w.Hq, w.Hkv, w.d, w.L, w.cs, w.k, w.n_q)
+    mode = dd.GATHER_MEMCPY if args.mode == "memcpy" else dd.GATHER_ZEROCOPY
+    cap = w.max_misses
+
+    layers = [LayerData(dd, shape, w, l, rank) for l in range(N_LAYERS)]
+    ctx = dd.Context(shape, max_misses=cap, hot_slots=0)
+    for L_ in layers:
+        ctx.build_landmarks(L_.Kh, L_.lm)
+    slot = torch.full((w.B * w.Hkv * w.C,), -1, dtype=torch.int32, device="cuda")
+    ns = cap * w.cs * w.d
+    Kst = [torch.empty(ns, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    Vst = [torch.empty(ns, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    out = torch.empty(w.B * w.n_q * w.Hq * w.d, dtype=torch.float32, device="cuda")
+    K = args.steps
+    miss_counts = torch.zeros(K, dtype=torch.int32, device="cuda")
+    union_cnts = torch.zeros(K, w.B * w.Hkv, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    assert ctx.status() == 0
+
+    link_memcpy, link_zc = host_link_peaks(dd, shape)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for row in ev:
+        for e in row:
+            e.record()                      # creates the event handles
+    torch.cuda.synchronize()
+
+    def step(i, layer, events=None, inter=None):
+        d_ = layers[layer % N_LAYERS]
+        ctx.step(layer, d_.q, d_.lm, d_.Kh, d_.Vh, slot, None, None, Kst, Vst, out, mode=mode,
+                 intermediates=inter, stage_events=events)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    for i in range(args.warmup):
+        step(i, i)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = ctx.launch_count()
+    t0 = time.perf_counter()
+    for i in range(K):
+        step(i, args.warmup + i, ev[i], {"miss_count": miss_counts[i:i + 1], "union_cnt": union_cnts[i]})
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    torch.cuda.synchronize()
+    launches = ctx.launch_count() - launches0
+    clocks = sampler.stop() if sampler else None
+    st = ctx.status()
+    if st != 0:
+        raise RuntimeError(f"device status after the timed steps: {dd.status_str(st)}")
+
+    gpu_s = ev[0][0].elapsed_time(ev[K - 1][5]) * 1e-3
+    t_max = max_over_ranks(gpu_s, world)
+    names = ("score", "topk", "resolve", "gather", "attention")
+    stage_ms = {n: float(np.mean([ev[i][s].elapsed_time(ev[i][s + 1]) for i in range(K)]))
+                for s, n in enumerate(names)}
+    M = miss_counts.double().mean().item()
+    U = union_cnts.double().sum(1).mean().item()
+    chunk_b = w.cs * w.d * 2
+
+    # algorithmic bytes per launch
+    q_b = w.B * w.n_q * w.Hq * w.d * 2
+    score_b = w.B * w.Hkv * w.C * w.d * 2 + q_b + w.B * w.n_q * w.Hkv * w.C * 4
+    attn_b = U * 2 * chunk_b + q_b + w.B * w.n_q * w.Hq * w.d * 4
+    gather_b = M * 2 * chunk_b                   # bytes read over the host link (written to HBM once more)
+    hbm_peak, hbm_kind = peaks()
+    stage_bytes = {"score": score_b, "attention": attn_b, "gather": gather_b}
+    dom = max(("score", "attention", "gather"), key=lambda n: stage_ms[n])
+    t_dom = stage_ms[dom] * 1e-3
+    if dom == "gather":
+        roof = {"bound": "host_link", "achieved": gather_b / t_dom / 1e9, "peak": link_memcpy, "unit": "GB/s",
+                "peak_kind": "pinned H2D cudaMemcpyAsync, best of 10 x 1 GiB, measured in this run",
+                "traffic": None, "kernel": "k_gather"}
+    else:
+        roof = {"bound": "hbm", "achieved": stage_bytes[dom] / t_dom / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                "peak_kind": hbm_kind, "traffic": None, "kernel": dom}
+    roof["frac"] = roof["achieved"] / roof["peak"] if roof["peak"] else None
+    t_sa = (stage_ms["score"] + stage_ms["attention"]) * 1e-3
+    roof_hbm = {"bound": "hbm", "kernels": "score + attention", "achieved": (score_b + attn_b) / t_sa / 1e9,
+                "peak": hbm_peak, "unit": "GB/s", "peak_kind": hbm_kind}
+    roof_hbm["frac"] = roof_hbm["achieved"] / hbm_peak
+
+    # end to end through the public call with host buffers: q in, out back
+    out_host = torch.empty(out.numel(), dtype=torch.float32, pin_memory=True)
+    for i in range(3):
+        d_ = layers[i % N_LAYERS]
+        d_.q.copy_(d_.q_host, non_blocking=True)
+        step(i, i)
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(K):
+        layer = args.warmup + i
+        d_ = layers[layer % N_LAYERS]
+        d_.q.copy_(d_.q_host, non_blocking=True)
+        step(i, layer)
+        out_host.copy_(out, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(a.elapsed_time(b) * 1e-3, world)
+    barrier(world)
+
+    cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    ctx.close()
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": world * K / t_max, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_max / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w, args.mode, world),
+        "roofline": roof, "roofline_hbm": roof_hbm,
+        "stages_us": {n: 1e3 * v for n, v in stage_ms.items()},
+        "per_step": {"union_chunks": U, "missing_chunks": M, "gather_bytes": gather_b,
+                     "host_link_gbs": gather_b / (stage_ms["gather"] * 1e-3) / 1e9},
+        "host_link_peaks_gbs": {"memcpy_h2d": link_memcpy, "zero_copy_gather_sequential": link_zc},
+        "wall_s": wall,
+        "e2e": {"value": world * K / e2e_s, "unit": UNIT, "h2d_bytes_per_step": q_b,
+                "d2h_bytes_per_step": w.B * w.n_q * w.Hq * w.d * 4},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=LLAMA8B_32K.name, choices=sorted(BY_NAME))
+    ap.add_argument("--mode", choices=("zerocopy", "memcpy"), default="zerocopy")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,185 @@
+/*
+ * dd.h -- C ABI of libdd: one layer of a predictive sparse-KV decode step on
+ * one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The step (DualDecoder: Accelerate Long Context LLM Inference by Predictive
+ * Prefetch, §4.1, §5.1-§5.4 and Figs. 8 and 11):
+ *   1. score the real query and the speculative query(ies) of every request
+ *      together against per-chunk mean-key landmarks,
+ *   2. keep the top-k chunks per (request, query, KV head),
+ *   3. take the union of the queries' selections per (request, KV head) and
+ *      resolve which chunks already sit in the HBM hot pool and which must
+ *      come from host memory (Adaptive DHiSparse, Figs. 2 and 3),
+ *   4. copy each distinct missing chunk once from pinned host memory into a
+ *      layer-scoped ping-pong HBM staging buffer,
+ *   5. run GQA attention of every query over the rows of its own selection.
+ *
+ * Notation: B requests, Hq query heads, Hkv KV heads, G = Hq/Hkv (query head h
+ * reads KV head floor(h/G)), d head dimension, L context tokens, cs tokens per
+ * chunk, C = L/cs chunks, k chunks per selection, n_q queries per request
+ * (j = 0 real, j >= 1 speculative), NQ = n_q*G query vectors per KV head,
+ * Umax = min(C, n_q*k) the largest possible union.
+ *
+ * Conventions
+ *   - bf16 is IEEE bfloat16 (uint16 storage).  All tensors are dense,
+ *     row-major in the layouts given per argument, and owned by the caller;
+ *     the library allocates only in dd_create (workspace, one status word,
+ *     two events, one copy stream, one pinned host list) and frees it in
+ *     dd_destroy.
+ *   - Device pointers must be 16-byte aligned.  "Host" K/V pointers must be
+ *     page-locked (cudaHostAlloc, cudaMallocHost or cudaHostRegister); the
+ *     kernels read them in place over the host link.
+ *   - Every call is asynchronous on the stream it is given (NULL = the legacy
+ *     default stream) and returns DD_ERR_INVALID_ARG / DD_ERR_CUDA at once for
+ *     errors the host can see.  Errors found on the device (an index out of
+ *     range, more misses than the staging capacity, a wait that ran out) are
+ *     written to the context's status word, first error wins; kernels never
+ *     trap.  While the word is non-zero the gather and attention kernels do no
+ *     work.  dd_get_status reads and clears it.
+ *   - A context serves one stream at a time; calls on one context must not
+ *     overlap on the GPU.
+ *   - Supported shapes: d = 128; cs in {16, 32, 64}; L a multiple of cs;
+ *     1 <= k <= C <= 16384; 1 <= n_q <= 8; Hq a multiple of Hkv; NQ <= 64;
+ *     B*Hkv*C < 2^31; B = 0 is accepted and every call is then a no-op.
+ */
+#ifndef DD_H_
+#define DD_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *dd_stream_t;
+
+typedef enum {
+  DD_OK = 0,
+  DD_ERR_INVALID_ARG = 1,   /* bad shape, pointer, alignment or enum (host-side check) */
+  DD_ERR_CUDA = 2,          /* a CUDA runtime call failed */
+  DD_ERR_CAPACITY = 3,      /* device: more missing chunks than the staging buffer holds */
+  DD_ERR_TIMEOUT = 4,       /* device: a bounded wait inside a kernel ran out */
+  DD_ERR_DEVICE_CHECK = 5   /* device: an index or slot read from memory was out of range */
+} dd_status;
+
+typedef struct {
+  int32_t B, Hq, Hkv, d, L, cs, k, n_q;
+} dd_dims;
+
+typedef enum {
+  DD_GATHER_ZEROCOPY = 0,   /* a kernel loads the host chunks over the host link (no host sync) */
+  DD_GATHER_MEMCPY = 1      /* miss list read back to the host, one cudaMemcpyAsync per run of
+                               consecutive chunks on the context's copy stream (host sync) */
+} dd_gather_mode;
+
+typedef struct dd_ctx dd_ctx;
+
+/* Create a context for one shape.  max_misses: capacity of each staging
+ * buffer in chunks (M_cap); B*Hkv*Umax guarantees DD_ERR_CAPACITY never
+ * occurs.  hot_slots: number of chunk slots of the caller's hot pool (0 when
+ * there is none); resident slots are checked against it.  The current CUDA
+ * device at creation is the context's device. */
+dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, dd_ctx **out);
+dd_status dd_destroy(dd_ctx *ctx);
+
+/* Chunk-mean key landmarks (DualDecoder §2.2 and §4.1; built once, before
+ * decoding).  K: bf16 [B,Hkv,L,d], device or pinned host.  lm: bf16
+ * [B,Hkv,C,d] device.  lm[b,g,c,i] = bf16_rne(fp32 sum over t = 0..cs-1 in
+ * order of K[b,g,c*cs+t,i], divided by cs). */
+dd_status dd_build_landmarks(dd_ctx *ctx, const void *K, void *lm, dd_stream_t stream);
+
+/* Landmark scores of all n_q queries in one pass over lm (DualDecoder §4.1,
+ * §5.2).  q: bf16 [B,n_q,Hq,d]; lm: bf16 [B,Hkv,C,d]; scores: fp32
+ * [B,n_q,Hkv,C] = sum over the G q-heads h of KV head g of q[b,j,h,:].lm[b,g,c,:]
+ * (unscaled; fp32 accumulation). */
+dd_status dd_score_landmarks(dd_ctx *ctx, const void *q, const void *lm, float *scores, dd_stream_t stream);
+
+/* Top-k chunks per row (OasisKV summary, Methodology: top-K per KV head).
+ * scores: fp32 [B,n_q,Hkv,C]; sel: int32 [B,n_q,Hkv,k], the k chunks with the
+ * largest scores ordered by (score desc, chunk asc), written in ascending
+ * chunk order.  -0.0 equals +0.0; NaN ranks below every number. */
+dd_status dd_select_topk(dd_ctx *ctx, const float *scores, int32_t *sel, dd_stream_t stream);
+
+/* Union of the queries' selections and residency resolution (Adaptive
+ * DHiSparse, Figs. 2 and 3).  sel: int32 [B,n_q,Hkv,k] ascending;
+ * resident_slot: int32 [B,Hkv,C], hot-pool slot or -1.  Outputs (device):
+ *   union_idx   int32 [B,Hkv,Umax]  union chunks, ascending (entries past union_cnt untouched)
+ *   union_slot  int32 [B,Hkv,Umax]  resident slot (>= 0) or -(m+1) for staging slot m
+ *   union_qmask uint8 [B,Hkv,Umax]  bit j set when query j selected the chunk
+ *   union_cnt   int32 [B,Hkv]
+ *   miss_list   int32 [max_misses]  miss m -> (b*Hkv+g)*C + c, m dense in (b,g,c) order
+ *   miss_count  int32 [1]           total misses M (may exceed max_misses: DD_ERR_CAPACITY)
+ *   attn_slot   int32 [B,n_q,Hkv,k] encoded slot of sel[b,j,g,r] (may be NULL: not written) */
+dd_status dd_resolve_union(dd_ctx *ctx, const int32_t *sel, const int32_t *resident_slot,
+                           int32_t *union_idx, int32_t *union_slot, uint8_t *union_qmask,
+                           int32_t *union_cnt, int32_t *miss_list, int32_t *miss_count,
+                           int32_t *attn_slot, dd_stream_t stream);
+
+/* Copy missing chunk m from the pinned host K/V (bf16 [B,Hkv,L,d]) into
+ * staging slot m of Kst/Vst (bf16 [max_misses,cs,d], device), byte-exact
+ * (DualDecoder §5.4, GPU-side sparse KV assembly).  miss_list/miss_count are
+ * device arrays as written by dd_resolve_union.  DD_GATHER_MEMCPY blocks the
+ * calling thread until the miss list is on the host. */
+dd_status dd_gather_kv(dd_ctx *ctx, const void *Kh, const void *Vh, const int32_t *miss_list,
+                       const int32_t *miss_count, void *Kst, void *Vst, dd_gather_mode mode,
+                       dd_stream_t stream);
+
+/* Split-K GQA decode attention of every query over its own selected rows,
+ * each union row read once for all queries that selected it (DualDecoder
+ * §5.2 co-batched dual-token attention; Adaptive DHiSparse Fig. 3).
+ * q: bf16 [B,n_q,Hq,d]; Khot/Vhot: bf16 [hot_slots,cs,d] (may be NULL when
+ * hot_slots = 0); Kst/Vst: bf16 [max_misses,cs,d]; union_slot, union_qmask,
+ * union_cnt, miss_count as written by dd_resolve_union.
+ * out: fp32 [B,n_q,Hq,d], out[b,j,h] = sum_t softmax_t(scale*q.K_t) V_t over
+ * the rows of the chunks whose qmask has bit j.  softmax_scale <= 0 selects
+ * 1/sqrt(d). */
+dd_status dd_sparse_attn_decode(dd_ctx *ctx, const void *q, const void *Khot, const void *Vhot,
+                                const void *Kst, const void *Vst, const int32_t *union_slot,
+                                const uint8_t *union_qmask, const int32_t *union_cnt,
+                                const int32_t *miss_count, float softmax_scale, float *out,
+                                dd_stream_t stream);
+
+/* One layer: score -> top-k -> resolve -> gather into staging buffer
+ * p = layer & 1 -> attention (DualDecoder §5.4, Fig. 11, two-layer ping-pong).
+ * The gather into buffer p waits on the event recorded when the attention of
+ * the previous use of p (layer - 2) finished; attention waits for the gather.
+ * Intermediate outputs are written to the caller's arrays when given, else to
+ * the context's workspace. */
+typedef struct {
+  int32_t layer;
+  const void *q;                 /* bf16 [B,n_q,Hq,d] device */
+  const void *lm;                /* bf16 [B,Hkv,C,d] device */
+  const void *Kh, *Vh;           /* bf16 [B,Hkv,L,d] pinned host */
+  const int32_t *resident_slot;  /* int32 [B,Hkv,C] device */
+  const void *Khot, *Vhot;       /* bf16 [hot_slots,cs,d] device or NULL */
+  void *Kst[2], *Vst[2];         /* bf16 [max_misses,cs,d] device: the ping-pong pair */
+  dd_gather_mode mode;
+  float softmax_scale;           /* <= 0: 1/sqrt(d) */
+  float *out;                    /* fp32 [B,n_q,Hq,d] device */
+  /* optional intermediates (NULL: context workspace) */
+  float *scores;
+  int32_t *sel, *union_idx, *union_slot, *union_cnt, *miss_list, *miss_count, *attn_slot;
+  uint8_t *union_qmask;
+  /* optional instrumentation: cudaEvent_t handles (NULL entries skipped)
+   * recorded on the stream before scoring and after scoring, top-k, resolve,
+   * gather and attention */
+  void *stage_events[6];
+} dd_step_args;
+
+dd_status dd_step(dd_ctx *ctx, const dd_step_args *args, dd_stream_t stream);
+
+/* Wait for the device, read the status word into *device_status (a dd_status
+ * value) and clear it. */
+dd_status dd_get_status(dd_ctx *ctx, int32_t *device_status);
+
+/* Number of kernel launches issued by the context since creation (all calls). */
+int64_t dd_launch_count(const dd_ctx *ctx);
+
+const char *dd_status_str(dd_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DD_H_ */

@@ -1,0 +1,408 @@
+// C ABI of libdd: context, argument checks, the per-stage entry points and
+// the one-layer step with its two-buffer ping-pong (DualDecoder §5.4,
+// Fig. 11: one staging buffer serves the current layer's attention while the
+// other receives a later layer's chunks; CUDA events order the copy into a
+// buffer after the attention that last read it, and the attention after the
+// copy).
+#include <math.h>
+#include <string.h>
+
+#include <vector>
+
+#include "dd_common.cuh"
+
+namespace dd {
+cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const void *Kst, const void *Vst,
+                        const int32_t *union_slot, const uint8_t *union_qmask, const int32_t *union_cnt,
+                        const int32_t *miss_count, float softmax_scale, float *out, float *part_o, float *part_ml,
+                        int32_t *status, int B, int n_q, int Hq, int Hkv, int cs, int umax, int64_t hot_slots,
+                        int64_t max_misses, const void *dummy_pool, cudaStream_t s);
+int attn_seg_chunks(int NQ, int cs);
+}  // namespace dd
+
+struct dd_ctx {
+  dd_dims dims;
+  int C, G, NQ, umax, units, device, sm_count;
+  int64_t max_misses, hot_slots;
+  // device workspace
+  void *ws = nullptr;
+  int32_t *status = nullptr;
+  float *scores = nullptr;
+  int32_t *sel = nullptr, *union_idx = nullptr, *union_slot = nullptr, *union_cnt = nullptr;
+  uint8_t *union_qmask = nullptr;
+  int32_t *unit_miss = nullptr, *miss_list = nullptr, *miss_count = nullptr, *attn_slot = nullptr;
+  float *part_o = nullptr, *part_ml = nullptr;
+  void *dummy_pool = nullptr;
+  // host side
+  int32_t *h_miss = nullptr;          // pinned: [1 + max_misses]
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t released[2] = {nullptr, nullptr};   // attention finished reading staging buffer p
+  cudaEvent_t gathered[2] = {nullptr, nullptr};   // copies into staging buffer p finished
+  cudaEvent_t ready = nullptr;                    // miss list available to the copy stream
+  bool used[2] = {false, false};
+  int64_t launches = 0;
+  // cached host -> device pointer translations for pinned host memory
+  const void *kh_host = nullptr, *vh_host = nullptr;
+  const void *kh_dev = nullptr, *vh_dev = nullptr;
+};
+
+namespace {
+
+using dd::kD;
+
+inline dd_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? DD_OK : DD_ERR_CUDA; }
+
+#define DD_TRY(expr)                       \
+  do {                                     \
+    const dd_status _s = (expr);           \
+    if (_s != DD_OK) return _s;            \
+  } while (0)
+
+#define DD_CUDA(expr) DD_TRY(cuda_ok(expr))
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dd_status check_dims(const dd_dims *d) {
+  if (!d) return DD_ERR_INVALID_ARG;
+  if (d->B < 0 || d->Hq <= 0 || d->Hkv <= 0 || d->Hq % d->Hkv) return DD_ERR_INVALID_ARG;
+  if (d->d != kD) return DD_ERR_INVALID_ARG;
+  if (d->cs != 16 && d->cs != 32 && d->cs != 64) return DD_ERR_INVALID_ARG;
+  if (d->L <= 0 || d->L % d->cs) return DD_ERR_INVALID_ARG;
+  const int C = d->L / d->cs;
+  if (C > dd::kMaxC || d->k < 1 || d->k > C) return DD_ERR_INVALID_ARG;
+  if (d->n_q < 1 || d->n_q > dd::kMaxNq) return DD_ERR_INVALID_ARG;
+  if (d->n_q * (d->Hq / d->Hkv) > dd::kMaxNQV) return DD_ERR_INVALID_ARG;
+  if ((int64_t)d->B * d->Hkv * C >= (int64_t(1) << 31)) return DD_ERR_INVALID_ARG;
+  return DD_OK;
+}
+
+// Device-visible address of a K/V pointer: device memory as is, pinned host
+// memory through its mapped device address.  Pageable memory is refused.
+dd_status device_view(const void *p, const void **out) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return DD_ERR_INVALID_ARG;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *out = p;
+    return DD_OK;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+    *out = a.devicePointer;
+    return DD_OK;
+  }
+  return DD_ERR_INVALID_ARG;
+}
+
+dd_status host_kv_views(dd_ctx *c, const void *Kh, const void *Vh, const void **kd, const void **vd) {
+  if (Kh != c->kh_host) {
+    DD_TRY(device_view(Kh, &c->kh_dev));
+    c->kh_host = Kh;
+  }
+  if (Vh != c->vh_host) {
+    DD_TRY(device_view(Vh, &c->vh_dev));
+    c->vh_host = Vh;
+  }
+  *kd = c->kh_dev;
+  *vd = c->vh_dev;
+  return DD_OK;
+}
+
+template <typename T>
+T *carve(uint8_t *&cur, int64_t n) {
+  T *p = reinterpret_cast<T *>(cur);
+  const int64_t bytes = ((n * (int64_t)sizeof(T)) + 255) & ~int64_t(255);
+  cur += bytes;
+  return p;
+}
+
+int64_t attn_max_seg(const dd_ctx *c) {
+  const int sc = dd::attn_seg_chunks(c->NQ, c->dims.cs);
+  return (c->umax + sc - 1) / sc;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dd_status_str(dd_status s) {
+  switch (s) {
+    case DD_OK: return "ok";
+    case DD_ERR_INVALID_ARG: return "invalid argument";
+    case DD_ERR_CUDA: return "CUDA runtime error";
+    case DD_ERR_CAPACITY: return "more missing chunks than the staging capacity";
+    case DD_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case DD_ERR_DEVICE_CHECK: return "an index read on the device was out of range";
+  }
+  return "unknown status";
+}
+
+dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, dd_ctx **out) {
+  if (!out) return DD_ERR_INVALID_ARG;
+  *out = nullptr;
+  DD_TRY(check_dims(dims));
+  if (max_misses < 0 || hot_slots < 0 || max_misses >= (int64_t(1) << 31) || hot_slots >= (int64_t(1) << 31))
+    return DD_ERR_INVALID_ARG;
+  dd_ctx *c = new dd_ctx();
+  c->dims = *dims;
+  c->C = dims->L / dims->cs;
+  c->G = dims->Hq / dims->Hkv;
+  c->NQ = dims->n_q * c->G;
+  c->umax = dims->n_q * dims->k < c->C ? dims->n_q * dims->k : c->C;
+  c->units = dims->B * dims->Hkv;
+  c->max_misses = max_misses;
+  c->hot_slots = hot_slots;
+  auto fail = [&](dd_status s) {
+    dd_destroy(c);
+    return s;
+  };
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess)
+    return fail(DD_ERR_CUDA);
+
+  const int64_t B = dims->B, Hkv = dims->Hkv, n_q = dims->n_q, k = dims->k, C = c->C;
+  const int64_t max_seg = attn_max_seg(c);
+  const int64_t units = c->units;
+  int64_t bytes = 0;
+  auto add = [&](int64_t n, int64_t sz) { bytes += ((n * sz) + 255) & ~int64_t(255); };
+  add(1, 4);                                   // status
+  add(B * n_q * Hkv * C, 4);                   // scores
+  add(B * n_q * Hkv * k, 4);                   // sel
+  add(units * c->umax, 4);                     // union_idx
+  add(units * c->umax, 4);                     // union_slot
+  add(units * c->umax, 1);                     // union_qmask
+  add(units, 4);                               // union_cnt
+  add(units, 4);                               // unit_miss
+  add(max_misses > 0 ? max_misses : 1, 4);     // miss_list
+  add(1, 4);                                   // miss_count
+  add(B * n_q * Hkv * k, 4);                   // attn_slot
+  add(units * max_seg * c->NQ * 128, 4);       // part_o
+  add(units * max_seg * c->NQ * 2, 4);         // part_ml
+  add(64 * 128, 2);                            // dummy pool (64 rows)
+  if (cudaMalloc(&c->ws, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
+  uint8_t *cur = static_cast<uint8_t *>(c->ws);
+  c->status = carve<int32_t>(cur, 1);
+  c->scores = carve<float>(cur, B * n_q * Hkv * C);
+  c->sel = carve<int32_t>(cur, B * n_q * Hkv * k);
+  c->union_idx = carve<int32_t>(cur, units * c->umax);
+  c->union_slot = carve<int32_t>(cur, units * c->umax);
+  c->union_qmask = carve<uint8_t>(cur, units * c->umax);
+  c->union_cnt = carve<int32_t>(cur, units);
+  c->unit_miss = carve<int32_t>(cur, units);
+  c->miss_list = carve<int32_t>(cur, max_misses > 0 ? max_misses : 1);
+  c->miss_count = carve<int32_t>(cur, 1);
+  c->attn_slot = carve<int32_t>(cur, B * n_q * Hkv * k);
+  c->part_o = carve<float>(cur, units * max_seg * c->NQ * 128);
+  c->part_ml = carve<float>(cur, units * max_seg * c->NQ * 2);
+  c->dummy_pool = carve<uint16_t>(cur, 64 * 128);
+  if (cudaMemset(c->ws, 0, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
+  if (cudaMallocHost(reinterpret_cast<void **>(&c->h_miss), (size_t)(1 + (max_misses > 0 ? max_misses : 1)) * 4) !=
+      cudaSuccess)
+    return fail(DD_ERR_CUDA);
+  if (cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking) != cudaSuccess) return fail(DD_ERR_CUDA);
+  for (int p = 0; p < 2; ++p) {
+    if (cudaEventCreateWithFlags(&c->released[p], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->gathered[p], cudaEventDisableTiming) != cudaSuccess)
+      return fail(DD_ERR_CUDA);
+  }
+  if (cudaEventCreateWithFlags(&c->ready, cudaEventDisableTiming) != cudaSuccess) return fail(DD_ERR_CUDA);
+  *out = c;
+  return DD_OK;
+}
+
+dd_status dd_destroy(dd_ctx *c) {
+  if (!c) return DD_ERR_INVALID_ARG;
+  if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
+  for (int p = 0; p < 2; ++p) {
+    if (c->released[p]) cudaEventDestroy(c->released[p]);
+    if (c->gathered[p]) cudaEventDestroy(c->gathered[p]);
+  }
+  if (c->ready) cudaEventDestroy(c->ready);
+  if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+  if (c->h_miss) cudaFreeHost(c->h_miss);
+  if (c->ws) cudaFree(c->ws);
+  delete c;
+  return DD_OK;
+}
+
+int64_t dd_launch_count(const dd_ctx *c) { return c ? c->launches : -1; }
+
+dd_status dd_get_status(dd_ctx *c, int32_t *device_status) {
+  if (!c || !device_status) return DD_ERR_INVALID_ARG;
+  DD_CUDA(cudaDeviceSynchronize());
+  DD_CUDA(cudaMemcpy(device_status, c->status, 4, cudaMemcpyDeviceToHost));
+  DD_CUDA(cudaMemset(c->status, 0, 4));
+  return DD_OK;
+}
+
+dd_status dd_build_landmarks(dd_ctx *c, const void *K, void *lm, dd_stream_t stream) {
+  if (!c) return DD_ERR_INVALID_ARG;
+  if (c->units == 0) return DD_OK;
+  if (!K || !lm || !aligned16(K) || !aligned16(lm)) return DD_ERR_INVALID_ARG;
+  const void *kd;
+  DD_TRY(device_view(K, &kd));
+  c->launches += 1;
+  return cuda_ok(dd::launch_build_landmarks(static_cast<const uint4 *>(kd), static_cast<uint4 *>(lm),
+                                            (int64_t)c->units * c->C, c->dims.cs, (cudaStream_t)stream));
+}
+
+dd_status dd_score_landmarks(dd_ctx *c, const void *q, const void *lm, float *scores, dd_stream_t stream) {
+  if (!c) return DD_ERR_INVALID_ARG;
+  if (c->units == 0) return DD_OK;
+  if (!q || !lm || !scores || !aligned16(q) || !aligned16(lm)) return DD_ERR_INVALID_ARG;
+  c->launches += 1;
+  return cuda_ok(dd::launch_score(static_cast<const uint4 *>(q), static_cast<const uint4 *>(lm), scores, c->dims.B,
+                                  c->dims.n_q, c->dims.Hq, c->dims.Hkv, c->C, (cudaStream_t)stream));
+}
+
+dd_status dd_select_topk(dd_ctx *c, const float *scores, int32_t *sel, dd_stream_t stream) {
+  if (!c) return DD_ERR_INVALID_ARG;
+  if (c->units == 0) return DD_OK;
+  if (!scores || !sel) return DD_ERR_INVALID_ARG;
+  c->launches += 1;
+  return cuda_ok(dd::launch_topk(scores, sel, c->dims.B * c->dims.n_q * c->dims.Hkv, c->C, c->dims.k,
+                                 (cudaStream_t)stream));
+}
+
+dd_status dd_resolve_union(dd_ctx *c, const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx,
+                           int32_t *union_slot, uint8_t *union_qmask, int32_t *union_cnt, int32_t *miss_list,
+                           int32_t *miss_count, int32_t *attn_slot, dd_stream_t stream) {
+  if (!c) return DD_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (c->units == 0) return miss_count ? cuda_ok(cudaMemsetAsync(miss_count, 0, 4, s)) : DD_OK;
+  if (!sel || !resident_slot || !union_idx || !union_slot || !union_qmask || !union_cnt || !miss_list ||
+      !miss_count)
+    return DD_ERR_INVALID_ARG;
+  const dd_dims &d = c->dims;
+  DD_CUDA(dd::launch_union(sel, resident_slot, union_idx, union_slot, union_qmask, union_cnt, c->unit_miss, c->units,
+                           d.n_q, d.Hkv, d.k, c->C, c->umax, c->hot_slots, c->status, s));
+  DD_CUDA(dd::launch_assign(sel, union_idx, union_slot, union_cnt, c->unit_miss, miss_list, miss_count, attn_slot,
+                            c->units, d.n_q, d.Hkv, d.k, c->C, c->umax, c->max_misses, c->status, s));
+  c->launches += 2;
+  return DD_OK;
+}
+
+// MEMCPY mode: miss list to the host, then one copy per run of consecutive
+// chunks (consecutive ordinals whose packed indices are consecutive are
+// contiguous in both the host tensor and the staging buffer).
+static dd_status gather_memcpy(dd_ctx *c, const void *Kh, const void *Vh, const int32_t *miss_list,
+                               const int32_t *miss_count, void *Kst, void *Vst, cudaStream_t s) {
+  DD_CUDA(cudaMemcpyAsync(c->h_miss, miss_count, 4, cudaMemcpyDeviceToHost, s));
+  DD_CUDA(cudaStreamSynchronize(s));
+  int64_t M = c->h_miss[0];
+  if (M < 0) return DD_ERR_DEVICE_CHECK;
+  if (M > c->max_misses) M = c->max_misses;   // the resolver already flagged DD_ERR_CAPACITY
+  if (M == 0) return DD_OK;
+  DD_CUDA(cudaMemcpyAsync(c->h_miss + 1, miss_list, (size_t)M * 4, cudaMemcpyDeviceToHost, s));
+  DD_CUDA(cudaStreamSynchronize(s));
+  const int64_t chunk_bytes = (int64_t)c->dims.cs * kD * 2;
+  const int64_t n_total = (int64_t)c->units * c->C;
+  DD_CUDA(cudaEventRecord(c->ready, s));
+  DD_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ready, 0));
+  const int32_t *ml = c->h_miss + 1;
+  int64_t m = 0;
+  while (m < M) {
+    int64_t run = 1;
+    while (m + run < M && ml[m + run] == ml[m] + run) ++run;
+    if (ml[m] < 0 || ml[m] + run > n_total) return DD_ERR_DEVICE_CHECK;
+    const int64_t src = (int64_t)ml[m] * chunk_bytes, dst = m * chunk_bytes;
+    DD_CUDA(cudaMemcpyAsync(static_cast<uint8_t *>(Kst) + dst, static_cast<const uint8_t *>(Kh) + src,
+                            (size_t)(run * chunk_bytes), cudaMemcpyDefault, c->copy_stream));
+    DD_CUDA(cudaMemcpyAsync(static_cast<uint8_t *>(Vst) + dst, static_cast<const uint8_t *>(Vh) + src,
+                            (size_t)(run * chunk_bytes), cudaMemcpyDefault, c->copy_stream));
+    m += run;
+  }
+  DD_CUDA(cudaEventRecord(c->ready, c->copy_stream));
+  DD_CUDA(cudaStreamWaitEvent(s, c->ready, 0));
+  return DD_OK;
+}
+
+dd_status dd_gather_kv(dd_ctx *c, const void *Kh, const void *Vh, const int32_t *miss_list, const int32_t *miss_count,
+                       void *Kst, void *Vst, dd_gather_mode mode, dd_stream_t stream) {
+  if (!c) return DD_ERR_INVALID_ARG;
+  if (mode != DD_GATHER_ZEROCOPY && mode != DD_GATHER_MEMCPY) return DD_ERR_INVALID_ARG;
+  if (c->units == 0) return DD_OK;
+  if (!Kh || !Vh || !miss_list || !miss_count) return DD_ERR_INVALID_ARG;
+  if (c->max_misses > 0 && (!Kst || !Vst || !aligned16(Kst) || !aligned16(Vst))) return DD_ERR_INVALID_ARG;
+  if (!aligned16(Kh) || !aligned16(Vh)) return DD_ERR_INVALID_ARG;
+  if (c->units == 0 || c->max_misses == 0) return DD_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (mode == DD_GATHER_MEMCPY) {
+    int32_t st = 0;
+    DD_CUDA(cudaMemcpyAsync(&c->h_miss[0], c->status, 4, cudaMemcpyDeviceToHost, s));
+    DD_CUDA(cudaStreamSynchronize(s));
+    st = c->h_miss[0];
+    if (st != 0) return DD_OK;   // a device error is pending: no work, as the kernels do
+    return gather_memcpy(c, Kh, Vh, miss_list, miss_count, Kst, Vst, s);
+  }
+  const void *kd, *vd;
+  DD_TRY(host_kv_views(c, Kh, Vh, &kd, &vd));
+  c->launches += 1;
+  return cuda_ok(dd::launch_gather(static_cast<const uint4 *>(kd), static_cast<const uint4 *>(vd), miss_list,
+                                   miss_count, static_cast<uint4 *>(Kst), static_cast<uint4 *>(Vst), c->max_misses,
+                                   (int64_t)c->units * c->C, c->dims.cs, c->status, c->sm_count, s));
+}
+
+dd_status dd_sparse_attn_decode(dd_ctx *c, const void *q, const void *Khot, const void *Vhot, const void *Kst,
+                                const void *Vst, const int32_t *union_slot, const uint8_t *union_qmask,
+                                const int32_t *union_cnt, const int32_t *miss_count, float softmax_scale, float *out,
+                                dd_stream_t stream) {
+  if (!c) return DD_ERR_INVALID_ARG;
+  if (c->units == 0) return DD_OK;
+  if (!q || !union_slot || !union_qmask || !union_cnt || !miss_count || !out || !aligned16(q))
+    return DD_ERR_INVALID_ARG;
+  if (c->hot_slots > 0 && (!Khot || !Vhot || !aligned16(Khot) || !aligned16(Vhot))) return DD_ERR_INVALID_ARG;
+  if (c->max_misses > 0 && (!Kst || !Vst || !aligned16(Kst) || !aligned16(Vst))) return DD_ERR_INVALID_ARG;
+  if (c->units == 0) return DD_OK;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)kD);
+  const dd_dims &d = c->dims;
+  c->launches += 2;
+  return cuda_ok(dd::launch_attn(q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count, scale, out,
+                                 c->part_o, c->part_ml, c->status, d.B, d.n_q, d.Hq, d.Hkv, d.cs, c->umax,
+                                 c->hot_slots, c->max_misses, c->dummy_pool, (cudaStream_t)stream));
+}
+
+dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
+  if (!c || !a || a->layer < 0) return DD_ERR_INVALID_ARG;
+  if (c->units == 0) return DD_OK;
+  if (!a->q || !a->lm || !a->Kh || !a->Vh || !a->resident_slot || !a->out) return DD_ERR_INVALID_ARG;
+  const int p = a->layer & 1;
+  if (c->max_misses > 0 && (!a->Kst[p] || !a->Vst[p])) return DD_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  float *scores = a->scores ? a->scores : c->scores;
+  int32_t *sel = a->sel ? a->sel : c->sel;
+  int32_t *union_idx = a->union_idx ? a->union_idx : c->union_idx;
+  int32_t *union_slot = a->union_slot ? a->union_slot : c->union_slot;
+  uint8_t *union_qmask = a->union_qmask ? a->union_qmask : c->union_qmask;
+  int32_t *union_cnt = a->union_cnt ? a->union_cnt : c->union_cnt;
+  int32_t *miss_list = a->miss_list ? a->miss_list : c->miss_list;
+  int32_t *miss_count = a->miss_count ? a->miss_count : c->miss_count;
+  int32_t *attn_slot = a->attn_slot ? a->attn_slot : c->attn_slot;
+
+  auto mark = [&](int i) -> dd_status {
+    return a->stage_events[i] ? cuda_ok(cudaEventRecord((cudaEvent_t)a->stage_events[i], s)) : DD_OK;
+  };
+  DD_TRY(mark(0));
+  DD_TRY(dd_score_landmarks(c, a->q, a->lm, scores, stream));
+  DD_TRY(mark(1));
+  DD_TRY(dd_select_topk(c, scores, sel, stream));
+  DD_TRY(mark(2));
+  DD_TRY(dd_resolve_union(c, sel, a->resident_slot, union_idx, union_slot, union_qmask, union_cnt, miss_list,
+                          miss_count, attn_slot, stream));
+  DD_TRY(mark(3));
+  // staging buffer p may still be read by the attention of layer - 2
+  if (c->used[p]) DD_CUDA(cudaStreamWaitEvent(s, c->released[p], 0));
+  DD_TRY(dd_gather_kv(c, a->Kh, a->Vh, miss_list, miss_count, a->Kst[p], a->Vst[p], a->mode, stream));
+  DD_CUDA(cudaEventRecord(c->gathered[p], s));
+  DD_CUDA(cudaStreamWaitEvent(s, c->gathered[p], 0));
+  DD_TRY(mark(4));
+  DD_TRY(dd_sparse_attn_decode(c, a->q, a->Khot, a->Vhot, a->Kst[p], a->Vst[p], union_slot, union_qmask, union_cnt,
+                               miss_count, a->softmax_scale, a->out, stream));
+  DD_TRY(mark(5));
+  DD_CUDA(cudaEventRecord(c->released[p], s));
+  c->used[p] = true;
+  return DD_OK;
+}
+
+}  // extern "C"

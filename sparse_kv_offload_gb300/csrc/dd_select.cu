@@ -1,0 +1,315 @@
+// Per-row top-k chunk selection and the cross-query union / residency resolver.
+//
+// OasisKV summary, Methodology: blocks are ranked independently for every KV
+// head and the top-K kept.  Adaptive DHiSparse, Figs. 2 and 3: the selections
+// of all queries of a request are resolved together (hot pool first, host for
+// the rest) so that each distinct missing row is copied once, while every
+// query keeps its own selection for attention.
+#include "dd_common.cuh"
+
+namespace dd {
+
+// ---------------------------------------------------------------------------
+// block-wide exclusive scan of one int per thread (blockDim a multiple of 32)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// `scratch` holds 33 ints of shared memory.  Returns the exclusive prefix and
+// the block total; ends with a barrier so scratch can be reused.
+__device__ int block_excl_scan(int v, int *scratch, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int incl = warp_incl_scan(v);
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int x = lane < nw ? scratch[lane] : 0;
+    const int xi = warp_incl_scan(x);
+    if (lane < nw) scratch[lane] = xi - x;
+    if (lane == 31) scratch[32] = xi;
+  }
+  __syncthreads();
+  const int r = scratch[warp] + incl - v;
+  *total = scratch[32];
+  __syncthreads();
+  return r;
+}
+
+// Order-preserving map fp32 -> uint32: larger float, larger key.  -0 maps to
+// +0's key; NaN maps to 0, below every number.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7FFFFFFFu) == 0) u = 0;
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------
+// a2: one CTA per (b, j, g) row.  Radix select (4 passes of 8 bits, most
+// significant first) finds the k-th largest key T and how many keys equal to
+// T are needed; a scan over the row in chunk order then emits every key > T
+// and the lowest-index keys == T, which yields the (score desc, index asc)
+// top-k listed in ascending chunk order.
+// ---------------------------------------------------------------------------
+constexpr int kTopkThreads = 512;
+
+__global__ void __launch_bounds__(kTopkThreads) k_topk(const float *__restrict__ scores, int32_t *__restrict__ sel,
+                                                       int C, int k) {
+  extern __shared__ uint32_t keys[];
+  __shared__ int hist[256];
+  __shared__ int scratch[33];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_remaining;
+
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float *src = scores + (int64_t)row * C;
+  for (int i = tid; i < C; i += kTopkThreads) keys[i] = order_key(src[i]);
+
+  uint32_t prefix = 0, pmask = 0;
+  int remaining = k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    if (tid < 256) hist[tid] = 0;
+    __syncthreads();
+    for (int i = tid; i < C; i += kTopkThreads) {
+      const uint32_t key = keys[i];
+      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins 255-8l down to 248-8l (descending digit order)
+      int cnt[8], s = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        cnt[e] = hist[255 - 8 * lane - e];
+        s += cnt[e];
+      }
+      const int incl = warp_incl_scan(s);
+      const int excl = incl - s;
+      if (excl < remaining && remaining <= incl) {
+        int r = remaining - excl;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (r > 0 && r <= cnt[e]) {
+            s_prefix = prefix | ((uint32_t)(255 - 8 * lane - e) << shift);
+            s_remaining = r;
+            r = 0;
+          } else if (r > 0) {
+            r -= cnt[e];
+          }
+        }
+      }
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    remaining = s_remaining;
+    pmask |= 0xFFu << shift;
+    __syncthreads();
+  }
+  const uint32_t T = prefix;
+  const int need = remaining;   // keys equal to T to take, lowest chunk first
+
+  const int per = (C + kTopkThreads - 1) / kTopkThreads;
+  const int lo = min(C, tid * per), hi = min(C, lo + per);
+  int eq_local = 0;
+  for (int c = lo; c < hi; ++c) eq_local += (keys[c] == T);
+  int tot;
+  const int eq_before = block_excl_scan(eq_local, scratch, &tot);
+  int take = 0;
+  {
+    int er = eq_before;
+    for (int c = lo; c < hi; ++c) {
+      const uint32_t key = keys[c];
+      if (key > T) ++take;
+      else if (key == T) { take += (er < need); ++er; }
+    }
+  }
+  int pos = block_excl_scan(take, scratch, &tot);
+  int32_t *dst = sel + (int64_t)row * k;
+  int er = eq_before;
+  for (int c = lo; c < hi; ++c) {
+    const uint32_t key = keys[c];
+    bool t = key > T;
+    if (key == T) { t = er < need; ++er; }
+    if (t) dst[pos++] = c;
+  }
+}
+
+cudaError_t launch_topk(const float *scores, int32_t *sel, int rows, int C, int k, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const size_t smem = (size_t)C * sizeof(uint32_t);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kMaxC * (int)sizeof(uint32_t));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  k_topk<<<rows, kTopkThreads, smem, s>>>(scores, sel, C, k);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// a3, pass 1 (one CTA per (b,g)): per-query bitmaps of the selections, their
+// union listed in ascending chunk order with the query mask of each chunk,
+// residency lookup, and the (b,g)-local ordinal of every miss, stored as
+// -(local+1) in union_slot until pass 2 adds the global offset.
+// ---------------------------------------------------------------------------
+constexpr int kUnionThreads = 512;
+constexpr int kMaxWords = kMaxC / 32;
+
+__global__ void __launch_bounds__(kUnionThreads) k_union(
+    const int32_t *__restrict__ sel, const int32_t *__restrict__ resident_slot, int32_t *__restrict__ union_idx,
+    int32_t *__restrict__ union_slot, uint8_t *__restrict__ union_qmask, int32_t *__restrict__ union_cnt,
+    int32_t *__restrict__ unit_miss, int n_q, int Hkv, int k, int C, int umax, int64_t hot_slots,
+    int32_t *status) {
+  __shared__ uint32_t qbits[kMaxNq * kMaxWords];
+  __shared__ uint32_t missw[kMaxWords];
+  __shared__ int scratch[33];
+  const int unit = blockIdx.x;
+  const int b = unit / Hkv, g = unit - b * Hkv;
+  const int tid = threadIdx.x;
+  const int W = (C + 31) >> 5;
+  for (int i = tid; i < n_q * W; i += kUnionThreads) qbits[i] = 0u;
+  __syncthreads();
+  for (int i = tid; i < n_q * k; i += kUnionThreads) {
+    const int j = i / k, r = i - j * k;
+    const int c = sel[((int64_t)(b * n_q + j) * Hkv + g) * k + r];
+    if (c < 0 || c >= C) {
+      set_status(status, DD_ERR_DEVICE_CHECK);
+      continue;
+    }
+    atomicOr(&qbits[j * W + (c >> 5)], 1u << (c & 31));
+  }
+  __syncthreads();
+
+  const int per = (W + kUnionThreads - 1) / kUnionThreads;
+  const int w0 = min(W, tid * per), w1 = min(W, w0 + per);
+  const int32_t *rs_unit = resident_slot + (int64_t)unit * C;
+  int cnt_u = 0, cnt_m = 0;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t ub = 0;
+    for (int j = 0; j < n_q; ++j) ub |= qbits[j * W + w];
+    uint32_t mb = 0, rest = ub;
+    while (rest) {
+      const int bit = __ffs(rest) - 1;
+      rest &= rest - 1;
+      const int32_t rs = rs_unit[w * 32 + bit];
+      if (rs >= hot_slots) set_status(status, DD_ERR_DEVICE_CHECK);
+      if (rs < 0 || rs >= hot_slots) mb |= 1u << bit;
+    }
+    missw[w] = mb;
+    cnt_u += __popc(ub);
+    cnt_m += __popc(mb);
+  }
+  int total;
+  const int excl = block_excl_scan((cnt_u << 16) | cnt_m, scratch, &total);
+  int upos = excl >> 16, mpos = excl & 0xFFFF;
+  const int64_t ubase = (int64_t)unit * umax;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t ub = 0;
+    for (int j = 0; j < n_q; ++j) ub |= qbits[j * W + w];
+    const uint32_t mb = missw[w];
+    while (ub) {
+      const int bit = __ffs(ub) - 1;
+      ub &= ub - 1;
+      const int c = w * 32 + bit;
+      uint32_t qm = 0;
+      for (int j = 0; j < n_q; ++j) qm |= ((qbits[j * W + w] >> bit) & 1u) << j;
+      union_idx[ubase + upos] = c;
+      union_qmask[ubase + upos] = (uint8_t)qm;
+      if ((mb >> bit) & 1u) {
+        union_slot[ubase + upos] = -(mpos + 1);
+        ++mpos;
+      } else {
+        union_slot[ubase + upos] = rs_unit[c];
+      }
+      ++upos;
+    }
+  }
+  if (tid == 0) {
+    union_cnt[unit] = total >> 16;
+    unit_miss[unit] = total & 0xFFFF;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a3, pass 2 (one CTA per (b,g)): global miss ordinals = misses of all
+// earlier (b,g) units + the local ordinal, written to the miss list and the
+// union slots; then every selection entry looks up its encoded slot.
+// ---------------------------------------------------------------------------
+constexpr int kAssignThreads = 256;
+
+__global__ void __launch_bounds__(kAssignThreads) k_assign(
+    const int32_t *__restrict__ sel, const int32_t *__restrict__ union_idx, int32_t *__restrict__ union_slot,
+    const int32_t *__restrict__ union_cnt, const int32_t *__restrict__ unit_miss, int32_t *__restrict__ miss_list,
+    int32_t *__restrict__ miss_count, int32_t *__restrict__ attn_slot, int units, int n_q, int Hkv, int k, int C,
+    int umax, int64_t max_misses, int32_t *status) {
+  __shared__ int scratch[33];
+  const int unit = blockIdx.x;
+  const int b = unit / Hkv, g = unit - b * Hkv;
+  const int tid = threadIdx.x;
+  int before = 0;
+  for (int u = tid; u < unit; u += kAssignThreads) before += unit_miss[u];
+  int offset;
+  block_excl_scan(before, scratch, &offset);
+
+  const int cnt = union_cnt[unit];
+  const int64_t ubase = (int64_t)unit * umax;
+  bool over = false;
+  for (int u = tid; u < cnt; u += kAssignThreads) {
+    const int32_t s = union_slot[ubase + u];
+    if (s < 0) {
+      const int64_t m = (int64_t)offset + (-(int64_t)s - 1);
+      if (m < max_misses) miss_list[m] = unit * C + union_idx[ubase + u];
+      else over = true;
+      union_slot[ubase + u] = (int32_t)(-(m + 1));
+    }
+  }
+  if (over) set_status(status, DD_ERR_CAPACITY);
+  if (unit == units - 1 && tid == 0) *miss_count = offset + unit_miss[unit];
+  __syncthreads();
+  if (attn_slot == nullptr) return;
+  for (int i = tid; i < n_q * k; i += kAssignThreads) {
+    const int j = i / k, r = i - j * k;
+    const int64_t si = ((int64_t)(b * n_q + j) * Hkv + g) * k + r;
+    const int c = sel[si];
+    int lo = 0, hi = cnt - 1, found = -1;
+    while (lo <= hi) {
+      const int mid = (lo + hi) >> 1;
+      const int v = union_idx[ubase + mid];
+      if (v == c) { found = mid; break; }
+      if (v < c) lo = mid + 1; else hi = mid - 1;
+    }
+    attn_slot[si] = found >= 0 ? union_slot[ubase + found] : INT32_MIN;
+  }
+}
+
+cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx, int32_t *union_slot,
+                         uint8_t *union_qmask, int32_t *union_cnt, int32_t *unit_miss, int units, int n_q, int Hkv,
+                         int k, int C, int umax, int64_t hot_slots, int32_t *status, cudaStream_t s) {
+  if (units == 0) return cudaSuccess;
+  k_union<<<units, kUnionThreads, 0, s>>>(sel, resident_slot, union_idx, union_slot, union_qmask, union_cnt,
+                                          unit_miss, n_q, Hkv, k, C, umax, hot_slots, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_assign(const int32_t *sel, const int32_t *union_idx, int32_t *union_slot,
+                          const int32_t *union_cnt, const int32_t *unit_miss, int32_t *miss_list,
+                          int32_t *miss_count, int32_t *attn_slot, int units, int n_q, int Hkv, int k, int C,
+                          int umax, int64_t max_misses, int32_t *status, cudaStream_t s) {
+  if (units == 0) return cudaSuccess;
+  k_assign<<<units, kAssignThreads, 0, s>>>(sel, union_idx, union_slot, union_cnt, unit_miss, miss_list,
+                                            miss_count, attn_slot, units, n_q, Hkv, k, C, umax, max_misses,
+                                            status);
+  return cudaGetLastError();
+}
+
+}  // namespace dd

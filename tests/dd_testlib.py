@@ -1,0 +1,109 @@
+"""Shared helpers of the test-suite: seeded inputs of a workload, host <-> torch
+conversion, and the parity checks (bit-exact indices modulo the score tie
+band, attention within max-abs 2e-2 and relative-L2 1e-3)."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from sparse_kv_offload_gb300 import synth
+from sparse_kv_offload_gb300.workloads import Workload
+
+ATOL_MAX = 2e-2       # attention: max |gpu - oracle|
+REL_L2 = 1e-3         # attention: ||gpu - oracle||_2 / ||oracle||_2
+TIE_REL = 1e-5        # top-k: a selection may differ only where the k-th and (k+1)-th scores are this close
+
+
+# --------------------------------------------------------------------- inputs
+
+def key_bias(w: Workload, q, layer=0):
+    if w.key_bias == "hot":
+        return synth.hot_chunk_bias(w.seed, w.B, w.Hkv, w.C, w.hot_frac, w.bias_sigma, layer), \
+            synth.query_direction(q, w.Hkv)
+    if w.key_bias == "zipf":
+        return synth.zipf_chunk_bias(w.seed, w.B, w.Hkv, w.C, w.zipf_alpha, w.bias_sigma, layer), \
+            synth.query_direction(q, w.Hkv)
+    return None, None
+
+
+def host_inputs(w: Workload, layer: int = 0) -> dict:
+    """Every input of one layer step as numpy arrays (bf16 as uint16 bits)."""
+    q = synth.queries(w.seed, w.B, w.n_q, w.Hq, w.d, w.spec_scale, layer)
+    bias, u_hat = key_bias(w, q, layer)
+    K = synth.kv_tensor(w.seed, synth.TID_K, w.B, w.Hkv, w.L, w.d, w.cs, bias, u_hat, layer)
+    V = synth.kv_tensor(w.seed, synth.TID_V, w.B, w.Hkv, w.L, w.d, w.cs, layer=layer)
+    lm = oracle.build_landmarks(K, w.cs)
+    if w.residency == "uniform":
+        slot = synth.uniform_residency(w.seed, w.B, w.Hkv, w.C, w.resident_frac, layer)
+    elif w.residency == "carry":
+        # the previous step's selection: the oracle's selection for this step's
+        # queries stands in for it (temporal locality), then a seeded share of
+        # it is resident
+        sel = oracle.select_topk(oracle.score_landmarks(q, lm), w.k)
+        U = [set(oracle.union_of_query_selections(sel, b, g)) for b in range(w.B) for g in range(w.Hkv)]
+        slot = synth.carried_residency(w.seed, U, w.B, w.Hkv, w.C, w.resident_frac, layer)
+    else:
+        slot = np.full((w.B, w.Hkv, w.C), -1, np.int32)
+    Khot = synth.hot_pool_from(K, slot, w.cs)
+    Vhot = synth.hot_pool_from(V, slot, w.cs)
+    return dict(q=q, K=K, V=V, lm=lm, slot=slot, Khot=Khot, Vhot=Vhot, bias=bias, u_hat=u_hat)
+
+
+# --------------------------------------------------------------------- torch
+
+def to_bf16(a: np.ndarray, device="cuda", pin=False):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    if device == "cpu":
+        return t.pin_memory() if pin else t.clone()
+    return t.to(device)
+
+
+def from_bf16(t) -> np.ndarray:
+    import torch
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def to_i32(a, device="cuda"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+
+# --------------------------------------------------------------------- checks
+
+def check_attention(got: np.ndarray, want: np.ndarray, mask=None):
+    """max-abs and relative-L2 over the selected outputs (mask over leading dims)."""
+    g = np.asarray(got, np.float64)
+    w = np.asarray(want, np.float64)
+    if mask is not None:
+        g, w = g[mask], w[mask]
+    if w.size == 0:
+        return 0.0, 0.0
+    err = np.abs(g - w).max()
+    rel = np.linalg.norm(g - w) / max(np.linalg.norm(w), 1e-300)
+    assert err <= ATOL_MAX, f"max-abs error {err:.3e} > {ATOL_MAX}"
+    assert rel <= REL_L2, f"relative-L2 error {rel:.3e} > {REL_L2}"
+    return err, rel
+
+
+def selection_rows_match(gpu_sel: np.ndarray, scores64: np.ndarray, oracle_sel: np.ndarray, k: int):
+    """Per row: True when the GPU selection equals the oracle's; rows that
+    differ must differ only inside the tie band.  Returns the bool row mask."""
+    C = scores64.shape[-1]
+    g = gpu_sel.reshape(-1, k)
+    o = oracle_sel.reshape(-1, k)
+    s = scores64.reshape(-1, C)
+    same = np.all(g == o, axis=1)
+    for r in np.nonzero(~same)[0]:
+        row = s[r]
+        order = np.lexsort((np.arange(C), -row))
+        sk = row[order[k - 1]]
+        sk1 = row[order[k]] if k < C else -np.inf
+        tau = TIE_REL * max(abs(sk), abs(sk1))
+        gset = set(g[r].tolist())
+        assert len(gset) == k and list(g[r]) == sorted(gset), f"row {r}: not k distinct ascending chunks"
+        must = set(np.nonzero(row > sk + tau)[0].tolist())
+        never = set(np.nonzero(row < sk1 - tau)[0].tolist())
+        assert must <= gset, f"row {r}: GPU dropped a chunk clearly above the k-th score"
+        assert not (gset & never), f"row {r}: GPU kept a chunk clearly below the (k+1)-th score"
+    return same.reshape(gpu_sel.shape[:-1])
