@@ -14,11 +14,11 @@ Sources (web pages, cited by title and section / equation / figure):
   §5.4 and Fig. 11 (two-layer ping-pong buffer, GPU-side sparse assembly).
 * "OasisKV" summary -- eqs. (1)-(3) (KV footprint, maximum batch, per-step
   byte budget); Methodology (top-K per KV head; normal and draft queries
-  attend together over one resident working set).
+  share one HBM working set).
 * "Adaptive DHiSparse: Speculative Decoding over a Load-Adaptive KV
   Hierarchy" -- Fig. 2 (resolver: resident tiers first, host copy for
   misses), Fig. 3 (the selections of several queries resolved together so
-  each distinct missing row is copied once; each query attends over its own
+  a chunk picked by several queries is fetched once; attention uses each query's own
   selection).
 
 Every function is pinned by the tests in ``tests/test_oracle_pins.py``

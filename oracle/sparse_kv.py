@@ -55,7 +55,7 @@ def build_landmarks(K: np.ndarray, cs: int) -> np.ndarray:
 
     DualDecoder §2.2: adjacent KV entries are grouped into chunks and each
     chunk keeps one compact landmark used to rank chunks for a query; §4.1:
-    the landmarks are produced before decoding and stay fixed.  The landmark
+    the landmarks are made once, ahead of the decode loop.  The landmark
     is the mean key of the chunk.  Reading: the sum runs in fp32 over the
     chunk's tokens in order t = 0..cs-1, is divided by cs in fp32 and rounded
     to bf16 (the KV dtype, as the "1/16 of the KV cache" summary size in the
@@ -141,9 +141,9 @@ def resolve_union(sel: np.ndarray, resident_slot: np.ndarray) -> dict:
     """Resolve the union of the queries' selections against the HBM pool.
 
     Adaptive DHiSparse Fig. 3: the selections of the several queries of a
-    request and KV source are handled together, so each distinct missing row
-    is copied from host once, while each query still attends over its own
-    selection.  Fig. 2: a selected row is looked up in the HBM tiers first
+    request and KV source are resolved in one pass, so a chunk picked by
+    several queries is fetched from the host a single time; attention still
+    uses every query's own top-k.  Fig. 2: a selected row is looked up in the HBM tiers first
     and copied from host DRAM only when it is found in none of them.
 
     Readings: per (b, g) the union U lists chunks in ascending order; a chunk
@@ -230,7 +230,7 @@ def sparse_attn_decode(q, Khot, Vhot, Kst, Vst, attn_slot, cs: int, scale: float
     DualDecoder §5.2: the output and speculative tokens attend in one pass;
     OasisKV Methodology: normal and draft queries attend together over one
     resident working set; Adaptive DHiSparse Fig. 3: each query attends over
-    its own selection.  Readings: scale = 1/sqrt(d); query head h uses KV
+    the chunks it picked itself.  Readings: scale = 1/sqrt(d); query head h uses KV
     head floor(h/G); the rows of query j are those of the k chunks in
     ``attn_slot[b,j,g,:]``; the current step's own new tokens are not part
     of the path.

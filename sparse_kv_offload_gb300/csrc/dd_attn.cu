@@ -3,8 +3,8 @@
 //
 // DualDecoder §5.2: the output token and the speculative token attend in one
 // pass instead of two.  Adaptive DHiSparse Fig. 3 / OasisKV Methodology: the
-// queries of a request attend over one resident working set, each over its
-// own selection.  Here one work item is a segment of the union of one
+// normal and draft queries share the HBM working set, but query j only sees
+// the chunks it picked.  Here one work item is a segment of the union of one
 // (request, KV head): every union row is streamed from HBM once and serves
 // all NQ = n_q*G query vectors of that KV head; rows of a chunk a query did
 // not select are masked for that query (the chunk's query mask).

@@ -3,8 +3,8 @@
 // OasisKV summary, Methodology: blocks are ranked independently for every KV
 // head and the top-K kept.  Adaptive DHiSparse, Figs. 2 and 3: the selections
 // of all queries of a request are resolved together (hot pool first, host for
-// the rest) so that each distinct missing row is copied once, while every
-// query keeps its own selection for attention.
+// the rest), so a chunk wanted by several queries crosses the host link a
+// single time; attention still uses each query's own top-k.
 #include "dd_common.cuh"
 
 namespace dd {
@@ -145,12 +145,9 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(const float *__restrict__
 cudaError_t launch_topk(const float *scores, int32_t *sel, int rows, int C, int k, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   const size_t smem = (size_t)C * sizeof(uint32_t);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kMaxC * (int)sizeof(uint32_t));
+  if (smem > 48 * 1024) {   // the opt-in is per device, so ask on every launch that needs it
+    cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   k_topk<<<rows, kTopkThreads, smem, s>>>(scores, sel, C, k);
   return cudaGetLastError();

@@ -156,7 +156,7 @@ def test_topk_ties_take_lowest_index_and_output_is_ascending():
 
 def test_union_worked_example_dedups_shared_rows():
     # Adaptive DHiSparse Fig. 3: K=4 queries, k=3; row a selected by three
-    # queries, row b by two -- each distinct missing row is copied once.
+    # queries, row b by two -- both must be fetched a single time.
     a, b_, C = 5, 9, 16
     sel = np.array([[[[a, b_, 1]], [[a, 2, 3]], [[a, b_, 4]], [[6, 7, 8]]]], dtype=np.int32)
     sel = np.sort(sel, axis=-1)
