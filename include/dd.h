@@ -140,6 +140,31 @@ dd_status dd_sparse_attn_decode(dd_ctx *ctx, const void *q, const void *Khot, co
                                 const int32_t *miss_count, float softmax_scale, float *out,
                                 dd_stream_t stream);
 
+/* Allocation-free variant of dd_sparse_attn_decode.  The pages have no
+ * counterpart: it exists for callers that cannot allocate device memory --
+ * a serving loop whose memory is already carved up by its own pool, or a
+ * host engine that forbids cudaMalloc between decode steps because the call
+ * can synchronise the device -- and therefore cannot create a dd_ctx.
+ * It takes no context: dims, hot_slots and max_misses describe the tensors as
+ * for dd_create, and the other arguments are those of dd_sparse_attn_decode.
+ * device_status: caller-owned device int32, zero before the call; a kernel
+ * that finds an error writes its dd_status code there (first error wins).
+ * The split-K partials live in one fixed 8 MiB device array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  A shape whose partials (B*Hkv * segments * NQ * 130 floats) do not
+ * fit is refused at once with DD_ERR_CAPACITY.  The first call on a device
+ * looks up that array's device address (once per device); make that first
+ * call before any stream capture.  Nothing in the array needs to start at
+ * zero, but every call shares it: calls that overlap on the GPU (on any
+ * streams, from any thread) race on it and must be serialised by the
+ * caller. */
+dd_status dd_sparse_attn_decode_noalloc(const dd_dims *dims, int64_t hot_slots, int64_t max_misses,
+                                        const void *q, const void *Khot, const void *Vhot,
+                                        const void *Kst, const void *Vst, const int32_t *union_slot,
+                                        const uint8_t *union_qmask, const int32_t *union_cnt,
+                                        const int32_t *miss_count, float softmax_scale, float *out,
+                                        int32_t *device_status, dd_stream_t stream);
+
 /* One layer: score -> top-k -> resolve -> gather into staging buffer
  * p = layer & 1 -> attention (DualDecoder §5.4, Fig. 11, two-layer ping-pong).
  * The gather into buffer p waits on the event recorded when the attention of

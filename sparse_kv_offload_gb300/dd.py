@@ -24,7 +24,7 @@ GATHER_ZEROCOPY, GATHER_MEMCPY = 0, 1
 EXPORTED = (
     "dd_create", "dd_destroy", "dd_build_landmarks", "dd_score_landmarks", "dd_select_topk",
     "dd_resolve_union", "dd_gather_kv", "dd_sparse_attn_decode", "dd_step", "dd_get_status",
-    "dd_launch_count", "dd_status_str", "dd_synth_kv", "dd_synth_queries",
+    "dd_launch_count", "dd_status_str", "dd_synth_kv", "dd_synth_queries", "dd_sparse_attn_decode_noalloc",
 )
 
 
@@ -72,6 +72,7 @@ def _load():
         "dd_status_str": (ctypes.c_char_p, [i32]),
         "dd_synth_kv": (i32, [ctypes.POINTER(Dims), ctypes.c_uint64, i32, _vp, _vp, _vp, i64, _vp, _vp]),
         "dd_synth_queries": (i32, [ctypes.POINTER(Dims), ctypes.c_uint64, i32, ctypes.POINTER(f32), _vp, _vp]),
+        "dd_sparse_attn_decode_noalloc": (i32, [ctypes.POINTER(Dims), i64, i64] + [_vp] * 9 + [f32, _vp, _vp, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -281,6 +282,34 @@ class Context:
 
     def launch_count(self) -> int:
         return int(_lib.dd_launch_count(self._h))
+
+
+# ---------------------------------------------------------------- allocation-free attention
+def sparse_attn_decode_noalloc(shape: Shape, hot_slots, max_misses, q, Khot, Vhot, Kst, Vst, union_slot,
+                               union_qmask, union_cnt, miss_count, out, device_status, softmax_scale=0.0,
+                               stream=None):
+    """dd_sparse_attn_decode without a context, for callers that cannot
+    allocate device memory: its split-K partials sit in the library's fixed
+    8 MiB device array.  ``device_status`` is a zeroed device int32 tensor that
+    receives a device-detected dd_status code.  Calls that overlap on the GPU
+    share that array and race; serialise them."""
+    s = shape
+    dims = s.dims()
+    nh = int(hot_slots) * s.cs * s.d
+    ns = int(max_misses) * s.cs * s.d
+    nu = s.B * s.Hkv * s.umax
+    _chk(_lib.dd_sparse_attn_decode_noalloc(
+        ctypes.byref(dims), int(hot_slots), int(max_misses),
+        _ptr(q, torch.bfloat16, s.B * s.n_q * s.Hq * s.d, name="q"),
+        _ptr(Khot, torch.bfloat16, nh, name="Khot", allow_none=True),
+        _ptr(Vhot, torch.bfloat16, nh, name="Vhot", allow_none=True),
+        _ptr(Kst, torch.bfloat16, ns, name="Kst", allow_none=True),
+        _ptr(Vst, torch.bfloat16, ns, name="Vst", allow_none=True),
+        _ptr(union_slot, torch.int32, nu, name="union_slot"), _ptr(union_qmask, torch.uint8, nu, name="union_qmask"),
+        _ptr(union_cnt, torch.int32, s.B * s.Hkv, name="union_cnt"), _ptr(miss_count, torch.int32, 1, name="miss_count"),
+        float(softmax_scale), _ptr(out, torch.float32, s.B * s.n_q * s.Hq * s.d, name="out"),
+        _ptr(device_status, torch.int32, 1, name="device_status"), _stream(stream)),
+        "dd_sparse_attn_decode_noalloc")
 
 
 # ---------------------------------------------------------------- generator
