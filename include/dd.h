@@ -203,6 +203,10 @@ int64_t dd_launch_count(const dd_ctx *ctx);
 
 const char *dd_status_str(dd_status status);
 
+/* Text of the CUDA runtime error behind the calling thread's most recent
+ * DD_ERR_CUDA ("" when there was none). */
+const char *dd_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -11,15 +11,6 @@
 
 #include "dd_common.cuh"
 
-namespace dd {
-cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const void *Kst, const void *Vst,
-                        const int32_t *union_slot, const uint8_t *union_qmask, const int32_t *union_cnt,
-                        const int32_t *miss_count, float softmax_scale, float *out, float *part_o, float *part_ml,
-                        int32_t *status, int B, int n_q, int Hq, int Hkv, int cs, int umax, int64_t hot_slots,
-                        int64_t max_misses, const void *dummy_pool, cudaStream_t s);
-int attn_seg_chunks(int NQ, int cs);
-}  // namespace dd
-
 struct dd_ctx {
   dd_dims dims;
   int C, G, NQ, umax, units, device, sm_count;
@@ -32,7 +23,11 @@ struct dd_ctx {
   uint8_t *union_qmask = nullptr;
   int32_t *unit_miss = nullptr, *miss_list = nullptr, *miss_count = nullptr, *attn_slot = nullptr;
   float *part_o = nullptr, *part_ml = nullptr;
+  int32_t *chunk_off = nullptr;
+  int4 *cta_tab = nullptr;
+  int2 *flat = nullptr;
   void *dummy_pool = nullptr;
+  dd::AttnPlan plan;
   // host side
   int32_t *h_miss = nullptr;          // pinned: [1 + max_misses]
   cudaStream_t copy_stream = nullptr;
@@ -50,7 +45,13 @@ namespace {
 
 using dd::kD;
 
-inline dd_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? DD_OK : DD_ERR_CUDA; }
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+inline dd_status cuda_ok(cudaError_t e) {
+  if (e == cudaSuccess) return DD_OK;
+  g_last_cuda_error = e;
+  return DD_ERR_CUDA;
+}
 
 #define DD_TRY(expr)                       \
   do {                                     \
@@ -117,11 +118,6 @@ T *carve(uint8_t *&cur, int64_t n) {
   return p;
 }
 
-int64_t attn_max_seg(const dd_ctx *c) {
-  const int sc = dd::attn_seg_chunks(c->NQ, c->dims.cs);
-  return (c->umax + sc - 1) / sc;
-}
-
 }  // namespace
 
 extern "C" {
@@ -142,7 +138,9 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   if (!out) return DD_ERR_INVALID_ARG;
   *out = nullptr;
   DD_TRY(check_dims(dims));
-  if (max_misses < 0 || hot_slots < 0 || max_misses >= (int64_t(1) << 31) || hot_slots >= (int64_t(1) << 31))
+  // pool rows are addressed with 32-bit coordinates
+  if (max_misses < 0 || hot_slots < 0 || max_misses * dims->cs >= (int64_t(1) << 31) ||
+      hot_slots * dims->cs >= (int64_t(1) << 31))
     return DD_ERR_INVALID_ARG;
   dd_ctx *c = new dd_ctx();
   c->dims = *dims;
@@ -157,13 +155,13 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
     dd_destroy(c);
     return s;
   };
-  if (cudaGetDevice(&c->device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess)
+  if (cuda_ok(cudaGetDevice(&c->device)) != DD_OK ||
+      cuda_ok(cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device)) != DD_OK)
     return fail(DD_ERR_CUDA);
 
   const int64_t B = dims->B, Hkv = dims->Hkv, n_q = dims->n_q, k = dims->k, C = c->C;
-  const int64_t max_seg = attn_max_seg(c);
   const int64_t units = c->units;
+  c->plan = dd::attn_plan(c->units, c->umax, c->NQ, c->sm_count);
   int64_t bytes = 0;
   auto add = [&](int64_t n, int64_t sz) { bytes += ((n * sz) + 255) & ~int64_t(255); };
   add(1, 4);                                   // status
@@ -177,8 +175,11 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   add(max_misses > 0 ? max_misses : 1, 4);     // miss_list
   add(1, 4);                                   // miss_count
   add(B * n_q * Hkv * k, 4);                   // attn_slot
-  add(units * max_seg * c->NQ * 128, 4);       // part_o
-  add(units * max_seg * c->NQ * 2, 4);         // part_ml
+  add(c->plan.part_o_floats, 4);               // part_o
+  add(c->plan.part_ml_floats, 4);              // part_ml
+  add(units + 1, 4);                           // chunk_off
+  add(c->plan.n_cta, 16);                      // cta_tab
+  add(c->plan.flat_entries, 8);                // flat chunk table
   add(64 * 128, 2);                            // dummy pool (64 rows)
   if (cudaMalloc(&c->ws, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
   uint8_t *cur = static_cast<uint8_t *>(c->ws);
@@ -193,8 +194,11 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   c->miss_list = carve<int32_t>(cur, max_misses > 0 ? max_misses : 1);
   c->miss_count = carve<int32_t>(cur, 1);
   c->attn_slot = carve<int32_t>(cur, B * n_q * Hkv * k);
-  c->part_o = carve<float>(cur, units * max_seg * c->NQ * 128);
-  c->part_ml = carve<float>(cur, units * max_seg * c->NQ * 2);
+  c->part_o = carve<float>(cur, c->plan.part_o_floats);
+  c->part_ml = carve<float>(cur, c->plan.part_ml_floats);
+  c->chunk_off = carve<int32_t>(cur, units + 1);
+  c->cta_tab = carve<int4>(cur, c->plan.n_cta);
+  c->flat = carve<int2>(cur, c->plan.flat_entries);
   c->dummy_pool = carve<uint16_t>(cur, 64 * 128);
   if (cudaMemset(c->ws, 0, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
   if (cudaMallocHost(reinterpret_cast<void **>(&c->h_miss), (size_t)(1 + (max_misses > 0 ? max_misses : 1)) * 4) !=
@@ -227,6 +231,10 @@ dd_status dd_destroy(dd_ctx *c) {
 }
 
 int64_t dd_launch_count(const dd_ctx *c) { return c ? c->launches : -1; }
+
+const char *dd_last_cuda_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "" : cudaGetErrorString(g_last_cuda_error);
+}
 
 dd_status dd_get_status(dd_ctx *c, int32_t *device_status) {
   if (!c || !device_status) return DD_ERR_INVALID_ARG;
@@ -265,9 +273,9 @@ dd_status dd_select_topk(dd_ctx *c, const float *scores, int32_t *sel, dd_stream
                                  (cudaStream_t)stream));
 }
 
-dd_status dd_resolve_union(dd_ctx *c, const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx,
-                           int32_t *union_slot, uint8_t *union_qmask, int32_t *union_cnt, int32_t *miss_list,
-                           int32_t *miss_count, int32_t *attn_slot, dd_stream_t stream) {
+static dd_status resolve_impl(dd_ctx *c, const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx,
+                              int32_t *union_slot, uint8_t *union_qmask, int32_t *union_cnt, int32_t *miss_list,
+                              int32_t *miss_count, int32_t *attn_slot, bool with_plan, dd_stream_t stream) {
   if (!c) return DD_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   if (c->units == 0) return miss_count ? cuda_ok(cudaMemsetAsync(miss_count, 0, 4, s)) : DD_OK;
@@ -277,10 +285,19 @@ dd_status dd_resolve_union(dd_ctx *c, const int32_t *sel, const int32_t *residen
   const dd_dims &d = c->dims;
   DD_CUDA(dd::launch_union(sel, resident_slot, union_idx, union_slot, union_qmask, union_cnt, c->unit_miss, c->units,
                            d.n_q, d.Hkv, d.k, c->C, c->umax, c->hot_slots, c->status, s));
-  DD_CUDA(dd::launch_assign(sel, union_idx, union_slot, union_cnt, c->unit_miss, miss_list, miss_count, attn_slot,
-                            c->units, d.n_q, d.Hkv, d.k, c->C, c->umax, c->max_misses, c->status, s));
+  const dd::AttnPlanOut po = {c->chunk_off, c->cta_tab, c->flat, c->plan.n_cta};
+  DD_CUDA(dd::launch_assign(sel, union_idx, union_slot, union_qmask, union_cnt, c->unit_miss, miss_list, miss_count,
+                            attn_slot, c->units, d.n_q, d.Hkv, d.k, c->C, c->umax, c->max_misses, c->hot_slots, d.cs,
+                            with_plan ? &po : nullptr, c->status, s));
   c->launches += 2;
   return DD_OK;
+}
+
+dd_status dd_resolve_union(dd_ctx *c, const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx,
+                           int32_t *union_slot, uint8_t *union_qmask, int32_t *union_cnt, int32_t *miss_list,
+                           int32_t *miss_count, int32_t *attn_slot, dd_stream_t stream) {
+  return resolve_impl(c, sel, resident_slot, union_idx, union_slot, union_qmask, union_cnt, miss_list, miss_count,
+                      attn_slot, false, stream);
 }
 
 // MEMCPY mode: miss list to the host, then one copy per run of consecutive
@@ -344,23 +361,31 @@ dd_status dd_gather_kv(dd_ctx *c, const void *Kh, const void *Vh, const int32_t 
                                    (int64_t)c->units * c->C, c->dims.cs, c->status, c->sm_count, s));
 }
 
-dd_status dd_sparse_attn_decode(dd_ctx *c, const void *q, const void *Khot, const void *Vhot, const void *Kst,
-                                const void *Vst, const int32_t *union_slot, const uint8_t *union_qmask,
-                                const int32_t *union_cnt, const int32_t *miss_count, float softmax_scale, float *out,
-                                dd_stream_t stream) {
+static dd_status attn_impl(dd_ctx *c, const void *q, const void *Khot, const void *Vhot, const void *Kst,
+                           const void *Vst, const int32_t *union_slot, const uint8_t *union_qmask,
+                           const int32_t *union_cnt, const int32_t *miss_count, float softmax_scale, float *out,
+                           bool plan_ready, dd_stream_t stream) {
   if (!c) return DD_ERR_INVALID_ARG;
   if (c->units == 0) return DD_OK;
   if (!q || !union_slot || !union_qmask || !union_cnt || !miss_count || !out || !aligned16(q))
     return DD_ERR_INVALID_ARG;
   if (c->hot_slots > 0 && (!Khot || !Vhot || !aligned16(Khot) || !aligned16(Vhot))) return DD_ERR_INVALID_ARG;
   if (c->max_misses > 0 && (!Kst || !Vst || !aligned16(Kst) || !aligned16(Vst))) return DD_ERR_INVALID_ARG;
-  if (c->units == 0) return DD_OK;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)kD);
   const dd_dims &d = c->dims;
-  c->launches += 2;
+  c->launches += plan_ready ? 2 : 3;
+  const dd::AttnScratch scr = {c->part_o, c->part_ml, c->chunk_off, c->cta_tab, c->flat, c->dummy_pool};
   return cuda_ok(dd::launch_attn(q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count, scale, out,
-                                 c->part_o, c->part_ml, c->status, d.B, d.n_q, d.Hq, d.Hkv, d.cs, c->umax,
-                                 c->hot_slots, c->max_misses, c->dummy_pool, (cudaStream_t)stream));
+                                 c->plan, scr, plan_ready, c->status, d.B, d.n_q, d.Hq, d.Hkv, d.cs, c->umax,
+                                 c->hot_slots, c->max_misses, (cudaStream_t)stream));
+}
+
+dd_status dd_sparse_attn_decode(dd_ctx *c, const void *q, const void *Khot, const void *Vhot, const void *Kst,
+                                const void *Vst, const int32_t *union_slot, const uint8_t *union_qmask,
+                                const int32_t *union_cnt, const int32_t *miss_count, float softmax_scale, float *out,
+                                dd_stream_t stream) {
+  return attn_impl(c, q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count, softmax_scale, out,
+                   false, stream);
 }
 
 dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
@@ -388,8 +413,8 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   DD_TRY(mark(1));
   DD_TRY(dd_select_topk(c, scores, sel, stream));
   DD_TRY(mark(2));
-  DD_TRY(dd_resolve_union(c, sel, a->resident_slot, union_idx, union_slot, union_qmask, union_cnt, miss_list,
-                          miss_count, attn_slot, stream));
+  DD_TRY(resolve_impl(c, sel, a->resident_slot, union_idx, union_slot, union_qmask, union_cnt, miss_list,
+                      miss_count, attn_slot, true, stream));
   DD_TRY(mark(3));
   // staging buffer p may still be read by the attention of layer - 2
   if (c->used[p]) DD_CUDA(cudaStreamWaitEvent(s, c->released[p], 0));
@@ -397,8 +422,8 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   DD_CUDA(cudaEventRecord(c->gathered[p], s));
   DD_CUDA(cudaStreamWaitEvent(s, c->gathered[p], 0));
   DD_TRY(mark(4));
-  DD_TRY(dd_sparse_attn_decode(c, a->q, a->Khot, a->Vhot, a->Kst[p], a->Vst[p], union_slot, union_qmask, union_cnt,
-                               miss_count, a->softmax_scale, a->out, stream));
+  DD_TRY(attn_impl(c, a->q, a->Khot, a->Vhot, a->Kst[p], a->Vst[p], union_slot, union_qmask, union_cnt, miss_count,
+                   a->softmax_scale, a->out, true, stream));
   DD_TRY(mark(5));
   DD_CUDA(cudaEventRecord(c->released[p], s));
   c->used[p] = true;

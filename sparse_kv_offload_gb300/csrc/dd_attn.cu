@@ -4,21 +4,29 @@
 // DualDecoder §5.2: the output token and the speculative token attend in one
 // pass instead of two.  Adaptive DHiSparse Fig. 3 / OasisKV Methodology: the
 // normal and draft queries share the HBM working set, but query j only sees
-// the chunks it picked.  Here one work item is a segment of the union of one
-// (request, KV head): every union row is streamed from HBM once and serves
-// all NQ = n_q*G query vectors of that KV head; rows of a chunk a query did
-// not select are masked for that query (the chunk's query mask).
+// the chunks it picked.  Every union row is streamed from HBM once and serves
+// all NQ = n_q*G query vectors of its KV head; rows of a chunk a query did not
+// pick are masked for that query (the chunk's query mask).
 //
-// Data movement: a producer warp stages 128-row tiles of K and V into shared
+// Work split ("stream-K"): the unions of all (request, KV head) units are
+// laid end to end (chunk_off = exclusive prefix of the union sizes) and one
+// persistent CTA per SM takes an equal contiguous slice of that sequence.  A
+// slice covers a few units ("runs").  At the end of a run every consumer
+// warp writes its partial (running max, sum and accumulator of its rows) into
+// slot CTA + unit, sub-slot warp -- slices are ordered like the units, so no
+// two (CTA, unit) pairs share a slot and n_cta + units slots suffice -- and a
+// combine kernel merges the partials of every unit.
+//
+// Data movement: a producer warp streams 128-row tiles of K and V into shared
 // memory with 2-D TMA loads (cp.async.bulk.tensor, 128-byte swizzle, one box
-// per chunk and per 64-column half) completing on mbarriers; kStages tiles
-// are in flight.  Math: consumer warps own 16 query vectors (one m16 tile)
-// and 16-row slices of the tile; S = Q.K^T and O += P.V run on the tensor
-// cores (mma.sync m16n8k16 bf16, fp32 accumulate) with an online softmax in
-// fp32; P is split into bf16 hi + lo parts so the PV product keeps ~16
-// significant bits.  Work is HBM-bound: the MMAs only keep the arithmetic
-// below the memory time.  Partial (max, sum, acc) per segment go to a
-// workspace and a combine kernel merges the segments.
+// per chunk and 64-column half) and each run's query vectors with bulk
+// copies, all completing on mbarriers; it runs ahead across run boundaries
+// with kStages tiles in flight.  Math: consumer warps own 16 query vectors
+// (one m16 tile) and 16-row slices of each tile; S = Q.K^T and O += P.V run on
+// the tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate) with an online
+// softmax in fp32; P is split into bf16 hi + lo parts so the PV product keeps
+// ~16 significant bits.  The work is HBM-bound: the MMAs only keep the
+// arithmetic under the memory time.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -29,26 +37,45 @@ namespace dd {
 constexpr int kStageRows = 128;
 constexpr int kHalfBytes = kStageRows * 128;          // 128 rows x 64 bf16
 constexpr int kStageBytes = 4 * kHalfBytes;           // K lo, K hi, V lo, V hi
-// Tiles in flight: three, except for four m-tiles where the merge buffer
-// leaves room for two within the 227 KiB of shared memory.
-__host__ __device__ constexpr int stages_for(int mt) { return mt >= 4 ? 2 : 3; }
-constexpr int kMergeStride = 136;                     // padded fp32 row of the merge buffer
 constexpr int kMaxChunksPerStage = kStageRows / 16;   // cs >= 16
+constexpr int kQStride = 272;                         // bytes per staged query vector (256 + pad)
+
+// Tiles in flight: three for one m-tile, two when the staged queries and the
+// merge buffers of more m-tiles need the room (227 KiB of shared memory).
+__host__ __device__ constexpr int stages_for(int mt) { return mt == 1 ? 3 : 2; }
+
+enum : int32_t { kFirst = 1, kLast = 2, kEnd = 4 };
+
+struct StageMeta {
+  int32_t unit, nch, flags, uoff, ucnt, pad;   // uoff/ucnt: the unit's range in the concatenated unions
+  uint8_t qm[kMaxChunksPerStage];
+};
 
 struct AttnParams {
-  const uint32_t *q;          // bf16 pairs [B,n_q,Hq,64]
-  const int32_t *union_slot;
-  const uint8_t *union_qmask;
-  const int32_t *union_cnt;
-  const int32_t *miss_count;
-  float *part_o;              // [units, max_seg, NQ, 128]
-  float *part_ml;             // [units, max_seg, NQ, 2]
+  const uint16_t *q;          // bf16 [B,n_q,Hq,128]
+  const int32_t *chunk_off;   // [units+1] exclusive prefix of the union sizes
+  const int4 *cta_tab;        // per CTA: {first chunk, end chunk, first unit, 0}
+  const int2 *flat;           // per chunk of the concatenated unions: {pool row code, query mask}
+  float *out;                 // fp32 [B,n_q,Hq,128]
+  float *part_o;              // [gridDim + units, NQ, 128], slot = CTA + unit
+  float *part_ml;             // [gridDim + units, NQ, 2]
   int32_t *status;
-  int n_q, Hq, Hkv, G, NQ, cs, umax, seg_chunks, max_seg;
-  int has_hot;
-  int64_t hot_slots, max_misses;
+  int n_q, Hq, Hkv, G, NQ, cs, umax, units;
   float scale_log2;           // softmax scale * log2(e)
 };
+
+// pool row code of a chunk in the flat table: first hot-pool row as is,
+// staging row r as -2 - r, -1 = not loaded
+
+// largest unit u with chunk_off[u] <= x (the unit whose union holds chunk x)
+__device__ __forceinline__ int unit_of_chunk(const int32_t *off, int units, int x) {
+  int lo = 0, hi = units - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
 
 // ----------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -130,37 +157,50 @@ __device__ __forceinline__ uint32_t swz(int row, int cg) {
   return (uint32_t)((cg >> 3) * kHalfBytes + row * 128 + ((((cg & 7) ^ (row & 7))) << 4));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) { return pack_bf2(lo, hi); }
+// two fp32 -> packed bf16x2 (round to nearest even), lo in the low half
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 
 // ----------------------------------------------------------------- the kernel
+// Registers per thread: the register file holds one CTA, whose warps are
+// charged in groups of four; at most 224 (no spills in the consumer loop).
+__host__ __device__ constexpr int attn_max_regs(int threads) {
+  return (65536 / ((threads + 127) / 128 * 128)) / 8 * 8 > 224 ? 224
+                                                                : (65536 / ((threads + 127) / 128 * 128)) / 8 * 8;
+}
+
 template <int MT, int WPM>
-__global__ void __launch_bounds__((MT * WPM + 1) * 32, 1)
+__global__ void __maxnreg__(attn_max_regs((MT * WPM + 1) * 32))
     k_attn(const __grid_constant__ CUtensorMap tm_khot, const __grid_constant__ CUtensorMap tm_vhot,
            const __grid_constant__ CUtensorMap tm_kst, const __grid_constant__ CUtensorMap tm_vst,
            const AttnParams p) {
   constexpr int kConsumers = MT * WPM;
   constexpr int kStages = stages_for(MT);
-  constexpr int kRowsPerWarp = kStageRows / WPM;      // 16, 32 or 64
-  constexpr int kGroups = kRowsPerWarp / 16;
+  constexpr int kRowsPerWarp = kStageRows / WPM;      // 32, 64 or 128
+  constexpr int kBlocks = kRowsPerWarp / 32;
+  constexpr int kQBytes = 16 * MT * kQStride;
 
-  const int unit = blockIdx.x;
-  const int seg = blockIdx.y;
-  const int U = p.union_cnt[unit];
-  const int seg_begin = seg * p.seg_chunks;
-  if (seg_begin >= U) return;
+  const int4 slice = p.cta_tab[blockIdx.x];
+  const int lo = slice.x, hi = slice.y, u0 = slice.z, per = slice.w;
+  if (lo >= hi) return;
   if (load_status(p.status) != 0) return;
-  const int nch_seg = min(p.seg_chunks, U - seg_begin);
-  const int chunks_per_stage = kStageRows / p.cs;
-  const int n_stages = (nch_seg + chunks_per_stage - 1) / chunks_per_stage;
 
   extern __shared__ uint8_t smem_raw[];
   // the 128-byte swizzle pattern is anchored at 1024-byte shared-memory boundaries
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t *stages = smem;
-  float *merge = reinterpret_cast<float *>(smem + kStages * kStageBytes);               // [MT][16][136]
-  float *wml = merge + MT * 16 * kMergeStride;                                           // [MT][WPM][16][2]
-  uint8_t *meta = reinterpret_cast<uint8_t *>(wml + MT * WPM * 16 * 2);                  // [kStages][8]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(meta + kStages * kMaxChunksPerStage);    // full[kStages], empty[kStages]
+  uint8_t *stages = smem;                                                    // [kStages][64 KiB]
+  uint8_t *qsm = stages + kStages * kStageBytes;                             // [kStages][16*MT][272 B]
+  StageMeta *meta = reinterpret_cast<StageMeta *>(qsm + kStages * kQBytes);  // [kStages]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(meta + kStages);             // full[kStages], empty[kStages]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
@@ -173,140 +213,204 @@ __global__ void __launch_bounds__((MT * WPM + 1) * 32, 1)
   }
   __syncthreads();
 
-  const int b = unit / p.Hkv, gkv = unit - b * p.Hkv;
-  const int64_t ubase = (int64_t)unit * p.umax + seg_begin;
-
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const int64_t m_valid = min((int64_t)*p.miss_count, p.max_misses);
-      const uint32_t box_bytes = (uint32_t)p.cs * 128u;
-      for (int s = 0; s < n_stages; ++s) {
-        const int buf = s % kStages;
-        if (s >= kStages && !mbar_wait(empty0 + 8 * buf, ((s / kStages) - 1) & 1, p.status)) break;
-        const int c0 = s * chunks_per_stage;
-        const int nch = min(chunks_per_stage, nch_seg - c0);
-        uint32_t bytes = 0;
-        for (int i = 0; i < kMaxChunksPerStage; ++i) {
-          uint8_t qm = 0;
-          if (i < nch) {
-            const int32_t slot = p.union_slot[ubase + c0 + i];
-            qm = p.union_qmask[ubase + c0 + i];
-            const bool hot_ok = slot >= 0 && p.has_hot && slot < p.hot_slots;
-            const bool st_ok = slot < 0 && (-(int64_t)slot - 1) < m_valid;
-            if (!hot_ok && !st_ok) {
-              set_status(p.status, DD_ERR_DEVICE_CHECK);
-              qm = 0;
-            }
-            if (qm) bytes += 4 * box_bytes;
+    // streams the flat chunk table of this slice in batches of 32 (the next
+    // batch already in flight) and cuts it into stages that never cross a
+    // unit boundary; lane i of `bnd` holds the end of unit ubase + i
+    const int chunks_per_stage = kStageRows / p.cs;
+    const uint32_t box_bytes = (uint32_t)p.cs * 128u;
+    int ubase = u0;
+    int bnd = (ubase + 1 + lane <= p.units) ? p.chunk_off[ubase + 1 + lane] : 0x7FFFFFFF;
+    int ustart = p.chunk_off[u0];
+    int x0 = lo;
+    int2 cur = (x0 + lane < hi) ? p.flat[x0 + lane] : make_int2(-1, 0);
+    int2 nxt = (x0 + 32 + lane < hi) ? p.flat[x0 + 32 + lane] : make_int2(-1, 0);
+    int s = 0, u = u0, x = lo;
+    bool first = true, alive = true;
+    while (x < hi && alive) {
+      if (u - ubase >= 32) {
+        ubase = u;
+        bnd = (ubase + 1 + lane <= p.units) ? p.chunk_off[ubase + 1 + lane] : 0x7FFFFFFF;
+      }
+      const int end_u = __shfl_sync(0xffffffffu, bnd, u - ubase);
+      if (x >= end_u) {   // unit u finished (or empty): next unit, new run
+        ++u;
+        ustart = end_u;
+        first = true;
+        continue;
+      }
+      const int stop = min(min(end_u, hi), x0 + 32);
+      const int nch = min(chunks_per_stage, stop - x);
+      const bool last = x + nch == min(end_u, hi);
+      const bool end = x + nch == hi;
+      const int b = u / p.Hkv, g = u - b * p.Hkv;
+      {
+          int32_t rows[kMaxChunksPerStage];
+          uint32_t qms[kMaxChunksPerStage];
+#pragma unroll
+          for (int i = 0; i < kMaxChunksPerStage; ++i) {
+            rows[i] = __shfl_sync(0xffffffffu, cur.x, (x - x0 + i) & 31);
+            qms[i] = (uint32_t)__shfl_sync(0xffffffffu, cur.y, (x - x0 + i) & 31);
           }
-          meta[buf * kMaxChunksPerStage + i] = qm;
-        }
-        mbar_arrive_expect_tx(full0 + 8 * buf, bytes);
-        const uint32_t sbase = smem_u32(stages + buf * kStageBytes);
-        for (int i = 0; i < nch; ++i) {
-          if (!meta[buf * kMaxChunksPerStage + i]) continue;
-          const int32_t slot = p.union_slot[ubase + c0 + i];
-          const CUtensorMap *mk = slot >= 0 ? &tm_khot : &tm_kst;
-          const CUtensorMap *mv = slot >= 0 ? &tm_vhot : &tm_vst;
-          const int y = (int)((slot >= 0 ? (int64_t)slot : (-(int64_t)slot - 1)) * p.cs);
-          const uint32_t roff = (uint32_t)(i * p.cs * 128);
-          const uint32_t bar = full0 + 8 * buf;
-          tma_load_2d(sbase + 0 * kHalfBytes + roff, mk, 0, y, bar);
-          tma_load_2d(sbase + 1 * kHalfBytes + roff, mk, 64, y, bar);
-          tma_load_2d(sbase + 2 * kHalfBytes + roff, mv, 0, y, bar);
-          tma_load_2d(sbase + 3 * kHalfBytes + roff, mv, 64, y, bar);
-        }
+          const int buf = s % kStages;
+          if (lane == 0) {
+            if (s >= kStages && !mbar_wait(empty0 + 8 * buf, ((s / kStages) - 1) & 1, p.status)) {
+              alive = false;
+            } else {
+              StageMeta &m = meta[buf];
+              m.unit = u;
+              m.nch = nch;
+              m.flags = (first ? kFirst : 0) | (last ? kLast : 0) | (end ? kEnd : 0);
+              m.uoff = ustart;
+              m.ucnt = end_u - ustart;
+              uint32_t bytes = first ? (uint32_t)p.NQ * 256u : 0u;
+#pragma unroll
+              for (int i = 0; i < kMaxChunksPerStage; ++i) {
+                const uint8_t q8 = (i < nch && rows[i] != -1) ? (uint8_t)qms[i] : 0;
+                m.qm[i] = q8;
+                if (q8) bytes += 4 * box_bytes;
+              }
+              const uint32_t bar = full0 + 8 * buf;
+              mbar_arrive_expect_tx(bar, bytes);
+              if (first) {
+                const uint32_t qdst = smem_u32(qsm + buf * kQBytes);
+                for (int qv = 0; qv < p.NQ; ++qv) {
+                  const int j = qv / p.G, h = g * p.G + (qv - j * p.G);
+                  bulk_load(qdst + qv * kQStride, p.q + ((int64_t)(b * p.n_q + j) * p.Hq + h) * 128, 256u, bar);
+                }
+              }
+              const uint32_t sbase = smem_u32(stages + buf * kStageBytes);
+#pragma unroll
+              for (int i = 0; i < kMaxChunksPerStage; ++i) {
+                if (i >= nch || rows[i] == -1 || qms[i] == 0) continue;
+                const bool hot = rows[i] >= 0;
+                const CUtensorMap *mk = hot ? &tm_khot : &tm_kst;
+                const CUtensorMap *mv = hot ? &tm_vhot : &tm_vst;
+                const int y = hot ? rows[i] : -2 - rows[i];
+                const uint32_t roff = (uint32_t)(i * p.cs * 128);
+                tma_load_2d(sbase + 0 * kHalfBytes + roff, mk, 0, y, bar);
+                tma_load_2d(sbase + 1 * kHalfBytes + roff, mk, 64, y, bar);
+                tma_load_2d(sbase + 2 * kHalfBytes + roff, mv, 0, y, bar);
+                tma_load_2d(sbase + 3 * kHalfBytes + roff, mv, 64, y, bar);
+              }
+            }
+          }
+          alive = __shfl_sync(0xffffffffu, alive, 0);
+          if (!alive) break;
+          first = false;
+          ++s;
+      }
+      x += nch;
+      if (x == x0 + 32) {   // batch used up: the prefetched one becomes current
+        x0 += 32;
+        cur = nxt;
+        nxt = (x0 + 32 + lane < hi) ? p.flat[x0 + 32 + lane] : make_int2(-1, 0);
       }
     }
-  } else {
-    // ------------------------------------------------------------ consumers
-    const int mt = warp / WPM, wq = warp - mt * WPM;
-    const int gr = lane >> 2, tq = lane & 3;
-    const int qv0 = mt * 16 + gr, qv1 = qv0 + 8;
-    const int j0 = qv0 < p.NQ ? qv0 / p.G : 31;
-    const int j1 = qv1 < p.NQ ? qv1 / p.G : 31;
+    return;
+  }
 
-    // Q A-fragments for the 8 k-steps over d
-    uint32_t qa[8][4];
-    {
-      const uint32_t *q0 = qv0 < p.NQ
-          ? p.q + ((int64_t)(b * p.n_q + j0) * p.Hq + gkv * p.G + (qv0 % p.G)) * 64 : nullptr;
-      const uint32_t *q1 = qv1 < p.NQ
-          ? p.q + ((int64_t)(b * p.n_q + j1) * p.Hq + gkv * p.G + (qv1 % p.G)) * 64 : nullptr;
+  // -------------------------------------------------------------- consumers
+  const int mt = warp / WPM, wq = warp - mt * WPM;
+  const int gr = lane >> 2, tq = lane & 3;
+  const int qv0 = mt * 16 + gr, qv1 = qv0 + 8;
+  const int j0 = qv0 < p.NQ ? qv0 / p.G : 31;
+  const int j1 = qv1 < p.NQ ? qv1 / p.G : 31;
+  const float sl2 = p.scale_log2;
+  const int rows_per_chunk_shift = 31 - __clz(p.cs);     // cs is a power of two
+
+  uint32_t qa[8][4];
+  float o[16][4];
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  for (int s = 0;; ++s) {
+    const int buf = s % kStages;
+    if (!mbar_wait(full0 + 8 * buf, (s / kStages) & 1, p.status)) break;
+    const int m_nch = meta[buf].nch, m_flags = meta[buf].flags, m_unit = meta[buf].unit;
+    const int m_uoff = meta[buf].uoff, m_ucnt = meta[buf].ucnt;
+    const uint8_t *m_qm = meta[buf].qm;
+    if (m_flags & kFirst) {
+      // this run's query vectors from shared memory (padded rows: no bank conflicts)
+      const uint8_t *qb = qsm + buf * kQBytes;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        qa[ks][0] = q0 ? q0[ks * 8 + tq] : 0u;
-        qa[ks][1] = q1 ? q1[ks * 8 + tq] : 0u;
-        qa[ks][2] = q0 ? q0[ks * 8 + 4 + tq] : 0u;
-        qa[ks][3] = q1 ? q1[ks * 8 + 4 + tq] : 0u;
+        const int c0 = (ks * 16 + 2 * tq) * 2, c1 = c0 + 16;
+        qa[ks][0] = qv0 < p.NQ ? *reinterpret_cast<const uint32_t *>(qb + qv0 * kQStride + c0) : 0u;
+        qa[ks][1] = qv1 < p.NQ ? *reinterpret_cast<const uint32_t *>(qb + qv1 * kQStride + c0) : 0u;
+        qa[ks][2] = qv0 < p.NQ ? *reinterpret_cast<const uint32_t *>(qb + qv0 * kQStride + c1) : 0u;
+        qa[ks][3] = qv1 < p.NQ ? *reinterpret_cast<const uint32_t *>(qb + qv1 * kQStride + c1) : 0u;
       }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      m0 = m1 = -INFINITY;
+      l0 = l1 = 0.f;
     }
+    const uint32_t kbase = smem_u32(stages + buf * kStageBytes);
+    const uint32_t vbase = kbase + 2 * kHalfBytes;
+#pragma unroll
+    for (int blk = 0; blk < kBlocks; ++blk) {
+      // 32 rows: halves A (rows row0..row0+15) and B (row0+16..row0+31), each
+      // inside one chunk; a half outside the stage or with an empty mask is
+      // skipped in both products (its shared memory may hold stale bytes)
+      const int row0 = wq * kRowsPerWarp + blk * 32;
+      const int ciA = row0 >> rows_per_chunk_shift, ciB = (row0 + 16) >> rows_per_chunk_shift;
+      const uint32_t qmA = ciA < m_nch ? m_qm[ciA] : 0u;
+      const uint32_t qmB = ciB < m_nch ? m_qm[ciB] : 0u;
+      if ((qmA | qmB) == 0) continue;
+      const bool okA0 = (qmA >> j0) & 1u, okA1 = (qmA >> j1) & 1u;
+      const bool okB0 = (qmB >> j0) & 1u, okB1 = (qmB >> j1) & 1u;
 
-    float o[16][4];
+      // S = Q K^T: n8 tiles 0,1 from half A, 2,3 from half B
+      float sc[4][4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    const float sl2 = p.scale_log2;
-
-    for (int s = 0; s < n_stages; ++s) {
-      const int buf = s % kStages;
-      if (!mbar_wait(full0 + 8 * buf, (s / kStages) & 1, p.status)) break;
-      const uint32_t kbase = smem_u32(stages + buf * kStageBytes);
-      const uint32_t vbase = kbase + 2 * kHalfBytes;
+      for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+      {
+        const int mi = lane >> 3, r = lane & 7;
+        const int krow = row0 + (mi >> 1) * 8 + r;
 #pragma unroll
-      for (int grp = 0; grp < kGroups; ++grp) {
-        const int row0 = wq * kRowsPerWarp + grp * 16;
-        const uint32_t qm = meta[buf * kMaxChunksPerStage + row0 / p.cs];
-        if (qm == 0) continue;
-        const bool ok0 = (qm >> j0) & 1u, ok1 = (qm >> j1) & 1u;
-
-        // S = Q K^T for 16 rows: two n8 tiles
-        float sc[2][4];
-#pragma unroll
-        for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-        {
-          const int mi = lane >> 3, r = lane & 7;
-          const int krow = row0 + (mi >> 1) * 8 + r;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t cg = swz(krow, ks * 2 + (mi & 1));
+          if (qmA) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + swz(krow, ks * 2 + (mi & 1)), b0, b1, b2, b3);
+            ldsm_x4(kbase + cg, b0, b1, b2, b3);
             mma_bf16(sc[0], qa[ks], b0, b1);
             mma_bf16(sc[1], qa[ks], b2, b3);
           }
+          if (qmB) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kbase + cg + 16 * 128, b0, b1, b2, b3);
+            mma_bf16(sc[2], qa[ks], b0, b1);
+            mma_bf16(sc[3], qa[ks], b2, b3);
+          }
         }
-        // scale to log2 units, mask, online softmax (rows gr and gr+8)
-        float x[2][4];
+      }
+      // scale to log2 units and mask (rows gr and gr+8 of the m-tile)
+      float x[4][4];
 #pragma unroll
-        for (int n = 0; n < 2; ++n) {
-          x[n][0] = ok0 ? sc[n][0] * sl2 : -INFINITY;
-          x[n][1] = ok0 ? sc[n][1] * sl2 : -INFINITY;
-          x[n][2] = ok1 ? sc[n][2] * sl2 : -INFINITY;
-          x[n][3] = ok1 ? sc[n][3] * sl2 : -INFINITY;
-        }
-        float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-        float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+      for (int n = 0; n < 4; ++n) {
+        const bool o0 = n < 2 ? okA0 : okB0, o1 = n < 2 ? okA1 : okB1;
+        x[n][0] = o0 ? sc[n][0] * sl2 : -INFINITY;
+        x[n][1] = o0 ? sc[n][1] * sl2 : -INFINITY;
+        x[n][2] = o1 ? sc[n][2] * sl2 : -INFINITY;
+        x[n][3] = o1 ? sc[n][3] * sl2 : -INFINITY;
+      }
+      float mx0 = fmaxf(fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1])),
+                        fmaxf(fmaxf(x[2][0], x[2][1]), fmaxf(x[3][0], x[3][1])));
+      float mx1 = fmaxf(fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3])),
+                        fmaxf(fmaxf(x[2][2], x[2][3]), fmaxf(x[3][2], x[3][3])));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+      // rescale the accumulator only when some row's maximum moved
+      if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
         const float a0 = exp2f(m0 - base0), a1 = exp2f(m1 - base1);
-        m0 = mn0;
-        m1 = mn1;
-        float pr[2][4];
-#pragma unroll
-        for (int n = 0; n < 2; ++n) {
-          pr[n][0] = exp2f(x[n][0] - base0);
-          pr[n][1] = exp2f(x[n][1] - base0);
-          pr[n][2] = exp2f(x[n][2] - base1);
-          pr[n][3] = exp2f(x[n][3] - base1);
-        }
-        l0 = l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-        l1 = l1 * a1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+        l0 *= a0;
+        l1 *= a1;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           o[i][0] *= a0;
@@ -314,125 +418,162 @@ __global__ void __launch_bounds__((MT * WPM + 1) * 32, 1)
           o[i][2] *= a1;
           o[i][3] *= a1;
         }
-        // P as the A operand (k = the 16 rows), split into bf16 hi and lo
-        uint32_t ph[4], pl[4];
-        {
-          const float v[4][2] = {{pr[0][0], pr[0][1]}, {pr[0][2], pr[0][3]}, {pr[1][0], pr[1][1]}, {pr[1][2], pr[1][3]}};
+      }
+      m0 = mn0;
+      m1 = mn1;
+      float pr[4][4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t h = pack_bf16x2_rn(v[i][0], v[i][1]);
-            ph[i] = h;
-            pl[i] = pack_bf16x2_rn(v[i][0] - bf_lo(h), v[i][1] - bf_hi(h));
-          }
+      for (int n = 0; n < 4; ++n) {
+        pr[n][0] = exp2f(x[n][0] - base0);
+        pr[n][1] = exp2f(x[n][1] - base0);
+        pr[n][2] = exp2f(x[n][2] - base1);
+        pr[n][3] = exp2f(x[n][3] - base1);
+      }
+      l0 += ((pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1])) + ((pr[2][0] + pr[2][1]) + (pr[3][0] + pr[3][1]));
+      l1 += ((pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3])) + ((pr[2][2] + pr[2][3]) + (pr[3][2] + pr[3][3]));
+      // P as the A operand of two k16 steps (halves A and B), split into bf16 hi + lo
+      uint32_t ph[2][4], pl[2][4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float v[4][2] = {{pr[2 * h][0], pr[2 * h][1]}, {pr[2 * h][2], pr[2 * h][3]},
+                               {pr[2 * h + 1][0], pr[2 * h + 1][1]}, {pr[2 * h + 1][2], pr[2 * h + 1][3]}};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t hi = cvt_bf16x2(v[i][0], v[i][1]);
+          ph[h][i] = hi;
+          pl[h][i] = cvt_bf16x2(v[i][0] - bf_lo(hi), v[i][1] - bf_hi(hi));
         }
-        // O += P V: V fragments by transposed ldmatrix, two 8-column tiles per load
-        {
-          const int mi = lane >> 3, r = lane & 7;
-          const int vrow = row0 + (mi & 1) * 8 + r;
+      }
+      // O += P V: V fragments by transposed ldmatrix, two 8-column tiles per load
+      {
+        const int mi = lane >> 3, r = lane & 7;
+        const int vrow = row0 + (mi & 1) * 8 + r;
 #pragma unroll
-          for (int dp = 0; dp < 8; ++dp) {
+        for (int dp = 0; dp < 8; ++dp) {
+          const uint32_t cg = swz(vrow, dp * 2 + (mi >> 1));
+          if (qmA) {
             uint32_t v0, v1, v2, v3;
-            ldsm_x4_t(vbase + swz(vrow, dp * 2 + (mi >> 1)), v0, v1, v2, v3);
-            mma_bf16(o[2 * dp], ph, v0, v1);
-            mma_bf16(o[2 * dp], pl, v0, v1);
-            mma_bf16(o[2 * dp + 1], ph, v2, v3);
-            mma_bf16(o[2 * dp + 1], pl, v2, v3);
+            ldsm_x4_t(vbase + cg, v0, v1, v2, v3);
+            mma_bf16(o[2 * dp], ph[0], v0, v1);
+            mma_bf16(o[2 * dp + 1], ph[0], v2, v3);
+            mma_bf16(o[2 * dp], pl[0], v0, v1);
+            mma_bf16(o[2 * dp + 1], pl[0], v2, v3);
+          }
+          if (qmB) {
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_t(vbase + cg + 16 * 128, v0, v1, v2, v3);
+            mma_bf16(o[2 * dp], ph[1], v0, v1);
+            mma_bf16(o[2 * dp + 1], ph[1], v2, v3);
+            mma_bf16(o[2 * dp], pl[1], v0, v1);
+            mma_bf16(o[2 * dp + 1], pl[1], v2, v3);
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * buf);
     }
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    if (tq == 0) {
-      float *w = wml + ((mt * WPM + wq) * 16) * 2;
-      w[gr * 2 + 0] = m0;
-      w[gr * 2 + 1] = l0;
-      w[(gr + 8) * 2 + 0] = m1;
-      w[(gr + 8) * 2 + 1] = l1;
-    }
-    // stash this warp's state in registers for the merge below
-    // (o, m0, m1 stay live across the barriers)
-    __syncthreads();
-    // common max over the WPM warps of this m-tile, per row
-    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
-    for (int w2 = 0; w2 < WPM; ++w2) {
-      const float *w = wml + ((mt * WPM + w2) * 16) * 2;
-      M0 = fmaxf(M0, w[gr * 2]);
-      M1 = fmaxf(M1, w[(gr + 8) * 2]);
-    }
-    for (int w2 = 0; w2 < WPM; ++w2) {
-      const float *w = wml + ((mt * WPM + w2) * 16) * 2;
-      if (M0 != -INFINITY) L0 += w[gr * 2 + 1] * exp2f(w[gr * 2] - M0);
-      if (M1 != -INFINITY) L1 += w[(gr + 8) * 2 + 1] * exp2f(w[(gr + 8) * 2] - M1);
-    }
-    const float f0 = M0 == -INFINITY ? 0.f : exp2f(m0 - M0);
-    const float f1 = M1 == -INFINITY ? 0.f : exp2f(m1 - M1);
-    float *acc = merge + mt * 16 * kMergeStride;
-    for (int w2 = 0; w2 < WPM; ++w2) {
-      if (wq == w2) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * buf);
+
+    if (m_flags & kLast) {
+      // this warp's partial for the run: rows of its m-tile, straight from
+      // registers into sub-slot wq of slot CTA + unit (no cross-warp merge;
+      // the combine kernel merges all partials of the unit)
+      float lq0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+      lq0 += __shfl_xor_sync(0xffffffffu, lq0, 2);
+      float lq1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+      lq1 += __shfl_xor_sync(0xffffffffu, lq1, 2);
+      const int64_t pbase = (((int64_t)blockIdx.x + m_unit) * WPM + wq) * p.NQ;
+      if (qv0 < p.NQ) {
+        float *dst = p.part_o + (pbase + qv0) * 128 + 2 * tq;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int col = i * 8 + 2 * tq;
-          float *r0p = acc + gr * kMergeStride + col;
-          float *r1p = acc + (gr + 8) * kMergeStride + col;
-          if (w2 == 0) {
-            r0p[0] = o[i][0] * f0; r0p[1] = o[i][1] * f0;
-            r1p[0] = o[i][2] * f1; r1p[1] = o[i][3] * f1;
-          } else {
-            r0p[0] += o[i][0] * f0; r0p[1] += o[i][1] * f0;
-            r1p[0] += o[i][2] * f1; r1p[1] += o[i][3] * f1;
-          }
-        }
+        for (int i = 0; i < 16; ++i) *reinterpret_cast<float2 *>(dst + i * 8) = make_float2(o[i][0], o[i][1]);
+        if (tq == 0) *reinterpret_cast<float2 *>(p.part_ml + (pbase + qv0) * 2) = make_float2(m0, lq0);
       }
-      asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32));
+      if (qv1 < p.NQ) {
+        float *dst = p.part_o + (pbase + qv1) * 128 + 2 * tq;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) *reinterpret_cast<float2 *>(dst + i * 8) = make_float2(o[i][2], o[i][3]);
+        if (tq == 0) *reinterpret_cast<float2 *>(p.part_ml + (pbase + qv1) * 2) = make_float2(m1, lq1);
+      }
     }
-    // write this m-tile's partial: rows of valid query vectors
-    const int64_t pbase = ((int64_t)unit * p.max_seg + seg) * p.NQ;
-    for (int e = wq * 32 + lane; e < 16 * 128; e += WPM * 32) {
-      const int r = e >> 7, col = e & 127;
-      const int qv = mt * 16 + r;
-      if (qv < p.NQ) p.part_o[(pbase + qv) * 128 + col] = acc[r * kMergeStride + col];
-    }
-    if (wq == 0 && tq == 0) {
-      if (qv0 < p.NQ) { p.part_ml[(pbase + qv0) * 2] = M0; p.part_ml[(pbase + qv0) * 2 + 1] = L0; }
-      if (qv1 < p.NQ) { p.part_ml[(pbase + qv1) * 2] = M1; p.part_ml[(pbase + qv1) * 2 + 1] = L1; }
-    }
-    return;
+    if (m_flags & kEnd) break;
   }
-  // producer warp joins the consumers' first barrier
-  __syncthreads();
+}
+
+// --------------------------------------------------------------- plan
+// Stand-alone plan for direct attention calls (the resolver builds the same
+// plan itself inside a step): one CTA per unit.  A unit with an empty union
+// gets zero outputs here, since no slice visits it.
+constexpr int kPlanThreads = 256;
+
+__global__ void __launch_bounds__(kPlanThreads) k_attn_plan(
+    const int32_t *__restrict__ union_cnt, const int32_t *__restrict__ union_slot,
+    const uint8_t *__restrict__ union_qmask, const int32_t *__restrict__ miss_count, AttnPlanOut po, float *out,
+    int units, int umax, int n_q, int Hq, int Hkv, int64_t hot_slots, int64_t max_misses, int cs, int32_t *status) {
+  __shared__ int scratch[33];
+  const int unit = blockIdx.x;
+  int before = 0, all = 0;
+  for (int u = threadIdx.x; u < units; u += kPlanThreads) {
+    int c = union_cnt[u];
+    if (c < 0 || c > umax) {
+      if (u == unit) set_status(status, DD_ERR_DEVICE_CHECK);
+      c = c < 0 ? 0 : umax;
+    }
+    all += c;
+    if (u < unit) before += c;
+  }
+  const int off = block_sum(before, scratch);
+  const int total = block_sum(all, scratch);
+  const int U = min(max(union_cnt[unit], 0), umax);
+  const int64_t ubase = (int64_t)unit * umax;
+  attn_plan_unit(po, unit, units, off, U, total, union_slot + ubase, union_qmask + ubase,
+                 min((int64_t)*miss_count, max_misses), hot_slots, cs, status);
+  if (U == 0) {
+    const int G = Hq / Hkv, b = unit / Hkv, g = unit - b * Hkv;
+    for (int e = threadIdx.x; e < n_q * G * 128; e += kPlanThreads) {
+      const int qv = e >> 7, col = e & 127, j = qv / G, h = g * G + (qv - j * G);
+      out[((int64_t)(b * n_q + j) * Hq + h) * 128 + col] = 0.f;
+    }
+  }
 }
 
 // --------------------------------------------------------------- combine
+// One CTA per (unit, query vector): merges the partials of every warp of
+// every CTA whose slice covered part of the unit's union.
 __global__ void __launch_bounds__(128) k_attn_combine(const float *__restrict__ part_o,
                                                       const float *__restrict__ part_ml,
-                                                      const int32_t *__restrict__ union_cnt, float *__restrict__ out,
-                                                      const int32_t *status, int n_q, int Hq, int Hkv, int G, int NQ,
-                                                      int seg_chunks, int max_seg) {
+                                                      const int32_t *__restrict__ chunk_off,
+                                                      const int4 *__restrict__ cta_tab, float *__restrict__ out,
+                                                      const int32_t *status, int n_q, int Hq, int Hkv, int NQ,
+                                                      int wpm) {
   if (load_status(status) != 0) return;
   const int unit = blockIdx.x, qv = blockIdx.y, col = threadIdx.x;
-  const int U = union_cnt[unit];
-  const int nseg = min(max_seg, (U + seg_chunks - 1) / seg_chunks);
-  const int64_t pbase = (int64_t)unit * max_seg * NQ + qv;
-  float M = -INFINITY;
-  for (int s = 0; s < nseg; ++s) M = fmaxf(M, part_ml[(pbase + (int64_t)s * NQ) * 2]);
-  float L = 0.f, acc = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < nseg; ++s) {
-      const int64_t i = pbase + (int64_t)s * NQ;
-      const float ms = part_ml[i * 2];
-      if (ms == -INFINITY) continue;
-      const float w = exp2f(ms - M);
-      L += w * part_ml[i * 2 + 1];
-      acc += w * part_o[i * 128 + col];
+  const int off = chunk_off[unit], U = chunk_off[unit + 1] - off, per = cta_tab[0].w;
+  if (U <= 0 || per <= 0) return;
+  const int c0 = off / per, c1 = (off + U - 1) / per;
+  const int n = (c1 - c0 + 1) * wpm;   // partials: (CTA c0 + i / wpm, warp i % wpm)
+  float M = -INFINITY, L = 0.f, acc = 0.f;
+  for (int ib = 0; ib < n; ib += 4) {
+    float ms[4], ls[4], os[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int i = ib + t;
+      const int64_t k = (((int64_t)c0 + i / wpm + unit) * wpm + i % wpm) * NQ + qv;
+      const bool ok = i < n;
+      ms[t] = ok ? part_ml[k * 2] : -INFINITY;
+      ls[t] = ok ? part_ml[k * 2 + 1] : 0.f;
+      os[t] = ok ? part_o[k * 128 + col] : 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (ms[t] == -INFINITY) continue;
+      const float Mn = fmaxf(M, ms[t]);
+      const float a = M == -INFINITY ? 0.f : exp2f(M - Mn), w = exp2f(ms[t] - Mn);
+      L = L * a + w * ls[t];
+      acc = acc * a + w * os[t];
+      M = Mn;
     }
   }
-  const int b = unit / Hkv, g = unit - b * Hkv;
-  const int j = qv / G, h = g * G + (qv - j * G);
+  const int G = Hq / Hkv, b = unit / Hkv, g = unit - b * Hkv, j = qv / G, h = g * G + (qv - j * G);
   out[((int64_t)(b * n_q + j) * Hq + h) * 128 + col] = L > 0.f ? acc / L : 0.f;
 }
 
@@ -472,81 +613,89 @@ struct AttnShape {
 AttnShape attn_shape(int NQ) {
   AttnShape s;
   s.mt = (NQ + 15) / 16;
-  s.wpm = s.mt == 1 ? 8 : (s.mt == 4 ? 2 : 4);
+  s.wpm = s.mt == 1 ? 4 : (s.mt == 4 ? 1 : 2);
   s.threads = (s.mt * s.wpm + 1) * 32;
   const int ns = stages_for(s.mt);
-  s.smem = 1024 + (size_t)ns * kStageBytes + (size_t)s.mt * 16 * kMergeStride * 4 +
-           (size_t)s.mt * s.wpm * 16 * 2 * 4 + ns * kMaxChunksPerStage + 2 * ns * 8 + 16;
+  s.smem = 1024 + (size_t)ns * kStageBytes + (size_t)ns * 16 * s.mt * kQStride + ns * sizeof(StageMeta) + 2 * ns * 8 + 16;
   return s;
 }
 
-int attn_seg_chunks(int NQ, int cs) {
-  const int mt = (NQ + 15) / 16;
-  return (512 * mt) / cs;
+// One persistent CTA per SM; partial slot CTA + unit for every (CTA, unit)
+// pair that shares chunks, one sub-slot per consumer warp of an m-tile.
+AttnPlan attn_plan(int units, int umax, int NQ, int sm_count) {
+  AttnPlan pl;
+  pl.n_cta = sm_count > 0 ? sm_count : 1;
+  const int wpm = attn_shape(NQ).wpm;
+  pl.part_o_floats = ((int64_t)pl.n_cta + units) * wpm * NQ * 128;
+  pl.part_ml_floats = ((int64_t)pl.n_cta + units) * wpm * NQ * 2;
+  pl.flat_entries = (int64_t)units * umax;
+  return pl;
 }
 
 template <int MT, int WPM>
-static cudaError_t launch_attn_t(dim3 grid, const AttnShape &sh, const CUtensorMap &a, const CUtensorMap &b,
+static cudaError_t launch_attn_t(int n_cta, const AttnShape &sh, const CUtensorMap &a, const CUtensorMap &b,
                                  const CUtensorMap &c, const CUtensorMap &d, const AttnParams &p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k_attn<MT, WPM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
   if (e != cudaSuccess) return e;
-  k_attn<MT, WPM><<<grid, sh.threads, sh.smem, s>>>(a, b, c, d, p);
+  k_attn<MT, WPM><<<n_cta, sh.threads, sh.smem, s>>>(a, b, c, d, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const void *Kst, const void *Vst,
                         const int32_t *union_slot, const uint8_t *union_qmask, const int32_t *union_cnt,
-                        const int32_t *miss_count, float softmax_scale, float *out, float *part_o, float *part_ml,
-                        int32_t *status, int B, int n_q, int Hq, int Hkv, int cs, int umax, int64_t hot_slots,
-                        int64_t max_misses, const void *dummy_pool, cudaStream_t s) {
+                        const int32_t *miss_count, float softmax_scale, float *out, const AttnPlan &plan,
+                        const AttnScratch &scr, bool plan_ready, int32_t *status, int B, int n_q, int Hq, int Hkv,
+                        int cs, int umax, int64_t hot_slots, int64_t max_misses, cudaStream_t s) {
   const int units = B * Hkv;
   if (units == 0) return cudaSuccess;
   const int G = Hq / Hkv, NQ = n_q * G;
   const AttnShape sh = attn_shape(NQ);
-  const int seg_chunks = attn_seg_chunks(NQ, cs);
-  const int max_seg = (umax + seg_chunks - 1) / seg_chunks;
 
   CUtensorMap tkh, tvh, tks, tvs;
   const bool has_hot = hot_slots > 0 && Khot && Vhot;
   const bool has_st = max_misses > 0 && Kst && Vst;
   // a map must always be valid; unused ones point at a small dummy pool
-  if (!(has_hot ? make_pool_map(&tkh, Khot, hot_slots * cs, cs) : make_pool_map(&tkh, dummy_pool, cs, cs)))
+  if (!(has_hot ? make_pool_map(&tkh, Khot, hot_slots * cs, cs) : make_pool_map(&tkh, scr.dummy_pool, cs, cs)))
     return cudaErrorInvalidValue;
-  if (!(has_hot ? make_pool_map(&tvh, Vhot, hot_slots * cs, cs) : make_pool_map(&tvh, dummy_pool, cs, cs)))
+  if (!(has_hot ? make_pool_map(&tvh, Vhot, hot_slots * cs, cs) : make_pool_map(&tvh, scr.dummy_pool, cs, cs)))
     return cudaErrorInvalidValue;
-  if (!(has_st ? make_pool_map(&tks, Kst, max_misses * cs, cs) : make_pool_map(&tks, dummy_pool, cs, cs)))
+  if (!(has_st ? make_pool_map(&tks, Kst, max_misses * cs, cs) : make_pool_map(&tks, scr.dummy_pool, cs, cs)))
     return cudaErrorInvalidValue;
-  if (!(has_st ? make_pool_map(&tvs, Vst, max_misses * cs, cs) : make_pool_map(&tvs, dummy_pool, cs, cs)))
+  if (!(has_st ? make_pool_map(&tvs, Vst, max_misses * cs, cs) : make_pool_map(&tvs, scr.dummy_pool, cs, cs)))
     return cudaErrorInvalidValue;
+
+  cudaError_t e = cudaSuccess;
+  if (!plan_ready) {
+    const AttnPlanOut po = {scr.chunk_off, scr.cta_tab, scr.flat, plan.n_cta};
+    k_attn_plan<<<units, kPlanThreads, 0, s>>>(union_cnt, union_slot, union_qmask, miss_count, po, out, units, umax,
+                                               n_q, Hq, Hkv, has_hot ? hot_slots : 0, has_st ? max_misses : 0, cs,
+                                               status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
 
   AttnParams p;
-  p.q = static_cast<const uint32_t *>(q);
-  p.union_slot = union_slot;
-  p.union_qmask = union_qmask;
-  p.union_cnt = union_cnt;
-  p.miss_count = miss_count;
-  p.part_o = part_o;
-  p.part_ml = part_ml;
+  p.q = static_cast<const uint16_t *>(q);
+  p.chunk_off = scr.chunk_off;
+  p.cta_tab = scr.cta_tab;
+  p.flat = scr.flat;
+  p.out = out;
+  p.part_o = scr.part_o;
+  p.part_ml = scr.part_ml;
   p.status = status;
-  p.n_q = n_q; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.NQ = NQ; p.cs = cs; p.umax = umax;
-  p.seg_chunks = seg_chunks; p.max_seg = max_seg;
-  p.has_hot = has_hot ? 1 : 0;
-  p.hot_slots = has_hot ? hot_slots : 0;
-  p.max_misses = has_st ? max_misses : 0;
+  p.n_q = n_q; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.NQ = NQ; p.cs = cs; p.umax = umax; p.units = units;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
 
-  dim3 grid(units, max_seg);
-  cudaError_t e;
   switch (sh.mt) {
-    case 1: e = launch_attn_t<1, 8>(grid, sh, tkh, tvh, tks, tvs, p, s); break;
-    case 2: e = launch_attn_t<2, 4>(grid, sh, tkh, tvh, tks, tvs, p, s); break;
-    case 3: e = launch_attn_t<3, 4>(grid, sh, tkh, tvh, tks, tvs, p, s); break;
-    case 4: e = launch_attn_t<4, 2>(grid, sh, tkh, tvh, tks, tvs, p, s); break;
+    case 1: e = launch_attn_t<1, 4>(plan.n_cta, sh, tkh, tvh, tks, tvs, p, s); break;
+    case 2: e = launch_attn_t<2, 2>(plan.n_cta, sh, tkh, tvh, tks, tvs, p, s); break;
+    case 3: e = launch_attn_t<3, 2>(plan.n_cta, sh, tkh, tvh, tks, tvs, p, s); break;
+    case 4: e = launch_attn_t<4, 1>(plan.n_cta, sh, tkh, tvh, tks, tvs, p, s); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  k_attn_combine<<<dim3(units, NQ), 128, 0, s>>>(part_o, part_ml, union_cnt, out, status, n_q, Hq, Hkv, G, NQ,
-                                                 seg_chunks, max_seg);
+  k_attn_combine<<<dim3(units, NQ), 128, 0, s>>>(scr.part_o, scr.part_ml, scr.chunk_off, scr.cta_tab, out, status,
+                                                 n_q, Hq, Hkv, NQ, sh.wpm);
   return cudaGetLastError();
 }
 

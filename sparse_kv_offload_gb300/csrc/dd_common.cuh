@@ -54,6 +54,92 @@ __device__ __forceinline__ uint4 ldg_nc(const uint4 *p) {
   return r;
 }
 
+// ---------------------------------------------------------------------------
+// block-wide exclusive scan of one int per thread (blockDim a multiple of 32)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// `scratch` holds 33 ints of shared memory.  Returns the exclusive prefix and
+// the block total; ends with a barrier so scratch can be reused.
+__device__ __forceinline__ int block_excl_scan(int v, int *scratch, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int incl = warp_incl_scan(v);
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int x = lane < nw ? scratch[lane] : 0;
+    const int xi = warp_incl_scan(x);
+    if (lane < nw) scratch[lane] = xi - x;
+    if (lane == 31) scratch[32] = xi;
+  }
+  __syncthreads();
+  const int r = scratch[warp] + incl - v;
+  *total = scratch[32];
+  __syncthreads();
+  return r;
+}
+
+// block-wide sum of one int per thread (blockDim a multiple of 32; scratch 33 ints)
+__device__ __forceinline__ int block_sum(int v, int *scratch) {
+  int tot;
+  block_excl_scan(v, scratch, &tot);
+  return tot;
+}
+
+// Work plan of the attention kernel (dd_attn.cu), built per (b, g) unit by
+// the resolver or by the attention's own plan kernel.  The unions of all
+// units are laid end to end: chunk x of that sequence is position
+// x - chunk_off[u] of unit u's union.
+struct AttnPlanOut {
+  int32_t *chunk_off;   // [units + 1] exclusive prefix of the union sizes
+  int4 *cta_tab;        // [n_cta] slice of persistent CTA c: {first chunk, end chunk, first unit, chunks per CTA}
+  int2 *flat;           // [units * umax] per chunk: {first pool row (hot) | -2 - row (staging) | -1, query mask}
+  int n_cta;
+};
+
+// One CTA, all threads: the plan entries that belong to `unit`.
+__device__ __forceinline__ void attn_plan_unit(const AttnPlanOut &po, int unit, int units, int off, int U, int total,
+                                               const int32_t *uslot, const uint8_t *uqm, int64_t m_valid,
+                                               int64_t hot_slots, int cs, int32_t *status) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int i = tid; i < U; i += nt) {
+    const int32_t slot = uslot[i];
+    uint32_t qm = uqm[i];
+    const bool hot_ok = slot >= 0 && slot < hot_slots;
+    const bool st_ok = slot < 0 && (-(int64_t)slot - 1) < m_valid;
+    int32_t row = -1;
+    if (!hot_ok && !st_ok) {
+      set_status(status, DD_ERR_DEVICE_CHECK);
+      qm = 0;
+    } else if (qm) {
+      const int32_t r = (int32_t)((slot >= 0 ? (int64_t)slot : (-(int64_t)slot - 1)) * cs);
+      row = slot >= 0 ? r : -2 - r;
+    }
+    po.flat[off + i] = make_int2(row, (int)qm);
+  }
+  if (tid == 0) {
+    po.chunk_off[unit] = off;
+    if (unit == units - 1) po.chunk_off[units] = total;
+  }
+  const int per = (total + po.n_cta - 1) / po.n_cta;
+  if (per > 0) {
+    for (int c = (off + per - 1) / per + tid; c < po.n_cta && (int64_t)c * per < (int64_t)off + U; c += nt)
+      po.cta_tab[c] = make_int4(c * per, min(total, c * per + per), unit, per);
+  }
+  if (unit == units - 1) {
+    const int c_end = per > 0 ? (total + per - 1) / per : 0;
+    for (int c = c_end + tid; c < po.n_cta; c += nt) po.cta_tab[c] = make_int4(total, total, 0, per);
+  }
+}
+
 }  // namespace dd
 
 // Host-side launch helpers, defined in dd_api.cu
@@ -68,9 +154,28 @@ cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32
                          int32_t *unit_miss, int units, int n_q, int Hkv, int k, int C, int umax,
                          int64_t hot_slots, int32_t *status, cudaStream_t s);
 cudaError_t launch_assign(const int32_t *sel, const int32_t *union_idx, int32_t *union_slot,
-                          const int32_t *union_cnt, const int32_t *unit_miss, int32_t *miss_list,
-                          int32_t *miss_count, int32_t *attn_slot, int units, int n_q, int Hkv, int k,
-                          int C, int umax, int64_t max_misses, int32_t *status, cudaStream_t s);
+                          const uint8_t *union_qmask, const int32_t *union_cnt, const int32_t *unit_miss,
+                          int32_t *miss_list, int32_t *miss_count, int32_t *attn_slot, int units, int n_q, int Hkv,
+                          int k, int C, int umax, int64_t max_misses, int64_t hot_slots, int cs,
+                          const AttnPlanOut *plan, int32_t *status, cudaStream_t s);
+// attention: launch plan (persistent CTAs, partial slots) and scratch
+struct AttnPlan {
+  int n_cta;
+  int64_t part_o_floats, part_ml_floats, flat_entries;
+};
+struct AttnScratch {
+  float *part_o, *part_ml;
+  int32_t *chunk_off;         // [units + 1]
+  int4 *cta_tab;              // [n_cta]
+  int2 *flat;                 // [units * umax]
+  const void *dummy_pool;     // >= 64 rows x 256 B, a valid base for unused tensor maps
+};
+AttnPlan attn_plan(int units, int umax, int NQ, int sm_count);
+cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const void *Kst, const void *Vst,
+                        const int32_t *union_slot, const uint8_t *union_qmask, const int32_t *union_cnt,
+                        const int32_t *miss_count, float softmax_scale, float *out, const AttnPlan &plan,
+                        const AttnScratch &scr, bool plan_ready, int32_t *status, int B, int n_q, int Hq, int Hkv,
+                        int cs, int umax, int64_t hot_slots, int64_t max_misses, cudaStream_t s);
 cudaError_t launch_gather(const uint4 *Kh, const uint4 *Vh, const int32_t *miss_list,
                           const int32_t *miss_count, uint4 *Kst, uint4 *Vst, int64_t max_misses,
                           int64_t n_chunks_total, int cs, int32_t *status, int sm_count, cudaStream_t s);

@@ -12,15 +12,6 @@
 
 #include "dd_common.cuh"
 
-namespace dd {
-cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const void *Kst, const void *Vst,
-                        const int32_t *union_slot, const uint8_t *union_qmask, const int32_t *union_cnt,
-                        const int32_t *miss_count, float softmax_scale, float *out, float *part_o, float *part_ml,
-                        int32_t *status, int B, int n_q, int Hq, int Hkv, int cs, int umax, int64_t hot_slots,
-                        int64_t max_misses, const void *dummy_pool, cudaStream_t s);
-int attn_seg_chunks(int NQ, int cs);
-}  // namespace dd
-
 namespace {
 
 // Largest scratch the allocation-free attention may use: 8 MiB.
@@ -72,16 +63,24 @@ extern "C" dd_status dd_sparse_attn_decode_noalloc(const dd_dims *dims, int64_t 
   if (C > dd::kMaxC || d.k < 1 || d.k > C || d.n_q < 1 || d.n_q > dd::kMaxNq) return DD_ERR_INVALID_ARG;
   const int G = d.Hq / d.Hkv, NQ = d.n_q * G;
   if (NQ > dd::kMaxNQV || (int64_t)d.B * d.Hkv * C >= (int64_t(1) << 31)) return DD_ERR_INVALID_ARG;
-  if (hot_slots < 0 || max_misses < 0) return DD_ERR_INVALID_ARG;
+  if (hot_slots < 0 || max_misses < 0 || hot_slots * d.cs >= (int64_t(1) << 31) ||
+      max_misses * d.cs >= (int64_t(1) << 31))
+    return DD_ERR_INVALID_ARG;
   const int units = d.B * d.Hkv;
   if (units == 0) return DD_OK;
-  // the split-K partials of this shape must fit the fixed scratch array
+  // the split-K partials and the chunk offsets of this shape must fit the fixed scratch array
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return DD_ERR_CUDA;
   const int umax = d.n_q * d.k < C ? d.n_q * d.k : C;
-  const int seg_chunks = dd::attn_seg_chunks(NQ, d.cs);
-  const int64_t max_seg = (umax + seg_chunks - 1) / seg_chunks;
-  const size_t o_bytes = round256((size_t)units * max_seg * NQ * 128 * sizeof(float));
-  const size_t ml_bytes = round256((size_t)units * max_seg * NQ * 2 * sizeof(float));
-  if (o_bytes + ml_bytes + kDummyPoolBytes > kNoAllocScratchBytes) return DD_ERR_CAPACITY;
+  const dd::AttnPlan plan = dd::attn_plan(units, umax, NQ, sms);
+  const size_t o_bytes = round256((size_t)plan.part_o_floats * sizeof(float));
+  const size_t ml_bytes = round256((size_t)plan.part_ml_floats * sizeof(float));
+  const size_t off_bytes = round256((size_t)(units + 1) * sizeof(int32_t));
+  const size_t tab_bytes = round256((size_t)plan.n_cta * 16);
+  const size_t flat_bytes = round256((size_t)plan.flat_entries * 8);
+  if (o_bytes + ml_bytes + off_bytes + tab_bytes + flat_bytes + kDummyPoolBytes > kNoAllocScratchBytes)
+    return DD_ERR_CAPACITY;
   if (!q || !union_slot || !union_qmask || !union_cnt || !miss_count || !out || !device_status || !aligned16(q))
     return DD_ERR_INVALID_ARG;
   if (hot_slots > 0 && (!Khot || !Vhot || !aligned16(Khot) || !aligned16(Vhot))) return DD_ERR_INVALID_ARG;
@@ -90,12 +89,21 @@ extern "C" dd_status dd_sparse_attn_decode_noalloc(const dd_dims *dims, int64_t 
   unsigned char *base = nullptr;
   const dd_status s = scratch_on_current_device(&base);
   if (s != DD_OK) return s;
-  float *part_o = reinterpret_cast<float *>(base);
-  float *part_ml = reinterpret_cast<float *>(base + o_bytes);
-  const void *dummy = base + o_bytes + ml_bytes;
+  unsigned char *cur = base;
+  float *part_o = reinterpret_cast<float *>(cur);
+  cur += o_bytes;
+  float *part_ml = reinterpret_cast<float *>(cur);
+  cur += ml_bytes;
+  int32_t *chunk_off = reinterpret_cast<int32_t *>(cur);
+  cur += off_bytes;
+  int4 *cta_tab = reinterpret_cast<int4 *>(cur);
+  cur += tab_bytes;
+  int2 *flat = reinterpret_cast<int2 *>(cur);
+  cur += flat_bytes;
+  const dd::AttnScratch scr = {part_o, part_ml, chunk_off, cta_tab, flat, cur};
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)dd::kD);
   const cudaError_t e = dd::launch_attn(q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count,
-                                        scale, out, part_o, part_ml, device_status, d.B, d.n_q, d.Hq, d.Hkv, d.cs,
-                                        umax, hot_slots, max_misses, dummy, (cudaStream_t)stream);
+                                        scale, out, plan, scr, false, device_status, d.B, d.n_q, d.Hq, d.Hkv, d.cs,
+                                        umax, hot_slots, max_misses, (cudaStream_t)stream);
   return e == cudaSuccess ? DD_OK : DD_ERR_CUDA;
 }

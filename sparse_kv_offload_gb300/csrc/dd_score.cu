@@ -55,19 +55,54 @@ cudaError_t launch_build_landmarks(const uint4 *K, uint4 *lm, int64_t n_chunks, 
 
 // ---------------------------------------------------------------------------
 // a1: scores[b,j,g,c] = qsum[b,j,g,:] . lm[b,g,c,:] with qsum the fp32 sum of
-// the group's G query heads.  One CTA scores kTile landmarks of one (b,g) for
-// all NQ queries, so every landmark byte is read once.  16 lanes share one
-// landmark row (one 16-byte load each) and reduce with shuffles; each thread
-// keeps kPass landmark loads in flight before using them.
+// the group's G query heads.  One CTA scores kTilesPerCta tiles of kTile
+// landmarks of one (b,g) for all NQ queries, so every landmark byte is read
+// once.  16 lanes share one landmark row (one 16-byte load each); each
+// thread holds kPass rows of a tile and the loads of the next tile are in
+// flight while the current one is reduced.  The 16-lane reduction of the
+// kPass*NQ partial dots is a butterfly that halves the value set at every
+// step (8+4+2+1 shuffles per 16 dots), leaving dot (lane position) in each
+// lane.
 // ---------------------------------------------------------------------------
 constexpr int kScoreThreads = 256;
-constexpr int kPass = 8;                                  // landmark rows in flight per thread
+constexpr int kPass = 8;                                  // landmark rows per thread per tile
 constexpr int kRowsPerPass = kScoreThreads / 16;          // 16
-constexpr int kTile = kPass * kRowsPerPass;               // 128 landmarks per CTA
+constexpr int kTile = kPass * kRowsPerPass;               // 128 landmarks per tile
+constexpr int kTilesPerCta = 4;
+
+// Butterfly over the 16 lanes sharing a row: x[0..15] in every lane ->
+// lane `part` returns the 16-lane sum of x[part].
+__device__ __forceinline__ float butterfly16(float (&x)[16], int part) {
+  float y[8], z[4], w[2];
+  const bool b3 = part & 8, b2 = part & 4, b1 = part & 2, b0 = part & 1;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float send = b3 ? x[i] : x[i + 8];
+    const float keep = b3 ? x[i + 8] : x[i];
+    y[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b2 ? y[i] : y[i + 4];
+    const float keep = b2 ? y[i + 4] : y[i];
+    z[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b1 ? z[i] : z[i + 2];
+    const float keep = b1 ? z[i + 2] : z[i];
+    w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  const float send = b0 ? w[0] : w[1];
+  const float keep = b0 ? w[1] : w[0];
+  return keep + __shfl_xor_sync(0xffffffffu, send, 1);
+}
 
 template <int NQ>
 __global__ void __launch_bounds__(kScoreThreads) k_score(const uint4 *__restrict__ q, const uint4 *__restrict__ lm,
                                                          float *__restrict__ scores, int Hq, int Hkv, int C) {
+  constexpr int kVals = kPass * NQ;                       // partial dots per lane per tile
+  constexpr int kChunks = (kVals + 15) / 16;
   __shared__ float sc[NQ][kTile];
   const int unit = blockIdx.x;
   const int b = unit / Hkv, g = unit - b * Hkv;
@@ -75,14 +110,13 @@ __global__ void __launch_bounds__(kScoreThreads) k_score(const uint4 *__restrict
   const int tid = threadIdx.x;
   const int part = tid & 15;
   const int sub = tid >> 4;
-  const int c0 = blockIdx.y * kTile;
-
-  // issue the landmark loads first
-  uint4 v[kPass];
+  const int cta_c0 = blockIdx.y * kTile * kTilesPerCta;
   const uint4 *base = lm + (int64_t)unit * C * kVecPerRow + part;
+
+  uint4 v[kPass], nv[kPass];
 #pragma unroll
   for (int p = 0; p < kPass; ++p) {
-    const int c = c0 + p * kRowsPerPass + sub;
+    const int c = cta_c0 + p * kRowsPerPass + sub;
     v[p] = (c < C) ? ldg_nc(base + (int64_t)c * kVecPerRow) : make_uint4(0, 0, 0, 0);
   }
 
@@ -100,34 +134,57 @@ __global__ void __launch_bounds__(kScoreThreads) k_score(const uint4 *__restrict
     }
   }
 
+  for (int t = 0; t < kTilesPerCta; ++t) {
+    const int c0 = cta_c0 + t * kTile;
+    if (c0 >= C) break;
+    if (t + 1 < kTilesPerCta) {
 #pragma unroll
-  for (int p = 0; p < kPass; ++p) {
-    float f[8];
-    unpack8(v[p], f);
-#pragma unroll
-    for (int j = 0; j < NQ; ++j) {
-      float acc = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc = fmaf(qs[j][e], f[e], acc);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 8);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      if (part == 0) sc[j][p * kRowsPerPass + sub] = acc;
+      for (int p = 0; p < kPass; ++p) {
+        const int c = c0 + kTile + p * kRowsPerPass + sub;
+        nv[p] = (c < C) ? ldg_nc(base + (int64_t)c * kVecPerRow) : make_uint4(0, 0, 0, 0);
+      }
     }
-  }
-  __syncthreads();
-  for (int i = tid; i < NQ * kTile; i += kScoreThreads) {
-    const int j = i / kTile, cc = i - j * kTile;
-    const int c = c0 + cc;
-    if (c < C) scores[((int64_t)(b * NQ + j) * Hkv + g) * C + c] = sc[j][cc];
+    // partial dots: value a = p*NQ + j
+    float x[kChunks * 16];
+#pragma unroll
+    for (int a = kVals; a < kChunks * 16; ++a) x[a] = 0.f;
+#pragma unroll
+    for (int p = 0; p < kPass; ++p) {
+      float f[8];
+      unpack8(v[p], f);
+#pragma unroll
+      for (int j = 0; j < NQ; ++j) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(qs[j][e], f[e], acc);
+        x[p * NQ + j] = acc;
+      }
+    }
+#pragma unroll
+    for (int ch = 0; ch < kChunks; ++ch) {
+      float xs[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) xs[i] = x[ch * 16 + i];
+      const float r = butterfly16(xs, part);
+      const int a = ch * 16 + part;
+      if (a < kVals) sc[a % NQ][(a / NQ) * kRowsPerPass + sub] = r;
+    }
+    __syncthreads();
+    for (int i = tid; i < NQ * kTile; i += kScoreThreads) {
+      const int j = i / kTile, cc = i - j * kTile;
+      const int c = c0 + cc;
+      if (c < C) scores[((int64_t)(b * NQ + j) * Hkv + g) * C + c] = sc[j][cc];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < kPass; ++p) v[p] = nv[p];
   }
 }
 
 cudaError_t launch_score(const uint4 *q, const uint4 *lm, float *scores, int B, int n_q, int Hq, int Hkv, int C,
                          cudaStream_t s) {
   if (B == 0) return cudaSuccess;
-  dim3 grid(B * Hkv, (C + kTile - 1) / kTile);
+  dim3 grid(B * Hkv, (C + kTile * kTilesPerCta - 1) / (kTile * kTilesPerCta));
   switch (n_q) {
 #define DD_SCORE_CASE(N) \
   case N: k_score<N><<<grid, kScoreThreads, 0, s>>>(q, lm, scores, Hq, Hkv, C); break;

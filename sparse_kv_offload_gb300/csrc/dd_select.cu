@@ -9,39 +9,6 @@
 
 namespace dd {
 
-// ---------------------------------------------------------------------------
-// block-wide exclusive scan of one int per thread (blockDim a multiple of 32)
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ int warp_incl_scan(int v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  return v;
-}
-
-// `scratch` holds 33 ints of shared memory.  Returns the exclusive prefix and
-// the block total; ends with a barrier so scratch can be reused.
-__device__ int block_excl_scan(int v, int *scratch, int *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int incl = warp_incl_scan(v);
-  if (lane == 31) scratch[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int x = lane < nw ? scratch[lane] : 0;
-    const int xi = warp_incl_scan(x);
-    if (lane < nw) scratch[lane] = xi - x;
-    if (lane == 31) scratch[32] = xi;
-  }
-  __syncthreads();
-  const int r = scratch[warp] + incl - v;
-  *total = scratch[32];
-  __syncthreads();
-  return r;
-}
-
 // Order-preserving map fp32 -> uint32: larger float, larger key.  -0 maps to
 // +0's key; NaN maps to 0, below every number.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -246,17 +213,29 @@ constexpr int kAssignThreads = 256;
 
 __global__ void __launch_bounds__(kAssignThreads) k_assign(
     const int32_t *__restrict__ sel, const int32_t *__restrict__ union_idx, int32_t *__restrict__ union_slot,
-    const int32_t *__restrict__ union_cnt, const int32_t *__restrict__ unit_miss, int32_t *__restrict__ miss_list,
-    int32_t *__restrict__ miss_count, int32_t *__restrict__ attn_slot, int units, int n_q, int Hkv, int k, int C,
-    int umax, int64_t max_misses, int32_t *status) {
+    const uint8_t *__restrict__ union_qmask, const int32_t *__restrict__ union_cnt,
+    const int32_t *__restrict__ unit_miss, int32_t *__restrict__ miss_list, int32_t *__restrict__ miss_count,
+    int32_t *__restrict__ attn_slot, int units, int n_q, int Hkv, int k, int C, int umax, int64_t max_misses,
+    int64_t hot_slots, int cs, AttnPlanOut po, int with_plan, int32_t *status) {
   __shared__ int scratch[33];
   const int unit = blockIdx.x;
   const int b = unit / Hkv, g = unit - b * Hkv;
   const int tid = threadIdx.x;
-  int before = 0;
-  for (int u = tid; u < unit; u += kAssignThreads) before += unit_miss[u];
-  int offset;
-  block_excl_scan(before, scratch, &offset);
+  // misses and union sizes of the earlier units, and of all units
+  int before_m = 0, all_m = 0, before_c = 0, all_c = 0;
+  for (int u = tid; u < units; u += kAssignThreads) {
+    const int m = unit_miss[u], c = union_cnt[u];
+    all_m += m;
+    all_c += c;
+    if (u < unit) {
+      before_m += m;
+      before_c += c;
+    }
+  }
+  const int offset = block_sum(before_m, scratch);
+  const int total_m = block_sum(all_m, scratch);
+  const int off_c = with_plan ? block_sum(before_c, scratch) : 0;
+  const int total_c = with_plan ? block_sum(all_c, scratch) : 0;
 
   const int cnt = union_cnt[unit];
   const int64_t ubase = (int64_t)unit * umax;
@@ -271,8 +250,11 @@ __global__ void __launch_bounds__(kAssignThreads) k_assign(
     }
   }
   if (over) set_status(status, DD_ERR_CAPACITY);
-  if (unit == units - 1 && tid == 0) *miss_count = offset + unit_miss[unit];
+  if (unit == units - 1 && tid == 0) *miss_count = total_m;
   __syncthreads();
+  if (with_plan)
+    attn_plan_unit(po, unit, units, off_c, cnt, total_c, union_slot + ubase, union_qmask + ubase,
+                   min((int64_t)total_m, max_misses), hot_slots, cs, status);
   if (attn_slot == nullptr) return;
   for (int i = tid; i < n_q * k; i += kAssignThreads) {
     const int j = i / k, r = i - j * k;
@@ -299,13 +281,16 @@ cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32
 }
 
 cudaError_t launch_assign(const int32_t *sel, const int32_t *union_idx, int32_t *union_slot,
-                          const int32_t *union_cnt, const int32_t *unit_miss, int32_t *miss_list,
-                          int32_t *miss_count, int32_t *attn_slot, int units, int n_q, int Hkv, int k, int C,
-                          int umax, int64_t max_misses, int32_t *status, cudaStream_t s) {
+                          const uint8_t *union_qmask, const int32_t *union_cnt, const int32_t *unit_miss,
+                          int32_t *miss_list, int32_t *miss_count, int32_t *attn_slot, int units, int n_q, int Hkv,
+                          int k, int C, int umax, int64_t max_misses, int64_t hot_slots, int cs,
+                          const AttnPlanOut *plan, int32_t *status, cudaStream_t s) {
   if (units == 0) return cudaSuccess;
-  k_assign<<<units, kAssignThreads, 0, s>>>(sel, union_idx, union_slot, union_cnt, unit_miss, miss_list,
-                                            miss_count, attn_slot, units, n_q, Hkv, k, C, umax, max_misses,
-                                            status);
+  AttnPlanOut po = {};
+  if (plan) po = *plan;
+  k_assign<<<units, kAssignThreads, 0, s>>>(sel, union_idx, union_slot, union_qmask, union_cnt, unit_miss, miss_list,
+                                            miss_count, attn_slot, units, n_q, Hkv, k, C, umax, max_misses, hot_slots,
+                                            cs, po, plan ? 1 : 0, status);
   return cudaGetLastError();
 }
 

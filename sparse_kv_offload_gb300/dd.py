@@ -24,14 +24,17 @@ GATHER_ZEROCOPY, GATHER_MEMCPY = 0, 1
 EXPORTED = (
     "dd_create", "dd_destroy", "dd_build_landmarks", "dd_score_landmarks", "dd_select_topk",
     "dd_resolve_union", "dd_gather_kv", "dd_sparse_attn_decode", "dd_step", "dd_get_status",
-    "dd_launch_count", "dd_status_str", "dd_synth_kv", "dd_synth_queries", "dd_sparse_attn_decode_noalloc",
+    "dd_launch_count", "dd_status_str", "dd_last_cuda_error", "dd_synth_kv", "dd_synth_queries", "dd_sparse_attn_decode_noalloc",
 )
 
 
 class DDError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {status_str(status)} ({status})")
+        detail = ""
+        if status == DD_ERR_CUDA:
+            detail = " [" + _lib.dd_last_cuda_error().decode() + "]"
+        super().__init__(f"{what}: {status_str(status)} ({status}){detail}")
 
 
 class Dims(ctypes.Structure):
@@ -70,6 +73,7 @@ def _load():
         "dd_get_status": (i32, [_vp, ctypes.POINTER(i32)]),
         "dd_launch_count": (i64, [_vp]),
         "dd_status_str": (ctypes.c_char_p, [i32]),
+        "dd_last_cuda_error": (ctypes.c_char_p, []),
         "dd_synth_kv": (i32, [ctypes.POINTER(Dims), ctypes.c_uint64, i32, _vp, _vp, _vp, i64, _vp, _vp]),
         "dd_synth_queries": (i32, [ctypes.POINTER(Dims), ctypes.c_uint64, i32, ctypes.POINTER(f32), _vp, _vp]),
         "dd_sparse_attn_decode_noalloc": (i32, [ctypes.POINTER(Dims), i64, i64] + [_vp] * 9 + [f32, _vp, _vp, _vp]),
