@@ -25,7 +25,7 @@ struct dd_ctx {
   float *part_o = nullptr, *part_ml = nullptr;
   int32_t *chunk_off = nullptr;
   int4 *cta_tab = nullptr;
-  int2 *flat = nullptr;
+  int4 *flat = nullptr;
   void *dummy_pool = nullptr;
   dd::AttnPlan plan;
   // host side
@@ -179,7 +179,7 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   add(c->plan.part_ml_floats, 4);              // part_ml
   add(units + 1, 4);                           // chunk_off
   add(c->plan.n_cta, 16);                      // cta_tab
-  add(c->plan.flat_entries, 8);                // flat chunk table
+  add(c->plan.flat_entries, 16);               // flat chunk table
   add(64 * 128, 2);                            // dummy pool (64 rows)
   if (cudaMalloc(&c->ws, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
   uint8_t *cur = static_cast<uint8_t *>(c->ws);
@@ -198,7 +198,7 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   c->part_ml = carve<float>(cur, c->plan.part_ml_floats);
   c->chunk_off = carve<int32_t>(cur, units + 1);
   c->cta_tab = carve<int4>(cur, c->plan.n_cta);
-  c->flat = carve<int2>(cur, c->plan.flat_entries);
+  c->flat = carve<int4>(cur, c->plan.flat_entries);
   c->dummy_pool = carve<uint16_t>(cur, 64 * 128);
   if (cudaMemset(c->ws, 0, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
   if (cudaMallocHost(reinterpret_cast<void **>(&c->h_miss), (size_t)(1 + (max_misses > 0 ? max_misses : 1)) * 4) !=
@@ -364,7 +364,7 @@ dd_status dd_gather_kv(dd_ctx *c, const void *Kh, const void *Vh, const int32_t 
 static dd_status attn_impl(dd_ctx *c, const void *q, const void *Khot, const void *Vhot, const void *Kst,
                            const void *Vst, const int32_t *union_slot, const uint8_t *union_qmask,
                            const int32_t *union_cnt, const int32_t *miss_count, float softmax_scale, float *out,
-                           bool plan_ready, dd_stream_t stream) {
+                           bool plan_ready, const void *kh_dev, const void *vh_dev, dd_stream_t stream) {
   if (!c) return DD_ERR_INVALID_ARG;
   if (c->units == 0) return DD_OK;
   if (!q || !union_slot || !union_qmask || !union_cnt || !miss_count || !out || !aligned16(q))
@@ -376,8 +376,8 @@ static dd_status attn_impl(dd_ctx *c, const void *q, const void *Khot, const voi
   c->launches += plan_ready ? 2 : 3;
   const dd::AttnScratch scr = {c->part_o, c->part_ml, c->chunk_off, c->cta_tab, c->flat, c->dummy_pool};
   return cuda_ok(dd::launch_attn(q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count, scale, out,
-                                 c->plan, scr, plan_ready, c->status, d.B, d.n_q, d.Hq, d.Hkv, d.cs, c->umax,
-                                 c->hot_slots, c->max_misses, (cudaStream_t)stream));
+                                 c->plan, scr, plan_ready, kh_dev, vh_dev, c->status, d.B, d.n_q, d.Hq, d.Hkv, d.cs,
+                                 c->umax, c->hot_slots, c->max_misses, (cudaStream_t)stream));
 }
 
 dd_status dd_sparse_attn_decode(dd_ctx *c, const void *q, const void *Khot, const void *Vhot, const void *Kst,
@@ -385,7 +385,7 @@ dd_status dd_sparse_attn_decode(dd_ctx *c, const void *q, const void *Khot, cons
                                 const int32_t *union_cnt, const int32_t *miss_count, float softmax_scale, float *out,
                                 dd_stream_t stream) {
   return attn_impl(c, q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count, softmax_scale, out,
-                   false, stream);
+                   false, nullptr, nullptr, stream);
 }
 
 dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
@@ -418,12 +418,19 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   DD_TRY(mark(3));
   // staging buffer p may still be read by the attention of layer - 2
   if (c->used[p]) DD_CUDA(cudaStreamWaitEvent(s, c->released[p], 0));
-  DD_TRY(dd_gather_kv(c, a->Kh, a->Vh, miss_list, miss_count, a->Kst[p], a->Vst[p], a->mode, stream));
+  const void *kh_dev = nullptr, *vh_dev = nullptr;
+  if (a->mode == DD_GATHER_ZEROCOPY) {
+    // the attention kernel itself copies the missing chunks from host memory
+    // into its tiles and into staging buffer p (one pass over the host link)
+    if (c->max_misses > 0) DD_TRY(host_kv_views(c, a->Kh, a->Vh, &kh_dev, &vh_dev));
+  } else {
+    DD_TRY(dd_gather_kv(c, a->Kh, a->Vh, miss_list, miss_count, a->Kst[p], a->Vst[p], a->mode, stream));
+  }
   DD_CUDA(cudaEventRecord(c->gathered[p], s));
   DD_CUDA(cudaStreamWaitEvent(s, c->gathered[p], 0));
   DD_TRY(mark(4));
   DD_TRY(attn_impl(c, a->q, a->Khot, a->Vhot, a->Kst[p], a->Vst[p], union_slot, union_qmask, union_cnt, miss_count,
-                   a->softmax_scale, a->out, true, stream));
+                   a->softmax_scale, a->out, true, kh_dev, vh_dev, stream));
   DD_TRY(mark(5));
   DD_CUDA(cudaEventRecord(c->released[p], s));
   c->used[p] = true;

@@ -39,6 +39,7 @@ constexpr int kHalfBytes = kStageRows * 128;          // 128 rows x 64 bf16
 constexpr int kStageBytes = 4 * kHalfBytes;           // K lo, K hi, V lo, V hi
 constexpr int kMaxChunksPerStage = kStageRows / 16;   // cs >= 16
 constexpr int kQStride = 272;                         // bytes per staged query vector (256 + pad)
+constexpr int kHostBatch = 8;                         // 16-byte host loads in flight per lane (fused gather)
 
 // Tiles in flight: three for one m-tile, two when the staged queries and the
 // merge buffers of more m-tiles need the room (227 KiB of shared memory).
@@ -55,7 +56,9 @@ struct AttnParams {
   const uint16_t *q;          // bf16 [B,n_q,Hq,128]
   const int32_t *chunk_off;   // [units+1] exclusive prefix of the union sizes
   const int4 *cta_tab;        // per CTA: {first chunk, end chunk, first unit, 0}
-  const int2 *flat;           // per chunk of the concatenated unions: {pool row code, query mask}
+  const int4 *flat;           // per chunk of the concatenated unions: {pool row code, query mask, host chunk, 0}
+  const uint4 *kh, *vh;       // fused gather: device view of the pinned host K/V (null: staging comes by TMA)
+  uint4 *kst, *vst;           // fused gather: staging buffers the host chunks are also written to
   float *out;                 // fp32 [B,n_q,Hq,128]
   float *part_o;              // [gridDim + units, NQ, 128], slot = CTA + unit
   float *part_ml;             // [gridDim + units, NQ, 2]
@@ -178,12 +181,20 @@ __host__ __device__ constexpr int attn_max_regs(int threads) {
                                                                 : (65536 / ((threads + 127) / 128 * 128)) / 8 * 8;
 }
 
+// Producer warps: warp 0 issues metadata and TMA; both share the host copies
+// of the fused gather.  Measured on the 16-request 32K layer, the host link
+// moved the most with about 16 loads of 16 bytes in flight per producer lane
+// in total: 2 warps x 8 (402 us per layer) beat 1 x 16 (407), 2 x 16 (414),
+// 4 x 16 (477) and 1 x 4 (499).
+__host__ __device__ constexpr int producers_for(int) { return 2; }
+
 template <int MT, int WPM>
-__global__ void __maxnreg__(attn_max_regs((MT * WPM + 1) * 32))
+__global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) * 32))
     k_attn(const __grid_constant__ CUtensorMap tm_khot, const __grid_constant__ CUtensorMap tm_vhot,
            const __grid_constant__ CUtensorMap tm_kst, const __grid_constant__ CUtensorMap tm_vst,
            const AttnParams p) {
   constexpr int kConsumers = MT * WPM;
+  constexpr int kProducers = producers_for(kConsumers);
   constexpr int kStages = stages_for(MT);
   constexpr int kRowsPerWarp = kStageRows / WPM;      // 32, 64 or 128
   constexpr int kBlocks = kRowsPerWarp / 32;
@@ -206,15 +217,15 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + 1) * 32))
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, p.kh != nullptr ? 1 + kProducers : 1);
       mbar_init(empty0 + 8 * s, kConsumers);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  if (warp == kConsumers) {
-    // ------------------------------------------------------------ producer
+  if (warp >= kConsumers) {
+    // ------------------------------------------------------------ producers
     // streams the flat chunk table of this slice in batches of 32 (the next
     // batch already in flight) and cuts it into stages that never cross a
     // unit boundary; lane i of `bnd` holds the end of unit ubase + i
@@ -224,8 +235,11 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + 1) * 32))
     int bnd = (ubase + 1 + lane <= p.units) ? p.chunk_off[ubase + 1 + lane] : 0x7FFFFFFF;
     int ustart = p.chunk_off[u0];
     int x0 = lo;
-    int2 cur = (x0 + lane < hi) ? p.flat[x0 + lane] : make_int2(-1, 0);
-    int2 nxt = (x0 + 32 + lane < hi) ? p.flat[x0 + 32 + lane] : make_int2(-1, 0);
+    int4 cur = (x0 + lane < hi) ? p.flat[x0 + lane] : make_int4(-1, 0, -1, 0);
+    int4 nxt = (x0 + 32 + lane < hi) ? p.flat[x0 + 32 + lane] : make_int4(-1, 0, -1, 0);
+    const bool fused = p.kh != nullptr;
+    const int pw = warp - kConsumers;
+    if (pw > 0 && !fused) return;
     int s = 0, u = u0, x = lo;
     bool first = true, alive = true;
     while (x < hi && alive) {
@@ -246,15 +260,18 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + 1) * 32))
       const bool end = x + nch == hi;
       const int b = u / p.Hkv, g = u - b * p.Hkv;
       {
-          int32_t rows[kMaxChunksPerStage];
+          int32_t rows[kMaxChunksPerStage], hosts[kMaxChunksPerStage];
           uint32_t qms[kMaxChunksPerStage];
 #pragma unroll
           for (int i = 0; i < kMaxChunksPerStage; ++i) {
             rows[i] = __shfl_sync(0xffffffffu, cur.x, (x - x0 + i) & 31);
             qms[i] = (uint32_t)__shfl_sync(0xffffffffu, cur.y, (x - x0 + i) & 31);
+            hosts[i] = __shfl_sync(0xffffffffu, cur.z, (x - x0 + i) & 31);
           }
           const int buf = s % kStages;
-          if (lane == 0) {
+          if (lane == 0 && pw > 0) {
+            if (s >= kStages && !mbar_wait(empty0 + 8 * buf, ((s / kStages) - 1) & 1, p.status)) alive = false;
+          } else if (lane == 0) {
             if (s >= kStages && !mbar_wait(empty0 + 8 * buf, ((s / kStages) - 1) & 1, p.status)) {
               alive = false;
             } else {
@@ -269,7 +286,8 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + 1) * 32))
               for (int i = 0; i < kMaxChunksPerStage; ++i) {
                 const uint8_t q8 = (i < nch && rows[i] != -1) ? (uint8_t)qms[i] : 0;
                 m.qm[i] = q8;
-                if (q8) bytes += 4 * box_bytes;
+                // chunks the warp copies from host memory arrive by stores, not by TMA
+                if (q8 && !(fused && rows[i] < -1)) bytes += 4 * box_bytes;
               }
               const uint32_t bar = full0 + 8 * buf;
               mbar_arrive_expect_tx(bar, bytes);
@@ -284,6 +302,7 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + 1) * 32))
 #pragma unroll
               for (int i = 0; i < kMaxChunksPerStage; ++i) {
                 if (i >= nch || rows[i] == -1 || qms[i] == 0) continue;
+                if (fused && rows[i] < -1) continue;
                 const bool hot = rows[i] >= 0;
                 const CUtensorMap *mk = hot ? &tm_khot : &tm_kst;
                 const CUtensorMap *mv = hot ? &tm_vhot : &tm_vst;
@@ -298,6 +317,62 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + 1) * 32))
           }
           alive = __shfl_sync(0xffffffffu, alive, 0);
           if (!alive) break;
+          if (fused) {
+            // missing chunks: 16-byte loads over the host link by all lanes,
+            // stored swizzled into the tile and written back to staging.  The
+            // stage's missing chunks are numbered k = 0..n-1 (lane k holds
+            // chunk k's host index, staging row and tile position) and their
+            // elements are walked as one sequence, kHostBatch loads per lane
+            // in flight.
+            const uint32_t sbase = smem_u32(stages + buf * kStageBytes);
+            const int vec = p.cs * 16;   // uint4 per chunk, K or V
+            uint32_t mask = 0;
+#pragma unroll
+            for (int i = 0; i < kMaxChunksPerStage; ++i)
+              if (i < nch && rows[i] < -1 && qms[i] != 0 && hosts[i] >= 0) mask |= 1u << i;
+            const int n_miss = __popc(mask);
+            int my_i = 0;   // stage position of missing chunk number `lane`
+            {
+              uint32_t m2 = mask;
+              for (int k = 0; k < lane && m2; ++k) m2 &= m2 - 1;
+              my_i = m2 ? __ffs(m2) - 1 : 0;
+            }
+            const int my_host = __shfl_sync(0xffffffffu, cur.z, (x - x0 + my_i) & 31);
+            const int my_row = __shfl_sync(0xffffffffu, cur.x, (x - x0 + my_i) & 31);
+            const int n_mine = (n_miss + kProducers - 1 - pw) / kProducers;   // chunks pw, pw+kProducers, ...
+            const int total_e = n_mine * 2 * vec;
+#pragma unroll 1
+            for (int e0 = 0; e0 < total_e; e0 += 32 * kHostBatch) {
+              uint4 v[kHostBatch];
+#pragma unroll
+              for (int u = 0; u < kHostBatch; ++u) {
+                const int eu = e0 + u * 32;                      // warp-uniform
+                const int kk = eu / (2 * vec), k = kk * kProducers + pw;
+                const int host = __shfl_sync(0xffffffffu, my_host, k & 31);
+                const int e = eu - kk * 2 * vec + lane;          // within the chunk: K then V
+                const uint4 *src = e >= vec ? p.vh + (int64_t)host * vec + (e - vec) : p.kh + (int64_t)host * vec + e;
+                v[u] = eu < total_e ? ldg_nc(src) : make_uint4(0, 0, 0, 0);
+              }
+#pragma unroll
+              for (int u = 0; u < kHostBatch; ++u) {
+                const int eu = e0 + u * 32;
+                const int kk = eu / (2 * vec), k = kk * kProducers + pw;
+                const int si = __shfl_sync(0xffffffffu, my_i, k & 31);
+                const int row = __shfl_sync(0xffffffffu, my_row, k & 31);
+                if (eu >= total_e) continue;
+                const int e = eu - kk * 2 * vec + lane;
+                const int kv = e >= vec, r = kv ? e - vec : e;
+                const int t = r >> 4, cg = r & 15;
+                const uint32_t dst = sbase + (kv ? 2 * kHalfBytes : 0) + swz(si * p.cs + t, cg);
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v[u].x), "r"(v[u].y),
+                             "r"(v[u].z), "r"(v[u].w) : "memory");
+                const int64_t mrow = -2 - row;                   // first staging row of the chunk
+                (kv ? p.vst : p.kst)[mrow * 16 + r] = v[u];
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full0 + 8 * buf);
+          }
           first = false;
           ++s;
       }
@@ -305,7 +380,7 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + 1) * 32))
       if (x == x0 + 32) {   // batch used up: the prefetched one becomes current
         x0 += 32;
         cur = nxt;
-        nxt = (x0 + 32 + lane < hi) ? p.flat[x0 + 32 + lane] : make_int2(-1, 0);
+        nxt = (x0 + 32 + lane < hi) ? p.flat[x0 + 32 + lane] : make_int4(-1, 0, -1, 0);
       }
     }
     return;
@@ -525,7 +600,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_attn_plan(
   const int total = block_sum(all, scratch);
   const int U = min(max(union_cnt[unit], 0), umax);
   const int64_t ubase = (int64_t)unit * umax;
-  attn_plan_unit(po, unit, units, off, U, total, union_slot + ubase, union_qmask + ubase,
+  attn_plan_unit(po, unit, units, off, U, total, union_slot + ubase, union_qmask + ubase, nullptr, 0,
                  min((int64_t)*miss_count, max_misses), hot_slots, cs, status);
   if (U == 0) {
     const int G = Hq / Hkv, b = unit / Hkv, g = unit - b * Hkv;
@@ -614,7 +689,7 @@ AttnShape attn_shape(int NQ) {
   AttnShape s;
   s.mt = (NQ + 15) / 16;
   s.wpm = s.mt == 1 ? 4 : (s.mt == 4 ? 1 : 2);
-  s.threads = (s.mt * s.wpm + 1) * 32;
+  s.threads = (s.mt * s.wpm + producers_for(s.mt * s.wpm)) * 32;
   const int ns = stages_for(s.mt);
   s.smem = 1024 + (size_t)ns * kStageBytes + (size_t)ns * 16 * s.mt * kQStride + ns * sizeof(StageMeta) + 2 * ns * 8 + 16;
   return s;
@@ -644,8 +719,9 @@ static cudaError_t launch_attn_t(int n_cta, const AttnShape &sh, const CUtensorM
 cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const void *Kst, const void *Vst,
                         const int32_t *union_slot, const uint8_t *union_qmask, const int32_t *union_cnt,
                         const int32_t *miss_count, float softmax_scale, float *out, const AttnPlan &plan,
-                        const AttnScratch &scr, bool plan_ready, int32_t *status, int B, int n_q, int Hq, int Hkv,
-                        int cs, int umax, int64_t hot_slots, int64_t max_misses, cudaStream_t s) {
+                        const AttnScratch &scr, bool plan_ready, const void *kh_dev, const void *vh_dev,
+                        int32_t *status, int B, int n_q, int Hq, int Hkv, int cs, int umax, int64_t hot_slots,
+                        int64_t max_misses, cudaStream_t s) {
   const int units = B * Hkv;
   if (units == 0) return cudaSuccess;
   const int G = Hq / Hkv, NQ = n_q * G;
@@ -679,6 +755,11 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
   p.chunk_off = scr.chunk_off;
   p.cta_tab = scr.cta_tab;
   p.flat = scr.flat;
+  const bool fused = kh_dev && vh_dev && has_st;
+  p.kh = fused ? static_cast<const uint4 *>(kh_dev) : nullptr;
+  p.vh = fused ? static_cast<const uint4 *>(vh_dev) : nullptr;
+  p.kst = fused ? static_cast<uint4 *>(const_cast<void *>(Kst)) : nullptr;
+  p.vst = fused ? static_cast<uint4 *>(const_cast<void *>(Vst)) : nullptr;
   p.out = out;
   p.part_o = scr.part_o;
   p.part_ml = scr.part_ml;

@@ -101,14 +101,15 @@ __device__ __forceinline__ int block_sum(int v, int *scratch) {
 struct AttnPlanOut {
   int32_t *chunk_off;   // [units + 1] exclusive prefix of the union sizes
   int4 *cta_tab;        // [n_cta] slice of persistent CTA c: {first chunk, end chunk, first unit, chunks per CTA}
-  int2 *flat;           // [units * umax] per chunk: {first pool row (hot) | -2 - row (staging) | -1, query mask}
+  int4 *flat;           // [units * umax] per chunk: {first pool row (hot) | -2 - row (staging) | -1, query mask,
+                        //  host chunk (b*Hkv+g)*C + c for staging chunks | -1, 0}
   int n_cta;
 };
 
 // One CTA, all threads: the plan entries that belong to `unit`.
 __device__ __forceinline__ void attn_plan_unit(const AttnPlanOut &po, int unit, int units, int off, int U, int total,
-                                               const int32_t *uslot, const uint8_t *uqm, int64_t m_valid,
-                                               int64_t hot_slots, int cs, int32_t *status) {
+                                               const int32_t *uslot, const uint8_t *uqm, const int32_t *uidx,
+                                               int C, int64_t m_valid, int64_t hot_slots, int cs, int32_t *status) {
   const int tid = threadIdx.x, nt = blockDim.x;
   for (int i = tid; i < U; i += nt) {
     const int32_t slot = uslot[i];
@@ -123,7 +124,8 @@ __device__ __forceinline__ void attn_plan_unit(const AttnPlanOut &po, int unit, 
       const int32_t r = (int32_t)((slot >= 0 ? (int64_t)slot : (-(int64_t)slot - 1)) * cs);
       row = slot >= 0 ? r : -2 - r;
     }
-    po.flat[off + i] = make_int2(row, (int)qm);
+    const int host = (uidx && slot < 0 && row != -1) ? unit * C + uidx[i] : -1;
+    po.flat[off + i] = make_int4(row, (int)qm, host, 0);
   }
   if (tid == 0) {
     po.chunk_off[unit] = off;
@@ -167,15 +169,16 @@ struct AttnScratch {
   float *part_o, *part_ml;
   int32_t *chunk_off;         // [units + 1]
   int4 *cta_tab;              // [n_cta]
-  int2 *flat;                 // [units * umax]
+  int4 *flat;                 // [units * umax]
   const void *dummy_pool;     // >= 64 rows x 256 B, a valid base for unused tensor maps
 };
 AttnPlan attn_plan(int units, int umax, int NQ, int sm_count);
 cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const void *Kst, const void *Vst,
                         const int32_t *union_slot, const uint8_t *union_qmask, const int32_t *union_cnt,
                         const int32_t *miss_count, float softmax_scale, float *out, const AttnPlan &plan,
-                        const AttnScratch &scr, bool plan_ready, int32_t *status, int B, int n_q, int Hq, int Hkv,
-                        int cs, int umax, int64_t hot_slots, int64_t max_misses, cudaStream_t s);
+                        const AttnScratch &scr, bool plan_ready, const void *kh_dev, const void *vh_dev,
+                        int32_t *status, int B, int n_q, int Hq, int Hkv, int cs, int umax, int64_t hot_slots,
+                        int64_t max_misses, cudaStream_t s);
 cudaError_t launch_gather(const uint4 *Kh, const uint4 *Vh, const int32_t *miss_list,
                           const int32_t *miss_count, uint4 *Kst, uint4 *Vst, int64_t max_misses,
                           int64_t n_chunks_total, int cs, int32_t *status, int sm_count, cudaStream_t s);

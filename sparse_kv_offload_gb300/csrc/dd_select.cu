@@ -253,8 +253,8 @@ __global__ void __launch_bounds__(kAssignThreads) k_assign(
   if (unit == units - 1 && tid == 0) *miss_count = total_m;
   __syncthreads();
   if (with_plan)
-    attn_plan_unit(po, unit, units, off_c, cnt, total_c, union_slot + ubase, union_qmask + ubase,
-                   min((int64_t)total_m, max_misses), hot_slots, cs, status);
+    attn_plan_unit(po, unit, units, off_c, cnt, total_c, union_slot + ubase, union_qmask + ubase, union_idx + ubase,
+                   C, min((int64_t)total_m, max_misses), hot_slots, cs, status);
   if (attn_slot == nullptr) return;
   for (int i = tid; i < n_q * k; i += kAssignThreads) {
     const int j = i / k, r = i - j * k;
