@@ -32,8 +32,8 @@ struct dd_ctx {
   int32_t *h_miss = nullptr;          // pinned: [1 + max_misses]
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t released[2] = {nullptr, nullptr};   // attention finished reading staging buffer p
-  cudaEvent_t gathered[2] = {nullptr, nullptr};   // copies into staging buffer p finished
-  cudaEvent_t ready = nullptr;                    // miss list available to the copy stream
+  cudaStream_t released_on[2] = {nullptr, nullptr};
+  cudaEvent_t ready = nullptr;                    // miss list available to the copy stream / copies done
   bool used[2] = {false, false};
   int64_t launches = 0;
   // cached host -> device pointer translations for pinned host memory
@@ -206,8 +206,7 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
     return fail(DD_ERR_CUDA);
   if (cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking) != cudaSuccess) return fail(DD_ERR_CUDA);
   for (int p = 0; p < 2; ++p) {
-    if (cudaEventCreateWithFlags(&c->released[p], cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&c->gathered[p], cudaEventDisableTiming) != cudaSuccess)
+    if (cudaEventCreateWithFlags(&c->released[p], cudaEventDisableTiming) != cudaSuccess)
       return fail(DD_ERR_CUDA);
   }
   if (cudaEventCreateWithFlags(&c->ready, cudaEventDisableTiming) != cudaSuccess) return fail(DD_ERR_CUDA);
@@ -220,7 +219,6 @@ dd_status dd_destroy(dd_ctx *c) {
   if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
   for (int p = 0; p < 2; ++p) {
     if (c->released[p]) cudaEventDestroy(c->released[p]);
-    if (c->gathered[p]) cudaEventDestroy(c->gathered[p]);
   }
   if (c->ready) cudaEventDestroy(c->ready);
   if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
@@ -416,8 +414,10 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   DD_TRY(resolve_impl(c, sel, a->resident_slot, union_idx, union_slot, union_qmask, union_cnt, miss_list,
                       miss_count, attn_slot, true, stream));
   DD_TRY(mark(3));
-  // staging buffer p may still be read by the attention of layer - 2
-  if (c->used[p]) DD_CUDA(cudaStreamWaitEvent(s, c->released[p], 0));
+  // staging buffer p may still be read by the attention of layer - 2; on the
+  // same stream the stream order already guarantees it, and leaving out the
+  // wait lets the attention kernel launch early behind the resolver
+  if (c->used[p] && c->released_on[p] != s) DD_CUDA(cudaStreamWaitEvent(s, c->released[p], 0));
   const void *kh_dev = nullptr, *vh_dev = nullptr;
   if (a->mode == DD_GATHER_ZEROCOPY) {
     // the attention kernel itself copies the missing chunks from host memory
@@ -426,13 +426,13 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   } else {
     DD_TRY(dd_gather_kv(c, a->Kh, a->Vh, miss_list, miss_count, a->Kst[p], a->Vst[p], a->mode, stream));
   }
-  DD_CUDA(cudaEventRecord(c->gathered[p], s));
-  DD_CUDA(cudaStreamWaitEvent(s, c->gathered[p], 0));
+  // memcpy mode: dd_gather_kv made this stream wait for the copy stream
   DD_TRY(mark(4));
   DD_TRY(attn_impl(c, a->q, a->Khot, a->Vhot, a->Kst[p], a->Vst[p], union_slot, union_qmask, union_cnt, miss_count,
                    a->softmax_scale, a->out, true, kh_dev, vh_dev, stream));
   DD_TRY(mark(5));
   DD_CUDA(cudaEventRecord(c->released[p], s));
+  c->released_on[p] = s;
   c->used[p] = true;
   return DD_OK;
 }

@@ -200,11 +200,6 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
   constexpr int kBlocks = kRowsPerWarp / 32;
   constexpr int kQBytes = 16 * MT * kQStride;
 
-  const int4 slice = p.cta_tab[blockIdx.x];
-  const int lo = slice.x, hi = slice.y, u0 = slice.z, per = slice.w;
-  if (lo >= hi) return;
-  if (load_status(p.status) != 0) return;
-
   extern __shared__ uint8_t smem_raw[];
   // the 128-byte swizzle pattern is anchored at 1024-byte shared-memory boundaries
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -223,6 +218,12 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  const int4 slice = p.cta_tab[blockIdx.x];
+  const int lo = slice.x, hi = slice.y, u0 = slice.z, per = slice.w;
+  if (lo >= hi) return;
+  if (load_status(p.status) != 0) return;
 
   if (warp >= kConsumers) {
     // ------------------------------------------------------------ producers
@@ -585,6 +586,8 @@ __global__ void __launch_bounds__(kPlanThreads) k_attn_plan(
     const uint8_t *__restrict__ union_qmask, const int32_t *__restrict__ miss_count, AttnPlanOut po, float *out,
     int units, int umax, int n_q, int Hq, int Hkv, int64_t hot_slots, int64_t max_misses, int cs, int32_t *status) {
   __shared__ int scratch[33];
+  pdl_wait();
+  pdl_trigger();
   const int unit = blockIdx.x;
   int before = 0, all = 0;
   for (int u = threadIdx.x; u < units; u += kPlanThreads) {
@@ -620,6 +623,8 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float *__restrict__ 
                                                       const int4 *__restrict__ cta_tab, float *__restrict__ out,
                                                       const int32_t *status, int n_q, int Hq, int Hkv, int NQ,
                                                       int wpm) {
+  pdl_wait();
+  pdl_trigger();
   if (load_status(status) != 0) return;
   const int unit = blockIdx.x, qv = blockIdx.y, col = threadIdx.x;
   const int off = chunk_off[unit], U = chunk_off[unit + 1] - off, per = cta_tab[0].w;
@@ -712,8 +717,7 @@ static cudaError_t launch_attn_t(int n_cta, const AttnShape &sh, const CUtensorM
                                  const CUtensorMap &c, const CUtensorMap &d, const AttnParams &p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k_attn<MT, WPM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
   if (e != cudaSuccess) return e;
-  k_attn<MT, WPM><<<n_cta, sh.threads, sh.smem, s>>>(a, b, c, d, p);
-  return cudaGetLastError();
+  return launch_k(k_attn<MT, WPM>, dim3(n_cta), dim3(sh.threads), sh.smem, s, a, b, c, d, p);
 }
 
 cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const void *Kst, const void *Vst,
@@ -743,10 +747,8 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
   cudaError_t e = cudaSuccess;
   if (!plan_ready) {
     const AttnPlanOut po = {scr.chunk_off, scr.cta_tab, scr.flat, plan.n_cta};
-    k_attn_plan<<<units, kPlanThreads, 0, s>>>(union_cnt, union_slot, union_qmask, miss_count, po, out, units, umax,
-                                               n_q, Hq, Hkv, has_hot ? hot_slots : 0, has_st ? max_misses : 0, cs,
-                                               status);
-    e = cudaGetLastError();
+    e = launch_k(k_attn_plan, dim3(units), dim3(kPlanThreads), 0, s, union_cnt, union_slot, union_qmask, miss_count,
+                 po, out, units, umax, n_q, Hq, Hkv, has_hot ? hot_slots : 0, has_st ? max_misses : 0, cs, status);
     if (e != cudaSuccess) return e;
   }
 
@@ -775,9 +777,8 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  k_attn_combine<<<dim3(units, NQ), 128, 0, s>>>(scr.part_o, scr.part_ml, scr.chunk_off, scr.cta_tab, out, status,
-                                                 n_q, Hq, Hkv, NQ, sh.wpm);
-  return cudaGetLastError();
+  return launch_k(k_attn_combine, dim3(units, NQ), dim3(128), 0, s, scr.part_o, scr.part_ml, scr.chunk_off,
+                  scr.cta_tab, out, status, n_q, Hq, Hkv, NQ, sh.wpm);
 }
 
 }  // namespace dd

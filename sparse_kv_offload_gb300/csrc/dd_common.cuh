@@ -55,6 +55,36 @@ __device__ __forceinline__ uint4 ldg_nc(const uint4 *p) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialization (launch_k below): its CTAs may become
+// resident while the previous kernel in the stream is still finishing, so the
+// launch and the shared-memory set-up overlap that kernel's tail.  Each kernel
+// therefore calls pdl_wait() unconditionally, before its first global-memory
+// access and before any early return: the wait returns once every earlier
+// kernel in the stream has completed and its writes are visible, which also
+// keeps the completion order transitive along the chain.  pdl_trigger() lets
+// the next kernel's CTAs launch early; it is issued right after the wait.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // block-wide exclusive scan of one int per thread (blockDim a multiple of 32)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int warp_incl_scan(int v) {

@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather(
     const uint4 *__restrict__ Kh, const uint4 *__restrict__ Vh, const int32_t *__restrict__ miss_list,
     const int32_t *__restrict__ miss_count, uint4 *__restrict__ Kst, uint4 *__restrict__ Vst, int64_t max_misses,
     int64_t n_chunks_total, int vec_per_chunk, int32_t *status) {
+  pdl_wait();
+  pdl_trigger();
   if (load_status(status) != 0) return;
   const int64_t M = min((int64_t)*miss_count, max_misses);
   const int lane = threadIdx.x & 31;
@@ -58,9 +60,8 @@ cudaError_t launch_gather(const uint4 *Kh, const uint4 *Vh, const int32_t *miss_
   int64_t blocks = (want_warps * 32 + kGatherThreads - 1) / kGatherThreads;
   const int64_t cap = (int64_t)sm_count * 8;
   if (blocks > cap) blocks = cap;
-  k_gather<<<(unsigned)blocks, kGatherThreads, 0, s>>>(Kh, Vh, miss_list, miss_count, Kst, Vst, max_misses,
-                                                        n_chunks_total, cs * kVecPerRow, status);
-  return cudaGetLastError();
+  return launch_k(k_gather, dim3((unsigned)blocks), dim3(kGatherThreads), 0, s, Kh, Vh, miss_list, miss_count, Kst,
+                  Vst, max_misses, n_chunks_total, cs * kVecPerRow, status);
 }
 
 }  // namespace dd

@@ -14,6 +14,8 @@ namespace dd {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_build_landmarks(const uint4 *__restrict__ K, uint4 *__restrict__ lm,
                                                           int64_t n_chunks, int cs) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t chunk = gid >> 4;
   const int part = (int)(gid & 15);
@@ -49,8 +51,7 @@ cudaError_t launch_build_landmarks(const uint4 *K, uint4 *lm, int64_t n_chunks, 
   if (n_chunks == 0) return cudaSuccess;
   const int64_t threads = n_chunks * 16;
   const int64_t blocks = (threads + 255) / 256;
-  k_build_landmarks<<<(unsigned)blocks, 256, 0, s>>>(K, lm, n_chunks, cs);
-  return cudaGetLastError();
+  return launch_k(k_build_landmarks, dim3((unsigned)blocks), dim3(256), 0, s, K, lm, n_chunks, cs);
 }
 
 // ---------------------------------------------------------------------------
@@ -104,6 +105,8 @@ __global__ void __launch_bounds__(kScoreThreads) k_score(const uint4 *__restrict
   constexpr int kVals = kPass * NQ;                       // partial dots per lane per tile
   constexpr int kChunks = (kVals + 15) / 16;
   __shared__ float sc[NQ][kTile];
+  pdl_wait();
+  pdl_trigger();
   const int unit = blockIdx.x;
   const int b = unit / Hkv, g = unit - b * Hkv;
   const int G = Hq / Hkv;
@@ -187,13 +190,12 @@ cudaError_t launch_score(const uint4 *q, const uint4 *lm, float *scores, int B, 
   dim3 grid(B * Hkv, (C + kTile * kTilesPerCta - 1) / (kTile * kTilesPerCta));
   switch (n_q) {
 #define DD_SCORE_CASE(N) \
-  case N: k_score<N><<<grid, kScoreThreads, 0, s>>>(q, lm, scores, Hq, Hkv, C); break;
+  case N: return launch_k(k_score<N>, grid, dim3(kScoreThreads), 0, s, q, lm, scores, Hq, Hkv, C);
     DD_SCORE_CASE(1) DD_SCORE_CASE(2) DD_SCORE_CASE(3) DD_SCORE_CASE(4)
     DD_SCORE_CASE(5) DD_SCORE_CASE(6) DD_SCORE_CASE(7) DD_SCORE_CASE(8)
 #undef DD_SCORE_CASE
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace dd

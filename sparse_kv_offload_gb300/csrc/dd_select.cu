@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(const float *__restrict__
   __shared__ int scratch[33];
   __shared__ uint32_t s_prefix;
   __shared__ int s_remaining;
+  pdl_wait();
+  pdl_trigger();
 
   const int row = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -116,8 +118,7 @@ cudaError_t launch_topk(const float *scores, int32_t *sel, int rows, int C, int 
     cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  k_topk<<<rows, kTopkThreads, smem, s>>>(scores, sel, C, k);
-  return cudaGetLastError();
+  return launch_k(k_topk, dim3(rows), dim3(kTopkThreads), smem, s, scores, sel, C, k);
 }
 
 // ---------------------------------------------------------------------------
@@ -142,6 +143,8 @@ __global__ void __launch_bounds__(kUnionThreads) k_union(
   const int tid = threadIdx.x;
   const int W = (C + 31) >> 5;
   for (int i = tid; i < n_q * W; i += kUnionThreads) qbits[i] = 0u;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   for (int i = tid; i < n_q * k; i += kUnionThreads) {
     const int j = i / k, r = i - j * k;
@@ -218,6 +221,8 @@ __global__ void __launch_bounds__(kAssignThreads) k_assign(
     int32_t *__restrict__ attn_slot, int units, int n_q, int Hkv, int k, int C, int umax, int64_t max_misses,
     int64_t hot_slots, int cs, AttnPlanOut po, int with_plan, int32_t *status) {
   __shared__ int scratch[33];
+  pdl_wait();
+  pdl_trigger();
   const int unit = blockIdx.x;
   const int b = unit / Hkv, g = unit - b * Hkv;
   const int tid = threadIdx.x;
@@ -275,9 +280,8 @@ cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32
                          uint8_t *union_qmask, int32_t *union_cnt, int32_t *unit_miss, int units, int n_q, int Hkv,
                          int k, int C, int umax, int64_t hot_slots, int32_t *status, cudaStream_t s) {
   if (units == 0) return cudaSuccess;
-  k_union<<<units, kUnionThreads, 0, s>>>(sel, resident_slot, union_idx, union_slot, union_qmask, union_cnt,
-                                          unit_miss, n_q, Hkv, k, C, umax, hot_slots, status);
-  return cudaGetLastError();
+  return launch_k(k_union, dim3(units), dim3(kUnionThreads), 0, s, sel, resident_slot, union_idx, union_slot,
+                  union_qmask, union_cnt, unit_miss, n_q, Hkv, k, C, umax, hot_slots, status);
 }
 
 cudaError_t launch_assign(const int32_t *sel, const int32_t *union_idx, int32_t *union_slot,
@@ -288,10 +292,9 @@ cudaError_t launch_assign(const int32_t *sel, const int32_t *union_idx, int32_t 
   if (units == 0) return cudaSuccess;
   AttnPlanOut po = {};
   if (plan) po = *plan;
-  k_assign<<<units, kAssignThreads, 0, s>>>(sel, union_idx, union_slot, union_qmask, union_cnt, unit_miss, miss_list,
-                                            miss_count, attn_slot, units, n_q, Hkv, k, C, umax, max_misses, hot_slots,
-                                            cs, po, plan ? 1 : 0, status);
-  return cudaGetLastError();
+  return launch_k(k_assign, dim3(units), dim3(kAssignThreads), 0, s, sel, union_idx, union_slot, union_qmask,
+                  union_cnt, unit_miss, miss_list, miss_count, attn_slot, units, n_q, Hkv, k, C, umax, max_misses,
+                  hot_slots, cs, po, plan ? 1 : 0, status);
 }
 
 }  // namespace dd
