@@ -23,6 +23,7 @@ __all__ = [
     "bf16_decode", "bf16_encode", "build_landmarks", "score_landmarks", "select_topk",
     "resolve_union", "gather_kv", "sparse_attn_decode", "step", "kv_footprint_bytes",
     "max_batch", "per_step_budget_bytes", "union_of_query_selections",
+    "build_minmax_landmarks", "score_minmax_landmarks", "bf16_total_order_key",
 ]
 
 
@@ -97,6 +98,65 @@ def score_landmarks(q: np.ndarray, lm: np.ndarray) -> np.ndarray:
     for g in range(Hkv):
         for h in range(g * G, (g + 1) * G):
             s[:, :, g, :] += np.einsum("bji,bci->bjc", qf[:, :, h, :], lf[:, g, :, :])
+    return s
+
+
+# ---------------------------------------------------------------------------
+# a0 / a1, second landmark kind: coordinate-wise min / max key per chunk
+# ---------------------------------------------------------------------------
+
+def bf16_total_order_key(u: np.ndarray) -> np.ndarray:
+    """uint16 bf16 bits -> uint32 keys that order the values (finite inputs),
+    with -0 below +0 (the IEEE 754 totalOrder predicate on non-NaN values)."""
+    u = np.asarray(u, dtype=np.uint16).astype(np.uint32)
+    return np.where(u & 0x8000, (~u) & 0xFFFF, u | 0x8000)
+
+
+def build_minmax_landmarks(K: np.ndarray, cs: int) -> np.ndarray:
+    """Per-chunk coordinate-wise minimum and maximum key, bf16 bits [B, Hkv, C, 2, d]
+    (index 0 of the fourth axis the minimum, 1 the maximum).
+
+    OasisKV Methodology: the draft query ranks blocks on compressed key
+    summaries made by Quest-style min/max pooling, two vectors per block
+    (coordinate-wise minimum and maximum).  The extremes of bf16 values are
+    bf16 values, so nothing is rounded.  Reading: -0 counts as below +0,
+    which makes the result a single well-defined bit pattern.
+    """
+    B, H, L, d = K.shape
+    if L % cs:
+        raise ValueError("L must be a multiple of the chunk size")
+    C = L // cs
+    bits = np.asarray(K, dtype=np.uint16).reshape(B, H, C, cs, d)
+    key = bf16_total_order_key(bits)
+    lo = np.take_along_axis(bits, np.argmin(key, axis=3)[:, :, :, None, :], axis=3)[:, :, :, 0, :]
+    hi = np.take_along_axis(bits, np.argmax(key, axis=3)[:, :, :, None, :], axis=3)[:, :, :, 0, :]
+    return np.stack([lo, hi], axis=3)
+
+
+def score_minmax_landmarks(q: np.ndarray, lm2: np.ndarray) -> np.ndarray:
+    """s[b, j, g, c] = sum_i max(Q_i * min_i, Q_i * max_i) with Q the sum of the
+    group's query heads q[b, j, h, :] (fp64).
+
+    OasisKV Methodology (Quest-style min/max summaries): the score of a block
+    is the largest value the query's dot product can take over any key whose
+    coordinates lie between the block's minimum and maximum, which bounds
+    every token of the block from above.  Reading: as for the mean
+    landmarks, the per-KV-head score is that of the group-summed query, so
+    it bounds the group's summed dot product sum_h q_h . k_t for every token
+    t of the chunk.
+    """
+    B, n_q, Hq, d = q.shape
+    _, Hkv, C, two, _ = lm2.shape
+    if Hq % Hkv or two != 2:
+        raise ValueError("need Hq a multiple of Hkv and lm2 of shape [B, Hkv, C, 2, d]")
+    G = Hq // Hkv
+    Q = bf16_decode(q).reshape(B, n_q, Hkv, G, d).sum(axis=3)   # [B, n_q, Hkv, d]
+    lo = bf16_decode(lm2[:, :, :, 0, :])                         # [B, Hkv, C, d]
+    hi = bf16_decode(lm2[:, :, :, 1, :])
+    s = np.zeros((B, n_q, Hkv, C), dtype=np.float64)
+    for j in range(n_q):
+        Qj = Q[:, j, :, None, :]                                  # [B, Hkv, 1, d]
+        s[:, j] = np.maximum(Qj * lo, Qj * hi).sum(axis=-1)
     return s
 
 
@@ -265,9 +325,11 @@ def step(q, lm, Kh, Vh, resident_slot, Khot, Vhot, k: int, cs: int, scale=None) 
 
     DualDecoder Fig. 8 / §5.1-§5.4: retrieval index from the query and the
     landmarks, missing entries fetched from host into the layer's staging
-    buffer, then sparse attention over the selected entries.
+    buffer, then sparse attention over the selected entries.  ``lm`` holds
+    mean landmarks [B, Hkv, C, d] or min/max landmarks [B, Hkv, C, 2, d];
+    the score follows the kind.
     """
-    s = score_landmarks(q, lm)
+    s = score_minmax_landmarks(q, lm) if lm.ndim == 5 else score_landmarks(q, lm)
     sel = select_topk(s, k)
     res = resolve_union(sel, resident_slot)
     Kst, Vst = gather_kv(Kh, Vh, res["miss_list"], cs)

@@ -315,3 +315,112 @@ def test_step_with_all_chunks_equals_dense_attention(resident_frac):
         for h in range(w["Hq"]):
             want = _sdpa(qf[0, j, h], Kf[0, h // G], Vf[0, h // G], 1 / math.sqrt(w["d"]))
             np.testing.assert_allclose(r["out"][0, j, h], want, rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- min/max landmarks (Quest-style)
+
+def _total_key(x):
+    """Python ordering of a float with -0 below +0."""
+    return (x, math.copysign(1.0, x))
+
+
+def test_minmax_landmarks_brute_force_with_signed_zeros():
+    rng = np.random.default_rng(11)
+    B, H, cs, C, d = 2, 2, 4, 3, 5
+    K = enc(rng.standard_normal((B, H, C * cs, d)))
+    # one chunk holds both zeros in one coordinate, another only -0 and +0 mixed with negatives
+    K[0, 1, 0:4, 2] = [0x8000, 0x0000, 0x8000, 0x0000]
+    K[1, 0, 4:8, 0] = [0x0000, 0xBF80, 0x8000, 0x0000]   # +0, -1, -0, +0
+    lm2 = oracle.build_minmax_landmarks(K, cs)
+    assert lm2.shape == (B, H, C, 2, d) and lm2.dtype == np.uint16
+    vals = synth.bf16_to_f32(K).astype(np.float64)
+    for b, h, c, i in itertools.product(range(B), range(H), range(C), range(d)):
+        col = [(vals[b, h, c * cs + t, i], K[b, h, c * cs + t, i]) for t in range(cs)]
+        lo = min(col, key=lambda e: _total_key(e[0]))[1]
+        hi = max(col, key=lambda e: _total_key(e[0]))[1]
+        assert lm2[b, h, c, 0, i] == lo and lm2[b, h, c, 1, i] == hi, (b, h, c, i)
+    assert lm2[0, 1, 0, 0, 2] == 0x8000 and lm2[0, 1, 0, 1, 2] == 0x0000
+    assert lm2[1, 0, 1, 0, 0] == 0xBF80 and lm2[1, 0, 1, 1, 0] == 0x0000
+
+
+def test_minmax_landmarks_of_one_token_chunks_are_the_keys():
+    rng = np.random.default_rng(12)
+    K = enc(rng.standard_normal((1, 3, 7, 128)))
+    lm2 = oracle.build_minmax_landmarks(K, 1)
+    assert np.array_equal(lm2[:, :, :, 0, :], K) and np.array_equal(lm2[:, :, :, 1, :], K)
+
+
+def test_minmax_score_is_best_corner_of_the_box():
+    # brute force over all 2^d corners of each chunk's box, group sum done by hand
+    rng = np.random.default_rng(13)
+    B, n_q, Hq, Hkv, C, cs, d = 2, 2, 4, 2, 3, 4, 5
+    G = Hq // Hkv
+    q = enc(rng.standard_normal((B, n_q, Hq, d)))
+    K = enc(rng.standard_normal((B, Hkv, C * cs, d)))
+    lm2 = oracle.build_minmax_landmarks(K, cs)
+    s = oracle.score_minmax_landmarks(q, lm2)
+    qf = synth.bf16_to_f32(q).astype(np.float64)
+    lf = synth.bf16_to_f32(lm2).astype(np.float64)
+    for b, j, g, c in itertools.product(range(B), range(n_q), range(Hkv), range(C)):
+        Q = sum(qf[b, j, h] for h in range(g * G, (g + 1) * G))
+        best = max(sum(Q[i] * lf[b, g, c, pick[i], i] for i in range(d))
+                   for pick in itertools.product((0, 1), repeat=d))
+        assert math.isclose(s[b, j, g, c], best, rel_tol=1e-12, abs_tol=1e-12), (b, j, g, c)
+
+
+def test_minmax_score_bounds_every_token_and_is_attained_at_the_corner():
+    rng = np.random.default_rng(14)
+    B, n_q, Hq, Hkv, C, cs, d = 2, 3, 8, 2, 6, 8, 128
+    G = Hq // Hkv
+    q = enc(rng.standard_normal((B, n_q, Hq, d)))
+    K = enc(rng.standard_normal((B, Hkv, C * cs, d)))
+    qf = synth.bf16_to_f32(q).astype(np.float64)
+    Q = qf.reshape(B, n_q, Hkv, G, d).sum(axis=3)
+    # chunk 2 of (b=1, g=0) gets, as token 5, the corner that query j=1 prefers
+    kf = synth.bf16_to_f32(K).astype(np.float64)
+    blk = kf[1, 0, 2 * cs:3 * cs]
+    corner = np.where(Q[1, 1, 0] >= 0, blk.max(axis=0), blk.min(axis=0))
+    K[1, 0, 2 * cs + 5] = enc(corner)
+    kf = synth.bf16_to_f32(K).astype(np.float64)
+    s = oracle.score_minmax_landmarks(q, oracle.build_minmax_landmarks(K, cs))
+    dots = np.einsum("bjgi,bgti->bjgt", Q, kf).reshape(B, n_q, Hkv, C, cs)
+    assert np.all(s >= dots.max(axis=-1) - 1e-9 * np.abs(s))
+    assert math.isclose(s[1, 1, 0, 2], dots[1, 1, 0, 2, 5], rel_tol=1e-12)
+
+
+def test_minmax_score_with_one_token_chunks_equals_mean_score():
+    rng = np.random.default_rng(15)
+    B, n_q, Hq, Hkv, L, d = 2, 2, 8, 2, 9, 128
+    q = enc(rng.standard_normal((B, n_q, Hq, d)))
+    K = enc(rng.standard_normal((B, Hkv, L, d)))
+    s_mm = oracle.score_minmax_landmarks(q, oracle.build_minmax_landmarks(K, 1))
+    s_mean = oracle.score_landmarks(q, oracle.build_landmarks(K, 1))
+    np.testing.assert_allclose(s_mm, s_mean, rtol=1e-12, atol=1e-12)
+
+
+def test_minmax_score_with_same_sign_query_uses_one_bound():
+    rng = np.random.default_rng(16)
+    B, n_q, Hq, Hkv, C, cs, d = 1, 2, 4, 1, 5, 4, 128
+    q = np.abs(rng.standard_normal((B, n_q, Hq, d))).astype(np.float32)
+    q[:, 1] = -q[:, 1]                              # query 0 all positive, query 1 all negative
+    q = enc(q)
+    K = enc(rng.standard_normal((B, Hkv, C * cs, d)))
+    lm2 = oracle.build_minmax_landmarks(K, cs)
+    s = oracle.score_minmax_landmarks(q, lm2)
+    Q = synth.bf16_to_f32(q).astype(np.float64).sum(axis=2)       # G = Hq, one KV head
+    lf = synth.bf16_to_f32(lm2).astype(np.float64)
+    np.testing.assert_allclose(s[0, 0, 0], lf[0, 0, :, 1, :] @ Q[0, 0], rtol=1e-12)
+    np.testing.assert_allclose(s[0, 1, 0], lf[0, 0, :, 0, :] @ Q[0, 1], rtol=1e-12)
+
+
+def test_step_with_minmax_landmarks_selects_by_the_bound():
+    rng = np.random.default_rng(17)
+    B, n_q, Hq, Hkv, C, cs, d, k = 1, 2, 4, 2, 6, 4, 128, 2
+    q = enc(rng.standard_normal((B, n_q, Hq, d)))
+    Kh = enc(rng.standard_normal((B, Hkv, C * cs, d)))
+    Vh = enc(rng.standard_normal((B, Hkv, C * cs, d)))
+    lm2 = oracle.build_minmax_landmarks(Kh, cs)
+    slot = np.full((B, Hkv, C), -1, np.int32)
+    r = oracle.step(q, lm2, Kh, Vh, slot, None, None, k, cs)
+    assert np.array_equal(r["scores"], oracle.score_minmax_landmarks(q, lm2))
+    assert np.array_equal(r["sel"], oracle.select_topk(r["scores"], k))
