@@ -136,10 +136,11 @@ class OracleSample:
     Hkv units, built from the host generator (the same definition the GPU
     path's inputs come from)."""
 
-    def __init__(self, w):
+    def __init__(self, w, landmarks="mean"):
         import oracle
         self.oracle = oracle
         self.w = w
+        build_lm = oracle.build_minmax_landmarks if landmarks == "minmax" else oracle.build_landmarks
         q = synth.queries(w.seed, 1, w.n_q, w.Hq, w.d, w.spec_scale)
         bias = u_hat = None
         if w.key_bias == "hot":
@@ -156,7 +157,7 @@ class OracleSample:
             V = synth.kv_rows(w.seed, synth.TID_V, 1, w.Hkv, w.L, w.d, w.cs, u, np.zeros(1, np.int64),
                               w.L).reshape(1, 1, w.L, w.d)
             qg = np.ascontiguousarray(q[:, :, g * w.G:(g + 1) * w.G])
-            self.units.append((qg, oracle.build_landmarks(K, w.cs), K, V))
+            self.units.append((qg, build_lm(K, w.cs), K, V))
         self.slot = np.full((1, 1, w.C), -1, np.int32)
         self.empty = np.zeros((0, w.cs, w.d), np.uint16)
         self.next = 0
@@ -175,8 +176,8 @@ class OracleSample:
                 f"timing, each 1/{w.B * w.Hkv} of a step; steps/s = units / ({w.B * w.Hkv} x seconds)")
 
 
-def cpu_baseline(w, budget_s=12.0):
-    s = OracleSample(w)
+def cpu_baseline(w, budget_s=12.0, landmarks="mean"):
+    s = OracleSample(w, landmarks)
     s.run_units(1)
     done, spent = 0, 0.0
     while spent < budget_s:
@@ -190,7 +191,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     w = BY_NAME[args.workload]
-    s = OracleSample(w)
+    s = OracleSample(w, args.landmarks)
     t_unit = s.run_units(1)
     # size each step's sample so that the whole run stays near two minutes
     per_step = min(2.0, 120.0 / (args.steps + args.warmup))
@@ -203,7 +204,7 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, "oracle"),
+        "config": config_of(w, "oracle", landmarks=args.landmarks),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": s.describe(n)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -234,11 +235,11 @@ def profiled_traffic(stage: str, workload: str):
     return int(t.group(1)) if cur.startswith(h.group(1)) else None
 
 
-def config_of(w, gather_mode, world=1):
+def config_of(w, gather_mode, world=1, landmarks="mean"):
     gather_desc = {"zerocopy": "zero-copy, fused into the attention kernel",
                    "memcpy": "miss list to host, cudaMemcpyAsync per run of chunks"}.get(gather_mode, gather_mode)
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "L": w.L, "cs": w.cs, "k": w.k,
-            "n_q": w.n_q, "residency": w.residency, "gather": gather_desc,
+            "n_q": w.n_q, "residency": w.residency, "gather": gather_desc, "landmarks": landmarks,
             "l2": f"inputs larger than L2 ({N_LAYERS} layers of landmarks and host KV cycled)",
             "host_pages": "every pinned host K/V page read once by the GPU before timing",
             "parallelism": f"independent batch per GPU x{world}"}
@@ -251,7 +252,7 @@ def rank_seed(seed: int, rank: int) -> int:
 
 
 class LayerData:
-    def __init__(self, dd, shape, w, layer, rank):
+    def __init__(self, dd, shape, w, layer, rank, lm_vectors=1):
         import torch
         seed = rank_seed(w.seed, rank)
         self.q = torch.empty(w.B * w.n_q * w.Hq * w.d, dtype=torch.bfloat16, device="cuda")
@@ -272,7 +273,7 @@ class LayerData:
         self.Vh = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
         dd.synth_kv(shape, seed, synth.tensor_id(synth.TID_K, layer), self.Kh, bias, u_hat)
         dd.synth_kv(shape, seed, synth.tensor_id(synth.TID_V, layer), self.Vh)
-        self.lm = torch.empty(w.B * w.Hkv * w.C * w.d, dtype=torch.bfloat16, device="cuda")
+        self.lm = torch.empty(w.B * w.Hkv * w.C * lm_vectors * w.d, dtype=torch.bfloat16, device="cuda")
         self.q_host = torch.empty(self.q.numel(), dtype=torch.bfloat16, pin_memory=True)
         torch.cuda.synchronize()
         self.q_host.copy_(self.q)
@@ -333,11 +334,16 @@ def run_ours(args, world, rank, local):
     mode = dd.GATHER_MEMCPY if args.mode == "memcpy" else dd.GATHER_ZEROCOPY
     cap = w.max_misses
 
-    layers = [LayerData(dd, shape, w, l, rank) for l in range(N_LAYERS)]
+    minmax = args.landmarks == "minmax"
+    lm_kind = dd.LM_MINMAX if minmax else dd.LM_MEAN
+    layers = [LayerData(dd, shape, w, l, rank, 2 if minmax else 1) for l in range(N_LAYERS)]
     ctx = dd.Context(shape, max_misses=cap, hot_slots=0)
-    touch = torch.empty_like(layers[0].lm)
+    touch = torch.empty(w.B * w.Hkv * w.C * w.d, dtype=torch.bfloat16, device="cuda")
     for L_ in layers:
-        ctx.build_landmarks(L_.Kh, L_.lm)
+        if minmax:
+            ctx.build_landmarks_minmax(L_.Kh, L_.lm)
+        else:
+            ctx.build_landmarks(L_.Kh, L_.lm)
         # the GPU's first access to a pinned host page pays for its address
         # translation; read every V page once too (K was just read in full),
         # so that the timed steps see the steady state
@@ -378,7 +384,7 @@ def run_ours(args, world, rank, local):
     def step(i, layer, events=None, inter=None):
         d_ = layers[layer % N_LAYERS]
         ctx.step(layer, d_.q, d_.lm, d_.Kh, d_.Vh, slot, None, None, Kst, Vst, out, mode=mode,
-                 intermediates=inter, stage_events=events)
+                 intermediates=inter, stage_events=events, lm_kind=lm_kind)
 
     sampler = ClockSampler(local) if rank == 0 else None
     for i in range(args.warmup):
@@ -421,7 +427,7 @@ def run_ours(args, world, rank, local):
 
     # algorithmic bytes per launch
     q_b = w.B * w.n_q * w.Hq * w.d * 2
-    score_b = w.B * w.Hkv * w.C * w.d * 2 + q_b + w.B * w.n_q * w.Hkv * w.C * 4
+    score_b = w.B * w.Hkv * w.C * w.d * 2 * (2 if minmax else 1) + q_b + w.B * w.n_q * w.Hkv * w.C * 4
     attn_b = U * 2 * chunk_b + q_b + w.B * w.n_q * w.Hq * w.d * 4
     gather_b = M * 2 * chunk_b                   # bytes read over the host link (written to HBM once more)
     hbm_peak, hbm_kind = peaks()
@@ -480,7 +486,7 @@ def run_ours(args, world, rank, local):
     e2e_s = max_over_ranks(a.elapsed_time(b) * 1e-3, world)
     barrier(world)
 
-    cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    cpu = cpu_baseline(w, landmarks=args.landmarks) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     ctx.close()
     if rank != 0:
         return 0
@@ -488,7 +494,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": world * K / t_max, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": 1e3 * t_max / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, args.mode, world),
+        "config": config_of(w, args.mode, world, args.landmarks),
         "roofline": roof, "roofline_hbm": roof_hbm,
         "stages_us": {n: 1e3 * v for n, v in stage_ms.items()},
         "stages_note": f"stages_us: mean over {n_stage} further steps with an event at every stage boundary; "
@@ -515,6 +521,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=LLAMA8B_32K.name, choices=sorted(BY_NAME))
     ap.add_argument("--mode", choices=("zerocopy", "memcpy"), default="zerocopy")
+    ap.add_argument("--landmarks", choices=("mean", "minmax"), default="mean")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -95,6 +95,26 @@ dd_status dd_build_landmarks(dd_ctx *ctx, const void *K, void *lm, dd_stream_t s
  * (unscaled; fp32 accumulation). */
 dd_status dd_score_landmarks(dd_ctx *ctx, const void *q, const void *lm, float *scores, dd_stream_t stream);
 
+/* Landmark kinds (dd_step_args.lm_kind). */
+typedef enum { DD_LM_MEAN = 0, DD_LM_MINMAX = 1 } dd_landmark_kind;
+
+/* Quest-style min/max landmarks (OasisKV summary, Methodology: two summary
+ * vectors per block, its coordinate-wise minimum and maximum key).  K: bf16
+ * [B,Hkv,L,d], device or pinned host.  lm2: bf16 [B,Hkv,C,2,d] device, twice
+ * the size of mean landmarks; lm2[b,g,c,0,i] and lm2[b,g,c,1,i] are the
+ * smallest and the largest of K[b,g,c*cs+t,i] over t < cs, -0 counting as
+ * below +0.  Exact (no rounding). */
+dd_status dd_build_landmarks_minmax(dd_ctx *ctx, const void *K, void *lm2, dd_stream_t stream);
+
+/* Upper-bound scores on min/max landmarks, all n_q queries in one pass.
+ * q: bf16 [B,n_q,Hq,d]; lm2: bf16 [B,Hkv,C,2,d]; scores: fp32 [B,n_q,Hkv,C] =
+ * sum_i max(Q_i * lm2[b,g,c,0,i], Q_i * lm2[b,g,c,1,i]) with Q the fp32 sum
+ * of the G q-heads of KV head g: the largest value Q.k takes over any key k
+ * inside the chunk's min/max box, hence never below Q.k_t for a token t of
+ * the chunk (fp32 accumulation). */
+dd_status dd_score_landmarks_minmax(dd_ctx *ctx, const void *q, const void *lm2, float *scores,
+                                    dd_stream_t stream);
+
 /* Top-k chunks per row (OasisKV summary, Methodology: top-K per KV head).
  * scores: fp32 [B,n_q,Hkv,C]; sel: int32 [B,n_q,Hkv,k], the k chunks with the
  * largest scores ordered by (score desc, chunk asc), written in ascending
@@ -174,7 +194,7 @@ dd_status dd_sparse_attn_decode_noalloc(const dd_dims *dims, int64_t hot_slots, 
 typedef struct {
   int32_t layer;
   const void *q;                 /* bf16 [B,n_q,Hq,d] device */
-  const void *lm;                /* bf16 [B,Hkv,C,d] device */
+  const void *lm;                /* bf16 [B,Hkv,C,d] device (mean) or [B,Hkv,C,2,d] (min/max, see lm_kind) */
   const void *Kh, *Vh;           /* bf16 [B,Hkv,L,d] pinned host */
   const int32_t *resident_slot;  /* int32 [B,Hkv,C] device */
   const void *Khot, *Vhot;       /* bf16 [hot_slots,cs,d] device or NULL */
@@ -190,6 +210,7 @@ typedef struct {
    * recorded on the stream before scoring and after scoring, top-k, resolve,
    * gather and attention */
   void *stage_events[6];
+  dd_landmark_kind lm_kind;      /* DD_LM_MEAN (0) or DD_LM_MINMAX: how lm is laid out and scored */
 } dd_step_args;
 
 dd_status dd_step(dd_ctx *ctx, const dd_step_args *args, dd_stream_t stream);

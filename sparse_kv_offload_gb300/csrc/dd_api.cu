@@ -262,6 +262,27 @@ dd_status dd_score_landmarks(dd_ctx *c, const void *q, const void *lm, float *sc
                                   c->dims.n_q, c->dims.Hq, c->dims.Hkv, c->C, (cudaStream_t)stream));
 }
 
+dd_status dd_build_landmarks_minmax(dd_ctx *c, const void *K, void *lm2, dd_stream_t stream) {
+  if (!c) return DD_ERR_INVALID_ARG;
+  if (c->units == 0) return DD_OK;
+  if (!K || !lm2 || !aligned16(K) || !aligned16(lm2)) return DD_ERR_INVALID_ARG;
+  const void *kd;
+  DD_TRY(device_view(K, &kd));
+  c->launches += 1;
+  return cuda_ok(dd::launch_build_minmax(static_cast<const uint4 *>(kd), static_cast<uint4 *>(lm2),
+                                         (int64_t)c->units * c->C, c->dims.cs, (cudaStream_t)stream));
+}
+
+dd_status dd_score_landmarks_minmax(dd_ctx *c, const void *q, const void *lm2, float *scores, dd_stream_t stream) {
+  if (!c) return DD_ERR_INVALID_ARG;
+  if (c->units == 0) return DD_OK;
+  if (!q || !lm2 || !scores || !aligned16(q) || !aligned16(lm2)) return DD_ERR_INVALID_ARG;
+  c->launches += 1;
+  return cuda_ok(dd::launch_score_minmax(static_cast<const uint4 *>(q), static_cast<const uint4 *>(lm2), scores,
+                                         c->dims.B, c->dims.n_q, c->dims.Hq, c->dims.Hkv, c->C,
+                                         (cudaStream_t)stream));
+}
+
 dd_status dd_select_topk(dd_ctx *c, const float *scores, int32_t *sel, dd_stream_t stream) {
   if (!c) return DD_ERR_INVALID_ARG;
   if (c->units == 0) return DD_OK;
@@ -388,6 +409,7 @@ dd_status dd_sparse_attn_decode(dd_ctx *c, const void *q, const void *Khot, cons
 
 dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   if (!c || !a || a->layer < 0) return DD_ERR_INVALID_ARG;
+  if (a->lm_kind != DD_LM_MEAN && a->lm_kind != DD_LM_MINMAX) return DD_ERR_INVALID_ARG;
   if (c->units == 0) return DD_OK;
   if (!a->q || !a->lm || !a->Kh || !a->Vh || !a->resident_slot || !a->out) return DD_ERR_INVALID_ARG;
   const int p = a->layer & 1;
@@ -407,7 +429,11 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
     return a->stage_events[i] ? cuda_ok(cudaEventRecord((cudaEvent_t)a->stage_events[i], s)) : DD_OK;
   };
   DD_TRY(mark(0));
-  DD_TRY(dd_score_landmarks(c, a->q, a->lm, scores, stream));
+  if (a->lm_kind == DD_LM_MINMAX) {
+    DD_TRY(dd_score_landmarks_minmax(c, a->q, a->lm, scores, stream));
+  } else {
+    DD_TRY(dd_score_landmarks(c, a->q, a->lm, scores, stream));
+  }
   DD_TRY(mark(1));
   DD_TRY(dd_select_topk(c, scores, sel, stream));
   DD_TRY(mark(2));

@@ -174,12 +174,15 @@ __device__ __forceinline__ void attn_plan_unit(const AttnPlanOut &po, int unit, 
 
 }  // namespace dd
 
-// Host-side launch helpers, defined in dd_api.cu
+// Host-side launch helpers, defined with their kernels
 namespace dd {
 struct Ctx;
 cudaError_t launch_build_landmarks(const uint4 *K, uint4 *lm, int64_t n_chunks, int cs, cudaStream_t s);
 cudaError_t launch_score(const uint4 *q, const uint4 *lm, float *scores, int B, int n_q, int Hq, int Hkv,
                          int C, cudaStream_t s);
+cudaError_t launch_build_minmax(const uint4 *K, uint4 *lm2, int64_t n_chunks, int cs, cudaStream_t s);
+cudaError_t launch_score_minmax(const uint4 *q, const uint4 *lm2, float *scores, int B, int n_q, int Hq, int Hkv,
+                                int C, cudaStream_t s);
 cudaError_t launch_topk(const float *scores, int32_t *sel, int rows, int C, int k, cudaStream_t s);
 cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx,
                          int32_t *union_slot, uint8_t *union_qmask, int32_t *union_cnt,

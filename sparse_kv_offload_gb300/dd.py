@@ -20,11 +20,13 @@ LIB_PATH = os.path.join(_PKG, "lib", "libdd.so")
 
 DD_OK, DD_ERR_INVALID_ARG, DD_ERR_CUDA, DD_ERR_CAPACITY, DD_ERR_TIMEOUT, DD_ERR_DEVICE_CHECK = range(6)
 GATHER_ZEROCOPY, GATHER_MEMCPY = 0, 1
+LM_MEAN, LM_MINMAX = 0, 1
 
 EXPORTED = (
     "dd_create", "dd_destroy", "dd_build_landmarks", "dd_score_landmarks", "dd_select_topk",
     "dd_resolve_union", "dd_gather_kv", "dd_sparse_attn_decode", "dd_step", "dd_get_status",
     "dd_launch_count", "dd_status_str", "dd_last_cuda_error", "dd_synth_kv", "dd_synth_queries", "dd_sparse_attn_decode_noalloc",
+    "dd_build_landmarks_minmax", "dd_score_landmarks_minmax",
 )
 
 
@@ -52,6 +54,7 @@ class StepArgs(ctypes.Structure):
         ("scores", _vp), ("sel", _vp), ("union_idx", _vp), ("union_slot", _vp), ("union_cnt", _vp),
         ("miss_list", _vp), ("miss_count", _vp), ("attn_slot", _vp), ("union_qmask", _vp),
         ("stage_events", _vp * 6),
+        ("lm_kind", ctypes.c_int),
     ]
 
 
@@ -65,6 +68,8 @@ def _load():
         "dd_destroy": (i32, [_vp]),
         "dd_build_landmarks": (i32, [_vp, _vp, _vp, _vp]),
         "dd_score_landmarks": (i32, [_vp, _vp, _vp, _vp, _vp]),
+        "dd_build_landmarks_minmax": (i32, [_vp, _vp, _vp, _vp]),
+        "dd_score_landmarks_minmax": (i32, [_vp, _vp, _vp, _vp, _vp]),
         "dd_select_topk": (i32, [_vp, _vp, _vp, _vp]),
         "dd_resolve_union": (i32, [_vp] * 11),
         "dd_gather_kv": (i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp]),
@@ -194,6 +199,22 @@ class Context:
             _ptr(scores, torch.float32, s.B * s.n_q * s.Hkv * s.C, name="scores"), _stream(stream)),
             "dd_score_landmarks")
 
+    def build_landmarks_minmax(self, K, lm2, stream=None):
+        s = self.shape
+        n = s.B * s.Hkv * s.L * s.d
+        kp = _ptr(K, torch.bfloat16, n, device=K.is_cuda, name="K")
+        _chk(_lib.dd_build_landmarks_minmax(
+            self._h, kp, _ptr(lm2, torch.bfloat16, s.B * s.Hkv * s.C * 2 * s.d, name="lm2"), _stream(stream)),
+            "dd_build_landmarks_minmax")
+
+    def score_landmarks_minmax(self, q, lm2, scores, stream=None):
+        s = self.shape
+        _chk(_lib.dd_score_landmarks_minmax(
+            self._h, _ptr(q, torch.bfloat16, s.B * s.n_q * s.Hq * s.d, name="q"),
+            _ptr(lm2, torch.bfloat16, s.B * s.Hkv * s.C * 2 * s.d, name="lm2"),
+            _ptr(scores, torch.float32, s.B * s.n_q * s.Hkv * s.C, name="scores"), _stream(stream)),
+            "dd_score_landmarks_minmax")
+
     def select_topk(self, scores, sel, stream=None):
         s = self.shape
         _chk(_lib.dd_select_topk(self._h, _ptr(scores, torch.float32, s.B * s.n_q * s.Hkv * s.C, name="scores"),
@@ -245,16 +266,19 @@ class Context:
             "dd_sparse_attn_decode")
 
     def step(self, layer, q, lm, Kh, Vh, resident_slot, Khot, Vhot, Kst_pair, Vst_pair, out,
-             mode=GATHER_ZEROCOPY, softmax_scale=0.0, intermediates=None, stage_events=None, stream=None):
+             mode=GATHER_ZEROCOPY, softmax_scale=0.0, intermediates=None, stage_events=None, stream=None,
+             lm_kind=LM_MEAN):
         """One layer; ``intermediates`` optionally maps names of dd_step_args' optional
         outputs (scores, sel, union_idx, union_slot, union_qmask, union_cnt, miss_list,
         miss_count, attn_slot) to caller tensors; ``stage_events`` optionally gives six
-        torch.cuda.Event objects recorded at the stage boundaries."""
+        torch.cuda.Event objects recorded at the stage boundaries; ``lm_kind`` says
+        whether ``lm`` holds mean landmarks or min/max landmarks (twice the size)."""
         s = self.shape
         a = StepArgs()
         a.layer = int(layer)
         a.q = _ptr(q, torch.bfloat16, s.B * s.n_q * s.Hq * s.d, name="q")
-        a.lm = _ptr(lm, torch.bfloat16, s.B * s.Hkv * s.C * s.d, name="lm")
+        a.lm_kind = int(lm_kind)
+        a.lm = _ptr(lm, torch.bfloat16, s.B * s.Hkv * s.C * s.d * (2 if lm_kind == LM_MINMAX else 1), name="lm")
         n = s.B * s.Hkv * s.L * s.d
         a.Kh = _ptr(Kh, torch.bfloat16, n, device=False, name="Kh")
         a.Vh = _ptr(Vh, torch.bfloat16, n, device=False, name="Vh")

@@ -56,9 +56,9 @@ class StepBuffers:
             attn_slot=torch.empty(w.B * w.n_q * w.Hkv * w.k, dtype=torch.int32, device="cuda"),
         )
 
-    def run(self, ctx, layer=0, mode=0):
-        ctx.step(layer, self.q, self.lm, self.Kh, self.Vh, self.slot, self.Khot, self.Vhot, self.Kst, self.Vst,
-                 self.out, mode=mode, intermediates=self.inter)
+    def run(self, ctx, layer=0, mode=0, lm=None, lm_kind=0):
+        ctx.step(layer, self.q, self.lm if lm is None else lm, self.Kh, self.Vh, self.slot, self.Khot, self.Vhot,
+                 self.Kst, self.Vst, self.out, mode=mode, intermediates=self.inter, lm_kind=lm_kind)
 
 
 @pytest.mark.parametrize("w", STEP_CASES, ids=lambda w: w.name)
