@@ -23,7 +23,7 @@ __all__ = [
     "bf16_decode", "bf16_encode", "build_landmarks", "score_landmarks", "select_topk",
     "resolve_union", "gather_kv", "sparse_attn_decode", "step", "kv_footprint_bytes",
     "max_batch", "per_step_budget_bytes", "union_of_query_selections",
-    "build_minmax_landmarks", "score_minmax_landmarks", "bf16_total_order_key",
+    "build_minmax_landmarks", "score_minmax_landmarks", "bf16_total_order_key", "update_residency",
 ]
 
 
@@ -284,7 +284,8 @@ def _rows(pool_hot, pool_stage, slot: int):
     return pool_hot[slot] if slot >= 0 else pool_stage[-slot - 1]
 
 
-def sparse_attn_decode(q, Khot, Vhot, Kst, Vst, attn_slot, cs: int, scale: float | None = None):
+def sparse_attn_decode(q, Khot, Vhot, Kst, Vst, attn_slot, cs: int, scale: float | None = None,
+                       K_tail=None, V_tail=None):
     """o[b,j,h,:] = sum over the selected rows t of softmax_t(scale * q . K_t) * V_t (fp64).
 
     DualDecoder §5.2: the output and speculative tokens attend in one pass;
@@ -292,8 +293,15 @@ def sparse_attn_decode(q, Khot, Vhot, Kst, Vst, attn_slot, cs: int, scale: float
     resident working set; Adaptive DHiSparse Fig. 3: each query attends over
     the chunks it picked itself.  Readings: scale = 1/sqrt(d); query head h uses KV
     head floor(h/G); the rows of query j are those of the k chunks in
-    ``attn_slot[b,j,g,:]``; the current step's own new tokens are not part
-    of the path.
+    ``attn_slot[b,j,g,:]``.
+
+    Tail rows (optional): ``K_tail, V_tail`` bf16 [B, n_q, Hkv, d] are the
+    keys and values of the step's own new tokens, token j being query j's.
+    DualDecoder §5.2 places the tokens of a step one after the other along
+    the sequence with a causal mask, so query j also attends to tail rows
+    0..j and never to a later token's row (Adaptive DHiSparse Fig. 3 (4):
+    every query's row is written to the tail, which the resolver reads
+    first).
     """
     B, n_q, Hq, d = q.shape
     Hkv = attn_slot.shape[2]
@@ -308,6 +316,9 @@ def sparse_attn_decode(q, Khot, Vhot, Kst, Vst, attn_slot, cs: int, scale: float
                 slots = [int(s) for s in attn_slot[b, j, g]]
                 Kr = bf16_decode(np.concatenate([_rows(Khot, Kst, s) for s in slots], axis=0))
                 Vr = bf16_decode(np.concatenate([_rows(Vhot, Vst, s) for s in slots], axis=0))
+                if K_tail is not None:
+                    Kr = np.concatenate([Kr, bf16_decode(K_tail[b, :j + 1, g])], axis=0)
+                    Vr = np.concatenate([Vr, bf16_decode(V_tail[b, :j + 1, g])], axis=0)
                 for h in range(g * G, (g + 1) * G):
                     z = (Kr @ qf[b, j, h]) * scale
                     p = np.exp(z - z.max())
@@ -317,10 +328,82 @@ def sparse_attn_decode(q, Khot, Vhot, Kst, Vst, attn_slot, cs: int, scale: float
 
 
 # ---------------------------------------------------------------------------
+# after a step: residency update of the per-(request, KV head) hot pools
+# ---------------------------------------------------------------------------
+
+def update_residency(step_id: int, cap: int, union_idx, union_slot, union_cnt, Kst, Vst,
+                     resident_slot, slot_chunk, last_used, Khot, Vhot):
+    """Delta selection with capped LRU eviction; returns the updated copies
+    (resident_slot, slot_chunk, last_used, Khot, Vhot) and the admitted count per unit.
+
+    OasisKV summary, Methodology (delta selection and capped eviction), per
+    KV head and decoding step: chunks of the selection that are resident
+    cost no traffic; resident chunks outside the selection are ranked by the
+    step they were last selected in; each admitted non-resident chunk is
+    paired with one eviction target, least recently used first; at most
+    ``cap`` pairs are admitted, which bounds the traffic to cap * H entries.
+    Adaptive DHiSparse Fig. 3 (3): promoted rows are copied from the staging
+    arena into the hot cache.
+
+    Readings: every (b, g) unit owns the S = slot_chunk.shape[-1] pool slots
+    u*S .. u*S+S-1 (resident_slot holds these global slot numbers, -1 when
+    absent); a slot whose slot_chunk is -1 is free and is used before any
+    eviction, lowest slot first; eviction order is (last_used ascending, slot
+    ascending); resident chunks of the current union get last_used = step_id
+    and are never evicted; the missing chunks of the union are admitted in
+    ascending chunk order, the i-th admitted one going into the i-th target;
+    its K and V come from staging slot m of union_slot = -(m+1).
+    """
+    resident_slot = np.array(resident_slot, dtype=np.int32, copy=True)
+    slot_chunk = np.array(slot_chunk, dtype=np.int32, copy=True)
+    last_used = np.array(last_used, dtype=np.int32, copy=True)
+    Khot = np.array(Khot, copy=True)
+    Vhot = np.array(Vhot, copy=True)
+    B, Hkv, C = resident_slot.shape
+    S = slot_chunk.shape[-1]
+    sc = slot_chunk.reshape(B * Hkv, S)
+    lu = last_used.reshape(B * Hkv, S)
+    rs = resident_slot.reshape(B * Hkv, C)
+    admitted = np.zeros(B * Hkv, dtype=np.int32)
+    umax = union_idx.shape[-1]
+    ui = np.asarray(union_idx).reshape(B * Hkv, umax)
+    us = np.asarray(union_slot).reshape(B * Hkv, umax)
+    for u in range(B * Hkv):
+        base = u * S
+        n = int(np.asarray(union_cnt).reshape(-1)[u])
+        entries = [(int(ui[u, i]), int(us[u, i])) for i in range(n)]
+        in_union = set()
+        for c, sl in entries:
+            if sl >= 0:
+                in_union.add(sl - base)
+                lu[u, sl - base] = step_id
+        misses = [(c, -sl - 1) for c, sl in entries if sl < 0]
+        free = [t for t in range(S) if sc[u, t] < 0]
+        evictable = sorted((t for t in range(S) if sc[u, t] >= 0 and t not in in_union),
+                           key=lambda t: (int(lu[u, t]), t))
+        targets = free + evictable
+        A = min(cap, len(misses), len(targets))
+        for i in range(A):
+            c, m = misses[i]
+            t = targets[i]
+            old = int(sc[u, t])
+            if old >= 0:
+                rs[u, old] = -1
+            rs[u, c] = base + t
+            sc[u, t] = c
+            lu[u, t] = step_id
+            Khot[base + t] = Kst[m]
+            Vhot[base + t] = Vst[m]
+        admitted[u] = A
+    return {"resident_slot": resident_slot, "slot_chunk": slot_chunk, "last_used": last_used,
+            "Khot": Khot, "Vhot": Vhot, "admitted": admitted.reshape(B, Hkv)}
+
+
+# ---------------------------------------------------------------------------
 # a6: one layer's step
 # ---------------------------------------------------------------------------
 
-def step(q, lm, Kh, Vh, resident_slot, Khot, Vhot, k: int, cs: int, scale=None) -> dict:
+def step(q, lm, Kh, Vh, resident_slot, Khot, Vhot, k: int, cs: int, scale=None, K_tail=None, V_tail=None) -> dict:
     """Score -> top-k -> union/resolve -> gather -> attention for one layer.
 
     DualDecoder Fig. 8 / §5.1-§5.4: retrieval index from the query and the
@@ -333,7 +416,7 @@ def step(q, lm, Kh, Vh, resident_slot, Khot, Vhot, k: int, cs: int, scale=None) 
     sel = select_topk(s, k)
     res = resolve_union(sel, resident_slot)
     Kst, Vst = gather_kv(Kh, Vh, res["miss_list"], cs)
-    out = sparse_attn_decode(q, Khot, Vhot, Kst, Vst, res["attn_slot"], cs, scale)
+    out = sparse_attn_decode(q, Khot, Vhot, Kst, Vst, res["attn_slot"], cs, scale, K_tail, V_tail)
     res.update(scores=s, sel=sel, Kst=Kst, Vst=Vst, out=out)
     return res
 

@@ -424,3 +424,168 @@ def test_step_with_minmax_landmarks_selects_by_the_bound():
     r = oracle.step(q, lm2, Kh, Vh, slot, None, None, k, cs)
     assert np.array_equal(r["scores"], oracle.score_minmax_landmarks(q, lm2))
     assert np.array_equal(r["sel"], oracle.select_topk(r["scores"], k))
+
+
+# ---------------------------------------------------------------- tail rows (the step's own tokens)
+
+def test_attention_tail_rows_equal_dense_causal_sdpa():
+    # every chunk selected + the n_q new tokens appended with a causal mask among them
+    rng = np.random.default_rng(21)
+    B, n_q, Hq, Hkv, L, d, cs = 2, 3, 4, 2, 64, 128, 16
+    C = L // cs
+    q = enc(rng.standard_normal((B, n_q, Hq, d)))
+    Kh = enc(rng.standard_normal((B, Hkv, L, d)))
+    Vh = enc(rng.standard_normal((B, Hkv, L, d)))
+    Kt = enc(rng.standard_normal((B, n_q, Hkv, d)))
+    Vt = enc(rng.standard_normal((B, n_q, Hkv, d)))
+    sel = np.broadcast_to(np.arange(C, dtype=np.int32), (B, n_q, Hkv, C)).copy()
+    res = oracle.resolve_union(sel, np.full((B, Hkv, C), -1, np.int32))
+    Kst, Vst = oracle.gather_kv(Kh, Vh, res["miss_list"], cs)
+    empty = np.zeros((0, cs, d), np.uint16)
+    out = oracle.sparse_attn_decode(q, empty, empty, Kst, Vst, res["attn_slot"], cs, K_tail=Kt, V_tail=Vt)
+    G = Hq // Hkv
+    qf, Kf, Vf, Ktf, Vtf = (torch.from_numpy(synth.bf16_to_f32(x).astype(np.float64)) for x in (q, Kh, Vh, Kt, Vt))
+    # sequence = L context rows then the n_q new tokens; query j sits at position L + j
+    Kseq = torch.cat([Kf, Ktf.permute(0, 2, 1, 3)], dim=2)             # [B, Hkv, L + n_q, d]
+    Vseq = torch.cat([Vf, Vtf.permute(0, 2, 1, 3)], dim=2)
+    Kseq = Kseq.repeat_interleave(G, dim=1)                              # query head h -> KV head h // G
+    Vseq = Vseq.repeat_interleave(G, dim=1)
+    Q = qf.permute(0, 2, 1, 3)                                           # [B, Hq, n_q, d]
+    pos_q = L + torch.arange(n_q)[:, None]
+    mask = torch.arange(L + n_q)[None, :] <= pos_q                       # causal
+    want = torch.nn.functional.scaled_dot_product_attention(Q, Kseq, Vseq, attn_mask=mask, scale=1 / math.sqrt(d))
+    np.testing.assert_allclose(out, want.permute(0, 2, 1, 3).numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_attention_tail_row_of_a_later_token_is_masked():
+    # a later token's tail row with an enormous logit must not reach an earlier query
+    rng = np.random.default_rng(22)
+    B, n_q, Hq, Hkv, d, cs, S = 1, 2, 2, 1, 128, 4, 3
+    Khot = enc(rng.standard_normal((S, cs, d)) * 0.1)
+    Vhot = enc(rng.standard_normal((S, cs, d)))
+    q = enc(np.ones((B, n_q, Hq, d), np.float32))
+    Kt = enc(np.stack([np.zeros((1, d)), np.full((1, d), 8.0)], axis=0)[None].astype(np.float32))  # [1,2,1,d]
+    Vt = enc(np.stack([np.zeros((1, d)), np.full((1, d), 5.0)], axis=0)[None].astype(np.float32))
+    slots = np.array([[[[0, 2]], [[0, 2]]]], np.int32)
+    out = oracle.sparse_attn_decode(q, Khot, Vhot, Khot[:0], Vhot[:0], slots, cs, K_tail=Kt, V_tail=Vt)
+    base = oracle.sparse_attn_decode(q, Khot, Vhot, Khot[:0], Vhot[:0], slots, cs)
+    # query 0 sees only its own tail row (K = V = 0): the context output diluted by that one zero row
+    z = (synth.bf16_to_f32(Khot[[0, 2]]).astype(np.float64).reshape(-1, d) @ np.ones(d)) / math.sqrt(d)
+    w0 = np.exp(z - z.max()).sum() / (np.exp(z - z.max()).sum() + np.exp(-z.max()))
+    np.testing.assert_allclose(out[0, 0], w0 * base[0, 0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out[0, 1], 5.0, rtol=0, atol=1e-9)   # its own row dominates (logit 8*128/sqrt(128))
+
+
+# ---------------------------------------------------------------- residency update (delta selection, capped LRU)
+
+def _res_step(state, union, step_id, cap, cs=1, d=2):
+    """Resolve `union` (one request, one KV head, one query) against the state and
+    update; staging rows of ordinal m hold the value 16*step + m (exact in bf16)."""
+    C = state["resident_slot"].shape[-1]
+    sel = np.array(sorted(union), np.int32)[None, None, None, :]
+    res = oracle.resolve_union(sel, state["resident_slot"])
+    M = res["miss_count"]
+    Kst = enc(np.repeat((16.0 * step_id + np.arange(M, dtype=np.float32))[:, None, None], cs, 1)
+              * np.ones((1, 1, d), np.float32))
+    new = oracle.update_residency(step_id, cap, res["union_idx"], res["union_slot"], res["union_cnt"], Kst, Kst,
+                                  state["resident_slot"], state["slot_chunk"], state["last_used"],
+                                  state["Khot"], state["Vhot"])
+    return new, res
+
+
+def test_residency_worked_example():
+    S, C, cs, d = 3, 10, 1, 2
+    st = {"resident_slot": np.full((1, 1, C), -1, np.int32), "slot_chunk": np.full((1, 1, S), -1, np.int32),
+          "last_used": np.full((1, 1, S), -1, np.int32), "Khot": np.zeros((S, cs, d), np.uint16),
+          "Vhot": np.zeros((S, cs, d), np.uint16)}
+    # step 0: four misses, cap 2 -> chunks 2 and 5 into the free slots 0 and 1
+    st, res = _res_step(st, [2, 5, 7, 9], 0, cap=2)
+    assert res["miss_count"] == 4 and st["admitted"][0, 0] == 2
+    assert st["slot_chunk"][0, 0].tolist() == [2, 5, -1] and st["last_used"][0, 0].tolist() == [0, 0, -1]
+    assert st["resident_slot"][0, 0, [2, 5, 7, 9]].tolist() == [0, 1, -1, -1]
+    assert synth.bf16_to_f32(st["Khot"][:2, 0, 0]).tolist() == [0.0, 1.0]       # staging ordinals 0, 1
+    # step 1: 2 is resident (refreshed), 7 goes to the last free slot
+    st, res = _res_step(st, [2, 7], 1, cap=2)
+    assert res["miss_count"] == 1
+    assert st["slot_chunk"][0, 0].tolist() == [2, 5, 7] and st["last_used"][0, 0].tolist() == [1, 0, 1]
+    assert synth.bf16_to_f32(st["Khot"][2, 0, 0]) == 16.0
+    # step 2: 7 resident; misses 1, 3; evict LRU first: slot 1 (chunk 5, step 0), then slot 0 (chunk 2, step 1)
+    st, res = _res_step(st, [1, 3, 7], 2, cap=2)
+    assert st["slot_chunk"][0, 0].tolist() == [3, 1, 7] and st["last_used"][0, 0].tolist() == [2, 2, 2]
+    assert st["resident_slot"][0, 0, [1, 2, 3, 5, 7]].tolist() == [1, -1, 0, -1, 2]
+    assert synth.bf16_to_f32(st["Khot"][:, 0, 0]).tolist() == [33.0, 32.0, 16.0]
+    # step 3: every slot holds a chunk of the union -> nothing can be evicted
+    st, res = _res_step(st, [0, 1, 3, 7, 8], 3, cap=1)
+    assert res["miss_count"] == 2 and st["admitted"][0, 0] == 0
+    assert st["slot_chunk"][0, 0].tolist() == [3, 1, 7] and st["last_used"][0, 0].tolist() == [3, 3, 3]
+
+
+@pytest.mark.parametrize("S,cap", [(4, 2), (16, 3), (40, 100)])
+def test_residency_invariants_over_random_steps(S, cap):
+    rng = np.random.default_rng(23 + S)
+    B, Hkv, n_q, C, k, cs, d = 2, 2, 2, 48, 6, 2, 4
+    units = B * Hkv
+    Kh = enc(rng.standard_normal((B, Hkv, C * cs, d)))
+    Vh = enc(rng.standard_normal((B, Hkv, C * cs, d)))
+    rs = np.full((B, Hkv, C), -1, np.int32)
+    sc = np.full((B, Hkv, S), -1, np.int32)
+    lu = np.full((B, Hkv, S), -1, np.int32)
+    Khot = np.zeros((units * S, cs, d), np.uint16)
+    Vhot = np.zeros((units * S, cs, d), np.uint16)
+    hot_pref = rng.permutation(C)[:10]                       # temporal locality: a hot set picked often
+    for step_id in range(12):
+        sel = np.empty((B, n_q, Hkv, k), np.int32)
+        for idx in np.ndindex(B, n_q, Hkv):
+            pool = np.concatenate([hot_pref, rng.permutation(C)[:k]])
+            sel[idx] = np.sort(rng.choice(np.unique(pool), size=k, replace=False))
+        res = oracle.resolve_union(sel, rs)
+        Kst, Vst = oracle.gather_kv(Kh, Vh, res["miss_list"], cs)
+        new = oracle.update_residency(step_id, cap, res["union_idx"], res["union_slot"], res["union_cnt"], Kst, Vst,
+                                      rs, sc, lu, Khot, Vhot)
+        for u in range(units):
+            b, g = divmod(u, Hkv)
+            n = int(res["union_cnt"][b, g])
+            U = res["union_idx"][b, g, :n]
+            slots = res["union_slot"][b, g, :n]
+            n_miss = int((slots < 0).sum())
+            old_sc, new_sc = sc[b, g], new["slot_chunk"][b, g]
+            union_res = {int(s) - u * S for s in slots if s >= 0}
+            n_free = int((old_sc < 0).sum())
+            n_evictable = int(((old_sc >= 0) & ~np.isin(np.arange(S), list(union_res))).sum())
+            A = int(new["admitted"][b, g])
+            assert A == min(cap, n_miss, n_free + n_evictable)          # the cap bounds the traffic
+            for t in union_res:                                          # union residents stay, refreshed
+                assert new_sc[t] == old_sc[t] and new["last_used"][b, g, t] == step_id
+            admitted = set(U[slots < 0][:A].tolist())                    # lowest missing chunks first
+            assert admitted == {int(c) for c in new_sc if c >= 0} - {int(c) for c in old_sc if c >= 0}
+            evicted = [t for t in range(S) if old_sc[t] >= 0 and new_sc[t] != old_sc[t]]
+            kept = [t for t in range(S) if old_sc[t] >= 0 and new_sc[t] == old_sc[t] and t not in union_res]
+            assert len(evicted) == max(0, A - n_free)                    # free slots go first
+            for e in evicted:                                            # least recently used go first
+                for kk in kept:
+                    assert (lu[b, g, e], e) < (lu[b, g, kk], kk)
+            # maps stay inverse and every resident chunk's hot rows are its host rows
+            for t in range(S):
+                c = int(new_sc[t])
+                if c >= 0:
+                    assert new["resident_slot"][b, g, c] == u * S + t
+                    assert np.array_equal(new["Khot"][u * S + t], Kh[b, g, c * cs:(c + 1) * cs])
+                    assert np.array_equal(new["Vhot"][u * S + t], Vh[b, g, c * cs:(c + 1) * cs])
+            assert int((new["resident_slot"][b, g] >= 0).sum()) == int((new_sc >= 0).sum())
+        rs, sc, lu, Khot, Vhot = (new[x] for x in ("resident_slot", "slot_chunk", "last_used", "Khot", "Vhot"))
+
+
+def test_residency_repeated_selection_needs_no_transfer():
+    # delta selection: once admitted, a repeated selection resolves entirely in HBM
+    rng = np.random.default_rng(24)
+    B, Hkv, n_q, C, k, cs, d, S = 1, 2, 2, 32, 5, 2, 4, 12
+    Kh = enc(rng.standard_normal((B, Hkv, C * cs, d)))
+    sel = np.sort(rng.permuted(np.tile(np.arange(C, dtype=np.int32), (B, n_q, Hkv, 1)), axis=-1)[..., :k], axis=-1)
+    rs = np.full((B, Hkv, C), -1, np.int32)
+    state = (rs, np.full((B, Hkv, S), -1, np.int32), np.full((B, Hkv, S), -1, np.int32),
+             np.zeros((B * Hkv * S, cs, d), np.uint16), np.zeros((B * Hkv * S, cs, d), np.uint16))
+    res = oracle.resolve_union(sel, rs)
+    Kst, Vst = oracle.gather_kv(Kh, Kh, res["miss_list"], cs)
+    new = oracle.update_residency(0, S, res["union_idx"], res["union_slot"], res["union_cnt"], Kst, Vst, *state)
+    again = oracle.resolve_union(sel, new["resident_slot"])
+    assert res["miss_count"] == int(res["union_cnt"].sum()) and again["miss_count"] == 0
