@@ -153,12 +153,16 @@ dd_status dd_gather_kv(dd_ctx *ctx, const void *Kh, const void *Vh, const int32_
  * union_cnt, miss_count as written by dd_resolve_union.
  * out: fp32 [B,n_q,Hq,d], out[b,j,h] = sum_t softmax_t(scale*q.K_t) V_t over
  * the rows of the chunks whose qmask has bit j.  softmax_scale <= 0 selects
- * 1/sqrt(d). */
+ * 1/sqrt(d).  K_tail/V_tail (both NULL, or both given): bf16 [B,n_q,Hkv,d]
+ * device, the keys and values of the step's own n_q new tokens; query j then
+ * also attends to tail rows 0..j of its KV head (DualDecoder §5.2: the
+ * tokens of a step lie one after the other along the sequence under a
+ * causal mask; Adaptive DHiSparse Fig. 3 (4)). */
 dd_status dd_sparse_attn_decode(dd_ctx *ctx, const void *q, const void *Khot, const void *Vhot,
-                                const void *Kst, const void *Vst, const int32_t *union_slot,
-                                const uint8_t *union_qmask, const int32_t *union_cnt,
-                                const int32_t *miss_count, float softmax_scale, float *out,
-                                dd_stream_t stream);
+                                const void *Kst, const void *Vst, const void *K_tail, const void *V_tail,
+                                const int32_t *union_slot, const uint8_t *union_qmask,
+                                const int32_t *union_cnt, const int32_t *miss_count, float softmax_scale,
+                                float *out, dd_stream_t stream);
 
 /* Allocation-free variant of dd_sparse_attn_decode.  The pages have no
  * counterpart: it exists for callers that cannot allocate device memory --
@@ -211,9 +215,37 @@ typedef struct {
    * gather and attention */
   void *stage_events[6];
   dd_landmark_kind lm_kind;      /* DD_LM_MEAN (0) or DD_LM_MINMAX: how lm is laid out and scored */
+  const void *K_tail, *V_tail;   /* bf16 [B,n_q,Hkv,d] device or NULL: the step's own tokens (causal) */
 } dd_step_args;
 
 dd_status dd_step(dd_ctx *ctx, const dd_step_args *args, dd_stream_t stream);
+
+/* Residency update after a step: delta selection with capped LRU eviction
+ * (OasisKV summary, Methodology; Adaptive DHiSparse Fig. 3 (3): promoted rows
+ * are copied from the staging arena into the hot cache).  The hot pool of the
+ * context (hot_slots = B*Hkv*slots_per_unit, 1 <= slots_per_unit <= 4096) is
+ * split per (b,g) unit u: slots u*S .. u*S+S-1, S = slots_per_unit.  State
+ * (device, updated in place): resident_slot int32 [B,Hkv,C] (global slot or
+ * -1), slot_chunk int32 [B,Hkv,S] (chunk in the slot or -1 = free),
+ * last_used int32 [B,Hkv,S] (step the slot's chunk was last selected; -1 or
+ * a step >= 0), Khot/Vhot bf16 [hot_slots,cs,d].  Per unit, in order:
+ *   1. every resident chunk of the union gets last_used = step and is kept;
+ *   2. targets: free slots by ascending slot, then the other resident slots
+ *      by (last_used, slot) ascending;
+ *   3. the union's missing chunks in ascending chunk order take the first
+ *      A = min(cap, #misses, #targets) targets: the target's old chunk leaves
+ *      resident_slot, the new chunk enters it, and its rows are copied from
+ *      staging slot m (union_slot = -(m+1)) of Kst/Vst.
+ * union_idx / union_slot / union_cnt / miss_count are the step's resolver
+ * outputs (NULL: the context's workspace, i.e. the last dd_step or
+ * dd_resolve_union that used it); Kst/Vst the staging buffer that step
+ * gathered into.  admitted: int32 [B,Hkv] or NULL, A per unit.  At most
+ * cap*B*Hkv chunks are copied per call. */
+dd_status dd_update_residency(dd_ctx *ctx, int32_t step, int32_t cap, int32_t slots_per_unit,
+                              const int32_t *union_idx, const int32_t *union_slot, const int32_t *union_cnt,
+                              const int32_t *miss_count, const void *Kst, const void *Vst,
+                              int32_t *resident_slot, int32_t *slot_chunk, int32_t *last_used, void *Khot,
+                              void *Vhot, int32_t *admitted, dd_stream_t stream);
 
 /* Wait for the device, read the status word into *device_status (a dd_status
  * value) and clear it. */

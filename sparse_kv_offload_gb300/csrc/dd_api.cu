@@ -383,9 +383,11 @@ dd_status dd_gather_kv(dd_ctx *c, const void *Kh, const void *Vh, const int32_t 
 static dd_status attn_impl(dd_ctx *c, const void *q, const void *Khot, const void *Vhot, const void *Kst,
                            const void *Vst, const int32_t *union_slot, const uint8_t *union_qmask,
                            const int32_t *union_cnt, const int32_t *miss_count, float softmax_scale, float *out,
-                           bool plan_ready, const void *kh_dev, const void *vh_dev, dd_stream_t stream) {
+                           bool plan_ready, const void *kh_dev, const void *vh_dev, const void *k_tail,
+                           const void *v_tail, dd_stream_t stream) {
   if (!c) return DD_ERR_INVALID_ARG;
   if (c->units == 0) return DD_OK;
+  if ((k_tail == nullptr) != (v_tail == nullptr)) return DD_ERR_INVALID_ARG;
   if (!q || !union_slot || !union_qmask || !union_cnt || !miss_count || !out || !aligned16(q))
     return DD_ERR_INVALID_ARG;
   if (c->hot_slots > 0 && (!Khot || !Vhot || !aligned16(Khot) || !aligned16(Vhot))) return DD_ERR_INVALID_ARG;
@@ -396,20 +398,44 @@ static dd_status attn_impl(dd_ctx *c, const void *q, const void *Khot, const voi
   const dd::AttnScratch scr = {c->part_o, c->part_ml, c->chunk_off, c->cta_tab, c->flat, c->dummy_pool};
   return cuda_ok(dd::launch_attn(q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count, scale, out,
                                  c->plan, scr, plan_ready, kh_dev, vh_dev, c->status, d.B, d.n_q, d.Hq, d.Hkv, d.cs,
-                                 c->umax, c->hot_slots, c->max_misses, (cudaStream_t)stream));
+                                 c->umax, c->hot_slots, c->max_misses, (cudaStream_t)stream, k_tail, v_tail));
 }
 
 dd_status dd_sparse_attn_decode(dd_ctx *c, const void *q, const void *Khot, const void *Vhot, const void *Kst,
-                                const void *Vst, const int32_t *union_slot, const uint8_t *union_qmask,
-                                const int32_t *union_cnt, const int32_t *miss_count, float softmax_scale, float *out,
-                                dd_stream_t stream) {
+                                const void *Vst, const void *K_tail, const void *V_tail, const int32_t *union_slot,
+                                const uint8_t *union_qmask, const int32_t *union_cnt, const int32_t *miss_count,
+                                float softmax_scale, float *out, dd_stream_t stream) {
   return attn_impl(c, q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count, softmax_scale, out,
-                   false, nullptr, nullptr, stream);
+                   false, nullptr, nullptr, K_tail, V_tail, stream);
+}
+
+dd_status dd_update_residency(dd_ctx *c, int32_t step, int32_t cap, int32_t slots_per_unit,
+                              const int32_t *union_idx, const int32_t *union_slot, const int32_t *union_cnt,
+                              const int32_t *miss_count, const void *Kst, const void *Vst, int32_t *resident_slot,
+                              int32_t *slot_chunk, int32_t *last_used, void *Khot, void *Vhot, int32_t *admitted,
+                              dd_stream_t stream) {
+  if (!c || step < 0 || cap < 0 || slots_per_unit < 1 || slots_per_unit > 4096) return DD_ERR_INVALID_ARG;
+  if (c->units == 0) return DD_OK;
+  if ((int64_t)c->units * slots_per_unit != c->hot_slots) return DD_ERR_INVALID_ARG;
+  if (!resident_slot || !slot_chunk || !last_used || !Khot || !Vhot || !aligned16(Khot) || !aligned16(Vhot))
+    return DD_ERR_INVALID_ARG;
+  if (c->max_misses > 0 && (!Kst || !Vst || !aligned16(Kst) || !aligned16(Vst))) return DD_ERR_INVALID_ARG;
+  if (!union_idx) union_idx = c->union_idx;
+  if (!union_slot) union_slot = c->union_slot;
+  if (!union_cnt) union_cnt = c->union_cnt;
+  if (!miss_count) miss_count = c->miss_count;
+  c->launches += 1;
+  return cuda_ok(dd::launch_update_residency(
+      step, cap, slots_per_unit, c->units, union_idx, union_slot, union_cnt, miss_count, c->max_misses,
+      static_cast<const uint4 *>(Kst), static_cast<const uint4 *>(Vst), resident_slot, slot_chunk, last_used,
+      static_cast<uint4 *>(Khot), static_cast<uint4 *>(Vhot), admitted, c->C, c->umax, c->dims.cs, c->status,
+      (cudaStream_t)stream));
 }
 
 dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   if (!c || !a || a->layer < 0) return DD_ERR_INVALID_ARG;
   if (a->lm_kind != DD_LM_MEAN && a->lm_kind != DD_LM_MINMAX) return DD_ERR_INVALID_ARG;
+  if ((a->K_tail == nullptr) != (a->V_tail == nullptr)) return DD_ERR_INVALID_ARG;
   if (c->units == 0) return DD_OK;
   if (!a->q || !a->lm || !a->Kh || !a->Vh || !a->resident_slot || !a->out) return DD_ERR_INVALID_ARG;
   const int p = a->layer & 1;
@@ -455,7 +481,7 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   // memcpy mode: dd_gather_kv made this stream wait for the copy stream
   DD_TRY(mark(4));
   DD_TRY(attn_impl(c, a->q, a->Khot, a->Vhot, a->Kst[p], a->Vst[p], union_slot, union_qmask, union_cnt, miss_count,
-                   a->softmax_scale, a->out, true, kh_dev, vh_dev, stream));
+                   a->softmax_scale, a->out, true, kh_dev, vh_dev, a->K_tail, a->V_tail, stream));
   DD_TRY(mark(5));
   DD_CUDA(cudaEventRecord(c->released[p], s));
   c->released_on[p] = s;

@@ -616,44 +616,83 @@ __global__ void __launch_bounds__(kPlanThreads) k_attn_plan(
 
 // --------------------------------------------------------------- combine
 // One CTA per (unit, query vector): merges the partials of every warp of
-// every CTA whose slice covered part of the unit's union.
+// every CTA whose slice covered part of the unit's union, then, when the
+// step's own tokens are given, their tail rows: query j of the unit also
+// attends to the new rows of tokens 0..j (DualDecoder §5.2: the tokens of a
+// step follow one another along the sequence under a causal mask).
 __global__ void __launch_bounds__(128) k_attn_combine(const float *__restrict__ part_o,
                                                       const float *__restrict__ part_ml,
                                                       const int32_t *__restrict__ chunk_off,
                                                       const int4 *__restrict__ cta_tab, float *__restrict__ out,
                                                       const int32_t *status, int n_q, int Hq, int Hkv, int NQ,
-                                                      int wpm) {
+                                                      int wpm, const uint16_t *__restrict__ q,
+                                                      const uint16_t *__restrict__ k_tail,
+                                                      const uint16_t *__restrict__ v_tail, float scale_log2) {
+  __shared__ float red[4][kMaxNq];
   pdl_wait();
   pdl_trigger();
   if (load_status(status) != 0) return;
   const int unit = blockIdx.x, qv = blockIdx.y, col = threadIdx.x;
   const int off = chunk_off[unit], U = chunk_off[unit + 1] - off, per = cta_tab[0].w;
-  if (U <= 0 || per <= 0) return;
-  const int c0 = off / per, c1 = (off + U - 1) / per;
-  const int n = (c1 - c0 + 1) * wpm;   // partials: (CTA c0 + i / wpm, warp i % wpm)
+  const bool tail = k_tail != nullptr;
+  if ((U <= 0 || per <= 0) && !tail) return;
+  const int G = Hq / Hkv, b = unit / Hkv, g = unit - b * Hkv, j = qv / G, h = g * G + (qv - j * G);
   float M = -INFINITY, L = 0.f, acc = 0.f;
-  for (int ib = 0; ib < n; ib += 4) {
-    float ms[4], ls[4], os[4];
+  if (U > 0 && per > 0) {
+    const int c0 = off / per, c1 = (off + U - 1) / per;
+    const int n = (c1 - c0 + 1) * wpm;   // partials: (CTA c0 + i / wpm, warp i % wpm)
+    for (int ib = 0; ib < n; ib += 4) {
+      float ms[4], ls[4], os[4];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int i = ib + t;
-      const int64_t k = (((int64_t)c0 + i / wpm + unit) * wpm + i % wpm) * NQ + qv;
-      const bool ok = i < n;
-      ms[t] = ok ? part_ml[k * 2] : -INFINITY;
-      ls[t] = ok ? part_ml[k * 2 + 1] : 0.f;
-      os[t] = ok ? part_o[k * 128 + col] : 0.f;
+      for (int t = 0; t < 4; ++t) {
+        const int i = ib + t;
+        const int64_t k = (((int64_t)c0 + i / wpm + unit) * wpm + i % wpm) * NQ + qv;
+        const bool ok = i < n;
+        ms[t] = ok ? part_ml[k * 2] : -INFINITY;
+        ls[t] = ok ? part_ml[k * 2 + 1] : 0.f;
+        os[t] = ok ? part_o[k * 128 + col] : 0.f;
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (ms[t] == -INFINITY) continue;
+        const float Mn = fmaxf(M, ms[t]);
+        const float a = M == -INFINITY ? 0.f : exp2f(M - Mn), w = exp2f(ms[t] - Mn);
+        L = L * a + w * ls[t];
+        acc = acc * a + w * os[t];
+        M = Mn;
+      }
     }
+  }
+  if (tail) {
+    // logits of tail rows 0..j: 128-lane dot products, reduced per warp, then across the 4 warps
+    const int lane = col & 31, warp = col >> 5;
+    const float qc = __uint_as_float((uint32_t)q[((int64_t)(b * n_q + j) * Hq + h) * 128 + col] << 16);
+    float z[kMaxNq];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      if (ms[t] == -INFINITY) continue;
-      const float Mn = fmaxf(M, ms[t]);
-      const float a = M == -INFINITY ? 0.f : exp2f(M - Mn), w = exp2f(ms[t] - Mn);
-      L = L * a + w * ls[t];
-      acc = acc * a + w * os[t];
+    for (int t = 0; t < kMaxNq; ++t) {
+      float x = 0.f;
+      if (t <= j) x = qc * __uint_as_float((uint32_t)k_tail[((int64_t)(b * n_q + t) * Hkv + g) * 128 + col] << 16);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      z[t] = x;
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int t = 0; t < kMaxNq; ++t) red[warp][t] = z[t];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < kMaxNq; ++t) {
+      if (t > j) break;
+      const float s2 = (red[0][t] + red[1][t] + red[2][t] + red[3][t]) * scale_log2;
+      const float vt = __uint_as_float((uint32_t)v_tail[((int64_t)(b * n_q + t) * Hkv + g) * 128 + col] << 16);
+      const float Mn = fmaxf(M, s2);
+      const float a = M == -INFINITY ? 0.f : exp2f(M - Mn), w = exp2f(s2 - Mn);
+      L = L * a + w;
+      acc = acc * a + w * vt;
       M = Mn;
     }
   }
-  const int G = Hq / Hkv, b = unit / Hkv, g = unit - b * Hkv, j = qv / G, h = g * G + (qv - j * G);
   out[((int64_t)(b * n_q + j) * Hq + h) * 128 + col] = L > 0.f ? acc / L : 0.f;
 }
 
@@ -725,7 +764,7 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
                         const int32_t *miss_count, float softmax_scale, float *out, const AttnPlan &plan,
                         const AttnScratch &scr, bool plan_ready, const void *kh_dev, const void *vh_dev,
                         int32_t *status, int B, int n_q, int Hq, int Hkv, int cs, int umax, int64_t hot_slots,
-                        int64_t max_misses, cudaStream_t s) {
+                        int64_t max_misses, cudaStream_t s, const void *k_tail, const void *v_tail) {
   const int units = B * Hkv;
   if (units == 0) return cudaSuccess;
   const int G = Hq / Hkv, NQ = n_q * G;
@@ -777,8 +816,11 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
+  const bool tail = k_tail && v_tail;
   return launch_k(k_attn_combine, dim3(units, NQ), dim3(128), 0, s, scr.part_o, scr.part_ml, scr.chunk_off,
-                  scr.cta_tab, out, status, n_q, Hq, Hkv, NQ, sh.wpm);
+                  scr.cta_tab, out, status, n_q, Hq, Hkv, NQ, sh.wpm, static_cast<const uint16_t *>(q),
+                  tail ? static_cast<const uint16_t *>(k_tail) : nullptr,
+                  tail ? static_cast<const uint16_t *>(v_tail) : nullptr, p.scale_log2);
 }
 
 }  // namespace dd

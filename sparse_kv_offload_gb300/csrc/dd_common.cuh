@@ -211,7 +211,13 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
                         const int32_t *miss_count, float softmax_scale, float *out, const AttnPlan &plan,
                         const AttnScratch &scr, bool plan_ready, const void *kh_dev, const void *vh_dev,
                         int32_t *status, int B, int n_q, int Hq, int Hkv, int cs, int umax, int64_t hot_slots,
-                        int64_t max_misses, cudaStream_t s);
+                        int64_t max_misses, cudaStream_t s, const void *k_tail = nullptr,
+                        const void *v_tail = nullptr);
+cudaError_t launch_update_residency(int32_t step, int32_t cap, int S, int units, const int32_t *union_idx,
+                                    const int32_t *union_slot, const int32_t *union_cnt, const int32_t *miss_count,
+                                    int64_t max_misses, const uint4 *Kst, const uint4 *Vst, int32_t *resident_slot,
+                                    int32_t *slot_chunk, int32_t *last_used, uint4 *Khot, uint4 *Vhot,
+                                    int32_t *admitted, int C, int umax, int cs, int32_t *status, cudaStream_t s);
 cudaError_t launch_gather(const uint4 *Kh, const uint4 *Vh, const int32_t *miss_list,
                           const int32_t *miss_count, uint4 *Kst, uint4 *Vst, int64_t max_misses,
                           int64_t n_chunks_total, int cs, int32_t *status, int sm_count, cudaStream_t s);

@@ -26,7 +26,7 @@ EXPORTED = (
     "dd_create", "dd_destroy", "dd_build_landmarks", "dd_score_landmarks", "dd_select_topk",
     "dd_resolve_union", "dd_gather_kv", "dd_sparse_attn_decode", "dd_step", "dd_get_status",
     "dd_launch_count", "dd_status_str", "dd_last_cuda_error", "dd_synth_kv", "dd_synth_queries", "dd_sparse_attn_decode_noalloc",
-    "dd_build_landmarks_minmax", "dd_score_landmarks_minmax",
+    "dd_build_landmarks_minmax", "dd_score_landmarks_minmax", "dd_update_residency",
 )
 
 
@@ -55,6 +55,8 @@ class StepArgs(ctypes.Structure):
         ("miss_list", _vp), ("miss_count", _vp), ("attn_slot", _vp), ("union_qmask", _vp),
         ("stage_events", _vp * 6),
         ("lm_kind", ctypes.c_int),
+        ("K_tail", _vp),
+        ("V_tail", _vp),
     ]
 
 
@@ -73,8 +75,9 @@ def _load():
         "dd_select_topk": (i32, [_vp, _vp, _vp, _vp]),
         "dd_resolve_union": (i32, [_vp] * 11),
         "dd_gather_kv": (i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp]),
-        "dd_sparse_attn_decode": (i32, [_vp] * 10 + [f32, _vp, _vp]),
+        "dd_sparse_attn_decode": (i32, [_vp] * 12 + [f32, _vp, _vp]),
         "dd_step": (i32, [_vp, ctypes.POINTER(StepArgs), _vp]),
+        "dd_update_residency": (i32, [_vp, i32, i32, i32] + [_vp] * 13),
         "dd_get_status": (i32, [_vp, ctypes.POINTER(i32)]),
         "dd_launch_count": (i64, [_vp]),
         "dd_status_str": (ctypes.c_char_p, [i32]),
@@ -248,26 +251,54 @@ class Context:
             _stream(stream)), "dd_gather_kv")
 
     def sparse_attn_decode(self, q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count, out,
-                           softmax_scale=0.0, stream=None):
+                           softmax_scale=0.0, stream=None, K_tail=None, V_tail=None):
         s = self.shape
         nh = self.hot_slots * s.cs * s.d
         ns = self.max_misses * s.cs * s.d
         nu = s.B * s.Hkv * s.umax
+        nt = s.B * s.n_q * s.Hkv * s.d
         _chk(_lib.dd_sparse_attn_decode(
             self._h, _ptr(q, torch.bfloat16, s.B * s.n_q * s.Hq * s.d, name="q"),
             _ptr(Khot, torch.bfloat16, nh, name="Khot", allow_none=True),
             _ptr(Vhot, torch.bfloat16, nh, name="Vhot", allow_none=True),
             _ptr(Kst, torch.bfloat16, ns, name="Kst", allow_none=True),
             _ptr(Vst, torch.bfloat16, ns, name="Vst", allow_none=True),
+            _ptr(K_tail, torch.bfloat16, nt, name="K_tail", allow_none=True),
+            _ptr(V_tail, torch.bfloat16, nt, name="V_tail", allow_none=True),
             _ptr(union_slot, torch.int32, nu, name="union_slot"), _ptr(union_qmask, torch.uint8, nu, name="union_qmask"),
             _ptr(union_cnt, torch.int32, s.B * s.Hkv, name="union_cnt"),
             _ptr(miss_count, torch.int32, 1, name="miss_count"), float(softmax_scale),
             _ptr(out, torch.float32, s.B * s.n_q * s.Hq * s.d, name="out"), _stream(stream)),
             "dd_sparse_attn_decode")
 
+    def update_residency(self, step, cap, slots_per_unit, Kst, Vst, resident_slot, slot_chunk, last_used, Khot,
+                         Vhot, admitted=None, union_idx=None, union_slot=None, union_cnt=None, miss_count=None,
+                         stream=None):
+        """Capped LRU residency update after a step (see dd.h); the union arrays default
+        to the context's workspace (the last step that used it)."""
+        s = self.shape
+        units = s.B * s.Hkv
+        nu = units * s.umax
+        nh = self.hot_slots * s.cs * s.d
+        ns = self.max_misses * s.cs * s.d
+        _chk(_lib.dd_update_residency(
+            self._h, int(step), int(cap), int(slots_per_unit),
+            _ptr(union_idx, torch.int32, nu, name="union_idx", allow_none=True),
+            _ptr(union_slot, torch.int32, nu, name="union_slot", allow_none=True),
+            _ptr(union_cnt, torch.int32, units, name="union_cnt", allow_none=True),
+            _ptr(miss_count, torch.int32, 1, name="miss_count", allow_none=True),
+            _ptr(Kst, torch.bfloat16, ns, name="Kst", allow_none=True),
+            _ptr(Vst, torch.bfloat16, ns, name="Vst", allow_none=True),
+            _ptr(resident_slot, torch.int32, units * s.C, name="resident_slot"),
+            _ptr(slot_chunk, torch.int32, units * slots_per_unit, name="slot_chunk"),
+            _ptr(last_used, torch.int32, units * slots_per_unit, name="last_used"),
+            _ptr(Khot, torch.bfloat16, nh, name="Khot"), _ptr(Vhot, torch.bfloat16, nh, name="Vhot"),
+            _ptr(admitted, torch.int32, units, name="admitted", allow_none=True), _stream(stream)),
+            "dd_update_residency")
+
     def step(self, layer, q, lm, Kh, Vh, resident_slot, Khot, Vhot, Kst_pair, Vst_pair, out,
              mode=GATHER_ZEROCOPY, softmax_scale=0.0, intermediates=None, stage_events=None, stream=None,
-             lm_kind=LM_MEAN):
+             lm_kind=LM_MEAN, K_tail=None, V_tail=None):
         """One layer; ``intermediates`` optionally maps names of dd_step_args' optional
         outputs (scores, sel, union_idx, union_slot, union_qmask, union_cnt, miss_list,
         miss_count, attn_slot) to caller tensors; ``stage_events`` optionally gives six
@@ -278,6 +309,8 @@ class Context:
         a.layer = int(layer)
         a.q = _ptr(q, torch.bfloat16, s.B * s.n_q * s.Hq * s.d, name="q")
         a.lm_kind = int(lm_kind)
+        a.K_tail = _ptr(K_tail, torch.bfloat16, s.B * s.n_q * s.Hkv * s.d, name="K_tail", allow_none=True)
+        a.V_tail = _ptr(V_tail, torch.bfloat16, s.B * s.n_q * s.Hkv * s.d, name="V_tail", allow_none=True)
         a.lm = _ptr(lm, torch.bfloat16, s.B * s.Hkv * s.C * s.d * (2 if lm_kind == LM_MINMAX else 1), name="lm")
         n = s.B * s.Hkv * s.L * s.d
         a.Kh = _ptr(Kh, torch.bfloat16, n, device=False, name="Kh")
