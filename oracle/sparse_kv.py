@@ -24,6 +24,7 @@ __all__ = [
     "resolve_union", "gather_kv", "sparse_attn_decode", "step", "kv_footprint_bytes",
     "max_batch", "per_step_budget_bytes", "union_of_query_selections",
     "build_minmax_landmarks", "score_minmax_landmarks", "bf16_total_order_key", "update_residency",
+    "prefetch_kv",
 ]
 
 
@@ -325,6 +326,42 @@ def sparse_attn_decode(q, Khot, Vhot, Kst, Vst, attn_slot, cs: int, scale: float
                     p /= p.sum()
                     out[b, j, h] = p @ Vr
     return out
+
+
+# ---------------------------------------------------------------------------
+# ahead of a step: predictive prefetch into the layer's transfer buffer
+# ---------------------------------------------------------------------------
+
+def prefetch_kv(sel_pred: np.ndarray, Kh: np.ndarray, Vh: np.ndarray, cs: int) -> dict:
+    """Fetch the chunks of a predicted selection ahead of the step that needs them.
+
+    DualDecoder §4.1-§4.2: the selection computed from the speculative token
+    of step i predicts the one the real token needs at step i+1, so its
+    chunks can be fetched before they are consumed; §5.3: for a layer the
+    prefetch runs ahead of its attention, and chunks the true selection needs
+    but the prediction missed are fetched urgently; §5.4: prefetched entries
+    sit in temporary slots of the layer's transfer buffer until the true
+    index is resolved.  The attention result does not depend on the
+    prediction.
+
+    Readings: per (b, g) unit the predicted chunks are the union of the
+    predicted rows ``sel_pred`` [B, n_pred, Hkv, k]; they take dense slots
+    m in (b, g, c) order, the same layout as the step's misses (so the
+    prefetch is the resolver and the gather run on the predicted selection
+    with nothing resident).  Returns ``pf_map`` [B, Hkv, C] (slot of each
+    prefetched chunk, -1 elsewhere), the rows ``K``, ``V`` [P, cs, d] and
+    ``count`` P.  The step that consumes the prefetch resolves its true
+    selection against ``pf_map`` as if it were the resident map, with the
+    prefetched rows as the pool.
+    """
+    B, Hkv, L, d = Kh.shape
+    C = L // cs
+    res = resolve_union(sel_pred, np.full((B, Hkv, C), -1, np.int32))
+    K, V = gather_kv(Kh, Vh, res["miss_list"], cs)
+    pf_map = np.full(B * Hkv * C, -1, np.int32)
+    for m, packed in enumerate(res["miss_list"].tolist()):
+        pf_map[packed] = m
+    return {"pf_map": pf_map.reshape(B, Hkv, C), "K": K, "V": V, "count": res["miss_count"]}
 
 
 # ---------------------------------------------------------------------------

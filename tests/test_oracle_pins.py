@@ -589,3 +589,39 @@ def test_residency_repeated_selection_needs_no_transfer():
     new = oracle.update_residency(0, S, res["union_idx"], res["union_slot"], res["union_cnt"], Kst, Vst, *state)
     again = oracle.resolve_union(sel, new["resident_slot"])
     assert res["miss_count"] == int(res["union_cnt"].sum()) and again["miss_count"] == 0
+
+
+# ---------------------------------------------------------------- predictive prefetch
+
+@pytest.mark.parametrize("overlap", [1.0, 0.6, 0.0])
+def test_prefetch_changes_no_output_and_leaves_only_unpredicted_misses(overlap):
+    # the prediction only moves transfers ahead of time: the step's output is the
+    # output without prefetch, and the urgent misses are the true union minus the predicted one
+    rng = np.random.default_rng(31)
+    B, n_q, Hq, Hkv, L, d, cs, k = 2, 2, 4, 2, 256, 128, 16, 5
+    C = L // cs
+    q = enc(rng.standard_normal((B, n_q, Hq, d)))
+    Kh = enc(rng.standard_normal((B, Hkv, L, d)))
+    Vh = enc(rng.standard_normal((B, Hkv, L, d)))
+    lm = oracle.build_landmarks(Kh, cs)
+    true_sel = oracle.select_topk(oracle.score_landmarks(q, lm), k)
+    pred = np.empty((B, 1, Hkv, k), np.int32)
+    for b, g in np.ndindex(B, Hkv):
+        keep = int(round(overlap * k))
+        own = list(true_sel[b, 0, g][:keep])
+        rest = [c for c in rng.permutation(C) if c not in set(true_sel[b, 0, g])][:k - keep]
+        pred[b, 0, g] = np.sort(np.array(own + rest, np.int32))
+    pf = oracle.prefetch_kv(pred, Kh, Vh, cs)
+    assert pf["count"] == sum(len(set(pred[b, 0, g])) for b, g in np.ndindex(B, Hkv))
+    for b, g, c in np.ndindex(B, Hkv, C):              # the map points at the chunk's host rows
+        m = pf["pf_map"][b, g, c]
+        assert (m >= 0) == (c in set(pred[b, 0, g]))
+        if m >= 0:
+            assert np.array_equal(pf["K"][m], Kh[b, g, c * cs:(c + 1) * cs])
+            assert np.array_equal(pf["V"][m], Vh[b, g, c * cs:(c + 1) * cs])
+    plain = oracle.step(q, lm, Kh, Vh, np.full((B, Hkv, C), -1, np.int32), None, None, k, cs)
+    with_pf = oracle.step(q, lm, Kh, Vh, pf["pf_map"], pf["K"], pf["V"], k, cs)
+    np.testing.assert_allclose(with_pf["out"], plain["out"], rtol=1e-12, atol=1e-14)
+    urgent = sum(len(set(oracle.union_of_query_selections(true_sel, b, g)) - set(pred[b, 0, g]))
+                 for b, g in np.ndindex(B, Hkv))
+    assert with_pf["miss_count"] == urgent
