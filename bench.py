@@ -513,6 +513,171 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+# ------------------------------------------------------------------ pipelined decode (predictive prefetch)
+DRIFT_T, SIGMA_DRIFT, SIGMA_SPEC = 8, 0.3, 0.1
+
+
+def run_pipeline(args, world, rank, local):
+    """Decode steps over N_LAYERS layers whose queries drift from step to step,
+    with the speculative rows of each layer's selection prefetched for its next
+    step: after layer l's attention, a low-priority stream fetches the predicted
+    chunks of layer l+2 into the transfer half of the staging buffer that layer
+    l has just released (same parity), while the high-priority stream runs the
+    next layers; each step resolves its true selection against the prefetch map
+    and fetches only the chunks the prediction missed (urgent, inside the
+    attention kernel).  The same drifting steps are also timed without prefetch."""
+    import torch
+    torch.cuda.set_device(local)
+    from sparse_kv_offload_gb300 import build
+    build.build()
+    from sparse_kv_offload_gb300 import dd
+    w = BY_NAME[args.workload]
+    shape = dd.Shape(w.B, w.Hq, w.Hkv, w.d, w.L, w.cs, w.k, w.n_q)
+    N, T, units = N_LAYERS, DRIFT_T, w.B * w.Hkv
+    if w.n_q < 2:
+        raise SystemExit("the pipelined mode predicts from speculative queries: n_q >= 2")
+    layers = [LayerData(dd, shape, w, l, rank) for l in range(N)]
+    seed = rank_seed(w.seed, rank)
+    qs = []
+    for l in range(N):
+        qh = synth.drift_queries(seed, w.B, w.n_q, w.Hq, w.d, T, SIGMA_DRIFT, SIGMA_SPEC, layer=l)
+        qs.append(torch.from_numpy(qh.reshape(T, -1).view(np.int16)).view(torch.bfloat16).cuda())
+    cap = w.max_misses
+    ctx_hi = dd.Context(shape, max_misses=cap, hot_slots=cap)
+    ctx_lo = dd.Context(shape, max_misses=cap)
+    touch = torch.empty(w.B * w.Hkv * w.C * w.d, dtype=torch.bfloat16, device="cuda")
+    for L_ in layers:
+        ctx_hi.build_landmarks(L_.Kh, L_.lm)
+        ctx_hi.build_landmarks(L_.Vh, touch)
+    del touch
+    ns = cap * w.cs * w.d
+    Kpf = [torch.empty(ns, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    Vpf = [torch.empty(ns, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    Kurg = [torch.empty(ns, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    Vurg = [torch.empty(ns, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    pf_map = [torch.full((units * w.C,), -1, dtype=torch.int32, device="cuda") for _ in range(2)]
+    none_res = torch.full((units * w.C,), -1, dtype=torch.int32, device="cuda")
+    sel_store = [torch.empty(w.B * w.n_q * w.Hkv * w.k, dtype=torch.int32, device="cuda") for _ in range(N)]
+    out = torch.empty(w.B * w.n_q * w.Hq * w.d, dtype=torch.float32, device="cuda")
+    K = args.steps
+    miss = torch.zeros(K * N, dtype=torch.int32, device="cuda")
+    ucnt = torch.zeros(K * N, units, dtype=torch.int32, device="cuda")
+    pfc = torch.zeros(K * N, dtype=torch.int32, device="cuda")
+    hi = torch.cuda.Stream(priority=-1)
+    lo = torch.cuda.Stream(priority=0)
+    ev_step = [torch.cuda.Event() for _ in range(N)]
+    ev_pf = [torch.cuda.Event() for _ in range(N)]
+    torch.cuda.synchronize()
+    link_memcpy, _ = host_link_peaks(dd, shape)
+
+    def q_of(i, l):
+        return qs[l][i % T]
+
+    n_rec = [0]
+
+    def prefetch(t, p, record=False):
+        count = None
+        if record and n_rec[0] < pfc.numel():
+            count = pfc[n_rec[0]:n_rec[0] + 1]
+            n_rec[0] += 1
+        L_ = layers[t]
+        ctx_lo.prefetch_kv(sel_store[t], w.n_q - 1, L_.Kh, L_.Vh, Kpf[p], Vpf[p], pf_map[p], pf_count=count,
+                           ctas_per_sm=2, stream=lo, sel_rows=w.n_q, first_row=1)
+        ev_pf[t].record(lo)
+
+    def pipelined(i, rec=None):
+        for l in range(N):
+            p, L_ = l & 1, layers[l]
+            hi.wait_event(ev_pf[l])
+            inter = {"sel": sel_store[l]}
+            if rec is not None:
+                inter.update(miss_count=miss[rec * N + l:rec * N + l + 1], union_cnt=ucnt[rec * N + l])
+            ctx_hi.step(i * N + l, q_of(i, l), L_.lm, L_.Kh, L_.Vh, pf_map[p], Kpf[p], Vpf[p], Kurg, Vurg, out,
+                        intermediates=inter, stream=hi)
+            ev_step[l].record(hi)
+            t = (l + 2) % N
+            lo.wait_event(ev_step[l])
+            prefetch(t, p, record=rec is not None)
+
+    def serialized(i):
+        for l in range(N):
+            L_ = layers[l]
+            ctx_hi.step(i * N + l, q_of(i, l), L_.lm, L_.Kh, L_.Vh, none_res, Kpf[0], Vpf[0], Kurg, Vurg, out,
+                        stream=hi)
+
+    # prime: one step of every layer without prediction fills the selections, then the
+    # prefetches of layers 0 and 1 for the first pipelined step
+    with torch.cuda.stream(hi):
+        for l in range(N):
+            L_ = layers[l]
+            ctx_hi.step(l, q_of(T - 1, l), L_.lm, L_.Kh, L_.Vh, none_res, Kpf[0], Vpf[0], Kurg, Vurg, out,
+                        intermediates={"sel": sel_store[l]}, stream=hi)
+            ev_step[l].record(hi)
+        for t in (0, 1):
+            lo.wait_event(ev_step[N - 1])
+            prefetch(t, t)
+    for i in range(args.warmup):
+        pipelined(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(hi)
+    for i in range(K):
+        pipelined(args.warmup + i, rec=i)
+    lo_done = torch.cuda.Event()
+    lo_done.record(lo)
+    hi.wait_event(lo_done)
+    b.record(hi)
+    torch.cuda.synchronize()
+    t_pipe = a.elapsed_time(b) * 1e-3
+    st_hi, st_lo = ctx_hi.status(), ctx_lo.status()
+    if st_hi or st_lo:
+        raise RuntimeError(f"device status after the pipelined steps: {dd.status_str(st_hi or st_lo)}")
+
+    # the same drifting steps, serialized, nothing prefetched
+    for i in range(args.warmup):
+        serialized(i)
+    torch.cuda.synchronize()
+    a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a2.record(hi)
+    for i in range(K):
+        serialized(args.warmup + i)
+    b2.record(hi)
+    torch.cuda.synchronize()
+    t_ser = a2.elapsed_time(b2) * 1e-3
+    assert ctx_hi.status() == 0
+    ctx_hi.close()
+    ctx_lo.close()
+    t_max = max_over_ranks(t_pipe, world)
+    U = ucnt.double().sum(1).mean().item()
+    M = miss.double().mean().item()
+    P = pfc[:max(1, n_rec[0])].double().mean().item()
+    chunk_b = 2 * w.cs * w.d * 2
+    if rank != 0:
+        return 0
+    steps = K * N
+    line = {
+        "metric": METRIC + " (pipelined, predictive prefetch)", "value": world * steps / t_max, "unit": UNIT,
+        "n_gpus": world, "steps": steps, "warmup": args.warmup * N, "ms_per_step": 1e3 * t_max / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(config_of(w, "zerocopy", world), workload=w.name + "_drift_pipelined", layers=N,
+                       queries=f"real query of step t = base + {SIGMA_DRIFT} N(0,1), cyclic over {T} steps; "
+                               f"speculative queries of step t = real query of step t+1 + {SIGMA_SPEC} N(0,1)",
+                       prefetch="rows 1..n_q-1 of each layer's selection, for its next step, issued after the "
+                                "attention of layer l-2 on a low-priority stream (2 CTAs/SM)"),
+        "per_layer_step": {"true_union_chunks": U, "urgent_chunks": M, "prefetched_chunks": P,
+                           "prediction_hit_rate": 1.0 - M / U if U else None,
+                           "urgent_bytes": M * chunk_b, "prefetch_bytes": P * chunk_b,
+                           "host_link_gbs": (M + P) * chunk_b * steps / t_pipe / 1e9},
+        "serialized_same_steps": {"value": steps / t_ser, "unit": UNIT, "ms_per_step": 1e3 * t_ser / steps},
+        "host_link_peaks_gbs": {"memcpy_h2d": link_memcpy},
+        "e2e": None,
+        "gpu_launches": None,
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -523,12 +688,16 @@ def main():
     ap.add_argument("--mode", choices=("zerocopy", "memcpy"), default="zerocopy")
     ap.add_argument("--landmarks", choices=("mean", "minmax"), default="mean")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pipeline", action="store_true",
+                    help="decode steps over several layers with drifting queries and predictive prefetch")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":
             return run_reference(args, world, rank)
+        if args.pipeline:
+            return run_pipeline(args, world, rank, local)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:

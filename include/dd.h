@@ -220,6 +220,32 @@ typedef struct {
 
 dd_status dd_step(dd_ctx *ctx, const dd_step_args *args, dd_stream_t stream);
 
+/* Predictive prefetch of a layer's predicted selection into its transfer
+ * buffer (DualDecoder §4.1-§4.2: the selection computed from the speculative
+ * token of step i predicts the one the real token needs at step i+1; §5.3:
+ * the layer's prefetch runs ahead of its attention on a low-priority stream
+ * and the chunks the prediction missed are fetched urgently by the step;
+ * §5.4: prefetched entries wait in temporary slots of the layer's buffer).
+ * sel: int32 [B,sel_rows,Hkv,k] device, ascending rows; rows first_row ..
+ * first_row+n_pred-1 of each request are the prediction, 1 <= n_pred <= n_q
+ * (e.g. the speculative rows j = 1..n_q-1 of the previous step's sel:
+ * sel_rows = n_q, first_row = 1).
+ * The union of the predicted rows of each (b,g) takes dense slots m in
+ * (b,g,c) order; chunk c of unit (b,g) is copied from the pinned host K/V
+ * (bf16 [B,Hkv,L,d]) into Kpf/Vpf[m] (bf16 [max_misses,cs,d] device) and
+ * pf_map[b,g,c] (int32 [B,Hkv,C] device) = m, -1 for chunks not predicted.
+ * pf_count (int32[1] device or NULL) = the number of predicted chunks; more
+ * than max_misses raises DD_ERR_CAPACITY and nothing is copied.
+ * ctas_per_sm (1..8, other values 8) caps the copy kernel's residency so it
+ * leaves room on the SMs for a step running concurrently.  The consuming
+ * dd_step passes pf_map as resident_slot and Kpf/Vpf as its hot pool
+ * (hot_slots = this context's max_misses).  The prefetch uses the
+ * context's resolver workspace: run it on its own context when it overlaps
+ * a step on another stream. */
+dd_status dd_prefetch_kv(dd_ctx *ctx, const int32_t *sel, int32_t sel_rows, int32_t first_row, int32_t n_pred,
+                         const void *Kh, const void *Vh, void *Kpf, void *Vpf, int32_t *pf_map, int32_t *pf_count,
+                         int32_t ctas_per_sm, dd_stream_t stream);
+
 /* Residency update after a step: delta selection with capped LRU eviction
  * (OasisKV summary, Methodology; Adaptive DHiSparse Fig. 3 (3): promoted rows
  * are copied from the staging arena into the hot cache).  The hot pool of the

@@ -24,7 +24,7 @@ __all__ = [
     "resolve_union", "gather_kv", "sparse_attn_decode", "step", "kv_footprint_bytes",
     "max_batch", "per_step_budget_bytes", "union_of_query_selections",
     "build_minmax_landmarks", "score_minmax_landmarks", "bf16_total_order_key", "update_residency",
-    "prefetch_kv",
+    "prefetch_kv", "select_by_mass", "NO_SLOT",
 ]
 
 
@@ -185,6 +185,41 @@ def select_topk(s: np.ndarray, k: int) -> np.ndarray:
     return out.reshape(*lead, k)
 
 
+def select_by_mass(s: np.ndarray, k_max: int, gamma: float, tau: float, k_min: int = 1):
+    """Per row, the smallest set of chunks whose estimated attention mass reaches gamma.
+
+    MOIRA (abstract): for every request, layer, KV head and step, a coverage
+    rule keeps the smallest set of pages whose estimated attention mass
+    reaches a fraction gamma, so the budget varies per head and layer.
+    Readings: the estimated mass of chunk c in a row is
+    w_c = exp(tau * (s_c - max s)) / sum_c' exp(tau * (s_c' - max s)) (fp64),
+    tau being the logit scale of one query head (the attention scale over G,
+    since s sums the group's G dot products); the smallest set is the
+    first k_row chunks in (score descending, chunk ascending) order, k_row
+    the least count whose mass sum reaches gamma, then clamped to
+    [k_min, k_max].  Returns sel [..., k_max] (the chosen chunks ascending,
+    then -1) and the per-row counts [...].
+    """
+    *lead, C = s.shape
+    if not 1 <= k_min <= k_max <= C:
+        raise ValueError("need 1 <= k_min <= k_max <= C")
+    rows = np.asarray(s, dtype=np.float64).reshape(-1, C)
+    sel = np.full((rows.shape[0], k_max), -1, dtype=np.int32)
+    cnt = np.empty(rows.shape[0], dtype=np.int32)
+    chunk = np.arange(C)
+    for r in range(rows.shape[0]):
+        row = rows[r]
+        w = np.exp(tau * (row - row.max()))
+        w /= w.sum()
+        order = np.lexsort((chunk, -row))
+        csum = np.cumsum(w[order])
+        k_row = int(np.searchsorted(csum, gamma, side="left")) + 1   # first prefix reaching gamma
+        k_row = min(max(k_row, k_min), k_max)
+        cnt[r] = k_row
+        sel[r, :k_row] = np.sort(order[:k_row])
+    return sel.reshape(*lead, k_max), cnt.reshape(*lead)
+
+
 # ---------------------------------------------------------------------------
 # a3: union across queries, residency, miss ordinals
 # ---------------------------------------------------------------------------
@@ -194,8 +229,11 @@ def union_of_query_selections(sel: np.ndarray, b: int, g: int) -> list:
     n_q = sel.shape[1]
     u = set()
     for j in range(n_q):
-        u |= set(int(c) for c in sel[b, j, g])
+        u |= set(int(c) for c in sel[b, j, g] if c >= 0)   # -1: padding of a shorter row
     return sorted(u)
+
+
+NO_SLOT = -(2 ** 31)   # attn_slot of a padding entry (-1) of a shorter selection row
 
 
 def resolve_union(sel: np.ndarray, resident_slot: np.ndarray) -> dict:
@@ -213,7 +251,8 @@ def resolve_union(sel: np.ndarray, resident_slot: np.ndarray) -> dict:
     (b, g, c) lexicographic order and are addressed as staging slot m,
     encoded -(m+1).  ``miss_list[m] = (b*Hkv + g)*C + c``.  ``union_qmask``
     has bit j set when query j selected the chunk.  ``attn_slot[b,j,g,r]`` is
-    the encoded slot of the r-th chunk of query j's selection.
+    the encoded slot of the r-th chunk of query j's selection (NO_SLOT for a
+    padding entry -1 of a row shorter than k).
     Entries of the union arrays past ``union_cnt`` are padding (-1 / 0).
     """
     B, n_q, Hkv, k = sel.shape
@@ -227,7 +266,7 @@ def resolve_union(sel: np.ndarray, resident_slot: np.ndarray) -> dict:
     miss_list = []
     for b in range(B):
         for g in range(Hkv):
-            per_query = [set(int(c) for c in sel[b, j, g]) for j in range(n_q)]
+            per_query = [set(int(c) for c in sel[b, j, g] if c >= 0) for j in range(n_q)]
             U = union_of_query_selections(sel, b, g)
             union_cnt[b, g] = len(U)
             slot_of = {}
@@ -244,7 +283,8 @@ def resolve_union(sel: np.ndarray, resident_slot: np.ndarray) -> dict:
                 union_qmask[b, g, u] = sum(1 << j for j in range(n_q) if c in per_query[j])
             for j in range(n_q):
                 for r in range(k):
-                    attn_slot[b, j, g, r] = slot_of[int(sel[b, j, g, r])]
+                    c = int(sel[b, j, g, r])
+                    attn_slot[b, j, g, r] = slot_of[c] if c >= 0 else NO_SLOT
     return {
         "union_idx": union_idx, "union_cnt": union_cnt, "union_slot": union_slot,
         "union_qmask": union_qmask, "miss_list": np.asarray(miss_list, dtype=np.int32),
@@ -314,7 +354,7 @@ def sparse_attn_decode(q, Khot, Vhot, Kst, Vst, attn_slot, cs: int, scale: float
     for b in range(B):
         for j in range(n_q):
             for g in range(Hkv):
-                slots = [int(s) for s in attn_slot[b, j, g]]
+                slots = [int(s) for s in attn_slot[b, j, g] if s != NO_SLOT]
                 Kr = bf16_decode(np.concatenate([_rows(Khot, Kst, s) for s in slots], axis=0))
                 Vr = bf16_decode(np.concatenate([_rows(Vhot, Vst, s) for s in slots], axis=0))
                 if K_tail is not None:
@@ -440,21 +480,29 @@ def update_residency(step_id: int, cap: int, union_idx, union_slot, union_cnt, K
 # a6: one layer's step
 # ---------------------------------------------------------------------------
 
-def step(q, lm, Kh, Vh, resident_slot, Khot, Vhot, k: int, cs: int, scale=None, K_tail=None, V_tail=None) -> dict:
+def step(q, lm, Kh, Vh, resident_slot, Khot, Vhot, k: int, cs: int, scale=None, K_tail=None, V_tail=None,
+         gamma=None, k_min: int = 1) -> dict:
     """Score -> top-k -> union/resolve -> gather -> attention for one layer.
 
     DualDecoder Fig. 8 / §5.1-§5.4: retrieval index from the query and the
     landmarks, missing entries fetched from host into the layer's staging
     buffer, then sparse attention over the selected entries.  ``lm`` holds
     mean landmarks [B, Hkv, C, d] or min/max landmarks [B, Hkv, C, 2, d];
-    the score follows the kind.
+    the score follows the kind.  With ``gamma`` the rows are chosen by the
+    coverage rule of ``select_by_mass`` (k is then the longest row allowed).
     """
     s = score_minmax_landmarks(q, lm) if lm.ndim == 5 else score_landmarks(q, lm)
-    sel = select_topk(s, k)
+    sel_cnt = None
+    if gamma is None:
+        sel = select_topk(s, k)
+    else:   # coverage budget: k is the largest row length
+        G = q.shape[2] // lm.shape[1]
+        tau = (1.0 / math.sqrt(q.shape[-1]) if scale is None else scale) / G
+        sel, sel_cnt = select_by_mass(s, k, gamma, tau, k_min)
     res = resolve_union(sel, resident_slot)
     Kst, Vst = gather_kv(Kh, Vh, res["miss_list"], cs)
     out = sparse_attn_decode(q, Khot, Vhot, Kst, Vst, res["attn_slot"], cs, scale, K_tail, V_tail)
-    res.update(scores=s, sel=sel, Kst=Kst, Vst=Vst, out=out)
+    res.update(scores=s, sel=sel, sel_cnt=sel_cnt, Kst=Kst, Vst=Vst, out=out)
     return res
 
 

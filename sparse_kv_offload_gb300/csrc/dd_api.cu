@@ -380,6 +380,36 @@ dd_status dd_gather_kv(dd_ctx *c, const void *Kh, const void *Vh, const int32_t 
                                    (int64_t)c->units * c->C, c->dims.cs, c->status, c->sm_count, s));
 }
 
+dd_status dd_prefetch_kv(dd_ctx *c, const int32_t *sel, int32_t sel_rows, int32_t first_row, int32_t n_pred,
+                         const void *Kh, const void *Vh, void *Kpf, void *Vpf, int32_t *pf_map, int32_t *pf_count,
+                         int32_t ctas_per_sm, dd_stream_t stream) {
+  if (!c || n_pred < 1 || n_pred > c->dims.n_q || sel_rows < 1 || first_row < 0 || first_row + n_pred > sel_rows)
+    return DD_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (c->units == 0) return pf_count ? cuda_ok(cudaMemsetAsync(pf_count, 0, 4, s)) : DD_OK;
+  if (!sel || !Kh || !Vh || !pf_map || !aligned16(Kh) || !aligned16(Vh)) return DD_ERR_INVALID_ARG;
+  const int32_t *sel_pred = sel + (int64_t)first_row * c->dims.Hkv * c->dims.k;
+  if (c->max_misses > 0 && (!Kpf || !Vpf || !aligned16(Kpf) || !aligned16(Vpf))) return DD_ERR_INVALID_ARG;
+  if (ctas_per_sm <= 0 || ctas_per_sm > 8) ctas_per_sm = 8;
+  const dd_dims &d = c->dims;
+  int32_t *cnt = pf_count ? pf_count : c->miss_count;
+  const void *kd, *vd;
+  DD_TRY(host_kv_views(c, Kh, Vh, &kd, &vd));
+  // nothing is resident for the resolver: every predicted chunk gets a slot
+  DD_CUDA(cudaMemsetAsync(pf_map, 0xFF, (size_t)c->units * c->C * sizeof(int32_t), s));
+  DD_CUDA(dd::launch_union(sel_pred, pf_map, c->union_idx, c->union_slot, c->union_qmask, c->union_cnt, c->unit_miss,
+                           c->units, n_pred, d.Hkv, d.k, c->C, c->umax, 0, c->status, s, sel_rows));
+  DD_CUDA(dd::launch_assign(sel_pred, c->union_idx, c->union_slot, c->union_qmask, c->union_cnt, c->unit_miss,
+                            c->miss_list, cnt, nullptr, c->units, n_pred, d.Hkv, d.k, c->C, c->umax, c->max_misses, 0,
+                            d.cs, nullptr, c->status, s));
+  c->launches += 2;
+  if (c->max_misses == 0) return DD_OK;
+  c->launches += 1;
+  return cuda_ok(dd::launch_gather(static_cast<const uint4 *>(kd), static_cast<const uint4 *>(vd), c->miss_list, cnt,
+                                   static_cast<uint4 *>(Kpf), static_cast<uint4 *>(Vpf), c->max_misses,
+                                   (int64_t)c->units * c->C, d.cs, c->status, c->sm_count, s, pf_map, ctas_per_sm));
+}
+
 static dd_status attn_impl(dd_ctx *c, const void *q, const void *Khot, const void *Vhot, const void *Kst,
                            const void *Vst, const int32_t *union_slot, const uint8_t *union_qmask,
                            const int32_t *union_cnt, const int32_t *miss_count, float softmax_scale, float *out,

@@ -187,7 +187,7 @@ cudaError_t launch_topk(const float *scores, int32_t *sel, int rows, int C, int 
 cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx,
                          int32_t *union_slot, uint8_t *union_qmask, int32_t *union_cnt,
                          int32_t *unit_miss, int units, int n_q, int Hkv, int k, int C, int umax,
-                         int64_t hot_slots, int32_t *status, cudaStream_t s);
+                         int64_t hot_slots, int32_t *status, cudaStream_t s, int sel_rows = 0);
 cudaError_t launch_assign(const int32_t *sel, const int32_t *union_idx, int32_t *union_slot,
                           const uint8_t *union_qmask, const int32_t *union_cnt, const int32_t *unit_miss,
                           int32_t *miss_list, int32_t *miss_count, int32_t *attn_slot, int units, int n_q, int Hkv,
@@ -220,5 +220,6 @@ cudaError_t launch_update_residency(int32_t step, int32_t cap, int S, int units,
                                     int32_t *admitted, int C, int umax, int cs, int32_t *status, cudaStream_t s);
 cudaError_t launch_gather(const uint4 *Kh, const uint4 *Vh, const int32_t *miss_list,
                           const int32_t *miss_count, uint4 *Kst, uint4 *Vst, int64_t max_misses,
-                          int64_t n_chunks_total, int cs, int32_t *status, int sm_count, cudaStream_t s);
+                          int64_t n_chunks_total, int cs, int32_t *status, int sm_count, cudaStream_t s,
+                          int32_t *map_out = nullptr, int ctas_per_sm = 8);
 }  // namespace dd

@@ -133,7 +133,7 @@ constexpr int kMaxWords = kMaxC / 32;
 __global__ void __launch_bounds__(kUnionThreads) k_union(
     const int32_t *__restrict__ sel, const int32_t *__restrict__ resident_slot, int32_t *__restrict__ union_idx,
     int32_t *__restrict__ union_slot, uint8_t *__restrict__ union_qmask, int32_t *__restrict__ union_cnt,
-    int32_t *__restrict__ unit_miss, int n_q, int Hkv, int k, int C, int umax, int64_t hot_slots,
+    int32_t *__restrict__ unit_miss, int n_q, int sel_rows, int Hkv, int k, int C, int umax, int64_t hot_slots,
     int32_t *status) {
   __shared__ uint32_t qbits[kMaxNq * kMaxWords];
   __shared__ uint32_t missw[kMaxWords];
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kUnionThreads) k_union(
   __syncthreads();
   for (int i = tid; i < n_q * k; i += kUnionThreads) {
     const int j = i / k, r = i - j * k;
-    const int c = sel[((int64_t)(b * n_q + j) * Hkv + g) * k + r];
+    const int c = sel[((int64_t)(b * sel_rows + j) * Hkv + g) * k + r];
     if (c < 0 || c >= C) {
       set_status(status, DD_ERR_DEVICE_CHECK);
       continue;
@@ -278,10 +278,11 @@ __global__ void __launch_bounds__(kAssignThreads) k_assign(
 
 cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx, int32_t *union_slot,
                          uint8_t *union_qmask, int32_t *union_cnt, int32_t *unit_miss, int units, int n_q, int Hkv,
-                         int k, int C, int umax, int64_t hot_slots, int32_t *status, cudaStream_t s) {
+                         int k, int C, int umax, int64_t hot_slots, int32_t *status, cudaStream_t s, int sel_rows) {
   if (units == 0) return cudaSuccess;
   return launch_k(k_union, dim3(units), dim3(kUnionThreads), 0, s, sel, resident_slot, union_idx, union_slot,
-                  union_qmask, union_cnt, unit_miss, n_q, Hkv, k, C, umax, hot_slots, status);
+                  union_qmask, union_cnt, unit_miss, n_q, sel_rows > 0 ? sel_rows : n_q, Hkv, k, C, umax, hot_slots,
+                  status);
 }
 
 cudaError_t launch_assign(const int32_t *sel, const int32_t *union_idx, int32_t *union_slot,

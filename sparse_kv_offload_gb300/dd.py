@@ -27,6 +27,7 @@ EXPORTED = (
     "dd_resolve_union", "dd_gather_kv", "dd_sparse_attn_decode", "dd_step", "dd_get_status",
     "dd_launch_count", "dd_status_str", "dd_last_cuda_error", "dd_synth_kv", "dd_synth_queries", "dd_sparse_attn_decode_noalloc",
     "dd_build_landmarks_minmax", "dd_score_landmarks_minmax", "dd_update_residency",
+    "dd_prefetch_kv",
 )
 
 
@@ -78,6 +79,7 @@ def _load():
         "dd_sparse_attn_decode": (i32, [_vp] * 12 + [f32, _vp, _vp]),
         "dd_step": (i32, [_vp, ctypes.POINTER(StepArgs), _vp]),
         "dd_update_residency": (i32, [_vp, i32, i32, i32] + [_vp] * 13),
+        "dd_prefetch_kv": (i32, [_vp, _vp, i32, i32, i32, _vp, _vp, _vp, _vp, _vp, _vp, i32, _vp]),
         "dd_get_status": (i32, [_vp, ctypes.POINTER(i32)]),
         "dd_launch_count": (i64, [_vp]),
         "dd_status_str": (ctypes.c_char_p, [i32]),
@@ -270,6 +272,24 @@ class Context:
             _ptr(miss_count, torch.int32, 1, name="miss_count"), float(softmax_scale),
             _ptr(out, torch.float32, s.B * s.n_q * s.Hq * s.d, name="out"), _stream(stream)),
             "dd_sparse_attn_decode")
+
+    def prefetch_kv(self, sel, n_pred, Kh, Vh, Kpf, Vpf, pf_map, pf_count=None, ctas_per_sm=8, stream=None,
+                    sel_rows=None, first_row=0):
+        """Predictive prefetch of rows first_row .. first_row+n_pred-1 of ``sel``
+        [B, sel_rows, Hkv, k] (sel_rows defaults to n_pred; see dd.h)."""
+        s = self.shape
+        n = s.B * s.Hkv * s.L * s.d
+        ns = self.max_misses * s.cs * s.d
+        rows = n_pred if sel_rows is None else sel_rows
+        _chk(_lib.dd_prefetch_kv(
+            self._h, _ptr(sel, torch.int32, s.B * max(rows, 0) * s.Hkv * s.k, name="sel"), int(rows),
+            int(first_row), int(n_pred),
+            _ptr(Kh, torch.bfloat16, n, device=False, name="Kh"), _ptr(Vh, torch.bfloat16, n, device=False, name="Vh"),
+            _ptr(Kpf, torch.bfloat16, ns, name="Kpf", allow_none=True),
+            _ptr(Vpf, torch.bfloat16, ns, name="Vpf", allow_none=True),
+            _ptr(pf_map, torch.int32, s.B * s.Hkv * s.C, name="pf_map"),
+            _ptr(pf_count, torch.int32, 1, name="pf_count", allow_none=True), int(ctas_per_sm), _stream(stream)),
+            "dd_prefetch_kv")
 
     def update_residency(self, step, cap, slots_per_unit, Kst, Vst, resident_slot, slot_chunk, last_used, Khot,
                          Vhot, admitted=None, union_idx=None, union_slot=None, union_cnt=None, miss_count=None,

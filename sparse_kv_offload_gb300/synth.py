@@ -55,6 +55,8 @@ TID_CARRY_PICK = 7
 TID_Q_NOISE = 8  # + j for speculative query j (1..7)
 TID_SCORE = 16   # seeded stand-alone score rows for select tests
 TID_SEL = 17     # seeded stand-alone selections for resolve tests
+TID_DRIFT = 32   # + t: drift of the real query at decode step t (t < 16)
+TID_DRIFT_SPEC = 48   # + t: error of the speculative queries of decode step t (t < 16)
 
 _BLOCK = 1 << 21
 
@@ -117,6 +119,30 @@ def bf16_to_f32(u: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # derived tensors
 # ---------------------------------------------------------------------------
+
+def drift_queries(seed: int, B: int, n_q: int, Hq: int, d: int, T: int, sigma_drift: float, sigma_spec: float,
+                  layer: int = 0) -> np.ndarray:
+    """bf16 bits [T, B, n_q, Hq, d]: T decode steps of one layer, cyclic.
+
+    The real query of step t is base + sigma_drift * xi_t, base being the
+    layer's real query of ``queries``; every speculative query of step t is
+    the real query of step t+1 (mod T) + sigma_spec * eta_t,j: a draft of
+    the next step's query."""
+    if not 1 <= T <= 16:
+        raise ValueError("1 <= T <= 16")
+    n = B * Hq * d
+    idx = np.arange(n, dtype=np.uint64)
+    base = bf16_to_f32(f32_to_bf16(normal_f32(seed, tensor_id(TID_Q_REAL, layer), idx)))
+    real = [bf16_to_f32(f32_to_bf16(base + np.float32(sigma_drift)
+                                    * normal_f32(seed, tensor_id(TID_DRIFT + t, layer), idx))) for t in range(T)]
+    out = np.empty((T, B, n_q, Hq, d), dtype=np.uint16)
+    for t in range(T):
+        out[t, :, 0] = f32_to_bf16(real[t]).reshape(B, Hq, d)
+        for j in range(1, n_q):
+            eta = normal_f32(seed, tensor_id(TID_DRIFT_SPEC + t, layer), idx + np.uint64(j * n))
+            out[t, :, j] = f32_to_bf16(real[(t + 1) % T] + np.float32(sigma_spec) * eta).reshape(B, Hq, d)
+    return out
+
 
 def queries(seed: int, B: int, n_q: int, Hq: int, d: int, spec_scale, layer: int = 0) -> np.ndarray:
     """bf16 bits [B, n_q, Hq, d]: query j=0 is the real query, j>=1 speculative."""

@@ -625,3 +625,81 @@ def test_prefetch_changes_no_output_and_leaves_only_unpredicted_misses(overlap):
     urgent = sum(len(set(oracle.union_of_query_selections(true_sel, b, g)) - set(pred[b, 0, g]))
                  for b, g in np.ndindex(B, Hkv))
     assert with_pf["miss_count"] == urgent
+
+
+# ---------------------------------------------------------------- coverage budgets (MOIRA reading)
+
+def _mass(row, tau):
+    w = np.exp(tau * (row - row.max()))
+    return w / w.sum()
+
+
+@pytest.mark.parametrize("gamma", [0.3, 0.6, 0.9, 0.99])
+def test_mass_selection_is_the_smallest_set_by_brute_force(gamma):
+    rng = np.random.default_rng(41)
+    C, tau = 8, 0.7
+    s = rng.standard_normal((5, C)) * 2.0
+    s[4, 3] = s[4, 5]                                     # a tie: the lower index ranks first
+    sel, cnt = oracle.select_by_mass(s, C, gamma, tau)
+    for r in range(s.shape[0]):
+        w = _mass(s[r], tau)
+        best = None
+        for size in range(1, C + 1):                      # the least size some subset reaching gamma has
+            if any(w[list(sub)].sum() >= gamma for sub in itertools.combinations(range(C), size)):
+                best = size
+                break
+        assert cnt[r] == best
+        chosen = sel[r, :cnt[r]]
+        assert list(chosen) == sorted(chosen) and np.all(sel[r, cnt[r]:] == -1)
+        assert w[chosen].sum() >= gamma
+        # the chosen set is the top cnt[r] by (score desc, index asc)
+        order = sorted(range(C), key=lambda c: (-s[r, c], c))
+        assert set(chosen.tolist()) == set(order[:cnt[r]])
+
+
+def test_mass_selection_uniform_peaked_and_clamped():
+    C = 16
+    flat = np.zeros((1, C))
+    for gamma, want in ((0.5, 8), (0.25, 4), (0.26, 5), (1.0, 16)):
+        assert oracle.select_by_mass(flat, C, gamma, 1.0)[1][0] == want      # ceil(gamma * C)
+    peaked = np.zeros((1, C))
+    peaked[0, 9] = 100.0
+    sel, cnt = oracle.select_by_mass(peaked, C, 0.99, 1.0)
+    assert cnt[0] == 1 and sel[0, 0] == 9
+    assert oracle.select_by_mass(peaked, C, 0.99, 1.0, k_min=3)[1][0] == 3   # clamped below
+    assert oracle.select_by_mass(flat, 6, 0.9, 1.0)[1][0] == 6               # clamped above (k_max)
+
+
+def test_padded_rows_resolve_and_attend_like_shorter_rows():
+    rng = np.random.default_rng(42)
+    B, n_q, Hq, Hkv, C, cs, d = 1, 2, 4, 2, 12, 4, 128
+    q = enc(rng.standard_normal((B, n_q, Hq, d)))
+    Kh = enc(rng.standard_normal((B, Hkv, C * cs, d)))
+    Vh = enc(rng.standard_normal((B, Hkv, C * cs, d)))
+    rows = {(0, 0): [1, 4, 7], (0, 1): [0, 2, 4, 6, 8], (1, 0): [3], (1, 1): [4, 5, 10]}
+    sel = np.full((B, n_q, Hkv, 5), -1, np.int32)
+    for (j, g), cs_ in rows.items():
+        sel[0, j, g, :len(cs_)] = cs_
+    res = oracle.resolve_union(sel, np.full((B, Hkv, C), -1, np.int32))
+    assert res["union_cnt"].tolist() == [[4, 7]]                              # {1,3,4,7}, {0,2,4,5,6,8,10}
+    assert np.all(res["attn_slot"][sel < 0] == oracle.NO_SLOT) and np.all(res["attn_slot"][sel >= 0] < 0)
+    Kst, Vst = oracle.gather_kv(Kh, Vh, res["miss_list"], cs)
+    out = oracle.sparse_attn_decode(q, Kst[:0], Vst[:0], Kst, Vst, res["attn_slot"], cs)
+    G = Hq // Hkv
+    qf, Kf, Vf = (synth.bf16_to_f32(x).astype(np.float64) for x in (q, Kh, Vh))
+    for (j, g), chunks in rows.items():
+        idx = np.concatenate([np.arange(c * cs, (c + 1) * cs) for c in chunks])
+        for h in range(g * G, (g + 1) * G):
+            want = _sdpa(qf[0, j, h], Kf[0, g, idx], Vf[0, g, idx], 1 / math.sqrt(d))
+            np.testing.assert_allclose(out[0, j, h], want, rtol=1e-10, atol=1e-12)
+
+
+def test_step_with_coverage_budget_uses_the_head_logit_scale():
+    rng = np.random.default_rng(43)
+    B, n_q, Hq, Hkv, L, d, cs, k = 1, 2, 8, 2, 256, 128, 16, 12
+    q = enc(rng.standard_normal((B, n_q, Hq, d)))
+    Kh = enc(rng.standard_normal((B, Hkv, L, d)))
+    lm = oracle.build_landmarks(Kh, cs)
+    r = oracle.step(q, lm, Kh, Kh, np.full((B, Hkv, L // cs), -1, np.int32), None, None, k, cs, gamma=0.8)
+    sel, cnt = oracle.select_by_mass(oracle.score_landmarks(q, lm), k, 0.8, 1 / math.sqrt(d) / (Hq // Hkv))
+    assert np.array_equal(r["sel"], sel) and np.array_equal(r["sel_cnt"], cnt)

@@ -57,3 +57,23 @@ def test_queries_spec_is_real_plus_scaled_noise():
     for j, s in ((1, 0.2), (2, 0.4)):
         diff = synth.bf16_to_f32(q[:, j]).astype(np.float64) - real
         assert 0.8 * s < diff.std() < 1.2 * s
+
+
+def test_drift_queries_follow_their_definition():
+    seed, B, n_q, Hq, d, T = 7, 2, 3, 4, 128, 5
+    q = synth.drift_queries(seed, B, n_q, Hq, d, T, 0.3, 0.1, layer=2)
+    assert q.shape == (T, B, n_q, Hq, d) and q.dtype == np.uint16
+    n = B * Hq * d
+    idx = np.arange(n, dtype=np.uint64)
+    base = synth.bf16_to_f32(synth.f32_to_bf16(synth.normal_f32(seed, synth.tensor_id(synth.TID_Q_REAL, 2), idx)))
+    # the base is the layer's real query of the plain generator
+    assert np.array_equal(synth.f32_to_bf16(base).reshape(B, Hq, d), synth.queries(seed, B, 1, Hq, d, (0.0,), 2)[:, 0])
+    real = [synth.bf16_to_f32(q[t, :, 0]).reshape(-1) for t in range(T)]
+    for t in range(T):
+        drift = synth.normal_f32(seed, synth.tensor_id(synth.TID_DRIFT + t, 2), idx)
+        assert np.array_equal(q[t, :, 0].reshape(-1), synth.f32_to_bf16(base + np.float32(0.3) * drift))
+        for j in range(1, n_q):
+            eta = synth.normal_f32(seed, synth.tensor_id(synth.TID_DRIFT_SPEC + t, 2), idx + np.uint64(j * n))
+            want = synth.f32_to_bf16(real[(t + 1) % T] + np.float32(0.1) * eta)
+            assert np.array_equal(q[t, :, j].reshape(-1), want)
+    assert np.array_equal(q, synth.drift_queries(seed, B, n_q, Hq, d, T, 0.3, 0.1, layer=2))
