@@ -582,7 +582,7 @@ def run_pipeline(args, world, rank, local):
             n_rec[0] += 1
         L_ = layers[t]
         ctx_lo.prefetch_kv(sel_store[t], w.n_q - 1, L_.Kh, L_.Vh, Kpf[p], Vpf[p], pf_map[p], pf_count=count,
-                           ctas_per_sm=2, stream=lo, sel_rows=w.n_q, first_row=1)
+                           ctas_per_sm=args.prefetch_ctas, stream=lo, sel_rows=w.n_q, first_row=1)
         ev_pf[t].record(lo)
 
     def pipelined(i, rec=None):
@@ -663,7 +663,7 @@ def run_pipeline(args, world, rank, local):
                        queries=f"real query of step t = base + {SIGMA_DRIFT} N(0,1), cyclic over {T} steps; "
                                f"speculative queries of step t = real query of step t+1 + {SIGMA_SPEC} N(0,1)",
                        prefetch="rows 1..n_q-1 of each layer's selection, for its next step, issued after the "
-                                "attention of layer l-2 on a low-priority stream (2 CTAs/SM)"),
+                                f"attention of layer l-2 on a low-priority stream ({args.prefetch_ctas} CTAs/SM)"),
         "per_layer_step": {"true_union_chunks": U, "urgent_chunks": M, "prefetched_chunks": P,
                            "prediction_hit_rate": 1.0 - M / U if U else None,
                            "urgent_bytes": M * chunk_b, "prefetch_bytes": P * chunk_b,
@@ -688,6 +688,7 @@ def main():
     ap.add_argument("--mode", choices=("zerocopy", "memcpy"), default="zerocopy")
     ap.add_argument("--landmarks", choices=("mean", "minmax"), default="mean")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefetch-ctas", type=int, default=2, help="pipelined mode: prefetch copy CTAs per SM")
     ap.add_argument("--pipeline", action="store_true",
                     help="decode steps over several layers with drifting queries and predictive prefetch")
     args = ap.parse_args()

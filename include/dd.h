@@ -95,6 +95,20 @@ dd_status dd_build_landmarks(dd_ctx *ctx, const void *K, void *lm, dd_stream_t s
  * (unscaled; fp32 accumulation). */
 dd_status dd_score_landmarks(dd_ctx *ctx, const void *q, const void *lm, float *scores, dd_stream_t stream);
 
+/* Top-k with a coverage budget (MOIRA: per request, layer, KV head and step,
+ * the smallest set of chunks whose estimated attention mass reaches gamma;
+ * the budget varies per row).  scores: fp32 [B,n_q,Hkv,C].  The estimated
+ * mass of chunk c in a row is w_c = exp(tau*(s_c - max s)) / sum exp(...),
+ * tau = softmax_scale/G (one query head's logit scale; softmax_scale <= 0
+ * selects 1/sqrt(d)); k_row = the least count of chunks, taken in (score
+ * desc, chunk asc) order, whose mass reaches gamma, clamped to
+ * [k_min, k] (k = the context's k, at most 4096).  sel: int32 [B,n_q,Hkv,k],
+ * each row's k_row chunks ascending then -1 (which the resolver skips);
+ * sel_cnt: int32 [B,n_q,Hkv] or NULL, k_row per row.  The masses are fp32
+ * sums in a fixed order, so the result repeats exactly from run to run. */
+dd_status dd_select_topk_mass(dd_ctx *ctx, const float *scores, int32_t *sel, int32_t *sel_cnt, float gamma,
+                              int32_t k_min, float softmax_scale, dd_stream_t stream);
+
 /* Landmark kinds (dd_step_args.lm_kind). */
 typedef enum { DD_LM_MEAN = 0, DD_LM_MINMAX = 1 } dd_landmark_kind;
 
@@ -216,6 +230,9 @@ typedef struct {
   void *stage_events[6];
   dd_landmark_kind lm_kind;      /* DD_LM_MEAN (0) or DD_LM_MINMAX: how lm is laid out and scored */
   const void *K_tail, *V_tail;   /* bf16 [B,n_q,Hkv,d] device or NULL: the step's own tokens (causal) */
+  float mass_gamma;              /* > 0: coverage budgets (dd_select_topk_mass) instead of a fixed k */
+  int32_t mass_k_min;            /* with mass_gamma: the shortest row */
+  int32_t *sel_cnt;              /* with mass_gamma: optional int32 [B,n_q,Hkv] row lengths */
 } dd_step_args;
 
 dd_status dd_step(dd_ctx *ctx, const dd_step_args *args, dd_stream_t stream);

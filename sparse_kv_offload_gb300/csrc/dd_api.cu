@@ -292,6 +292,20 @@ dd_status dd_select_topk(dd_ctx *c, const float *scores, int32_t *sel, dd_stream
                                  (cudaStream_t)stream));
 }
 
+dd_status dd_select_topk_mass(dd_ctx *c, const float *scores, int32_t *sel, int32_t *sel_cnt, float gamma,
+                              int32_t k_min, float softmax_scale, dd_stream_t stream) {
+  if (!c) return DD_ERR_INVALID_ARG;
+  if (!(gamma > 0.f) || k_min < 1 || k_min > c->dims.k || c->dims.k > 4096) return DD_ERR_INVALID_ARG;
+  if (c->units == 0) return DD_OK;
+  if (!scores || !sel) return DD_ERR_INVALID_ARG;
+  // one query head's logit scale: the score sums the group's G dot products
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)kD);
+  const float tau_log2e = scale / (float)c->G * 1.4426950408889634f;
+  c->launches += 1;
+  return cuda_ok(dd::launch_topk_mass(scores, sel, sel_cnt, c->dims.B * c->dims.n_q * c->dims.Hkv, c->C, c->dims.k,
+                                      k_min, gamma, tau_log2e, (cudaStream_t)stream));
+}
+
 static dd_status resolve_impl(dd_ctx *c, const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx,
                               int32_t *union_slot, uint8_t *union_qmask, int32_t *union_cnt, int32_t *miss_list,
                               int32_t *miss_count, int32_t *attn_slot, bool with_plan, dd_stream_t stream) {
@@ -466,6 +480,8 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   if (!c || !a || a->layer < 0) return DD_ERR_INVALID_ARG;
   if (a->lm_kind != DD_LM_MEAN && a->lm_kind != DD_LM_MINMAX) return DD_ERR_INVALID_ARG;
   if ((a->K_tail == nullptr) != (a->V_tail == nullptr)) return DD_ERR_INVALID_ARG;
+  if (a->mass_gamma > 0.f && (a->mass_k_min < 1 || a->mass_k_min > c->dims.k || c->dims.k > 4096))
+    return DD_ERR_INVALID_ARG;
   if (c->units == 0) return DD_OK;
   if (!a->q || !a->lm || !a->Kh || !a->Vh || !a->resident_slot || !a->out) return DD_ERR_INVALID_ARG;
   const int p = a->layer & 1;
@@ -491,7 +507,11 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
     DD_TRY(dd_score_landmarks(c, a->q, a->lm, scores, stream));
   }
   DD_TRY(mark(1));
-  DD_TRY(dd_select_topk(c, scores, sel, stream));
+  if (a->mass_gamma > 0.f) {
+    DD_TRY(dd_select_topk_mass(c, scores, sel, a->sel_cnt, a->mass_gamma, a->mass_k_min, a->softmax_scale, stream));
+  } else {
+    DD_TRY(dd_select_topk(c, scores, sel, stream));
+  }
   DD_TRY(mark(2));
   DD_TRY(resolve_impl(c, sel, a->resident_slot, union_idx, union_slot, union_qmask, union_cnt, miss_list,
                       miss_count, attn_slot, true, stream));

@@ -184,6 +184,8 @@ cudaError_t launch_build_minmax(const uint4 *K, uint4 *lm2, int64_t n_chunks, in
 cudaError_t launch_score_minmax(const uint4 *q, const uint4 *lm2, float *scores, int B, int n_q, int Hq, int Hkv,
                                 int C, cudaStream_t s);
 cudaError_t launch_topk(const float *scores, int32_t *sel, int rows, int C, int k, cudaStream_t s);
+cudaError_t launch_topk_mass(const float *scores, int32_t *sel, int32_t *sel_cnt, int rows, int C, int k_max,
+                             int k_min, float gamma, float tau_log2e, cudaStream_t s);
 cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx,
                          int32_t *union_slot, uint8_t *union_qmask, int32_t *union_cnt,
                          int32_t *unit_miss, int units, int n_q, int Hkv, int k, int C, int umax,

@@ -27,21 +27,11 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 // ---------------------------------------------------------------------------
 constexpr int kTopkThreads = 512;
 
-__global__ void __launch_bounds__(kTopkThreads) k_topk(const float *__restrict__ scores, int32_t *__restrict__ sel,
-                                                       int C, int k) {
-  extern __shared__ uint32_t keys[];
-  __shared__ int hist[256];
-  __shared__ int scratch[33];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_remaining;
-  pdl_wait();
-  pdl_trigger();
-
-  const int row = blockIdx.x;
+// Radix select over the order keys of one row: the k-th largest key T and how
+// many keys equal to T belong to the top k (the lowest chunks first).
+__device__ __forceinline__ void radix_threshold(const uint32_t *keys, int C, int k, int *hist, uint32_t *s_prefix,
+                                                int *s_remaining, uint32_t &T, int &need) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float *src = scores + (int64_t)row * C;
-  for (int i = tid; i < C; i += kTopkThreads) keys[i] = order_key(src[i]);
-
   uint32_t prefix = 0, pmask = 0;
   int remaining = k;
   for (int shift = 24; shift >= 0; shift -= 8) {
@@ -67,8 +57,8 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(const float *__restrict__
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           if (r > 0 && r <= cnt[e]) {
-            s_prefix = prefix | ((uint32_t)(255 - 8 * lane - e) << shift);
-            s_remaining = r;
+            *s_prefix = prefix | ((uint32_t)(255 - 8 * lane - e) << shift);
+            *s_remaining = r;
             r = 0;
           } else if (r > 0) {
             r -= cnt[e];
@@ -77,14 +67,20 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(const float *__restrict__
       }
     }
     __syncthreads();
-    prefix = s_prefix;
-    remaining = s_remaining;
+    prefix = *s_prefix;
+    remaining = *s_remaining;
     pmask |= 0xFFu << shift;
     __syncthreads();
   }
-  const uint32_t T = prefix;
-  const int need = remaining;   // keys equal to T to take, lowest chunk first
+  T = prefix;
+  need = remaining;
+}
 
+// Writes the top-k chunks of the row (every key > T, and the `need` lowest
+// chunks with key == T) to dst in ascending chunk order.
+__device__ __forceinline__ void emit_topk(const uint32_t *keys, int C, uint32_t T, int need, int *scratch,
+                                          int32_t *dst) {
+  const int tid = threadIdx.x;
   const int per = (C + kTopkThreads - 1) / kTopkThreads;
   const int lo = min(C, tid * per), hi = min(C, lo + per);
   int eq_local = 0;
@@ -101,7 +97,6 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(const float *__restrict__
     }
   }
   int pos = block_excl_scan(take, scratch, &tot);
-  int32_t *dst = sel + (int64_t)row * k;
   int er = eq_before;
   for (int c = lo; c < hi; ++c) {
     const uint32_t key = keys[c];
@@ -109,6 +104,26 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(const float *__restrict__
     if (key == T) { t = er < need; ++er; }
     if (t) dst[pos++] = c;
   }
+}
+
+__global__ void __launch_bounds__(kTopkThreads) k_topk(const float *__restrict__ scores, int32_t *__restrict__ sel,
+                                                       int C, int k) {
+  extern __shared__ uint32_t keys[];
+  __shared__ int hist[256];
+  __shared__ int scratch[33];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_remaining;
+  pdl_wait();
+  pdl_trigger();
+
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x;
+  const float *src = scores + (int64_t)row * C;
+  for (int i = tid; i < C; i += kTopkThreads) keys[i] = order_key(src[i]);
+  uint32_t T;
+  int need;
+  radix_threshold(keys, C, k, hist, &s_prefix, &s_remaining, T, need);
+  emit_topk(keys, C, T, need, scratch, sel + (int64_t)row * k);
 }
 
 cudaError_t launch_topk(const float *scores, int32_t *sel, int rows, int C, int k, cudaStream_t s) {
@@ -119,6 +134,196 @@ cudaError_t launch_topk(const float *scores, int32_t *sel, int rows, int C, int 
     if (e != cudaSuccess) return e;
   }
   return launch_k(k_topk, dim3(rows), dim3(kTopkThreads), smem, s, scores, sel, C, k);
+}
+
+// ---------------------------------------------------------------------------
+// a2 with a coverage budget (MOIRA: per request, layer, KV head and step, the
+// smallest set of chunks whose estimated attention mass reaches gamma).  One
+// CTA per row: the top k_max chunks by radix select as above; their scores
+// sorted by (score desc, chunk asc) with a bitonic sort in shared memory;
+// masses w = exp2((s - max s) * tau_log2e) and Z = the sum over the whole
+// row, both in fp32 in a fixed order (per-thread sequential sums, then a
+// fixed tree), so the result is the same on every run; k_row = 1 + the
+// number of sorted prefixes below gamma * Z, clamped to [k_min, k_max].  The
+// row is written as its k_row chunks ascending, then -1.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float block_sum_f(float v, float *scratchf) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) scratchf[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < nw; ++w) t += scratchf[w];
+    scratchf[32] = t;
+  }
+  __syncthreads();
+  const float r = scratchf[32];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ float block_max_f(float v, float *scratchf) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (lane == 0) scratchf[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = -INFINITY;
+    for (int w = 0; w < nw; ++w) t = fmaxf(t, scratchf[w]);
+    scratchf[32] = t;
+  }
+  __syncthreads();
+  const float r = scratchf[32];
+  __syncthreads();
+  return r;
+}
+
+// exclusive scan of one float per thread in thread order (fixed order); total in *total
+__device__ __forceinline__ float block_excl_scan_f(float v, float *scratchf, float *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  float incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) scratchf[warp] = incl;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < nw; ++w) {
+      const float x = scratchf[w];
+      scratchf[w] = t;
+      t += x;
+    }
+    scratchf[32] = t;
+  }
+  __syncthreads();
+  const float r = scratchf[warp] + incl - v;
+  *total = scratchf[32];
+  __syncthreads();
+  return r;
+}
+
+constexpr int kMaxMassK = 4096;
+
+__global__ void __launch_bounds__(kTopkThreads) k_topk_mass(const float *__restrict__ scores,
+                                                            int32_t *__restrict__ sel, int32_t *__restrict__ sel_cnt,
+                                                            int C, int k_max, int k_min, float gamma,
+                                                            float tau_log2e) {
+  extern __shared__ unsigned long long smem_ull[];
+  __shared__ int hist[256];
+  __shared__ int scratch[33];
+  __shared__ float scratchf[33];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_remaining;
+  pdl_wait();
+  pdl_trigger();
+  int k_pow = 1;
+  while (k_pow < k_max) k_pow <<= 1;
+  const int W = (C + 31) >> 5;
+  unsigned long long *skey = smem_ull;                                      // [k_pow]
+  uint32_t *keys = reinterpret_cast<uint32_t *>(skey + k_pow);              // [C]
+  int32_t *list = reinterpret_cast<int32_t *>(keys + C);                    // [k_max]
+  uint32_t *bits = reinterpret_cast<uint32_t *>(list + k_max);              // [W]
+
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x;
+  const float *src = scores + (int64_t)row * C;
+  float mx = -INFINITY;
+  for (int i = tid; i < C; i += kTopkThreads) {
+    const float v = src[i];
+    keys[i] = order_key(v);
+    mx = fmaxf(mx, v);
+  }
+  for (int i = tid; i < W; i += kTopkThreads) bits[i] = 0u;
+  mx = block_max_f(mx, scratchf);
+  uint32_t T;
+  int need;
+  radix_threshold(keys, C, k_max, hist, &s_prefix, &s_remaining, T, need);
+  emit_topk(keys, C, T, need, scratch, list);
+
+  // Z over the whole row, sequential per thread, then the fixed tree
+  float z = 0.f;
+  for (int i = tid; i < C; i += kTopkThreads) z += exp2f((src[i] - mx) * tau_log2e);
+  const float Z = block_sum_f(z, scratchf);   // its barriers also publish `list`
+
+  for (int r = tid; r < k_pow; r += kTopkThreads) {
+    unsigned long long key = ~0ull;
+    if (r < k_max) {
+      const int c = list[r];
+      key = ((unsigned long long)(~keys[c]) << 32) | (unsigned long long)(uint32_t)c;
+    }
+    skey[r] = key;
+  }
+  __syncthreads();
+  for (int kk = 2; kk <= k_pow; kk <<= 1) {
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < k_pow; i += kTopkThreads) {
+        const int x = i ^ j;
+        if (x > i) {
+          const unsigned long long a = skey[i], b = skey[x];
+          if ((a > b) == ((i & kk) == 0)) {
+            skey[i] = b;
+            skey[x] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // prefix masses of the sorted list: thread t owns a contiguous segment
+  const int per = (k_max + kTopkThreads - 1) / kTopkThreads;
+  const int r0 = min(k_max, tid * per), r1 = min(k_max, r0 + per);
+  float seg = 0.f;
+  for (int r = r0; r < r1; ++r) seg += exp2f((src[(uint32_t)skey[r]] - mx) * tau_log2e);
+  float tot;
+  float run = block_excl_scan_f(seg, scratchf, &tot);
+  const float target = gamma * Z;
+  int below = 0;
+  for (int r = r0; r < r1; ++r) {
+    run += exp2f((src[(uint32_t)skey[r]] - mx) * tau_log2e);
+    below += run < target;
+  }
+  const int n_below = block_sum(below, scratch);
+  const int k_row = max(k_min, min(k_max, n_below + 1));
+  for (int r = tid; r < k_row; r += kTopkThreads) {
+    const uint32_t c = (uint32_t)skey[r];
+    atomicOr(&bits[c >> 5], 1u << (c & 31));
+  }
+  __syncthreads();
+  // the chosen chunks in ascending order (list is ascending), then padding
+  int32_t *dst = sel + (int64_t)row * k_max;
+  int take = 0;
+  for (int r = r0; r < r1; ++r) {
+    const int c = list[r];
+    take += (bits[c >> 5] >> (c & 31)) & 1u;
+  }
+  int itot;
+  int pos = block_excl_scan(take, scratch, &itot);
+  for (int r = r0; r < r1; ++r) {
+    const int c = list[r];
+    if ((bits[c >> 5] >> (c & 31)) & 1u) dst[pos++] = c;
+  }
+  for (int r = k_row + tid; r < k_max; r += kTopkThreads) dst[r] = -1;
+  if (tid == 0 && sel_cnt) sel_cnt[row] = k_row;
+}
+
+cudaError_t launch_topk_mass(const float *scores, int32_t *sel, int32_t *sel_cnt, int rows, int C, int k_max,
+                             int k_min, float gamma, float tau_log2e, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  int k_pow = 1;
+  while (k_pow < k_max) k_pow <<= 1;
+  const size_t smem = (size_t)k_pow * 8 + (size_t)C * 4 + (size_t)k_max * 4 + (size_t)((C + 31) / 32) * 4;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_topk_mass, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_k(k_topk_mass, dim3(rows), dim3(kTopkThreads), smem, s, scores, sel, sel_cnt, C, k_max, k_min,
+                  gamma, tau_log2e);
 }
 
 // ---------------------------------------------------------------------------
@@ -149,6 +354,7 @@ __global__ void __launch_bounds__(kUnionThreads) k_union(
   for (int i = tid; i < n_q * k; i += kUnionThreads) {
     const int j = i / k, r = i - j * k;
     const int c = sel[((int64_t)(b * sel_rows + j) * Hkv + g) * k + r];
+    if (c == -1) continue;   // padding of a row shorter than k (coverage budgets)
     if (c < 0 || c >= C) {
       set_status(status, DD_ERR_DEVICE_CHECK);
       continue;

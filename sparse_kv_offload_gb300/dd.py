@@ -27,7 +27,7 @@ EXPORTED = (
     "dd_resolve_union", "dd_gather_kv", "dd_sparse_attn_decode", "dd_step", "dd_get_status",
     "dd_launch_count", "dd_status_str", "dd_last_cuda_error", "dd_synth_kv", "dd_synth_queries", "dd_sparse_attn_decode_noalloc",
     "dd_build_landmarks_minmax", "dd_score_landmarks_minmax", "dd_update_residency",
-    "dd_prefetch_kv",
+    "dd_prefetch_kv", "dd_select_topk_mass",
 )
 
 
@@ -58,6 +58,9 @@ class StepArgs(ctypes.Structure):
         ("lm_kind", ctypes.c_int),
         ("K_tail", _vp),
         ("V_tail", _vp),
+        ("mass_gamma", ctypes.c_float),
+        ("mass_k_min", ctypes.c_int32),
+        ("sel_cnt", _vp),
     ]
 
 
@@ -79,6 +82,7 @@ def _load():
         "dd_sparse_attn_decode": (i32, [_vp] * 12 + [f32, _vp, _vp]),
         "dd_step": (i32, [_vp, ctypes.POINTER(StepArgs), _vp]),
         "dd_update_residency": (i32, [_vp, i32, i32, i32] + [_vp] * 13),
+        "dd_select_topk_mass": (i32, [_vp, _vp, _vp, _vp, f32, i32, f32, _vp]),
         "dd_prefetch_kv": (i32, [_vp, _vp, i32, i32, i32, _vp, _vp, _vp, _vp, _vp, _vp, i32, _vp]),
         "dd_get_status": (i32, [_vp, ctypes.POINTER(i32)]),
         "dd_launch_count": (i64, [_vp]),
@@ -273,6 +277,16 @@ class Context:
             _ptr(out, torch.float32, s.B * s.n_q * s.Hq * s.d, name="out"), _stream(stream)),
             "dd_sparse_attn_decode")
 
+    def select_topk_mass(self, scores, sel, gamma, k_min=1, sel_cnt=None, softmax_scale=0.0, stream=None):
+        """Coverage-budget top-k (see dd.h): rows padded with -1, lengths in sel_cnt."""
+        s = self.shape
+        rows = s.B * s.n_q * s.Hkv
+        _chk(_lib.dd_select_topk_mass(
+            self._h, _ptr(scores, torch.float32, rows * s.C, name="scores"),
+            _ptr(sel, torch.int32, rows * s.k, name="sel"),
+            _ptr(sel_cnt, torch.int32, rows, name="sel_cnt", allow_none=True), float(gamma), int(k_min),
+            float(softmax_scale), _stream(stream)), "dd_select_topk_mass")
+
     def prefetch_kv(self, sel, n_pred, Kh, Vh, Kpf, Vpf, pf_map, pf_count=None, ctas_per_sm=8, stream=None,
                     sel_rows=None, first_row=0):
         """Predictive prefetch of rows first_row .. first_row+n_pred-1 of ``sel``
@@ -318,7 +332,7 @@ class Context:
 
     def step(self, layer, q, lm, Kh, Vh, resident_slot, Khot, Vhot, Kst_pair, Vst_pair, out,
              mode=GATHER_ZEROCOPY, softmax_scale=0.0, intermediates=None, stage_events=None, stream=None,
-             lm_kind=LM_MEAN, K_tail=None, V_tail=None):
+             lm_kind=LM_MEAN, K_tail=None, V_tail=None, mass_gamma=0.0, mass_k_min=1, sel_cnt=None):
         """One layer; ``intermediates`` optionally maps names of dd_step_args' optional
         outputs (scores, sel, union_idx, union_slot, union_qmask, union_cnt, miss_list,
         miss_count, attn_slot) to caller tensors; ``stage_events`` optionally gives six
@@ -329,6 +343,9 @@ class Context:
         a.layer = int(layer)
         a.q = _ptr(q, torch.bfloat16, s.B * s.n_q * s.Hq * s.d, name="q")
         a.lm_kind = int(lm_kind)
+        a.mass_gamma = float(mass_gamma)
+        a.mass_k_min = int(mass_k_min)
+        a.sel_cnt = _ptr(sel_cnt, torch.int32, s.B * s.n_q * s.Hkv, name="sel_cnt", allow_none=True)
         a.K_tail = _ptr(K_tail, torch.bfloat16, s.B * s.n_q * s.Hkv * s.d, name="K_tail", allow_none=True)
         a.V_tail = _ptr(V_tail, torch.bfloat16, s.B * s.n_q * s.Hkv * s.d, name="V_tail", allow_none=True)
         a.lm = _ptr(lm, torch.bfloat16, s.B * s.Hkv * s.C * s.d * (2 if lm_kind == LM_MINMAX else 1), name="lm")
