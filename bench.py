@@ -515,6 +515,7 @@ def run_ours(args, world, rank, local):
 
 # ------------------------------------------------------------------ pipelined decode (predictive prefetch)
 DRIFT_T, SIGMA_DRIFT, SIGMA_SPEC = 8, 0.3, 0.1
+RES_SLOTS_PER_K, RES_CAP_PER_K = 4, 4     # hot pool of 4k slots per (b,g); admit up to k/2 per step
 
 
 def run_pipeline(args, world, rank, local):
@@ -647,6 +648,49 @@ def run_pipeline(args, world, rank, local):
     assert ctx_hi.status() == 0
     ctx_hi.close()
     ctx_lo.close()
+
+    # the same drifting steps with a per-(b,g) hot pool kept by the capped LRU
+    # residency update after every step (OasisKV delta selection)
+    S, cap_r = RES_SLOTS_PER_K * w.k, RES_CAP_PER_K * w.k // 8
+    ctx_r = dd.Context(shape, max_misses=cap, hot_slots=units * S)
+    nh = units * S * w.cs * w.d
+    pools = []
+    for _ in range(N):
+        pools.append(dict(rs=torch.full((units * w.C,), -1, dtype=torch.int32, device="cuda"),
+                          sc=torch.full((units * S,), -1, dtype=torch.int32, device="cuda"),
+                          lu=torch.full((units * S,), -1, dtype=torch.int32, device="cuda"),
+                          K=torch.empty(nh, dtype=torch.bfloat16, device="cuda"),
+                          V=torch.empty(nh, dtype=torch.bfloat16, device="cuda")))
+    inter_r = {"union_idx": torch.empty(units * shape.umax, dtype=torch.int32, device="cuda"),
+               "union_slot": torch.empty(units * shape.umax, dtype=torch.int32, device="cuda"),
+               "union_cnt": torch.empty(units, dtype=torch.int32, device="cuda")}
+    miss_r = torch.zeros(K * N, dtype=torch.int32, device="cuda")
+
+    def with_residency(i, rec=None):
+        for l in range(N):
+            L_, P_ = layers[l], pools[l]
+            g_ = i * N + l
+            inter = dict(inter_r)
+            inter["miss_count"] = miss_r[rec * N + l:rec * N + l + 1] if rec is not None else miss_r[:1]
+            ctx_r.step(g_, q_of(i, l), L_.lm, L_.Kh, L_.Vh, P_["rs"], P_["K"], P_["V"], Kurg, Vurg, out,
+                       intermediates=inter, stream=hi)
+            ctx_r.update_residency(i + 1, cap_r, S, Kurg[g_ & 1], Vurg[g_ & 1], P_["rs"], P_["sc"], P_["lu"],
+                                   P_["K"], P_["V"], union_idx=inter["union_idx"], union_slot=inter["union_slot"],
+                                   union_cnt=inter["union_cnt"], miss_count=inter["miss_count"], stream=hi)
+
+    for i in range(max(args.warmup, 2 * T)):       # fill the pools
+        with_residency(i)
+    torch.cuda.synchronize()
+    a3, b3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a3.record(hi)
+    for i in range(K):
+        with_residency(max(args.warmup, 2 * T) + i, rec=i)
+    b3.record(hi)
+    torch.cuda.synchronize()
+    t_res = a3.elapsed_time(b3) * 1e-3
+    assert ctx_r.status() == 0
+    ctx_r.close()
+    M_res = miss_r.double().mean().item()
     t_max = max_over_ranks(t_pipe, world)
     U = ucnt.double().sum(1).mean().item()
     M = miss.double().mean().item()
@@ -669,6 +713,10 @@ def run_pipeline(args, world, rank, local):
                            "urgent_bytes": M * chunk_b, "prefetch_bytes": P * chunk_b,
                            "host_link_gbs": (M + P) * chunk_b * steps / t_pipe / 1e9},
         "serialized_same_steps": {"value": steps / t_ser, "unit": UNIT, "ms_per_step": 1e3 * t_ser / steps},
+        "residency_same_steps": {"value": steps / t_res, "unit": UNIT, "ms_per_step": 1e3 * t_res / steps,
+                                 "slots_per_unit": S, "cap_per_unit_and_step": cap_r,
+                                 "missing_chunks_per_layer_step": M_res,
+                                 "note": "serialized steps, each followed by the capped LRU residency update"},
         "host_link_peaks_gbs": {"memcpy_h2d": link_memcpy},
         "e2e": None,
         "gpu_launches": None,

@@ -476,6 +476,9 @@ dd_status dd_update_residency(dd_ctx *c, int32_t step, int32_t cap, int32_t slot
       (cudaStream_t)stream));
 }
 
+// shared memory a fused selection kernel may ask for beyond its ~27 KB of static arrays
+constexpr size_t kFusedSelectSmem = 160 * 1024;
+
 dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   if (!c || !a || a->layer < 0) return DD_ERR_INVALID_ARG;
   if (a->lm_kind != DD_LM_MEAN && a->lm_kind != DD_LM_MINMAX) return DD_ERR_INVALID_ARG;
@@ -501,20 +504,42 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
     return a->stage_events[i] ? cuda_ok(cudaEventRecord((cudaEvent_t)a->stage_events[i], s)) : DD_OK;
   };
   DD_TRY(mark(0));
-  if (a->lm_kind == DD_LM_MINMAX) {
-    DD_TRY(dd_score_landmarks_minmax(c, a->q, a->lm, scores, stream));
+  const dd_dims &d = c->dims;
+  // scoring, top-k and the union in one kernel per (b,g) when a unit's score
+  // rows fit in shared memory (fixed k only); scores, selections and slots per
+  // selection entry are then produced only when the caller asks for them
+  const bool fused = a->mass_gamma <= 0.f && dd::fused_select_smem(d.n_q, c->C, d.k) <= kFusedSelectSmem;
+  if (fused) {
+    if (!aligned16(a->q) || !aligned16(a->lm)) return DD_ERR_INVALID_ARG;
+    int32_t *sel_out = (a->sel || a->attn_slot) ? sel : nullptr;
+    DD_CUDA(dd::launch_select_fused(a->lm_kind == DD_LM_MINMAX, static_cast<const uint4 *>(a->q),
+                                    static_cast<const uint4 *>(a->lm), a->scores, sel_out, a->resident_slot,
+                                    union_idx, union_slot, union_qmask, union_cnt, c->unit_miss, c->units, d.n_q,
+                                    d.Hq, d.Hkv, c->C, d.k, c->umax, c->hot_slots, c->status, s));
+    DD_TRY(mark(1));
+    DD_TRY(mark(2));
+    const dd::AttnPlanOut po = {c->chunk_off, c->cta_tab, c->flat, c->plan.n_cta};
+    DD_CUDA(dd::launch_assign(sel_out, union_idx, union_slot, union_qmask, union_cnt, c->unit_miss, miss_list,
+                              miss_count, sel_out ? a->attn_slot : nullptr, c->units, d.n_q, d.Hkv, d.k, c->C,
+                              c->umax, c->max_misses, c->hot_slots, d.cs, &po, c->status, s));
+    c->launches += 2;
   } else {
-    DD_TRY(dd_score_landmarks(c, a->q, a->lm, scores, stream));
+    if (a->lm_kind == DD_LM_MINMAX) {
+      DD_TRY(dd_score_landmarks_minmax(c, a->q, a->lm, scores, stream));
+    } else {
+      DD_TRY(dd_score_landmarks(c, a->q, a->lm, scores, stream));
+    }
+    DD_TRY(mark(1));
+    if (a->mass_gamma > 0.f) {
+      DD_TRY(dd_select_topk_mass(c, scores, sel, a->sel_cnt, a->mass_gamma, a->mass_k_min, a->softmax_scale,
+                                 stream));
+    } else {
+      DD_TRY(dd_select_topk(c, scores, sel, stream));
+    }
+    DD_TRY(mark(2));
+    DD_TRY(resolve_impl(c, sel, a->resident_slot, union_idx, union_slot, union_qmask, union_cnt, miss_list,
+                        miss_count, attn_slot, true, stream));
   }
-  DD_TRY(mark(1));
-  if (a->mass_gamma > 0.f) {
-    DD_TRY(dd_select_topk_mass(c, scores, sel, a->sel_cnt, a->mass_gamma, a->mass_k_min, a->softmax_scale, stream));
-  } else {
-    DD_TRY(dd_select_topk(c, scores, sel, stream));
-  }
-  DD_TRY(mark(2));
-  DD_TRY(resolve_impl(c, sel, a->resident_slot, union_idx, union_slot, union_qmask, union_cnt, miss_list,
-                      miss_count, attn_slot, true, stream));
   DD_TRY(mark(3));
   // staging buffer p may still be read by the attention of layer - 2; on the
   // same stream the stream order already guarantees it, and leaving out the

@@ -54,6 +54,34 @@ __device__ __forceinline__ uint4 ldg_nc(const uint4 *p) {
   return r;
 }
 
+// Butterfly over the 16 lanes sharing a row: x[0..15] in every lane ->
+// lane `part` returns the 16-lane sum of x[part].
+__device__ __forceinline__ float butterfly16(float (&x)[16], int part) {
+  float y[8], z[4], w[2];
+  const bool b3 = part & 8, b2 = part & 4, b1 = part & 2, b0 = part & 1;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float send = b3 ? x[i] : x[i + 8];
+    const float keep = b3 ? x[i + 8] : x[i];
+    y[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b2 ? y[i] : y[i + 4];
+    const float keep = b2 ? y[i + 4] : y[i];
+    z[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b1 ? z[i] : z[i + 2];
+    const float keep = b1 ? z[i + 2] : z[i];
+    w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  const float send = b0 ? w[0] : w[1];
+  const float keep = b0 ? w[1] : w[0];
+  return keep + __shfl_xor_sync(0xffffffffu, send, 1);
+}
+
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Every kernel of the library is launched with
 // programmatic stream serialization (launch_k below): its CTAs may become
@@ -184,6 +212,12 @@ cudaError_t launch_build_minmax(const uint4 *K, uint4 *lm2, int64_t n_chunks, in
 cudaError_t launch_score_minmax(const uint4 *q, const uint4 *lm2, float *scores, int B, int n_q, int Hq, int Hkv,
                                 int C, cudaStream_t s);
 cudaError_t launch_topk(const float *scores, int32_t *sel, int rows, int C, int k, cudaStream_t s);
+size_t fused_select_smem(int n_q, int C, int k);
+cudaError_t launch_select_fused(bool minmax, const uint4 *q, const uint4 *lm, float *scores, int32_t *sel,
+                                const int32_t *resident_slot, int32_t *union_idx, int32_t *union_slot,
+                                uint8_t *union_qmask, int32_t *union_cnt, int32_t *unit_miss, int units, int n_q,
+                                int Hq, int Hkv, int C, int k, int umax, int64_t hot_slots, int32_t *status,
+                                cudaStream_t s);
 cudaError_t launch_topk_mass(const float *scores, int32_t *sel, int32_t *sel_cnt, int rows, int C, int k_max,
                              int k_min, float gamma, float tau_log2e, cudaStream_t s);
 cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx,

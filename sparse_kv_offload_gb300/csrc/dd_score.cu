@@ -130,34 +130,6 @@ constexpr int kTilesPerCta = 4;
 __host__ __device__ constexpr int score_pass(bool mm) { return mm ? 4 : 8; }
 __host__ __device__ constexpr int score_tile(bool mm) { return score_pass(mm) * kRowsPerPass; }
 
-// Butterfly over the 16 lanes sharing a row: x[0..15] in every lane ->
-// lane `part` returns the 16-lane sum of x[part].
-__device__ __forceinline__ float butterfly16(float (&x)[16], int part) {
-  float y[8], z[4], w[2];
-  const bool b3 = part & 8, b2 = part & 4, b1 = part & 2, b0 = part & 1;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float send = b3 ? x[i] : x[i + 8];
-    const float keep = b3 ? x[i + 8] : x[i];
-    y[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float send = b2 ? y[i] : y[i + 4];
-    const float keep = b2 ? y[i + 4] : y[i];
-    z[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float send = b1 ? z[i] : z[i + 2];
-    const float keep = b1 ? z[i + 2] : z[i];
-    w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-  }
-  const float send = b0 ? w[0] : w[1];
-  const float keep = b0 ? w[1] : w[0];
-  return keep + __shfl_xor_sync(0xffffffffu, send, 1);
-}
-
 template <int NQ, bool MM>
 __global__ void __launch_bounds__(kScoreThreads) k_score(const uint4 *__restrict__ q, const uint4 *__restrict__ lm,
                                                          float *__restrict__ scores, int Hq, int Hkv, int C) {

@@ -335,25 +335,22 @@ cudaError_t launch_topk_mass(const float *scores, int32_t *sel, int32_t *sel_cnt
 constexpr int kUnionThreads = 512;
 constexpr int kMaxWords = kMaxC / 32;
 
-__global__ void __launch_bounds__(kUnionThreads) k_union(
-    const int32_t *__restrict__ sel, const int32_t *__restrict__ resident_slot, int32_t *__restrict__ union_idx,
-    int32_t *__restrict__ union_slot, uint8_t *__restrict__ union_qmask, int32_t *__restrict__ union_cnt,
-    int32_t *__restrict__ unit_miss, int n_q, int sel_rows, int Hkv, int k, int C, int umax, int64_t hot_slots,
-    int32_t *status) {
-  __shared__ uint32_t qbits[kMaxNq * kMaxWords];
-  __shared__ uint32_t missw[kMaxWords];
-  __shared__ int scratch[33];
-  const int unit = blockIdx.x;
-  const int b = unit / Hkv, g = unit - b * Hkv;
-  const int tid = threadIdx.x;
+// The union of one unit's n_q selection rows (row j at selb + j * jstride,
+// device or shared memory) and its residency lookup; `qbits` (n_q * W words)
+// and `missw` (W words) are shared scratch.  All threads of the CTA.
+__device__ __forceinline__ void union_unit(const int32_t *selb, int64_t jstride, int unit, int n_q, int k, int C,
+                                           int umax, int64_t hot_slots, const int32_t *__restrict__ resident_slot,
+                                           int32_t *__restrict__ union_idx, int32_t *__restrict__ union_slot,
+                                           uint8_t *__restrict__ union_qmask, int32_t *__restrict__ union_cnt,
+                                           int32_t *__restrict__ unit_miss, uint32_t *qbits, uint32_t *missw,
+                                           int *scratch, int32_t *status) {
+  const int tid = threadIdx.x, nt = blockDim.x;
   const int W = (C + 31) >> 5;
-  for (int i = tid; i < n_q * W; i += kUnionThreads) qbits[i] = 0u;
-  pdl_wait();
-  pdl_trigger();
+  for (int i = tid; i < n_q * W; i += nt) qbits[i] = 0u;
   __syncthreads();
-  for (int i = tid; i < n_q * k; i += kUnionThreads) {
+  for (int i = tid; i < n_q * k; i += nt) {
     const int j = i / k, r = i - j * k;
-    const int c = sel[((int64_t)(b * sel_rows + j) * Hkv + g) * k + r];
+    const int c = selb[j * jstride + r];
     if (c == -1) continue;   // padding of a row shorter than k (coverage budgets)
     if (c < 0 || c >= C) {
       set_status(status, DD_ERR_DEVICE_CHECK);
@@ -363,7 +360,7 @@ __global__ void __launch_bounds__(kUnionThreads) k_union(
   }
   __syncthreads();
 
-  const int per = (W + kUnionThreads - 1) / kUnionThreads;
+  const int per = (W + nt - 1) / nt;
   const int w0 = min(W, tid * per), w1 = min(W, w0 + per);
   const int32_t *rs_unit = resident_slot + (int64_t)unit * C;
   int cnt_u = 0, cnt_m = 0;
@@ -411,6 +408,245 @@ __global__ void __launch_bounds__(kUnionThreads) k_union(
     union_cnt[unit] = total >> 16;
     unit_miss[unit] = total & 0xFFFF;
   }
+}
+
+__global__ void __launch_bounds__(kUnionThreads) k_union(
+    const int32_t *__restrict__ sel, const int32_t *__restrict__ resident_slot, int32_t *__restrict__ union_idx,
+    int32_t *__restrict__ union_slot, uint8_t *__restrict__ union_qmask, int32_t *__restrict__ union_cnt,
+    int32_t *__restrict__ unit_miss, int n_q, int sel_rows, int Hkv, int k, int C, int umax, int64_t hot_slots,
+    int32_t *status) {
+  __shared__ uint32_t qbits[kMaxNq * kMaxWords];
+  __shared__ uint32_t missw[kMaxWords];
+  __shared__ int scratch[33];
+  pdl_wait();
+  pdl_trigger();
+  const int unit = blockIdx.x;
+  const int b = unit / Hkv, g = unit - b * Hkv;
+  union_unit(sel + ((int64_t)b * sel_rows * Hkv + g) * k, (int64_t)Hkv * k, unit, n_q, k, C, umax, hot_slots,
+             resident_slot, union_idx, union_slot, union_qmask, union_cnt, unit_miss, qbits, missw, scratch, status);
+}
+
+cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx, int32_t *union_slot,
+                         uint8_t *union_qmask, int32_t *union_cnt, int32_t *unit_miss, int units, int n_q, int Hkv,
+                         int k, int C, int umax, int64_t hot_slots, int32_t *status, cudaStream_t s, int sel_rows) {
+  if (units == 0) return cudaSuccess;
+  return launch_k(k_union, dim3(units), dim3(kUnionThreads), 0, s, sel, resident_slot, union_idx, union_slot,
+                  union_qmask, union_cnt, unit_miss, n_q, sel_rows > 0 ? sel_rows : n_q, Hkv, k, C, umax, hot_slots,
+                  status);
+}
+
+// ---------------------------------------------------------------------------
+// a1 + a2 + a3 pass 1 fused, one CTA (512 threads) per (b,g) unit, when the
+// unit's n_q score rows fit in shared memory: the landmarks of the unit are
+// scored for all queries exactly as k_score does (16 lanes per landmark row,
+// same per-lane FMA order and butterfly, so the scores are the same bits),
+// kept in shared memory; the top-k of every row comes from one radix select
+// over all rows at once (per-row histograms, warp j settles row j); the
+// union and residency lookup then read the selections from shared memory.
+// Scores and selections are also written to device memory when asked for.
+// ---------------------------------------------------------------------------
+constexpr int kFusedThreads = 512;
+constexpr int kFusedRowsPerPass = kFusedThreads / 16;   // 32 landmarks per pass
+
+template <int NQ, bool MM>
+__global__ void __launch_bounds__(kFusedThreads) k_select_fused(
+    const uint4 *__restrict__ q, const uint4 *__restrict__ lm, float *__restrict__ scores_out,
+    int32_t *__restrict__ sel_out, const int32_t *__restrict__ resident_slot, int32_t *__restrict__ union_idx,
+    int32_t *__restrict__ union_slot, uint8_t *__restrict__ union_qmask, int32_t *__restrict__ union_cnt,
+    int32_t *__restrict__ unit_miss, int Hq, int Hkv, int C, int k, int umax, int64_t hot_slots, int32_t *status) {
+  // landmarks per thread per tile: fewer for many queries (512 threads leave 128 registers each)
+  constexpr int kPass = (MM ? 4 : 8) / (NQ >= 5 ? 2 : 1);
+  constexpr int kTile = kPass * kFusedRowsPerPass;
+  constexpr int kVecs = MM ? 2 : 1;
+  constexpr int kVals = kPass * NQ;
+  constexpr int kChunks = (kVals + 15) / 16;
+  extern __shared__ uint32_t fsm[];                        // keys [NQ][C], then selections [NQ][k]
+  __shared__ uint32_t qbits[kMaxNq * kMaxWords];
+  __shared__ uint32_t missw[kMaxWords];
+  __shared__ int hist[NQ][256];
+  __shared__ int scratch[33];
+  __shared__ uint32_t s_prefix[NQ];
+  __shared__ int s_remaining[NQ];
+  pdl_wait();
+  pdl_trigger();
+  const int unit = blockIdx.x;
+  const int b = unit / Hkv, g = unit - b * Hkv;
+  const int G = Hq / Hkv;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int part = tid & 15, sub = tid >> 4;
+  float *sc = reinterpret_cast<float *>(fsm);
+  int32_t *sel_s = reinterpret_cast<int32_t *>(fsm + NQ * C);
+  const uint4 *base = lm + (int64_t)unit * C * kVecs * kVecPerRow + part;
+
+  // ---- a1: scores of the whole unit, into shared memory
+  uint4 v[kPass][kVecs], nv[kPass][kVecs];
+#pragma unroll
+  for (int p = 0; p < kPass; ++p) {
+    const int c = p * kFusedRowsPerPass + sub;
+#pragma unroll
+    for (int e = 0; e < kVecs; ++e)
+      v[p][e] = (c < C) ? ldg_nc(base + ((int64_t)c * kVecs + e) * kVecPerRow) : make_uint4(0, 0, 0, 0);
+  }
+  float qs[NQ][8];
+#pragma unroll
+  for (int j = 0; j < NQ; ++j) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qs[j][e] = 0.f;
+    for (int h = g * G; h < (g + 1) * G; ++h) {
+      float f[8];
+      unpack8(q[((int64_t)(b * NQ + j) * Hq + h) * kVecPerRow + part], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qs[j][e] += f[e];
+    }
+  }
+  for (int c0 = 0; c0 < C; c0 += kTile) {
+#pragma unroll
+    for (int p = 0; p < kPass; ++p) {
+      const int c = c0 + kTile + p * kFusedRowsPerPass + sub;
+#pragma unroll
+      for (int e = 0; e < kVecs; ++e)
+        nv[p][e] = (c < C) ? ldg_nc(base + ((int64_t)c * kVecs + e) * kVecPerRow) : make_uint4(0, 0, 0, 0);
+    }
+    float x[kChunks * 16];
+#pragma unroll
+    for (int a = kVals; a < kChunks * 16; ++a) x[a] = 0.f;
+#pragma unroll
+    for (int p = 0; p < kPass; ++p) {
+      float f[8], fh[8];
+      unpack8(v[p][0], f);
+      if (MM) unpack8(v[p][kVecs - 1], fh);
+#pragma unroll
+      for (int j = 0; j < NQ; ++j) {
+        float acc = 0.f;
+        if (MM) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc += fmaxf(qs[j][e] * f[e], qs[j][e] * fh[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc = fmaf(qs[j][e], f[e], acc);
+        }
+        x[p * NQ + j] = acc;
+      }
+    }
+#pragma unroll
+    for (int ch = 0; ch < kChunks; ++ch) {
+      float xs[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) xs[i] = x[ch * 16 + i];
+      const float r = butterfly16(xs, part);
+      const int a = ch * 16 + part;
+      const int c = c0 + (a / NQ) * kFusedRowsPerPass + sub;
+      if (a < kVals && c < C) sc[(a % NQ) * C + c] = r;
+    }
+#pragma unroll
+    for (int p = 0; p < kPass; ++p)
+#pragma unroll
+      for (int e = 0; e < kVecs; ++e) v[p][e] = nv[p][e];
+  }
+  __syncthreads();
+  if (scores_out) {
+    for (int i = tid; i < NQ * C; i += kFusedThreads) {
+      const int j = i / C, c = i - j * C;
+      scores_out[((int64_t)(b * NQ + j) * Hkv + g) * C + c] = sc[i];
+    }
+  }
+  // ---- a2: radix select of all NQ rows at once (scores become order keys in place)
+  uint32_t *keys = fsm;
+  for (int i = tid; i < NQ * C; i += kFusedThreads) keys[i] = order_key(sc[i]);
+  uint32_t prefix = 0, pmask = 0;   // of row `warp` (warps >= NQ carry no row)
+  int remaining = k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < NQ * 256; i += kFusedThreads) (&hist[0][0])[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < NQ * C; i += kFusedThreads) {
+      const int j = i / C;
+      const uint32_t key = keys[i];
+      const uint32_t pj = shift == 24 ? 0u : s_prefix[j];
+      if ((key & pmask) == pj) atomicAdd(&hist[j][(key >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (warp < NQ) {
+      int cnt[8], s = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        cnt[e] = hist[warp][255 - 8 * lane - e];
+        s += cnt[e];
+      }
+      const int incl = warp_incl_scan(s);
+      const int excl = incl - s;
+      if (excl < remaining && remaining <= incl) {
+        int r = remaining - excl;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (r > 0 && r <= cnt[e]) {
+            s_prefix[warp] = prefix | ((uint32_t)(255 - 8 * lane - e) << shift);
+            s_remaining[warp] = r;
+            r = 0;
+          } else if (r > 0) {
+            r -= cnt[e];
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (warp < NQ) {
+      prefix = s_prefix[warp];
+      remaining = s_remaining[warp];
+    }
+    pmask |= 0xFFu << shift;
+    __syncthreads();
+  }
+  for (int j = 0; j < NQ; ++j) emit_topk(keys + j * C, C, s_prefix[j], s_remaining[j], scratch, sel_s + j * k);
+  __syncthreads();
+  if (sel_out) {
+    for (int i = tid; i < NQ * k; i += kFusedThreads) {
+      const int j = i / k, r = i - j * k;
+      sel_out[((int64_t)(b * NQ + j) * Hkv + g) * k + r] = sel_s[i];
+    }
+  }
+  // ---- a3 pass 1: union and residency from the shared selections
+  union_unit(sel_s, k, unit, NQ, k, C, umax, hot_slots, resident_slot, union_idx, union_slot, union_qmask,
+             union_cnt, unit_miss, qbits, missw, scratch, status);
+}
+
+size_t fused_select_smem(int n_q, int C, int k) { return (size_t)n_q * C * 4 + (size_t)n_q * k * 4; }
+
+template <bool MM>
+static cudaError_t launch_select_fused_t(const uint4 *q, const uint4 *lm, float *scores, int32_t *sel,
+                                         const int32_t *resident_slot, int32_t *union_idx, int32_t *union_slot,
+                                         uint8_t *union_qmask, int32_t *union_cnt, int32_t *unit_miss, int units,
+                                         int n_q, int Hq, int Hkv, int C, int k, int umax, int64_t hot_slots,
+                                         int32_t *status, cudaStream_t s) {
+  const size_t smem = fused_select_smem(n_q, C, k);
+  switch (n_q) {
+#define DD_FUSED_CASE(N)                                                                                        \
+  case N: {                                                                                                      \
+    cudaError_t e = cudaFuncSetAttribute(k_select_fused<N, MM>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                                         (int)smem);                                                             \
+    if (e != cudaSuccess) return e;                                                                              \
+    return launch_k(k_select_fused<N, MM>, dim3(units), dim3(kFusedThreads), smem, s, q, lm, scores, sel,       \
+                    resident_slot, union_idx, union_slot, union_qmask, union_cnt, unit_miss, Hq, Hkv, C, k, umax, \
+                    hot_slots, status);                                                                         \
+  }
+    DD_FUSED_CASE(1) DD_FUSED_CASE(2) DD_FUSED_CASE(3) DD_FUSED_CASE(4)
+    DD_FUSED_CASE(5) DD_FUSED_CASE(6) DD_FUSED_CASE(7) DD_FUSED_CASE(8)
+#undef DD_FUSED_CASE
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_select_fused(bool minmax, const uint4 *q, const uint4 *lm, float *scores, int32_t *sel,
+                                const int32_t *resident_slot, int32_t *union_idx, int32_t *union_slot,
+                                uint8_t *union_qmask, int32_t *union_cnt, int32_t *unit_miss, int units, int n_q,
+                                int Hq, int Hkv, int C, int k, int umax, int64_t hot_slots, int32_t *status,
+                                cudaStream_t s) {
+  if (units == 0) return cudaSuccess;
+  return minmax ? launch_select_fused_t<true>(q, lm, scores, sel, resident_slot, union_idx, union_slot, union_qmask,
+                                              union_cnt, unit_miss, units, n_q, Hq, Hkv, C, k, umax, hot_slots,
+                                              status, s)
+                : launch_select_fused_t<false>(q, lm, scores, sel, resident_slot, union_idx, union_slot,
+                                               union_qmask, union_cnt, unit_miss, units, n_q, Hq, Hkv, C, k, umax,
+                                               hot_slots, status, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -480,15 +716,6 @@ __global__ void __launch_bounds__(kAssignThreads) k_assign(
     }
     attn_slot[si] = found >= 0 ? union_slot[ubase + found] : INT32_MIN;
   }
-}
-
-cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx, int32_t *union_slot,
-                         uint8_t *union_qmask, int32_t *union_cnt, int32_t *unit_miss, int units, int n_q, int Hkv,
-                         int k, int C, int umax, int64_t hot_slots, int32_t *status, cudaStream_t s, int sel_rows) {
-  if (units == 0) return cudaSuccess;
-  return launch_k(k_union, dim3(units), dim3(kUnionThreads), 0, s, sel, resident_slot, union_idx, union_slot,
-                  union_qmask, union_cnt, unit_miss, n_q, sel_rows > 0 ? sel_rows : n_q, Hkv, k, C, umax, hot_slots,
-                  status);
 }
 
 cudaError_t launch_assign(const int32_t *sel, const int32_t *union_idx, int32_t *union_slot,

@@ -163,3 +163,21 @@ def test_invalid_arguments_are_rejected_on_the_host(dd):
                           torch.zeros(1, dtype=torch.int32, device="cuda"),
                           torch.empty(4 * w.cs * w.d, dtype=torch.bfloat16, device="cuda"),
                           torch.empty(4 * w.cs * w.d, dtype=torch.bfloat16, device="cuda"))
+
+
+@pytest.mark.parametrize("w", STEP_CASES[:3], ids=lambda w: w.name)
+def test_step_without_intermediates_gives_the_same_output(dd, w):
+    # the step produces scores, selections and per-entry slots only when asked;
+    # the attention output must not depend on that
+    import torch
+    x = tl.host_inputs(w)
+    buf = StepBuffers(w, x)
+    with dd.Context(shape_of(w), max_misses=buf.cap, hot_slots=buf.hot) as ctx:
+        buf.run(ctx, layer=0)
+        full = buf.out.clone()
+        mc = torch.empty(1, dtype=torch.int32, device="cuda")
+        ctx.step(2, buf.q, buf.lm, buf.Kh, buf.Vh, buf.slot, buf.Khot, buf.Vhot, buf.Kst, buf.Vst, buf.out,
+                 intermediates={"miss_count": mc})
+        assert ctx.status() == 0
+    assert torch.equal(full, buf.out)
+    assert int(mc.item()) == int(buf.inter["miss_count"].item())
