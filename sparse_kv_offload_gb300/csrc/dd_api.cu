@@ -24,8 +24,10 @@ struct dd_ctx {
   int32_t *unit_miss = nullptr, *miss_list = nullptr, *miss_count = nullptr, *attn_slot = nullptr;
   float *part_o = nullptr, *part_ml = nullptr;
   int32_t *chunk_off = nullptr;
-  int4 *cta_tab = nullptr;
   int4 *flat = nullptr;
+  unsigned long long *lb_word = nullptr;        // fused selection: look-back words, ticket
+  int32_t *ticket = nullptr;
+  uint32_t epoch = 0;
   void *dummy_pool = nullptr;
   dd::AttnPlan plan;
   // host side
@@ -178,9 +180,10 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   add(c->plan.part_o_floats, 4);               // part_o
   add(c->plan.part_ml_floats, 4);              // part_ml
   add(units + 1, 4);                           // chunk_off
-  add(c->plan.n_cta, 16);                      // cta_tab
   add(c->plan.flat_entries, 16);               // flat chunk table
   add(64 * 128, 2);                            // dummy pool (64 rows)
+  add(units, 8);                               // look-back words
+  add(2, 4);                                   // ticket
   if (cudaMalloc(&c->ws, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
   uint8_t *cur = static_cast<uint8_t *>(c->ws);
   c->status = carve<int32_t>(cur, 1);
@@ -197,9 +200,10 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   c->part_o = carve<float>(cur, c->plan.part_o_floats);
   c->part_ml = carve<float>(cur, c->plan.part_ml_floats);
   c->chunk_off = carve<int32_t>(cur, units + 1);
-  c->cta_tab = carve<int4>(cur, c->plan.n_cta);
   c->flat = carve<int4>(cur, c->plan.flat_entries);
   c->dummy_pool = carve<uint16_t>(cur, 64 * 128);
+  c->lb_word = carve<unsigned long long>(cur, units);
+  c->ticket = carve<int32_t>(cur, 2);
   if (cudaMemset(c->ws, 0, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
   if (cudaMallocHost(reinterpret_cast<void **>(&c->h_miss), (size_t)(1 + (max_misses > 0 ? max_misses : 1)) * 4) !=
       cudaSuccess)
@@ -318,7 +322,7 @@ static dd_status resolve_impl(dd_ctx *c, const int32_t *sel, const int32_t *resi
   const dd_dims &d = c->dims;
   DD_CUDA(dd::launch_union(sel, resident_slot, union_idx, union_slot, union_qmask, union_cnt, c->unit_miss, c->units,
                            d.n_q, d.Hkv, d.k, c->C, c->umax, c->hot_slots, c->status, s));
-  const dd::AttnPlanOut po = {c->chunk_off, c->cta_tab, c->flat, c->plan.n_cta};
+  const dd::AttnPlanOut po = {c->chunk_off, c->flat};
   DD_CUDA(dd::launch_assign(sel, union_idx, union_slot, union_qmask, union_cnt, c->unit_miss, miss_list, miss_count,
                             attn_slot, c->units, d.n_q, d.Hkv, d.k, c->C, c->umax, c->max_misses, c->hot_slots, d.cs,
                             with_plan ? &po : nullptr, c->status, s));
@@ -439,7 +443,7 @@ static dd_status attn_impl(dd_ctx *c, const void *q, const void *Khot, const voi
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)kD);
   const dd_dims &d = c->dims;
   c->launches += plan_ready ? 2 : 3;
-  const dd::AttnScratch scr = {c->part_o, c->part_ml, c->chunk_off, c->cta_tab, c->flat, c->dummy_pool};
+  const dd::AttnScratch scr = {c->part_o, c->part_ml, c->chunk_off, c->flat, c->dummy_pool};
   return cuda_ok(dd::launch_attn(q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count, scale, out,
                                  c->plan, scr, plan_ready, kh_dev, vh_dev, c->status, d.B, d.n_q, d.Hq, d.Hkv, d.cs,
                                  c->umax, c->hot_slots, c->max_misses, (cudaStream_t)stream, k_tail, v_tail));
@@ -476,9 +480,6 @@ dd_status dd_update_residency(dd_ctx *c, int32_t step, int32_t cap, int32_t slot
       (cudaStream_t)stream));
 }
 
-// shared memory a fused selection kernel may ask for beyond its ~27 KB of static arrays
-constexpr size_t kFusedSelectSmem = 160 * 1024;
-
 dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   if (!c || !a || a->layer < 0) return DD_ERR_INVALID_ARG;
   if (a->lm_kind != DD_LM_MEAN && a->lm_kind != DD_LM_MINMAX) return DD_ERR_INVALID_ARG;
@@ -508,21 +509,43 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   // scoring, top-k and the union in one kernel per (b,g) when a unit's score
   // rows fit in shared memory (fixed k only); scores, selections and slots per
   // selection entry are then produced only when the caller asks for them
-  const bool fused = a->mass_gamma <= 0.f && dd::fused_select_smem(d.n_q, c->C, d.k) <= kFusedSelectSmem;
+  const bool fused = a->mass_gamma <= 0.f && dd::fused_select_smem(d.n_q, c->C, d.k) > 0;
   if (fused) {
     if (!aligned16(a->q) || !aligned16(a->lm)) return DD_ERR_INVALID_ARG;
-    int32_t *sel_out = (a->sel || a->attn_slot) ? sel : nullptr;
+    c->epoch = (c->epoch + 1) & 0x3FFFFFFFu;   // 30 bits, never 0 (0 is the zeroed words' epoch)
+    if (c->epoch == 0) c->epoch = 1;
+    dd::SelectOut o;
+    o.scores = a->scores;
+    o.sel = a->sel;
+    o.attn_slot = a->attn_slot;
+    o.resident_slot = a->resident_slot;
+    o.union_idx = union_idx;
+    o.union_slot = union_slot;
+    o.union_qmask = union_qmask;
+    o.union_cnt = union_cnt;
+    o.unit_miss = c->unit_miss;
+    o.miss_list = miss_list;
+    o.miss_count = miss_count;
+    o.chunk_off = c->chunk_off;
+    o.flat = c->flat;
+    o.lb_word = c->lb_word;
+    o.ticket = c->ticket;
+    o.epoch = c->epoch;
+    o.units = c->units;
+    o.Hq = d.Hq;
+    o.Hkv = d.Hkv;
+    o.C = c->C;
+    o.k = d.k;
+    o.umax = c->umax;
+    o.cs = d.cs;
+    o.hot_slots = c->hot_slots;
+    o.max_misses = c->max_misses;
+    o.status = c->status;
     DD_CUDA(dd::launch_select_fused(a->lm_kind == DD_LM_MINMAX, static_cast<const uint4 *>(a->q),
-                                    static_cast<const uint4 *>(a->lm), a->scores, sel_out, a->resident_slot,
-                                    union_idx, union_slot, union_qmask, union_cnt, c->unit_miss, c->units, d.n_q,
-                                    d.Hq, d.Hkv, c->C, d.k, c->umax, c->hot_slots, c->status, s));
+                                    static_cast<const uint4 *>(a->lm), o, d.n_q, s));
     DD_TRY(mark(1));
     DD_TRY(mark(2));
-    const dd::AttnPlanOut po = {c->chunk_off, c->cta_tab, c->flat, c->plan.n_cta};
-    DD_CUDA(dd::launch_assign(sel_out, union_idx, union_slot, union_qmask, union_cnt, c->unit_miss, miss_list,
-                              miss_count, sel_out ? a->attn_slot : nullptr, c->units, d.n_q, d.Hkv, d.k, c->C,
-                              c->umax, c->max_misses, c->hot_slots, d.cs, &po, c->status, s));
-    c->launches += 2;
+    c->launches += 1;
   } else {
     if (a->lm_kind == DD_LM_MINMAX) {
       DD_TRY(dd_score_landmarks_minmax(c, a->q, a->lm, scores, stream));

@@ -55,7 +55,6 @@ struct StageMeta {
 struct AttnParams {
   const uint16_t *q;          // bf16 [B,n_q,Hq,128]
   const int32_t *chunk_off;   // [units+1] exclusive prefix of the union sizes
-  const int4 *cta_tab;        // per CTA: {first chunk, end chunk, first unit, 0}
   const int4 *flat;           // per chunk of the concatenated unions: {pool row code, query mask, host chunk, 0}
   const uint4 *kh, *vh;       // fused gather: device view of the pinned host K/V (null: staging comes by TMA)
   uint4 *kst, *vst;           // fused gather: staging buffers the host chunks are also written to
@@ -70,62 +69,26 @@ struct AttnParams {
 // pool row code of a chunk in the flat table: first hot-pool row as is,
 // staging row r as -2 - r, -1 = not loaded
 
-// largest unit u with chunk_off[u] <= x (the unit whose union holds chunk x)
-__device__ __forceinline__ int unit_of_chunk(const int32_t *off, int units, int x) {
-  int lo = 0, hi = units - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (off[mid] <= x) lo = mid; else hi = mid - 1;
+// Largest unit u with chunk_off[u] <= x (the unit whose union holds chunk x),
+// found by one warp: 32 probes per round (two rounds up to 1024 units).
+// Invariant: off[lo] <= x; the answer lies in [lo, lo + n).
+__device__ __forceinline__ int unit_of_chunk_warp(const int32_t *off, int units, int x) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, n = units;
+  while (n > 1) {
+    const int step = (n + 31) / 32;
+    const int idx = lo + lane * step;
+    const bool le = lane * step < n && off[idx] <= x;
+    const unsigned m = __ballot_sync(0xffffffffu, le);   // lane 0 always set
+    const int l = 31 - __clz(m);
+    lo += l * step;
+    n = min(step, n - l * step);
   }
   return lo;
 }
 
+
 // ----------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Bounded wait: gives up after ~2 s, records DD_ERR_TIMEOUT and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t *status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && globaltimer_ns() - t0 > 2000000000ull) {
-      set_status(status, DD_ERR_TIMEOUT);
-      return false;
-    }
-  }
-}
-
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
@@ -167,11 +130,6 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
   return r;
 }
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
 
 // ----------------------------------------------------------------- the kernel
 // Registers per thread: the register file holds one CTA, whose warps are
@@ -220,8 +178,10 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
   __syncthreads();
   pdl_wait();
   pdl_trigger();
-  const int4 slice = p.cta_tab[blockIdx.x];
-  const int lo = slice.x, hi = slice.y, u0 = slice.z, per = slice.w;
+  // self-planned slice of the concatenated unions (the same split the combine assumes)
+  const int total = p.chunk_off[p.units];
+  const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int lo = min(total, (int)blockIdx.x * per), hi = min(total, lo + per);
   if (lo >= hi) return;
   if (load_status(p.status) != 0) return;
 
@@ -232,6 +192,7 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
     // unit boundary; lane i of `bnd` holds the end of unit ubase + i
     const int chunks_per_stage = kStageRows / p.cs;
     const uint32_t box_bytes = (uint32_t)p.cs * 128u;
+    const int u0 = unit_of_chunk_warp(p.chunk_off, p.units, lo);
     int ubase = u0;
     int bnd = (ubase + 1 + lane <= p.units) ? p.chunk_off[ubase + 1 + lane] : 0x7FFFFFFF;
     int ustart = p.chunk_off[u0];
@@ -404,7 +365,6 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
     const int buf = s % kStages;
     if (!mbar_wait(full0 + 8 * buf, (s / kStages) & 1, p.status)) break;
     const int m_nch = meta[buf].nch, m_flags = meta[buf].flags, m_unit = meta[buf].unit;
-    const int m_uoff = meta[buf].uoff, m_ucnt = meta[buf].ucnt;
     const uint8_t *m_qm = meta[buf].qm;
     if (m_flags & kFirst) {
       // this run's query vectors from shared memory (padded rows: no bank conflicts)
@@ -622,8 +582,8 @@ __global__ void __launch_bounds__(kPlanThreads) k_attn_plan(
 // step follow one another along the sequence under a causal mask).
 __global__ void __launch_bounds__(128) k_attn_combine(const float *__restrict__ part_o,
                                                       const float *__restrict__ part_ml,
-                                                      const int32_t *__restrict__ chunk_off,
-                                                      const int4 *__restrict__ cta_tab, float *__restrict__ out,
+                                                      const int32_t *__restrict__ chunk_off, int n_cta,
+                                                      float *__restrict__ out,
                                                       const int32_t *status, int n_q, int Hq, int Hkv, int NQ,
                                                       int wpm, const uint16_t *__restrict__ q,
                                                       const uint16_t *__restrict__ k_tail,
@@ -633,7 +593,8 @@ __global__ void __launch_bounds__(128) k_attn_combine(const float *__restrict__ 
   pdl_trigger();
   if (load_status(status) != 0) return;
   const int unit = blockIdx.x, qv = blockIdx.y, col = threadIdx.x;
-  const int off = chunk_off[unit], U = chunk_off[unit + 1] - off, per = cta_tab[0].w;
+  const int off = chunk_off[unit], U = chunk_off[unit + 1] - off;
+  const int per = (chunk_off[gridDim.x] + n_cta - 1) / n_cta;   // the attention kernel's split
   const bool tail = k_tail != nullptr;
   if ((U <= 0 || per <= 0) && !tail) return;
   const int G = Hq / Hkv, b = unit / Hkv, g = unit - b * Hkv, j = qv / G, h = g * G + (qv - j * G);
@@ -785,7 +746,7 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
 
   cudaError_t e = cudaSuccess;
   if (!plan_ready) {
-    const AttnPlanOut po = {scr.chunk_off, scr.cta_tab, scr.flat, plan.n_cta};
+    const AttnPlanOut po = {scr.chunk_off, scr.flat};
     e = launch_k(k_attn_plan, dim3(units), dim3(kPlanThreads), 0, s, union_cnt, union_slot, union_qmask, miss_count,
                  po, out, units, umax, n_q, Hq, Hkv, has_hot ? hot_slots : 0, has_st ? max_misses : 0, cs, status);
     if (e != cudaSuccess) return e;
@@ -794,7 +755,6 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
   AttnParams p;
   p.q = static_cast<const uint16_t *>(q);
   p.chunk_off = scr.chunk_off;
-  p.cta_tab = scr.cta_tab;
   p.flat = scr.flat;
   const bool fused = kh_dev && vh_dev && has_st;
   p.kh = fused ? static_cast<const uint4 *>(kh_dev) : nullptr;
@@ -818,7 +778,7 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
   if (e != cudaSuccess) return e;
   const bool tail = k_tail && v_tail;
   return launch_k(k_attn_combine, dim3(units, NQ), dim3(128), 0, s, scr.part_o, scr.part_ml, scr.chunk_off,
-                  scr.cta_tab, out, status, n_q, Hq, Hkv, NQ, sh.wpm, static_cast<const uint16_t *>(q),
+                  plan.n_cta, out, status, n_q, Hq, Hkv, NQ, sh.wpm, static_cast<const uint16_t *>(q),
                   tail ? static_cast<const uint16_t *>(k_tail) : nullptr,
                   tail ? static_cast<const uint16_t *>(v_tail) : nullptr, p.scale_log2);
 }

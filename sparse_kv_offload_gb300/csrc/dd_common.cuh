@@ -83,6 +83,60 @@ __device__ __forceinline__ float butterfly16(float (&x)[16], int part) {
 }
 
 // ---------------------------------------------------------------------------
+// mbarriers (shared memory) with a bounded wait
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: gives up after ~2 s, records DD_ERR_TIMEOUT and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0 && globaltimer_ns() - t0 > 2000000000ull) {
+      set_status(status, DD_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// 1-D bulk copy global -> shared, completion counted on an mbarrier (16-byte
+// aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Every kernel of the library is launched with
 // programmatic stream serialization (launch_k below): its CTAs may become
 // resident while the previous kernel in the stream is still finishing, so the
@@ -155,13 +209,13 @@ __device__ __forceinline__ int block_sum(int v, int *scratch) {
 // Work plan of the attention kernel (dd_attn.cu), built per (b, g) unit by
 // the resolver or by the attention's own plan kernel.  The unions of all
 // units are laid end to end: chunk x of that sequence is position
-// x - chunk_off[u] of unit u's union.
+// x - chunk_off[u] of unit u's union.  The attention kernel plans itself
+// from it: persistent CTA c takes chunks [c*per, (c+1)*per) with
+// per = ceil(chunk_off[units] / number of CTAs).
 struct AttnPlanOut {
   int32_t *chunk_off;   // [units + 1] exclusive prefix of the union sizes
-  int4 *cta_tab;        // [n_cta] slice of persistent CTA c: {first chunk, end chunk, first unit, chunks per CTA}
   int4 *flat;           // [units * umax] per chunk: {first pool row (hot) | -2 - row (staging) | -1, query mask,
                         //  host chunk (b*Hkv+g)*C + c for staging chunks | -1, 0}
-  int n_cta;
 };
 
 // One CTA, all threads: the plan entries that belong to `unit`.
@@ -189,15 +243,6 @@ __device__ __forceinline__ void attn_plan_unit(const AttnPlanOut &po, int unit, 
     po.chunk_off[unit] = off;
     if (unit == units - 1) po.chunk_off[units] = total;
   }
-  const int per = (total + po.n_cta - 1) / po.n_cta;
-  if (per > 0) {
-    for (int c = (off + per - 1) / per + tid; c < po.n_cta && (int64_t)c * per < (int64_t)off + U; c += nt)
-      po.cta_tab[c] = make_int4(c * per, min(total, c * per + per), unit, per);
-  }
-  if (unit == units - 1) {
-    const int c_end = per > 0 ? (total + per - 1) / per : 0;
-    for (int c = c_end + tid; c < po.n_cta; c += nt) po.cta_tab[c] = make_int4(total, total, 0, per);
-  }
 }
 
 }  // namespace dd
@@ -212,11 +257,26 @@ cudaError_t launch_build_minmax(const uint4 *K, uint4 *lm2, int64_t n_chunks, in
 cudaError_t launch_score_minmax(const uint4 *q, const uint4 *lm2, float *scores, int B, int n_q, int Hq, int Hkv,
                                 int C, cudaStream_t s);
 cudaError_t launch_topk(const float *scores, int32_t *sel, int rows, int C, int k, cudaStream_t s);
+// outputs and state of the fused selection kernel (dd_select.cu)
+struct SelectOut {
+  float *scores;                  // [B,n_q,Hkv,C] or null
+  int32_t *sel;                   // [B,n_q,Hkv,k] or null
+  int32_t *attn_slot;             // [B,n_q,Hkv,k] or null
+  const int32_t *resident_slot;   // [B,Hkv,C]
+  int32_t *union_idx, *union_slot;
+  uint8_t *union_qmask;
+  int32_t *union_cnt, *unit_miss, *miss_list, *miss_count;
+  int32_t *chunk_off;             // attention plan: [units + 1]
+  int4 *flat;                     // attention plan: [units * umax]
+  unsigned long long *lb_word;    // look-back: [units] {epoch:30, union count:17, miss count:17}
+  int32_t *ticket;                // [2] next unit, CTAs done
+  uint32_t epoch;                 // distinct per launch, never 0
+  int units, Hq, Hkv, C, k, umax, cs;
+  int64_t hot_slots, max_misses;
+  int32_t *status;
+};
 size_t fused_select_smem(int n_q, int C, int k);
-cudaError_t launch_select_fused(bool minmax, const uint4 *q, const uint4 *lm, float *scores, int32_t *sel,
-                                const int32_t *resident_slot, int32_t *union_idx, int32_t *union_slot,
-                                uint8_t *union_qmask, int32_t *union_cnt, int32_t *unit_miss, int units, int n_q,
-                                int Hq, int Hkv, int C, int k, int umax, int64_t hot_slots, int32_t *status,
+cudaError_t launch_select_fused(bool minmax, const uint4 *q, const uint4 *lm, const SelectOut &o, int n_q,
                                 cudaStream_t s);
 cudaError_t launch_topk_mass(const float *scores, int32_t *sel, int32_t *sel_cnt, int rows, int C, int k_max,
                              int k_min, float gamma, float tau_log2e, cudaStream_t s);
@@ -237,7 +297,6 @@ struct AttnPlan {
 struct AttnScratch {
   float *part_o, *part_ml;
   int32_t *chunk_off;         // [units + 1]
-  int4 *cta_tab;              // [n_cta]
   int4 *flat;                 // [units * umax]
   const void *dummy_pool;     // >= 64 rows x 256 B, a valid base for unused tensor maps
 };

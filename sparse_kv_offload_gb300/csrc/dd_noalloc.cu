@@ -77,9 +77,8 @@ extern "C" dd_status dd_sparse_attn_decode_noalloc(const dd_dims *dims, int64_t 
   const size_t o_bytes = round256((size_t)plan.part_o_floats * sizeof(float));
   const size_t ml_bytes = round256((size_t)plan.part_ml_floats * sizeof(float));
   const size_t off_bytes = round256((size_t)(units + 1) * sizeof(int32_t));
-  const size_t tab_bytes = round256((size_t)plan.n_cta * 16);
   const size_t flat_bytes = round256((size_t)plan.flat_entries * 16);
-  if (o_bytes + ml_bytes + off_bytes + tab_bytes + flat_bytes + kDummyPoolBytes > kNoAllocScratchBytes)
+  if (o_bytes + ml_bytes + off_bytes + flat_bytes + kDummyPoolBytes > kNoAllocScratchBytes)
     return DD_ERR_CAPACITY;
   if (!q || !union_slot || !union_qmask || !union_cnt || !miss_count || !out || !device_status || !aligned16(q))
     return DD_ERR_INVALID_ARG;
@@ -96,11 +95,9 @@ extern "C" dd_status dd_sparse_attn_decode_noalloc(const dd_dims *dims, int64_t 
   cur += ml_bytes;
   int32_t *chunk_off = reinterpret_cast<int32_t *>(cur);
   cur += off_bytes;
-  int4 *cta_tab = reinterpret_cast<int4 *>(cur);
-  cur += tab_bytes;
   int4 *flat = reinterpret_cast<int4 *>(cur);
   cur += flat_bytes;
-  const dd::AttnScratch scr = {part_o, part_ml, chunk_off, cta_tab, flat, cur};
+  const dd::AttnScratch scr = {part_o, part_ml, chunk_off, flat, cur};
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)dd::kD);
   const cudaError_t e = dd::launch_attn(q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count,
                                         scale, out, plan, scr, false, nullptr, nullptr, device_status, d.B, d.n_q,

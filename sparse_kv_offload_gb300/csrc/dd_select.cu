@@ -208,8 +208,6 @@ __device__ __forceinline__ float block_excl_scan_f(float v, float *scratchf, flo
   return r;
 }
 
-constexpr int kMaxMassK = 4096;
-
 __global__ void __launch_bounds__(kTopkThreads) k_topk_mass(const float *__restrict__ scores,
                                                             int32_t *__restrict__ sel, int32_t *__restrict__ sel_cnt,
                                                             int C, int k_max, int k_min, float gamma,
@@ -436,57 +434,105 @@ cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32
 }
 
 // ---------------------------------------------------------------------------
-// a1 + a2 + a3 pass 1 fused, one CTA (512 threads) per (b,g) unit, when the
-// unit's n_q score rows fit in shared memory: the landmarks of the unit are
-// scored for all queries exactly as k_score does (16 lanes per landmark row,
-// same per-lane FMA order and butterfly, so the scores are the same bits),
-// kept in shared memory; the top-k of every row comes from one radix select
-// over all rows at once (per-row histograms, warp j settles row j); the
-// union and residency lookup then read the selections from shared memory.
-// Scores and selections are also written to device memory when asked for.
+// The whole selection of a step in one kernel, one CTA (512 threads) per
+// (b,g) unit, when a unit's n_q score rows fit in shared memory:
+//  a1  the unit's landmarks are scored for all queries exactly as k_score
+//      does (16 lanes per landmark row, same per-lane FMA order and
+//      butterfly, so the scores are the same bits), kept in shared memory;
+//  a2  the top-k of every row comes from one radix select over all rows at
+//      once (per-row histograms, warp j settles row j);
+//  a3  the union and residency lookup read the selections from shared
+//      memory; the global miss ordinals and union offsets (sums over the
+//      earlier units) come from a look-back: each CTA takes its unit from a
+//      ticket counter, so it only ever waits for units whose CTAs are
+//      already running, publishes its union and miss counts, and sums the
+//      counts of all earlier units as they are published; every wait is
+//      bounded (DD_ERR_TIMEOUT).  The CTA then writes its union lists with
+//      global slots, its miss-list entries and its part of the attention
+//      plan; the last unit writes the totals.
+// Scores, selections and per-entry slots go to device memory only when asked for.
 // ---------------------------------------------------------------------------
 constexpr int kFusedThreads = 512;
 constexpr int kFusedRowsPerPass = kFusedThreads / 16;   // 32 landmarks per pass
 
+constexpr int kLookBatch = 8;   // look-back words per lane in flight (256 units per round)
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t select_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+constexpr int kRingMaxStages = 6;            // landmark ring: up to 6 x 32 KB in flight per SM
+constexpr int kRingStageBytes = 32 * 1024;
+constexpr size_t kSelectDynSmem = 208 * 1024; // dynamic shared memory the fused kernel may use
+
+// ring stages that fit beside a unit's score rows and selections (at least 4
+// whenever the fused kernel is used at all)
+__host__ __device__ inline int ring_stages(int n_q, int C, int k) {
+  const long long rest = (long long)kSelectDynSmem - (long long)n_q * C * 4 - (long long)n_q * k * 4;
+  const long long st = rest / kRingStageBytes;
+  return (int)(st > kRingMaxStages ? kRingMaxStages : st);
+}
+
 template <int NQ, bool MM>
-__global__ void __launch_bounds__(kFusedThreads) k_select_fused(
-    const uint4 *__restrict__ q, const uint4 *__restrict__ lm, float *__restrict__ scores_out,
-    int32_t *__restrict__ sel_out, const int32_t *__restrict__ resident_slot, int32_t *__restrict__ union_idx,
-    int32_t *__restrict__ union_slot, uint8_t *__restrict__ union_qmask, int32_t *__restrict__ union_cnt,
-    int32_t *__restrict__ unit_miss, int Hq, int Hkv, int C, int k, int umax, int64_t hot_slots, int32_t *status) {
-  // landmarks per thread per tile: fewer for many queries (512 threads leave 128 registers each)
-  constexpr int kPass = (MM ? 4 : 8) / (NQ >= 5 ? 2 : 1);
-  constexpr int kTile = kPass * kFusedRowsPerPass;
+__global__ void __launch_bounds__(kFusedThreads) k_select_fused(const uint4 *__restrict__ q,
+                                                                const uint4 *__restrict__ lm, SelectOut o) {
   constexpr int kVecs = MM ? 2 : 1;
+  constexpr int kRowBytes = 256 * kVecs;                          // one landmark (one or two vectors)
+  constexpr int kStageLm = kRingStageBytes / kRowBytes;           // 128 or 64 landmarks per stage
+  constexpr int kPass = kStageLm / kFusedRowsPerPass;             // landmarks per thread per stage
   constexpr int kVals = kPass * NQ;
   constexpr int kChunks = (kVals + 15) / 16;
-  extern __shared__ uint32_t fsm[];                        // keys [NQ][C], then selections [NQ][k]
-  __shared__ uint32_t qbits[kMaxNq * kMaxWords];
-  __shared__ uint32_t missw[kMaxWords];
+  // dynamic shared memory: [ring, then the union scratch][scores -> keys, NQ*C][selections, NQ*k]
+  extern __shared__ __align__(128) unsigned char fsm_raw[];
+  const int n_ring = ring_stages(NQ, o.C, o.k);
+  unsigned char *ring = fsm_raw;
+  uint32_t *fsm = reinterpret_cast<uint32_t *>(fsm_raw + n_ring * kRingStageBytes);
+  __shared__ __align__(8) uint64_t ring_bar[kRingMaxStages];
   __shared__ int hist[NQ][256];
   __shared__ int scratch[33];
   __shared__ uint32_t s_prefix[NQ];
   __shared__ int s_remaining[NQ];
+  __shared__ int s_unit, s_uoff, s_moff;
   pdl_wait();
   pdl_trigger();
-  const int unit = blockIdx.x;
-  const int b = unit / Hkv, g = unit - b * Hkv;
-  const int G = Hq / Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_unit = atomicAdd(o.ticket, 1);                       // units in the order their CTAs start
+    for (int st = 0; st < n_ring; ++st) mbar_init(smem_u32(&ring_bar[st]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int unit = s_unit;
+  const int C = o.C, k = o.k, Hkv = o.Hkv;
+  const int b = unit / Hkv, g = unit - b * Hkv;
+  const int G = o.Hq / Hkv;
   const int part = tid & 15, sub = tid >> 4;
   float *sc = reinterpret_cast<float *>(fsm);
   int32_t *sel_s = reinterpret_cast<int32_t *>(fsm + NQ * C);
-  const uint4 *base = lm + (int64_t)unit * C * kVecs * kVecPerRow + part;
 
-  // ---- a1: scores of the whole unit, into shared memory
-  uint4 v[kPass][kVecs], nv[kPass][kVecs];
-#pragma unroll
-  for (int p = 0; p < kPass; ++p) {
-    const int c = p * kFusedRowsPerPass + sub;
-#pragma unroll
-    for (int e = 0; e < kVecs; ++e)
-      v[p][e] = (c < C) ? ldg_nc(base + ((int64_t)c * kVecs + e) * kVecPerRow) : make_uint4(0, 0, 0, 0);
-  }
+  // ---- a1: the unit's landmarks stream through the ring (one thread issues
+  // the bulk copies); every warp scores its rows of each stage from shared memory
+  const int n_st = (C + kStageLm - 1) / kStageLm;
+  const unsigned char *lm_unit = reinterpret_cast<const unsigned char *>(lm) + (int64_t)unit * C * kRowBytes;
+  auto issue = [&](int st) {
+    const int r0 = st * kStageLm;
+    const uint32_t bytes = (uint32_t)min(kStageLm, C - r0) * kRowBytes;
+    const uint32_t bar = smem_u32(&ring_bar[st % n_ring]);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load(smem_u32(ring + (st % n_ring) * kRingStageBytes), lm_unit + (int64_t)r0 * kRowBytes, bytes, bar);
+  };
+  if (tid == 0)
+    for (int st = 0; st < min(n_ring, n_st); ++st) issue(st);
   float qs[NQ][8];
 #pragma unroll
   for (int j = 0; j < NQ; ++j) {
@@ -494,27 +540,27 @@ __global__ void __launch_bounds__(kFusedThreads) k_select_fused(
     for (int e = 0; e < 8; ++e) qs[j][e] = 0.f;
     for (int h = g * G; h < (g + 1) * G; ++h) {
       float f[8];
-      unpack8(q[((int64_t)(b * NQ + j) * Hq + h) * kVecPerRow + part], f);
+      unpack8(q[((int64_t)(b * NQ + j) * o.Hq + h) * kVecPerRow + part], f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) qs[j][e] += f[e];
     }
   }
-  for (int c0 = 0; c0 < C; c0 += kTile) {
-#pragma unroll
-    for (int p = 0; p < kPass; ++p) {
-      const int c = c0 + kTile + p * kFusedRowsPerPass + sub;
-#pragma unroll
-      for (int e = 0; e < kVecs; ++e)
-        nv[p][e] = (c < C) ? ldg_nc(base + ((int64_t)c * kVecs + e) * kVecPerRow) : make_uint4(0, 0, 0, 0);
-    }
+  for (int st = 0; st < n_st; ++st) {
+    const int rb = st % n_ring;
+    mbar_wait(smem_u32(&ring_bar[rb]), (uint32_t)(st / n_ring) & 1u, o.status);
+    const unsigned char *stage = ring + rb * kRingStageBytes;
+    const int r0 = st * kStageLm;
     float x[kChunks * 16];
 #pragma unroll
     for (int a = kVals; a < kChunks * 16; ++a) x[a] = 0.f;
 #pragma unroll
     for (int p = 0; p < kPass; ++p) {
+      const int row = p * kFusedRowsPerPass + sub;
+      const bool live = r0 + row < C;
+      const uint4 *src = reinterpret_cast<const uint4 *>(stage + row * kRowBytes) + part;
       float f[8], fh[8];
-      unpack8(v[p][0], f);
-      if (MM) unpack8(v[p][kVecs - 1], fh);
+      unpack8(live ? src[0] : make_uint4(0, 0, 0, 0), f);
+      if (MM) unpack8(live ? src[kVecPerRow * (kVecs - 1)] : make_uint4(0, 0, 0, 0), fh);
 #pragma unroll
       for (int j = 0; j < NQ; ++j) {
         float acc = 0.f;
@@ -535,19 +581,21 @@ __global__ void __launch_bounds__(kFusedThreads) k_select_fused(
       for (int i = 0; i < 16; ++i) xs[i] = x[ch * 16 + i];
       const float r = butterfly16(xs, part);
       const int a = ch * 16 + part;
-      const int c = c0 + (a / NQ) * kFusedRowsPerPass + sub;
+      const int c = r0 + (a / NQ) * kFusedRowsPerPass + sub;
       if (a < kVals && c < C) sc[(a % NQ) * C + c] = r;
     }
-#pragma unroll
-    for (int p = 0; p < kPass; ++p)
-#pragma unroll
-      for (int e = 0; e < kVecs; ++e) v[p][e] = nv[p][e];
+    __syncthreads();                                       // stage rb consumed by every warp
+    if (tid == 0 && st + n_ring < n_st) issue(st + n_ring);
   }
-  __syncthreads();
-  if (scores_out) {
+  // the ring is free from here on: the union scratch lives there
+  const int W = (C + 31) >> 5;
+  uint32_t *qbits = reinterpret_cast<uint32_t *>(ring);     // [NQ][W]
+  uint32_t *ubw = qbits + NQ * kMaxWords, *mbw = ubw + kMaxWords;
+  int *upre = reinterpret_cast<int *>(mbw + kMaxWords), *mpre = upre + kMaxWords;
+  if (o.scores) {
     for (int i = tid; i < NQ * C; i += kFusedThreads) {
       const int j = i / C, c = i - j * C;
-      scores_out[((int64_t)(b * NQ + j) * Hkv + g) * C + c] = sc[i];
+      o.scores[((int64_t)(b * NQ + j) * Hkv + g) * C + c] = sc[i];
     }
   }
   // ---- a2: radix select of all NQ rows at once (scores become order keys in place)
@@ -598,35 +646,182 @@ __global__ void __launch_bounds__(kFusedThreads) k_select_fused(
   }
   for (int j = 0; j < NQ; ++j) emit_topk(keys + j * C, C, s_prefix[j], s_remaining[j], scratch, sel_s + j * k);
   __syncthreads();
-  if (sel_out) {
+  if (o.sel) {
     for (int i = tid; i < NQ * k; i += kFusedThreads) {
       const int j = i / k, r = i - j * k;
-      sel_out[((int64_t)(b * NQ + j) * Hkv + g) * k + r] = sel_s[i];
+      o.sel[((int64_t)(b * NQ + j) * Hkv + g) * k + r] = sel_s[i];
     }
   }
-  // ---- a3 pass 1: union and residency from the shared selections
-  union_unit(sel_s, k, unit, NQ, k, C, umax, hot_slots, resident_slot, union_idx, union_slot, union_qmask,
-             union_cnt, unit_miss, qbits, missw, scratch, status);
+
+  // ---- a3: union bitmaps, residency, one union word per thread (W <= 512)
+  for (int i = tid; i < NQ * W; i += kFusedThreads) qbits[i] = 0u;
+  __syncthreads();
+  for (int i = tid; i < NQ * k; i += kFusedThreads) {
+    const int j = i / k, c = sel_s[i];
+    if (c < 0 || c >= C) {
+      set_status(o.status, DD_ERR_DEVICE_CHECK);
+      continue;
+    }
+    atomicOr(&qbits[j * W + (c >> 5)], 1u << (c & 31));
+  }
+  __syncthreads();
+  const int32_t *rs_unit = o.resident_slot + (int64_t)unit * C;
+  int cu = 0, cm = 0;
+  if (tid < W) {
+    uint32_t ub = 0, mb = 0;
+    for (int j = 0; j < NQ; ++j) ub |= qbits[j * W + tid];
+    uint32_t rest = ub;
+    while (rest) {
+      const int bit = __ffs(rest) - 1;
+      rest &= rest - 1;
+      const int32_t rs = rs_unit[tid * 32 + bit];
+      if (rs >= o.hot_slots) set_status(o.status, DD_ERR_DEVICE_CHECK);
+      if (rs < 0 || rs >= o.hot_slots) mb |= 1u << bit;
+    }
+    ubw[tid] = ub;
+    mbw[tid] = mb;
+    cu = __popc(ub);
+    cm = __popc(mb);
+  }
+  int tot;
+  const int ex = block_excl_scan((cu << 16) | cm, scratch, &tot);   // unions never exceed C <= 16384
+  if (tid < W) {
+    upre[tid] = ex >> 16;
+    mpre[tid] = ex & 0xFFFF;
+  }
+  const int U = tot >> 16, M = tot & 0xFFFF;
+
+  // look-back over the earlier units: every unit publishes one 64-bit word
+  // {epoch:30, union count:17, miss count:17} as soon as it has its counts
+  // (counts never exceed C <= 16384, and a single aligned 64-bit store is
+  // seen whole, so the word is its own message), and sums all of its
+  // predecessors' counts: each lane loads its strided share of their words
+  // at once and re-polls only those not yet published; one round trip
+  // after the slowest predecessor, no chain
+  if (warp == 0) {
+    const unsigned long long ep = (unsigned long long)o.epoch << 34;
+    if (lane == 0) st_relaxed_u64(&o.lb_word[unit], ep | ((unsigned long long)U << 17) | (unsigned long long)M);
+    int su = 0, sm = 0;
+    bool ok = true;
+    const uint64_t t0 = select_timer_ns();
+    for (int base = 0; base < unit; base += 32 * kLookBatch) {
+      unsigned long long w8[kLookBatch];
+#pragma unroll
+      for (int t = 0; t < kLookBatch; ++t) {
+        const int idx = base + t * 32 + lane;
+        w8[t] = idx < unit ? ld_relaxed_u64(&o.lb_word[idx]) : ep;
+      }
+#pragma unroll
+      for (int t = 0; t < kLookBatch; ++t) {
+        const int idx = base + t * 32 + lane;
+        for (uint32_t it = 0; ok && (w8[t] >> 34) != o.epoch; ++it) {
+          w8[t] = ld_relaxed_u64(&o.lb_word[idx]);
+          if ((it & 63u) == 63u && select_timer_ns() - t0 > 2000000000ull) ok = false;
+        }
+        su += (int)((w8[t] >> 17) & 0x1FFFFull);
+        sm += (int)(w8[t] & 0x1FFFFull);
+      }
+      if (!__all_sync(0xffffffffu, ok)) break;
+    }
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) {
+      su += __shfl_xor_sync(0xffffffffu, su, sh);
+      sm += __shfl_xor_sync(0xffffffffu, sm, sh);
+    }
+    if (!__all_sync(0xffffffffu, ok) && lane == 0) set_status(o.status, DD_ERR_TIMEOUT);
+    if (lane == 0) {
+      s_uoff = su;
+      s_moff = sm;
+    }
+  }
+  __syncthreads();
+  const int uoff = s_uoff, moff = s_moff;
+
+  // union lists with global slots, miss list, attention plan entries
+  const int64_t ubase = (int64_t)unit * o.umax;
+  if (tid < W) {
+    uint32_t rest = ubw[tid];
+    const uint32_t mb = mbw[tid];
+    int up = upre[tid], mp = mpre[tid];
+    while (rest) {
+      const int bit = __ffs(rest) - 1;
+      rest &= rest - 1;
+      const int c = tid * 32 + bit;
+      uint32_t qm = 0;
+      for (int j = 0; j < NQ; ++j) qm |= ((qbits[j * W + tid] >> bit) & 1u) << j;
+      o.union_idx[ubase + up] = c;
+      o.union_qmask[ubase + up] = (uint8_t)qm;
+      int32_t row, host = -1;
+      if ((mb >> bit) & 1u) {
+        const int64_t m = (int64_t)moff + mp++;
+        o.union_slot[ubase + up] = -(int32_t)(m + 1);
+        if (m < o.max_misses) {
+          o.miss_list[m] = unit * C + c;
+          row = -2 - (int32_t)(m * o.cs);
+          host = unit * C + c;
+        } else {
+          row = -1;   // beyond the staging capacity: the last unit reports it
+          qm = 0;
+        }
+      } else {
+        const int32_t rs = rs_unit[c];
+        o.union_slot[ubase + up] = rs;
+        row = rs * o.cs;
+      }
+      o.flat[uoff + up] = make_int4(row, (int)qm, host, 0);
+      ++up;
+    }
+  }
+  if (o.attn_slot) {
+    for (int i = tid; i < NQ * k; i += kFusedThreads) {
+      const int j = i / k, r = i - j * k, c = sel_s[i];
+      int32_t val = INT32_MIN;
+      if (c >= 0 && c < C) {
+        const int w = c >> 5;
+        const uint32_t low = (1u << (c & 31)) - 1u;
+        if ((mbw[w] >> (c & 31)) & 1u) val = -(int32_t)((int64_t)moff + mpre[w] + __popc(mbw[w] & low) + 1);
+        else val = rs_unit[c];
+      }
+      o.attn_slot[((int64_t)(b * NQ + j) * Hkv + g) * k + r] = val;
+    }
+  }
+  if (tid == 0) {
+    o.union_cnt[unit] = U;
+    o.unit_miss[unit] = M;
+    o.chunk_off[unit] = uoff;
+    if (unit == o.units - 1) {
+      o.chunk_off[o.units] = uoff + U;
+      *o.miss_count = moff + M;
+      if ((int64_t)moff + M > o.max_misses) set_status(o.status, DD_ERR_CAPACITY);
+    }
+    // the last CTA to finish resets the ticket counter for the next launch
+    __threadfence();
+    if (atomicAdd(o.ticket + 1, 1) == o.units - 1) {
+      o.ticket[0] = 0;
+      o.ticket[1] = 0;
+      __threadfence();
+    }
+  }
 }
 
-size_t fused_select_smem(int n_q, int C, int k) { return (size_t)n_q * C * 4 + (size_t)n_q * k * 4; }
+// the fused kernel's dynamic shared memory; 0 when its ring would be shallower than 4 stages
+size_t fused_select_smem(int n_q, int C, int k) {
+  const int st = ring_stages(n_q, C, k);
+  if (st < 4) return 0;
+  return (size_t)st * kRingStageBytes + (size_t)n_q * C * 4 + (size_t)n_q * k * 4;
+}
 
 template <bool MM>
-static cudaError_t launch_select_fused_t(const uint4 *q, const uint4 *lm, float *scores, int32_t *sel,
-                                         const int32_t *resident_slot, int32_t *union_idx, int32_t *union_slot,
-                                         uint8_t *union_qmask, int32_t *union_cnt, int32_t *unit_miss, int units,
-                                         int n_q, int Hq, int Hkv, int C, int k, int umax, int64_t hot_slots,
-                                         int32_t *status, cudaStream_t s) {
-  const size_t smem = fused_select_smem(n_q, C, k);
+static cudaError_t launch_select_fused_t(const uint4 *q, const uint4 *lm, const SelectOut &o, int n_q,
+                                         cudaStream_t s) {
+  const size_t smem = fused_select_smem(n_q, o.C, o.k);
   switch (n_q) {
-#define DD_FUSED_CASE(N)                                                                                        \
-  case N: {                                                                                                      \
-    cudaError_t e = cudaFuncSetAttribute(k_select_fused<N, MM>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                                         (int)smem);                                                             \
-    if (e != cudaSuccess) return e;                                                                              \
-    return launch_k(k_select_fused<N, MM>, dim3(units), dim3(kFusedThreads), smem, s, q, lm, scores, sel,       \
-                    resident_slot, union_idx, union_slot, union_qmask, union_cnt, unit_miss, Hq, Hkv, C, k, umax, \
-                    hot_slots, status);                                                                         \
+#define DD_FUSED_CASE(N)                                                                                      \
+  case N: {                                                                                                    \
+    cudaError_t e = cudaFuncSetAttribute(k_select_fused<N, MM>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                         (int)smem);                                                           \
+    if (e != cudaSuccess) return e;                                                                            \
+    return launch_k(k_select_fused<N, MM>, dim3(o.units), dim3(kFusedThreads), smem, s, q, lm, o);            \
   }
     DD_FUSED_CASE(1) DD_FUSED_CASE(2) DD_FUSED_CASE(3) DD_FUSED_CASE(4)
     DD_FUSED_CASE(5) DD_FUSED_CASE(6) DD_FUSED_CASE(7) DD_FUSED_CASE(8)
@@ -635,18 +830,10 @@ static cudaError_t launch_select_fused_t(const uint4 *q, const uint4 *lm, float 
   }
 }
 
-cudaError_t launch_select_fused(bool minmax, const uint4 *q, const uint4 *lm, float *scores, int32_t *sel,
-                                const int32_t *resident_slot, int32_t *union_idx, int32_t *union_slot,
-                                uint8_t *union_qmask, int32_t *union_cnt, int32_t *unit_miss, int units, int n_q,
-                                int Hq, int Hkv, int C, int k, int umax, int64_t hot_slots, int32_t *status,
+cudaError_t launch_select_fused(bool minmax, const uint4 *q, const uint4 *lm, const SelectOut &o, int n_q,
                                 cudaStream_t s) {
-  if (units == 0) return cudaSuccess;
-  return minmax ? launch_select_fused_t<true>(q, lm, scores, sel, resident_slot, union_idx, union_slot, union_qmask,
-                                              union_cnt, unit_miss, units, n_q, Hq, Hkv, C, k, umax, hot_slots,
-                                              status, s)
-                : launch_select_fused_t<false>(q, lm, scores, sel, resident_slot, union_idx, union_slot,
-                                               union_qmask, union_cnt, unit_miss, units, n_q, Hq, Hkv, C, k, umax,
-                                               hot_slots, status, s);
+  if (o.units == 0) return cudaSuccess;
+  return minmax ? launch_select_fused_t<true>(q, lm, o, n_q, s) : launch_select_fused_t<false>(q, lm, o, n_q, s);
 }
 
 // ---------------------------------------------------------------------------
