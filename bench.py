@@ -9,10 +9,15 @@ Four layers of independent data are cycled so that no step finds its inputs
 in L2.  Prints one JSON line (see the keys below).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--mode zerocopy|memcpy]
+                    [--workload NAME] [--mode zerocopy|memcpy] [--landmarks mean|minmax]
+                    [--pipeline [--prefetch-ctas N]]
 
 ``--impl reference`` times the CPU oracle instead (a bounded sample of the
-same workload per step).  Under torchrun every rank runs its own independent
+same workload per step).  The default line also reports the oracle on one
+core and on every host core (independent units, one process per core).
+``--pipeline`` runs several layers with drifting queries: predictive prefetch
+on a low-priority stream, the same steps serialized, and the same steps with
+the capped LRU residency update.  Under torchrun every rank runs its own independent
 batch (weak scaling, no collective on the data path); the time is the max over
 ranks.
 """
@@ -136,7 +141,7 @@ class OracleSample:
     Hkv units, built from the host generator (the same definition the GPU
     path's inputs come from)."""
 
-    def __init__(self, w, landmarks="mean"):
+    def __init__(self, w, landmarks="mean", heads=None):
         import oracle
         self.oracle = oracle
         self.w = w
@@ -150,7 +155,7 @@ class OracleSample:
             bias = synth.zipf_chunk_bias(w.seed, 1, w.Hkv, w.C, w.zipf_alpha, w.bias_sigma)
             u_hat = synth.query_direction(q, w.Hkv)
         self.units = []
-        for g in range(w.Hkv):
+        for g in (range(w.Hkv) if heads is None else heads):
             u = np.array([g])
             K = synth.kv_rows(w.seed, synth.TID_K, 1, w.Hkv, w.L, w.d, w.cs, u, np.zeros(1, np.int64), w.L,
                               bias, u_hat).reshape(1, 1, w.L, w.d)
@@ -185,6 +190,32 @@ def cpu_baseline(w, budget_s=12.0, landmarks="mean"):
         done += 1
     return {"value": done / (w.units * spent), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": s.describe(done) + f"; {done} units in {spent:.1f} s"}
+
+
+def _oracle_worker(task):
+    """One process of the all-cores baseline: the oracle step on one (request 0,
+    KV head) unit, repeated for `budget` seconds (inputs built before timing)."""
+    wname, head, landmarks, budget = task
+    s = OracleSample(BY_NAME[wname], landmarks, heads=[head])
+    s.run_units(1)
+    done, spent = 0, 0.0
+    while spent < budget:
+        spent += s.run_units(1)
+        done += 1
+    return done, spent
+
+
+def cpu_baseline_all_cores(w, budget_s=8.0, landmarks="mean"):
+    """The same oracle code over independent (b, g) units on every host core
+    (one process per core, spawned: numerics unchanged, units are independent)."""
+    import multiprocessing as mp
+    n = os.cpu_count() or 1
+    with mp.get_context("spawn").Pool(n) as pool:
+        res = pool.map(_oracle_worker, [(w.name, i % w.Hkv, landmarks, budget_s) for i in range(n)])
+    rate = sum(d / t for d, t in res)              # units per second, all processes together
+    return {"value": rate / w.units, "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"{n} processes, each the oracle step on one (request 0, KV head) unit for "
+                      f"{budget_s:.0f} s; steps/s = sum of units/s / {w.units}"}
 
 
 def run_reference(args, world, rank):
@@ -490,6 +521,8 @@ def run_ours(args, world, rank, local):
     barrier(world)
 
     cpu = cpu_baseline(w, landmarks=args.landmarks) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    cpu_all = (cpu_baseline_all_cores(w, landmarks=args.landmarks)
+               if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None)
     ctx.close()
     if rank != 0:
         return 0
@@ -512,6 +545,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
     }
     print(json.dumps(line), flush=True)
     return 0
