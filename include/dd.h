@@ -290,6 +290,16 @@ dd_status dd_update_residency(dd_ctx *ctx, int32_t step, int32_t cap, int32_t sl
                               int32_t *resident_slot, int32_t *slot_chunk, int32_t *last_used, void *Khot,
                               void *Vhot, int32_t *admitted, dd_stream_t stream);
 
+/* Diagnostics for failure detection: runs one of the library's bounded
+ * device waits on something that nothing will ever signal -- kind 0: an
+ * mbarrier no thread arrives on and no copy completes (the waits of the
+ * attention pipeline and of the selection's landmark ring); kind 1: a
+ * look-back word no unit publishes (the selection's sum over earlier
+ * units).  The wait gives up by itself after about 2 s and records
+ * DD_ERR_TIMEOUT in the status word; the context stays usable once
+ * dd_get_status has read and cleared it.  No fault or trap is involved. */
+dd_status dd_selftest_bounded_wait(dd_ctx *ctx, int32_t kind, dd_stream_t stream);
+
 /* Wait for the device, read the status word into *device_status (a dd_status
  * value) and clear it. */
 dd_status dd_get_status(dd_ctx *ctx, int32_t *device_status);

@@ -26,6 +26,7 @@ struct dd_ctx {
   int32_t *chunk_off = nullptr;
   int4 *flat = nullptr;
   unsigned long long *lb_word = nullptr;        // fused selection: look-back words, ticket
+  unsigned long long *diag_word = nullptr;      // a word nothing publishes (bounded-wait self-test)
   int32_t *ticket = nullptr;
   uint32_t epoch = 0;
   void *dummy_pool = nullptr;
@@ -184,6 +185,7 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   add(64 * 128, 2);                            // dummy pool (64 rows)
   add(units, 8);                               // look-back words
   add(2, 4);                                   // ticket
+  add(1, 8);                                   // self-test word
   if (cudaMalloc(&c->ws, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
   uint8_t *cur = static_cast<uint8_t *>(c->ws);
   c->status = carve<int32_t>(cur, 1);
@@ -204,6 +206,7 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   c->dummy_pool = carve<uint16_t>(cur, 64 * 128);
   c->lb_word = carve<unsigned long long>(cur, units);
   c->ticket = carve<int32_t>(cur, 2);
+  c->diag_word = carve<unsigned long long>(cur, 1);
   if (cudaMemset(c->ws, 0, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
   if (cudaMallocHost(reinterpret_cast<void **>(&c->h_miss), (size_t)(1 + (max_misses > 0 ? max_misses : 1)) * 4) !=
       cudaSuccess)
@@ -478,6 +481,12 @@ dd_status dd_update_residency(dd_ctx *c, int32_t step, int32_t cap, int32_t slot
       static_cast<const uint4 *>(Kst), static_cast<const uint4 *>(Vst), resident_slot, slot_chunk, last_used,
       static_cast<uint4 *>(Khot), static_cast<uint4 *>(Vhot), admitted, c->C, c->umax, c->dims.cs, c->status,
       (cudaStream_t)stream));
+}
+
+dd_status dd_selftest_bounded_wait(dd_ctx *c, int32_t kind, dd_stream_t stream) {
+  if (!c || (kind != 0 && kind != 1)) return DD_ERR_INVALID_ARG;
+  c->launches += 1;
+  return cuda_ok(dd::launch_selftest_wait(kind, c->diag_word, c->status, (cudaStream_t)stream));
 }
 
 dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {

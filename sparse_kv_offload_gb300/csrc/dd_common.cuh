@@ -128,6 +128,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
   }
 }
 
+// Bounded wait until a 64-bit word carries `epoch` in its top 30 bits (the
+// look-back words of the fused selection).  Returns the word; sets *ok to
+// false and stops waiting ~2 s after t0 (the caller records DD_ERR_TIMEOUT).
+__device__ __forceinline__ unsigned long long wait_published(const unsigned long long *word, uint32_t epoch,
+                                                             uint64_t t0, bool *ok) {
+  unsigned long long w;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(word) : "memory");
+  for (uint32_t it = 0; *ok && (w >> 34) != epoch; ++it) {
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(word) : "memory");
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > 2000000000ull) *ok = false;
+  }
+  return w;
+}
+
 // 1-D bulk copy global -> shared, completion counted on an mbarrier (16-byte
 // aligned addresses, size a multiple of 16)
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
@@ -278,6 +292,7 @@ struct SelectOut {
 size_t fused_select_smem(int n_q, int C, int k);
 cudaError_t launch_select_fused(bool minmax, const uint4 *q, const uint4 *lm, const SelectOut &o, int n_q,
                                 cudaStream_t s);
+cudaError_t launch_selftest_wait(int kind, const unsigned long long *word, int32_t *status, cudaStream_t s);
 cudaError_t launch_topk_mass(const float *scores, int32_t *sel, int32_t *sel_cnt, int rows, int C, int k_max,
                              int k_min, float gamma, float tau_log2e, cudaStream_t s);
 cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32_t *union_idx,

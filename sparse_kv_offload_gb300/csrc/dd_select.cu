@@ -465,11 +465,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ uint64_t select_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
 
 constexpr int kRingMaxStages = 6;            // landmark ring: up to 6 x 32 KB in flight per SM
 constexpr int kRingStageBytes = 32 * 1024;
@@ -703,7 +698,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_select_fused(const uint4 *__r
     if (lane == 0) st_relaxed_u64(&o.lb_word[unit], ep | ((unsigned long long)U << 17) | (unsigned long long)M);
     int su = 0, sm = 0;
     bool ok = true;
-    const uint64_t t0 = select_timer_ns();
+    const uint64_t t0 = globaltimer_ns();
     for (int base = 0; base < unit; base += 32 * kLookBatch) {
       unsigned long long w8[kLookBatch];
 #pragma unroll
@@ -714,10 +709,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_select_fused(const uint4 *__r
 #pragma unroll
       for (int t = 0; t < kLookBatch; ++t) {
         const int idx = base + t * 32 + lane;
-        for (uint32_t it = 0; ok && (w8[t] >> 34) != o.epoch; ++it) {
-          w8[t] = ld_relaxed_u64(&o.lb_word[idx]);
-          if ((it & 63u) == 63u && select_timer_ns() - t0 > 2000000000ull) ok = false;
-        }
+        if ((w8[t] >> 34) != o.epoch) w8[t] = wait_published(&o.lb_word[idx], o.epoch, t0, &ok);
         su += (int)((w8[t] >> 17) & 0x1FFFFull);
         sm += (int)(w8[t] & 0x1FFFFull);
       }

@@ -27,7 +27,7 @@ EXPORTED = (
     "dd_resolve_union", "dd_gather_kv", "dd_sparse_attn_decode", "dd_step", "dd_get_status",
     "dd_launch_count", "dd_status_str", "dd_last_cuda_error", "dd_synth_kv", "dd_synth_queries", "dd_sparse_attn_decode_noalloc",
     "dd_build_landmarks_minmax", "dd_score_landmarks_minmax", "dd_update_residency",
-    "dd_prefetch_kv", "dd_select_topk_mass",
+    "dd_prefetch_kv", "dd_select_topk_mass", "dd_selftest_bounded_wait",
 )
 
 
@@ -82,6 +82,7 @@ def _load():
         "dd_sparse_attn_decode": (i32, [_vp] * 12 + [f32, _vp, _vp]),
         "dd_step": (i32, [_vp, ctypes.POINTER(StepArgs), _vp]),
         "dd_update_residency": (i32, [_vp, i32, i32, i32] + [_vp] * 13),
+        "dd_selftest_bounded_wait": (i32, [_vp, i32, _vp]),
         "dd_select_topk_mass": (i32, [_vp, _vp, _vp, _vp, f32, i32, f32, _vp]),
         "dd_prefetch_kv": (i32, [_vp, _vp, i32, i32, i32, _vp, _vp, _vp, _vp, _vp, _vp, i32, _vp]),
         "dd_get_status": (i32, [_vp, ctypes.POINTER(i32)]),
@@ -276,6 +277,11 @@ class Context:
             _ptr(miss_count, torch.int32, 1, name="miss_count"), float(softmax_scale),
             _ptr(out, torch.float32, s.B * s.n_q * s.Hq * s.d, name="out"), _stream(stream)),
             "dd_sparse_attn_decode")
+
+    def selftest_bounded_wait(self, kind, stream=None):
+        """Run a bounded device wait that nothing signals (see dd.h); the status
+        word then holds DD_ERR_TIMEOUT."""
+        _chk(_lib.dd_selftest_bounded_wait(self._h, int(kind), _stream(stream)), "dd_selftest_bounded_wait")
 
     def select_topk_mass(self, scores, sel, gamma, k_min=1, sel_cnt=None, softmax_scale=0.0, stream=None):
         """Coverage-budget top-k (see dd.h): rows padded with -1, lengths in sel_cnt."""

@@ -30,7 +30,10 @@ V_ALL = Workload("k_equals_C", B=1, Hq=8, Hkv=2, d=128, L=1024, cs=16, k=64, n_q
                  spec_scale=(0.0, 0.3), seed=78)
 V_ONEQ = Workload("one_query", B=3, Hq=16, Hkv=4, d=128, L=2048, cs=32, k=7, n_q=1, seed=79,
                   residency="uniform", resident_frac=0.25)
-STEP_CASES = [TINY, V_HOT, V_CARRY, V_5Q, V_ZIPF, V_NQ64, V_ALL, V_ONEQ]
+# C = 1000: a ragged last landmark stage, union words not a multiple of 32, three queries
+V_ODD = Workload("odd_c", B=3, Hq=12, Hkv=3, d=128, L=16000, cs=16, k=37, n_q=3, spec_scale=(0.0, 0.2, 0.4),
+                 seed=83, residency="uniform", resident_frac=0.3)
+STEP_CASES = [TINY, V_HOT, V_CARRY, V_5Q, V_ZIPF, V_NQ64, V_ALL, V_ONEQ, V_ODD]
 
 
 @pytest.fixture(scope="module")

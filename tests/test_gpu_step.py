@@ -181,3 +181,22 @@ def test_step_without_intermediates_gives_the_same_output(dd, w):
         assert ctx.status() == 0
     assert torch.equal(full, buf.out)
     assert int(mc.item()) == int(buf.inter["miss_count"].item())
+
+
+@pytest.mark.parametrize("kind", [0, 1], ids=["mbarrier", "lookback_word"])
+def test_bounded_wait_runs_out_and_the_context_stays_usable(dd, kind):
+    # a wait on something nothing signals gives up by itself (~2 s), reports a
+    # timeout through the status word, and the next step on the context works
+    import time
+    w = TINY
+    x = tl.host_inputs(w)
+    buf = StepBuffers(w, x)
+    with dd.Context(shape_of(w), max_misses=buf.cap) as ctx:
+        t0 = time.perf_counter()
+        ctx.selftest_bounded_wait(kind)
+        assert ctx.status() == dd.DD_ERR_TIMEOUT
+        assert 1.0 < time.perf_counter() - t0 < 30.0
+        assert ctx.status() == 0                       # read and cleared
+        buf.run(ctx)
+        assert ctx.status() == 0
+        assert not bool(buf.out.isnan().any())
