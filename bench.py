@@ -306,6 +306,7 @@ class LayerData:
         dd.synth_kv(shape, seed, synth.tensor_id(synth.TID_K, layer), self.Kh, bias, u_hat)
         dd.synth_kv(shape, seed, synth.tensor_id(synth.TID_V, layer), self.Vh)
         self.lm = torch.empty(w.B * w.Hkv * w.C * lm_vectors * w.d, dtype=torch.bfloat16, device="cuda")
+        self.Khot = self.Vhot = None   # an HBM copy of K / V when every chunk is resident
         self.q_host = torch.empty(self.q.numel(), dtype=torch.bfloat16, pin_memory=True)
         torch.cuda.synchronize()
         self.q_host.copy_(self.q)
@@ -369,7 +370,14 @@ def run_ours(args, world, rank, local):
     minmax = args.landmarks == "minmax"
     lm_kind = dd.LM_MINMAX if minmax else dd.LM_MEAN
     layers = [LayerData(dd, shape, w, l, rank, 2 if minmax else 1) for l in range(N_LAYERS)]
-    ctx = dd.Context(shape, max_misses=cap, hot_slots=0)
+    resident_all = args.residency == "all"
+    if resident_all:
+        # every chunk resident: the layers' K and V also live in an HBM pool, in the
+        # host layout ([B*Hkv*C] chunks of cs rows), and the residency map is the identity
+        for L_ in layers:
+            L_.Khot = L_.Kh.to("cuda")
+            L_.Vhot = L_.Vh.to("cuda")
+    ctx = dd.Context(shape, max_misses=cap, hot_slots=w.B * w.Hkv * w.C if resident_all else 0)
     touch = torch.empty(w.B * w.Hkv * w.C * w.d, dtype=torch.bfloat16, device="cuda")
     for L_ in layers:
         if minmax:
@@ -381,7 +389,8 @@ def run_ours(args, world, rank, local):
         # so that the timed steps see the steady state
         ctx.build_landmarks(L_.Vh, touch)
     del touch
-    slot = torch.full((w.B * w.Hkv * w.C,), -1, dtype=torch.int32, device="cuda")
+    slot = (torch.arange(w.B * w.Hkv * w.C, dtype=torch.int32, device="cuda") if resident_all
+            else torch.full((w.B * w.Hkv * w.C,), -1, dtype=torch.int32, device="cuda"))
     ns = cap * w.cs * w.d
     Kst = [torch.empty(ns, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     Vst = [torch.empty(ns, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
@@ -415,7 +424,7 @@ def run_ours(args, world, rank, local):
 
     def step(i, layer, events=None, inter=None):
         d_ = layers[layer % N_LAYERS]
-        ctx.step(layer, d_.q, d_.lm, d_.Kh, d_.Vh, slot, None, None, Kst, Vst, out, mode=mode,
+        ctx.step(layer, d_.q, d_.lm, d_.Kh, d_.Vh, slot, d_.Khot, d_.Vhot, Kst, Vst, out, mode=mode,
                  intermediates=inter, stage_events=events, lm_kind=lm_kind)
 
     sampler = ClockSampler(local) if rank == 0 else None
@@ -468,7 +477,11 @@ def run_ours(args, world, rank, local):
     # the dominant kernel's duration is the one measured inside the timed region
     t_dom = (dom_ms_timed if dom == dom_timed else stage_ms[dom]) * 1e-3
     traffic = profiled_traffic(dom, w.name)
-    if fused and dom == "attention":
+    if fused and dom == "attention" and M == 0:
+        roof = {"bound": "hbm", "achieved": attn_b / t_dom / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                "peak_kind": hbm_kind, "traffic": None,
+                "kernel": "k_attn (every chunk resident: K and V by TMA from the HBM pool)"}
+    elif fused and dom == "attention":
         roof = {"bound": "host_link", "achieved": gather_b / t_dom / 1e9, "peak": link_memcpy, "unit": "GB/s",
                 "peak_kind": "pinned H2D cudaMemcpyAsync, best of 10 x 1 GiB, measured in this run",
                 "traffic": traffic, "kernel": "k_attn (gather fused: missing chunks read over the host link)",
@@ -497,6 +510,41 @@ def run_ours(args, world, rank, local):
                     "traffic": {"score": profiled_traffic("score", w.name),
                                 "attention": profiled_traffic("attention", w.name)}}
     roof_hbm["frac"] = roof_hbm["achieved"] / hbm_peak
+
+    # the same steps captured in a CUDA graph (one capture of all layers) and replayed
+    graph = None
+    if mode == dd.GATHER_ZEROCOPY:
+        gs = torch.cuda.Stream()
+        with torch.cuda.stream(gs):
+            for l in range(N_LAYERS):          # warm-up on the capture stream
+                d_ = layers[l]
+                ctx.step(l, d_.q, d_.lm, d_.Kh, d_.Vh, slot, d_.Khot, d_.Vhot, Kst, Vst, out, mode=mode,
+                         lm_kind=lm_kind, stream=gs)
+        torch.cuda.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=gs, capture_error_mode="relaxed"):
+            for l in range(N_LAYERS):
+                d_ = layers[l]
+                ctx.step(l, d_.q, d_.lm, d_.Kh, d_.Vh, slot, d_.Khot, d_.Vhot, Kst, Vst, out, mode=mode,
+                         lm_kind=lm_kind, stream=gs)
+        reps = max(1, K // N_LAYERS)
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(gs):                  # a replay runs on the current stream
+            for _ in range(3):
+                cg.replay()
+            torch.cuda.synchronize()
+            ga.record(gs)
+            for _ in range(reps):
+                cg.replay()
+            gb.record(gs)
+        torch.cuda.synchronize()
+        if ctx.status() != 0:
+            raise RuntimeError("device status after the graph replays is not OK")
+        g_s = max_over_ranks(ga.elapsed_time(gb) * 1e-3, world)
+        graph = {"value": world * reps * N_LAYERS / g_s, "unit": UNIT,
+                 "ms_per_step": 1e3 * g_s / (reps * N_LAYERS), "steps": reps * N_LAYERS,
+                 "note": f"all {N_LAYERS} layers' steps captured once in a CUDA graph, replayed {reps} times"}
+        del cg
 
     # end to end through the public call with host buffers: q in, out back
     out_host = torch.empty(out.numel(), dtype=torch.float32, pin_memory=True)
@@ -530,7 +578,9 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": world * K / t_max, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": 1e3 * t_max / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, args.mode, world, args.landmarks),
+        "config": dict(config_of(w, args.mode, world, args.landmarks),
+                       **({"residency": "all: every chunk in an HBM pool, no host reads",
+                           "workload": w.name + "_all_resident"} if resident_all else {})),
         "roofline": roof, "roofline_hbm": roof_hbm,
         "stages_us": {n: 1e3 * v for n, v in stage_ms.items()},
         "stages_note": f"stages_us: mean over {n_stage} further steps with an event at every stage boundary "
@@ -542,6 +592,7 @@ def run_ours(args, world, rank, local):
         "wall_s": wall,
         "e2e": {"value": world * K / e2e_s, "unit": UNIT, "h2d_bytes_per_step": q_b,
                 "d2h_bytes_per_step": w.B * w.n_q * w.Hq * w.d * 4},
+        "graph_replay": graph,
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -773,6 +824,8 @@ def main():
     ap.add_argument("--workload", default=LLAMA8B_32K.name, choices=sorted(BY_NAME))
     ap.add_argument("--mode", choices=("zerocopy", "memcpy"), default="zerocopy")
     ap.add_argument("--landmarks", choices=("mean", "minmax"), default="mean")
+    ap.add_argument("--residency", choices=("none", "all"), default="none",
+                    help="all: the whole KV also in an HBM pool (no misses; attention bound by HBM)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefetch-ctas", type=int, default=2, help="pipelined mode: prefetch copy CTAs per SM")
     ap.add_argument("--pipeline", action="store_true",

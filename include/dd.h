@@ -235,6 +235,12 @@ typedef struct {
   int32_t *sel_cnt;              /* with mass_gamma: optional int32 [B,n_q,Hkv] row lengths */
 } dd_step_args;
 
+/* dd_step may be captured into a CUDA graph (zero-copy mode; the memcpy
+ * mode reads the miss list on the host): it keeps no per-call state on the
+ * host that a replay would repeat wrongly.  While the stream is capturing, the
+ * release events of the staging buffers are left alone -- the graph orders
+ * its own steps -- so a caller that replays such a graph and also runs steps
+ * on another stream orders the two itself. */
 dd_status dd_step(dd_ctx *ctx, const dd_step_args *args, dd_stream_t stream);
 
 /* Predictive prefetch of a layer's predicted selection into its transfer

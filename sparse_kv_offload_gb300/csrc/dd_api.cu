@@ -28,7 +28,6 @@ struct dd_ctx {
   unsigned long long *lb_word = nullptr;        // fused selection: look-back words, ticket
   unsigned long long *diag_word = nullptr;      // a word nothing publishes (bounded-wait self-test)
   int32_t *ticket = nullptr;
-  uint32_t epoch = 0;
   void *dummy_pool = nullptr;
   dd::AttnPlan plan;
   // host side
@@ -184,7 +183,7 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   add(c->plan.flat_entries, 16);               // flat chunk table
   add(64 * 128, 2);                            // dummy pool (64 rows)
   add(units, 8);                               // look-back words
-  add(2, 4);                                   // ticket
+  add(3, 4);                                   // ticket counters + look-back epoch
   add(1, 8);                                   // self-test word
   if (cudaMalloc(&c->ws, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
   uint8_t *cur = static_cast<uint8_t *>(c->ws);
@@ -205,9 +204,12 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   c->flat = carve<int4>(cur, c->plan.flat_entries);
   c->dummy_pool = carve<uint16_t>(cur, 64 * 128);
   c->lb_word = carve<unsigned long long>(cur, units);
-  c->ticket = carve<int32_t>(cur, 2);
+  c->ticket = carve<int32_t>(cur, 3);
   c->diag_word = carve<unsigned long long>(cur, 1);
   if (cudaMemset(c->ws, 0, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
+  const int32_t first_epoch = 1;   // look-back words start zeroed, i.e. with epoch 0
+  if (cudaMemcpy(c->ticket + 2, &first_epoch, sizeof(first_epoch), cudaMemcpyHostToDevice) != cudaSuccess)
+    return fail(DD_ERR_CUDA);
   if (cudaMallocHost(reinterpret_cast<void **>(&c->h_miss), (size_t)(1 + (max_misses > 0 ? max_misses : 1)) * 4) !=
       cudaSuccess)
     return fail(DD_ERR_CUDA);
@@ -521,8 +523,6 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   const bool fused = a->mass_gamma <= 0.f && dd::fused_select_smem(d.n_q, c->C, d.k) > 0;
   if (fused) {
     if (!aligned16(a->q) || !aligned16(a->lm)) return DD_ERR_INVALID_ARG;
-    c->epoch = (c->epoch + 1) & 0x3FFFFFFFu;   // 30 bits, never 0 (0 is the zeroed words' epoch)
-    if (c->epoch == 0) c->epoch = 1;
     dd::SelectOut o;
     o.scores = a->scores;
     o.sel = a->sel;
@@ -539,7 +539,6 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
     o.flat = c->flat;
     o.lb_word = c->lb_word;
     o.ticket = c->ticket;
-    o.epoch = c->epoch;
     o.units = c->units;
     o.Hq = d.Hq;
     o.Hkv = d.Hkv;
@@ -576,7 +575,13 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   // staging buffer p may still be read by the attention of layer - 2; on the
   // same stream the stream order already guarantees it, and leaving out the
   // wait lets the attention kernel launch early behind the resolver
-  if (c->used[p] && c->released_on[p] != s) DD_CUDA(cudaStreamWaitEvent(s, c->released[p], 0));
+  // While the stream is being captured into a CUDA graph the step leaves the
+  // release events alone: the captured steps are ordered by the graph itself,
+  // and an event recorded during a capture cannot be waited on outside it.
+  cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+  DD_CUDA(cudaStreamIsCapturing(s, &capturing));
+  const bool captured = capturing != cudaStreamCaptureStatusNone;
+  if (!captured && c->used[p] && c->released_on[p] != s) DD_CUDA(cudaStreamWaitEvent(s, c->released[p], 0));
   const void *kh_dev = nullptr, *vh_dev = nullptr;
   if (a->mode == DD_GATHER_ZEROCOPY) {
     // the attention kernel itself copies the missing chunks from host memory
@@ -590,9 +595,11 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   DD_TRY(attn_impl(c, a->q, a->Khot, a->Vhot, a->Kst[p], a->Vst[p], union_slot, union_qmask, union_cnt, miss_count,
                    a->softmax_scale, a->out, true, kh_dev, vh_dev, a->K_tail, a->V_tail, stream));
   DD_TRY(mark(5));
-  DD_CUDA(cudaEventRecord(c->released[p], s));
-  c->released_on[p] = s;
-  c->used[p] = true;
+  if (!captured) {
+    DD_CUDA(cudaEventRecord(c->released[p], s));
+    c->released_on[p] = s;
+    c->used[p] = true;
+  }
   return DD_OK;
 }
 

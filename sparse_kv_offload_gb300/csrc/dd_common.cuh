@@ -283,8 +283,7 @@ struct SelectOut {
   int32_t *chunk_off;             // attention plan: [units + 1]
   int4 *flat;                     // attention plan: [units * umax]
   unsigned long long *lb_word;    // look-back: [units] {epoch:30, union count:17, miss count:17}
-  int32_t *ticket;                // [2] next unit, CTAs done
-  uint32_t epoch;                 // distinct per launch, never 0
+  int32_t *ticket;                // [3] next unit, CTAs done, look-back epoch of the next launch (never 0)
   int units, Hq, Hkv, C, k, umax, cs;
   int64_t hot_slots, max_misses;
   int32_t *status;

@@ -501,13 +501,17 @@ __global__ void __launch_bounds__(kFusedThreads) k_select_fused(const uint4 *__r
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ uint32_t s_epoch;
   if (tid == 0) {
     s_unit = atomicAdd(o.ticket, 1);                       // units in the order their CTAs start
+    // this launch's look-back epoch; the previous launch's last CTA advanced it
+    s_epoch = *reinterpret_cast<volatile uint32_t *>(o.ticket + 2);
     for (int st = 0; st < n_ring; ++st) mbar_init(smem_u32(&ring_bar[st]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   const int unit = s_unit;
+  const uint32_t epoch = s_epoch;
   const int C = o.C, k = o.k, Hkv = o.Hkv;
   const int b = unit / Hkv, g = unit - b * Hkv;
   const int G = o.Hq / Hkv;
@@ -694,7 +698,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_select_fused(const uint4 *__r
   // at once and re-polls only those not yet published; one round trip
   // after the slowest predecessor, no chain
   if (warp == 0) {
-    const unsigned long long ep = (unsigned long long)o.epoch << 34;
+    const unsigned long long ep = (unsigned long long)epoch << 34;
     if (lane == 0) st_relaxed_u64(&o.lb_word[unit], ep | ((unsigned long long)U << 17) | (unsigned long long)M);
     int su = 0, sm = 0;
     bool ok = true;
@@ -709,7 +713,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_select_fused(const uint4 *__r
 #pragma unroll
       for (int t = 0; t < kLookBatch; ++t) {
         const int idx = base + t * 32 + lane;
-        if ((w8[t] >> 34) != o.epoch) w8[t] = wait_published(&o.lb_word[idx], o.epoch, t0, &ok);
+        if ((w8[t] >> 34) != epoch) w8[t] = wait_published(&o.lb_word[idx], epoch, t0, &ok);
         su += (int)((w8[t] >> 17) & 0x1FFFFull);
         sm += (int)(w8[t] & 0x1FFFFull);
       }
@@ -786,11 +790,16 @@ __global__ void __launch_bounds__(kFusedThreads) k_select_fused(const uint4 *__r
       *o.miss_count = moff + M;
       if ((int64_t)moff + M > o.max_misses) set_status(o.status, DD_ERR_CAPACITY);
     }
-    // the last CTA to finish resets the ticket counter for the next launch
+    // the last CTA to finish resets the ticket counters and advances the
+    // epoch (30 bits, never 0: zeroed words carry epoch 0) for the next launch;
+    // every CTA of this launch has read the epoch by then.  Kept on the device,
+    // so replaying a captured step in a CUDA graph stays correct.
     __threadfence();
     if (atomicAdd(o.ticket + 1, 1) == o.units - 1) {
+      uint32_t next = (epoch + 1u) & 0x3FFFFFFFu;
       o.ticket[0] = 0;
       o.ticket[1] = 0;
+      o.ticket[2] = (int32_t)(next == 0u ? 1u : next);
       __threadfence();
     }
   }

@@ -200,3 +200,51 @@ def test_bounded_wait_runs_out_and_the_context_stays_usable(dd, kind):
         buf.run(ctx)
         assert ctx.status() == 0
         assert not bool(buf.out.isnan().any())
+
+
+def test_step_replays_in_a_cuda_graph(dd):
+    # the step keeps no per-call state on the host that a replay would repeat
+    # wrongly (the look-back epoch lives on the device), so a captured step
+    # replays correctly, also after its inputs change in place
+    import torch
+    from test_gpu_parity import V_HOT
+    w = V_HOT
+    x = tl.host_inputs(w)
+    buf = StepBuffers(w, x)
+    q2 = synth.queries(w.seed + 1, w.B, w.n_q, w.Hq, w.d, w.spec_scale)
+    want = oracle.step(x["q"], x["lm"], x["K"], x["V"], x["slot"], x["Khot"], x["Vhot"], w.k, w.cs)
+    want2 = oracle.step(q2, x["lm"], x["K"], x["V"], x["slot"], x["Khot"], x["Vhot"], w.k, w.cs)
+    s = torch.cuda.Stream()
+    mc = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sel = torch.zeros(w.B * w.n_q * w.Hkv * w.k, dtype=torch.int32, device="cuda")
+
+    def step():
+        ctx.step(0, buf.q, buf.lm, buf.Kh, buf.Vh, buf.slot, buf.Khot, buf.Vhot, buf.Kst, buf.Vst, buf.out,
+                 intermediates={"miss_count": mc, "sel": sel}, stream=s)
+
+    def check(ref):
+        got_sel = sel.cpu().numpy().reshape(ref["sel"].shape)
+        unit_ok = tl.selection_rows_match(got_sel, ref["scores"], ref["sel"], w.k).all(axis=1)
+        if unit_ok.all():
+            assert int(mc.item()) == ref["miss_count"]
+        mask = np.broadcast_to(unit_ok[:, None, :, None], (w.B, w.n_q, w.Hkv, w.G)).reshape(w.B, w.n_q, w.Hq)
+        tl.check_attention(buf.out.cpu().numpy().reshape(ref["out"].shape), ref["out"], mask)
+
+    with dd.Context(shape_of(w), max_misses=buf.cap, hot_slots=buf.hot) as ctx:
+        with torch.cuda.stream(s):
+            step()                                  # warm-up: host views, kernel attributes
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+            step()
+        for _ in range(3):
+            buf.out.fill_(float("nan"))
+            g.replay()
+            torch.cuda.synchronize()
+            assert ctx.status() == 0
+            check(want)
+        buf.q.copy_(tl.to_bf16(q2))
+        g.replay()
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+        check(want2)
