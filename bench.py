@@ -425,7 +425,8 @@ def run_ours(args, world, rank, local):
     def step(i, layer, events=None, inter=None):
         d_ = layers[layer % N_LAYERS]
         ctx.step(layer, d_.q, d_.lm, d_.Kh, d_.Vh, slot, d_.Khot, d_.Vhot, Kst, Vst, out, mode=mode,
-                 intermediates=inter, stage_events=events, lm_kind=lm_kind)
+                 intermediates=inter, stage_events=events, lm_kind=lm_kind, mass_gamma=args.mass_gamma,
+                 softmax_scale=args.softmax_scale)
 
     sampler = ClockSampler(local) if rank == 0 else None
     for i in range(args.warmup):
@@ -498,8 +499,10 @@ def run_ours(args, world, rank, local):
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["peak"] else None
     if fused:
         # attention is bound by the host link here; the HBM-bound kernel is the scoring pass
-        roof_hbm = {"bound": "hbm", "kernels": "k_select_fused (scoring + top-k + union + plan; bytes: the "
-                                               "landmark and query reads and the score rows)",
+        roof_hbm = {"bound": "hbm",
+                    "kernels": ("k_score (coverage budgets run the stage kernels)" if args.mass_gamma > 0 else
+                                "k_select_fused (scoring + top-k + union + plan; bytes: the landmark and query "
+                                "reads and the score rows)"),
                     "achieved": score_b / (stage_ms["score"] * 1e-3) / 1e9,
                     "peak": hbm_peak, "unit": "GB/s", "peak_kind": hbm_kind,
                     "traffic": {"score": profiled_traffic("score", w.name)}}
@@ -519,14 +522,16 @@ def run_ours(args, world, rank, local):
             for l in range(N_LAYERS):          # warm-up on the capture stream
                 d_ = layers[l]
                 ctx.step(l, d_.q, d_.lm, d_.Kh, d_.Vh, slot, d_.Khot, d_.Vhot, Kst, Vst, out, mode=mode,
-                         lm_kind=lm_kind, stream=gs)
+                         lm_kind=lm_kind, stream=gs, mass_gamma=args.mass_gamma,
+                         softmax_scale=args.softmax_scale)
         torch.cuda.synchronize()
         cg = torch.cuda.CUDAGraph()
         with torch.cuda.graph(cg, stream=gs, capture_error_mode="relaxed"):
             for l in range(N_LAYERS):
                 d_ = layers[l]
                 ctx.step(l, d_.q, d_.lm, d_.Kh, d_.Vh, slot, d_.Khot, d_.Vhot, Kst, Vst, out, mode=mode,
-                         lm_kind=lm_kind, stream=gs)
+                         lm_kind=lm_kind, stream=gs, mass_gamma=args.mass_gamma,
+                         softmax_scale=args.softmax_scale)
         reps = max(1, K // N_LAYERS)
         ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(gs):                  # a replay runs on the current stream
@@ -579,6 +584,9 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": 1e3 * t_max / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(config_of(w, args.mode, world, args.landmarks),
+                       **({"selection": f"coverage budgets: gamma {args.mass_gamma}, at most k chunks",
+                           "softmax_scale": args.softmax_scale or 1 / math.sqrt(w.d)}
+                          if args.mass_gamma > 0 else {}),
                        **({"residency": "all: every chunk in an HBM pool, no host reads",
                            "workload": w.name + "_all_resident"} if resident_all else {})),
         "roofline": roof, "roofline_hbm": roof_hbm,
@@ -824,6 +832,9 @@ def main():
     ap.add_argument("--workload", default=LLAMA8B_32K.name, choices=sorted(BY_NAME))
     ap.add_argument("--mode", choices=("zerocopy", "memcpy"), default="zerocopy")
     ap.add_argument("--landmarks", choices=("mean", "minmax"), default="mean")
+    ap.add_argument("--mass-gamma", type=float, default=0.0,
+                    help="> 0: coverage budgets (smallest chunk set reaching this attention mass, at most k)")
+    ap.add_argument("--softmax-scale", type=float, default=0.0, help="<= 0: 1/sqrt(d)")
     ap.add_argument("--residency", choices=("none", "all"), default="none",
                     help="all: the whole KV also in an HBM pool (no misses; attention bound by HBM)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -14,6 +14,12 @@
  *      layer-scoped ping-pong HBM staging buffer,
  *   5. run GQA attention of every query over the rows of its own selection.
  *
+ * Extensions of the same step: Quest-style min/max landmarks and coverage
+ * budgets for the selection, the step's own tokens as causal tail rows of
+ * the attention, a capped LRU residency update of per-(request, KV head) hot
+ * pools after a step, and a predictive prefetch of a layer's predicted
+ * chunks ahead of its step (each documented at its entry point below).
+ *
  * Notation: B requests, Hq query heads, Hkv KV heads, G = Hq/Hkv (query head h
  * reads KV head floor(h/G)), d head dimension, L context tokens, cs tokens per
  * chunk, C = L/cs chunks, k chunks per selection, n_q queries per request
