@@ -98,7 +98,12 @@ dd_status dd_build_landmarks(dd_ctx *ctx, const void *K, void *lm, dd_stream_t s
 /* Landmark scores of all n_q queries in one pass over lm (DualDecoder §4.1,
  * §5.2).  q: bf16 [B,n_q,Hq,d]; lm: bf16 [B,Hkv,C,d]; scores: fp32
  * [B,n_q,Hkv,C] = sum over the G q-heads h of KV head g of q[b,j,h,:].lm[b,g,c,:]
- * (unscaled; fp32 accumulation). */
+ * (unscaled; fp32 accumulation).  Ordering: the kernel starts reading lm
+ * while the kernel before it on the stream may still be finishing (it waits
+ * for that kernel only before reading q and writing scores), so lm must not
+ * be written by that kernel.  libdd's landmark builders and any kernel
+ * launched without programmatic dependent launch are safe predecessors; so
+ * is a copy.  The same holds for the lm of dd_step. */
 dd_status dd_score_landmarks(dd_ctx *ctx, const void *q, const void *lm, float *scores, dd_stream_t stream);
 
 /* Top-k with a coverage budget (MOIRA: per request, layer, KV head and step,

@@ -268,7 +268,8 @@ dd_status dd_score_landmarks(dd_ctx *c, const void *q, const void *lm, float *sc
   if (!q || !lm || !scores || !aligned16(q) || !aligned16(lm)) return DD_ERR_INVALID_ARG;
   c->launches += 1;
   return cuda_ok(dd::launch_score(static_cast<const uint4 *>(q), static_cast<const uint4 *>(lm), scores, c->dims.B,
-                                  c->dims.n_q, c->dims.Hq, c->dims.Hkv, c->C, (cudaStream_t)stream));
+                                  c->dims.n_q, c->dims.Hq, c->dims.Hkv, c->C, c->sm_count, c->status,
+                                  (cudaStream_t)stream));
 }
 
 dd_status dd_build_landmarks_minmax(dd_ctx *c, const void *K, void *lm2, dd_stream_t stream) {
@@ -288,8 +289,8 @@ dd_status dd_score_landmarks_minmax(dd_ctx *c, const void *q, const void *lm2, f
   if (!q || !lm2 || !scores || !aligned16(q) || !aligned16(lm2)) return DD_ERR_INVALID_ARG;
   c->launches += 1;
   return cuda_ok(dd::launch_score_minmax(static_cast<const uint4 *>(q), static_cast<const uint4 *>(lm2), scores,
-                                         c->dims.B, c->dims.n_q, c->dims.Hq, c->dims.Hkv, c->C,
-                                         (cudaStream_t)stream));
+                                         c->dims.B, c->dims.n_q, c->dims.Hq, c->dims.Hkv, c->C, c->sm_count,
+                                         c->status, (cudaStream_t)stream));
 }
 
 dd_status dd_select_topk(dd_ctx *c, const float *scores, int32_t *sel, dd_stream_t stream) {
@@ -517,14 +518,20 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   };
   DD_TRY(mark(0));
   const dd_dims &d = c->dims;
-  // scoring, top-k and the union in one kernel per (b,g) when a unit's score
-  // rows fit in shared memory (fixed k only); scores, selections and slots per
-  // selection entry are then produced only when the caller asks for them
+  // scoring streams every landmark once over all SMs; then top-k, union,
+  // residency, global ordinals and the attention plan run in one kernel per
+  // (b,g) when a unit's score rows fit in shared memory (fixed k only), and as
+  // separate stage kernels otherwise
+  if (a->lm_kind == DD_LM_MINMAX) {
+    DD_TRY(dd_score_landmarks_minmax(c, a->q, a->lm, scores, stream));
+  } else {
+    DD_TRY(dd_score_landmarks(c, a->q, a->lm, scores, stream));
+  }
+  DD_TRY(mark(1));
   const bool fused = a->mass_gamma <= 0.f && dd::fused_select_smem(d.n_q, c->C, d.k) > 0;
   if (fused) {
-    if (!aligned16(a->q) || !aligned16(a->lm)) return DD_ERR_INVALID_ARG;
     dd::SelectOut o;
-    o.scores = a->scores;
+    o.scores = scores;
     o.sel = a->sel;
     o.attn_slot = a->attn_slot;
     o.resident_slot = a->resident_slot;
@@ -549,18 +556,10 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
     o.hot_slots = c->hot_slots;
     o.max_misses = c->max_misses;
     o.status = c->status;
-    DD_CUDA(dd::launch_select_fused(a->lm_kind == DD_LM_MINMAX, static_cast<const uint4 *>(a->q),
-                                    static_cast<const uint4 *>(a->lm), o, d.n_q, s));
-    DD_TRY(mark(1));
+    DD_CUDA(dd::launch_select_fused(o, d.n_q, s));
     DD_TRY(mark(2));
     c->launches += 1;
   } else {
-    if (a->lm_kind == DD_LM_MINMAX) {
-      DD_TRY(dd_score_landmarks_minmax(c, a->q, a->lm, scores, stream));
-    } else {
-      DD_TRY(dd_score_landmarks(c, a->q, a->lm, scores, stream));
-    }
-    DD_TRY(mark(1));
     if (a->mass_gamma > 0.f) {
       DD_TRY(dd_select_topk_mass(c, scores, sel, a->sel_cnt, a->mass_gamma, a->mass_k_min, a->softmax_scale,
                                  stream));

@@ -160,6 +160,10 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 // kernel in the stream has completed and its writes are visible, which also
 // keeps the completion order transitive along the chain.  pdl_trigger() lets
 // the next kernel's CTAs launch early; it is issued right after the wait.
+// One exception: the scoring kernel requests its first landmark tiles before
+// its wait (landmarks are an input of the step, not an output of the kernel
+// before it), so the landmark builders skip pdl_trigger and release their
+// dependents only at exit.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -266,14 +270,14 @@ namespace dd {
 struct Ctx;
 cudaError_t launch_build_landmarks(const uint4 *K, uint4 *lm, int64_t n_chunks, int cs, cudaStream_t s);
 cudaError_t launch_score(const uint4 *q, const uint4 *lm, float *scores, int B, int n_q, int Hq, int Hkv,
-                         int C, cudaStream_t s);
+                         int C, int sm_count, int32_t *status, cudaStream_t s);
 cudaError_t launch_build_minmax(const uint4 *K, uint4 *lm2, int64_t n_chunks, int cs, cudaStream_t s);
 cudaError_t launch_score_minmax(const uint4 *q, const uint4 *lm2, float *scores, int B, int n_q, int Hq, int Hkv,
-                                int C, cudaStream_t s);
+                                int C, int sm_count, int32_t *status, cudaStream_t s);
 cudaError_t launch_topk(const float *scores, int32_t *sel, int rows, int C, int k, cudaStream_t s);
 // outputs and state of the fused selection kernel (dd_select.cu)
 struct SelectOut {
-  float *scores;                  // [B,n_q,Hkv,C] or null
+  const float *scores;            // [B,n_q,Hkv,C] input: the scoring kernel's rows
   int32_t *sel;                   // [B,n_q,Hkv,k] or null
   int32_t *attn_slot;             // [B,n_q,Hkv,k] or null
   const int32_t *resident_slot;   // [B,Hkv,C]
@@ -289,8 +293,7 @@ struct SelectOut {
   int32_t *status;
 };
 size_t fused_select_smem(int n_q, int C, int k);
-cudaError_t launch_select_fused(bool minmax, const uint4 *q, const uint4 *lm, const SelectOut &o, int n_q,
-                                cudaStream_t s);
+cudaError_t launch_select_fused(const SelectOut &o, int n_q, cudaStream_t s);
 cudaError_t launch_selftest_wait(int kind, const unsigned long long *word, int32_t *status, cudaStream_t s);
 cudaError_t launch_topk_mass(const float *scores, int32_t *sel, int32_t *sel_cnt, int rows, int C, int k_max,
                              int k_min, float gamma, float tau_log2e, cudaStream_t s);

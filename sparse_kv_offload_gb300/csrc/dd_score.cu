@@ -14,8 +14,10 @@ namespace dd {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_build_landmarks(const uint4 *__restrict__ K, uint4 *__restrict__ lm,
                                                           int64_t n_chunks, int cs) {
+  // no early trigger: the scoring kernel reads landmarks before its
+  // dependency wait, so a kernel that writes them releases its dependents
+  // only when it exits
   pdl_wait();
-  pdl_trigger();
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t chunk = gid >> 4;
   const int part = (int)(gid & 15);
@@ -73,8 +75,7 @@ __device__ __forceinline__ uint32_t bf2_from_order_key(uint32_t k) {
 
 __global__ void __launch_bounds__(256) k_build_minmax(const uint4 *__restrict__ K, uint4 *__restrict__ lm2,
                                                        int64_t n_chunks, int cs) {
-  pdl_wait();
-  pdl_trigger();
+  pdl_wait();   // no early trigger (see k_build_landmarks)
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t chunk = gid >> 4;
   const int part = (int)(gid & 15);
@@ -114,86 +115,120 @@ cudaError_t launch_build_minmax(const uint4 *K, uint4 *lm2, int64_t n_chunks, in
 // a1: scores[b,j,g,c] = qsum[b,j,g,:] . lm[b,g,c,:] with qsum the fp32 sum of
 // the group's G query heads (mean landmarks), or
 // sum_i max(qsum_i * min_i, qsum_i * max_i) (min/max landmarks: the largest
-// value qsum . k can take over any key k inside the chunk's box).  One CTA
-// scores kTilesPerCta tiles of landmarks of one (b,g) for all NQ queries, so
-// every landmark byte is read once.  16 lanes share one landmark (one
-// 16-byte load per vector each); each thread holds kPass landmarks of a tile
-// (8, or 4 of the twice as large min/max ones) and the loads of the next tile
-// are in flight while the current one is reduced.  The 16-lane reduction of
-// the kPass*NQ partial dots is a butterfly that halves the value set at every
-// step (8+4+2+1 shuffles per 16 dots), leaving dot (lane position) in each
-// lane.
+// value qsum . k can take over any key k inside the chunk's box).
+//
+// The landmarks of all (b,g) units lie end to end in HBM, and scoring reads
+// each of their bytes once, so the kernel is a stream: one CTA per SM takes an
+// equal contiguous span of landmark rows (a multiple of a ring stage) and
+// pulls it through a ring of kScoreStages 32 KB shared-memory stages with
+// 1-D bulk copies (one thread issues; completion on an mbarrier per stage,
+// bounded waits).  A stage never crosses a unit boundary, so every stage
+// scores against one unit's group sums (rebuilt when the unit changes).
+// 16 lanes share one landmark row (one 16-byte shared-memory load per
+// vector each) and every thread scores kPass rows of a stage for all NQ
+// queries; the 16-lane reduction of the kPass*NQ partial dots is a butterfly
+// that halves the value set at every step (8+4+2+1 shuffles per 16 dots),
+// leaving dot (lane position) in each lane.  Each (row, query) sum therefore
+// has one fixed order: an fmaf chain over the lane's 8 coordinates, then the
+// xor-8/4/2/1 tree over the 16 lanes.  A stage's scores are gathered in
+// shared memory and written out as contiguous runs of each query row.
 // ---------------------------------------------------------------------------
-constexpr int kScoreThreads = 256;
-constexpr int kRowsPerPass = kScoreThreads / 16;          // 16
-constexpr int kTilesPerCta = 4;
-__host__ __device__ constexpr int score_pass(bool mm) { return mm ? 4 : 8; }
-__host__ __device__ constexpr int score_tile(bool mm) { return score_pass(mm) * kRowsPerPass; }
+constexpr int kScoreThreads = 512;
+constexpr int kScoreRowsPerPass = kScoreThreads / 16;     // 32 landmark rows per pass
+constexpr int kScoreStages = 6;
+constexpr int kScoreStageBytes = 32 * 1024;
+__host__ __device__ constexpr int score_stage_rows(bool mm) { return kScoreStageBytes / (mm ? 512 : 256); }
+__host__ __device__ constexpr size_t score_smem(int n_q, bool mm) {
+  return (size_t)kScoreStages * kScoreStageBytes + 2 * (size_t)n_q * score_stage_rows(mm) * 4;
+}
 
 template <int NQ, bool MM>
-__global__ void __launch_bounds__(kScoreThreads) k_score(const uint4 *__restrict__ q, const uint4 *__restrict__ lm,
-                                                         float *__restrict__ scores, int Hq, int Hkv, int C) {
-  constexpr int kPass = score_pass(MM);
-  constexpr int kTile = score_tile(MM);
+__global__ void __launch_bounds__(kScoreThreads, 1) k_score(const uint4 *__restrict__ q, const uint4 *__restrict__ lm,
+                                                            float *__restrict__ scores, int Hq, int Hkv, int C,
+                                                            int64_t total_rows, int64_t rows_per_cta,
+                                                            int32_t *status) {
   constexpr int kVecs = MM ? 2 : 1;                       // vectors per landmark
-  constexpr int kVals = kPass * NQ;                       // partial dots per lane per tile
+  constexpr int kRowBytes = 256 * kVecs;
+  constexpr int kStageRows = score_stage_rows(MM);       // 128 or 64
+  constexpr int kPass = kStageRows / kScoreRowsPerPass;   // rows per thread per stage: 4 or 2
+  constexpr int kVals = kPass * NQ;                       // partial dots per lane per stage
   constexpr int kChunks = (kVals + 15) / 16;
-  __shared__ float sc[NQ][kTile];
+  extern __shared__ __align__(128) unsigned char ssm[];
+  unsigned char *ring = ssm;
+  float *outb = reinterpret_cast<float *>(ssm + kScoreStages * kScoreStageBytes);   // [2][NQ][kStageRows]
+  __shared__ __align__(8) uint64_t bar[kScoreStages];
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int i = 0; i < kScoreStages; ++i) mbar_init(smem_u32(&bar[i]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int64_t lo = (int64_t)blockIdx.x * rows_per_cta;
+  const int span = (int)((lo + rows_per_cta < total_rows ? lo + rows_per_cta : total_rows) - lo);
+  const unsigned char *src = reinterpret_cast<const unsigned char *>(lm) + lo * kRowBytes;
+  const int unit0 = (int)(lo / C), c_first = (int)(lo - (int64_t)unit0 * C);
+  // a stage: up to kStageRows rows, within the span and within one unit; the
+  // issuing thread and the consumers walk the same sequence with their own
+  // cursors (row offset in the span, chunk index in the unit)
+  auto stage_rows = [&](int done, int c) { return min(min(kStageRows, span - done), C - c); };
+  int i_done = 0, i_c = c_first, st_issue = 0;   // issuing thread only
+  auto issue = [&]() {
+    const int n = stage_rows(i_done, i_c);
+    const int rb = st_issue % kScoreStages;
+    const uint32_t b = smem_u32(&bar[rb]);
+    mbar_arrive_expect_tx(b, (uint32_t)n * kRowBytes);
+    bulk_load(smem_u32(ring + rb * kScoreStageBytes), src + (int64_t)i_done * kRowBytes, (uint32_t)n * kRowBytes, b);
+    i_done += n;
+    i_c += n;
+    if (i_c == C) i_c = 0;
+    ++st_issue;
+  };
+  // The landmarks are not written by the kernel this one may overlap (the
+  // landmark builders release their dependents only at exit), so the first
+  // ring stages are requested before the dependency wait: the stream's ramp
+  // overlaps the previous kernel's tail.  The queries and the score rows wait.
+  if (tid == 0)
+    while (st_issue < kScoreStages && i_done < span) issue();
   pdl_wait();
   pdl_trigger();
-  const int unit = blockIdx.x;
-  const int b = unit / Hkv, g = unit - b * Hkv;
+
+  const int part = tid & 15, sub = tid >> 4;
   const int G = Hq / Hkv;
-  const int tid = threadIdx.x;
-  const int part = tid & 15;
-  const int sub = tid >> 4;
-  const int cta_c0 = blockIdx.y * kTile * kTilesPerCta;
-  const uint4 *base = lm + (int64_t)unit * C * kVecs * kVecPerRow + part;
-
-  uint4 v[kPass][kVecs], nv[kPass][kVecs];
-#pragma unroll
-  for (int p = 0; p < kPass; ++p) {
-    const int c = cta_c0 + p * kRowsPerPass + sub;
-#pragma unroll
-    for (int e = 0; e < kVecs; ++e)
-      v[p][e] = (c < C) ? ldg_nc(base + ((int64_t)c * kVecs + e) * kVecPerRow) : make_uint4(0, 0, 0, 0);
-  }
-
-  // this lane's 8 coordinates of each query's group sum
   float qs[NQ][8];
+  int unit = unit0, c0 = c_first, done = 0, st = 0;
+  bool fresh = true;   // the group sums of `unit` are still to be built
+  for (; done < span; ++st) {
+    const int n = stage_rows(done, c0);
+    const int b = unit / Hkv, g = unit - b * Hkv;
+    if (fresh) {   // this lane's 8 coordinates of each query's group sum
+      fresh = false;
 #pragma unroll
-  for (int j = 0; j < NQ; ++j) {
+      for (int j = 0; j < NQ; ++j) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) qs[j][e] = 0.f;
-    for (int h = g * G; h < (g + 1) * G; ++h) {
-      float f[8];
-      unpack8(q[((int64_t)(b * NQ + j) * Hq + h) * kVecPerRow + part], f);
+        for (int e = 0; e < 8; ++e) qs[j][e] = 0.f;
+        for (int h = g * G; h < (g + 1) * G; ++h) {
+          float f[8];
+          unpack8(q[((int64_t)(b * NQ + j) * Hq + h) * kVecPerRow + part], f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) qs[j][e] += f[e];
-    }
-  }
-
-  for (int t = 0; t < kTilesPerCta; ++t) {
-    const int c0 = cta_c0 + t * kTile;
-    if (c0 >= C) break;
-    if (t + 1 < kTilesPerCta) {
-#pragma unroll
-      for (int p = 0; p < kPass; ++p) {
-        const int c = c0 + kTile + p * kRowsPerPass + sub;
-#pragma unroll
-        for (int e = 0; e < kVecs; ++e)
-          nv[p][e] = (c < C) ? ldg_nc(base + ((int64_t)c * kVecs + e) * kVecPerRow) : make_uint4(0, 0, 0, 0);
+          for (int e = 0; e < 8; ++e) qs[j][e] += f[e];
+        }
       }
     }
-    // partial dots: value a = p*NQ + j
+    const int rb = st % kScoreStages;
+    const bool ok = mbar_wait(smem_u32(&bar[rb]), (uint32_t)(st / kScoreStages) & 1u, status);
+    const unsigned char *stage = ring + rb * kScoreStageBytes;
+    float *out = outb + (st & 1) * NQ * kStageRows;
     float x[kChunks * 16];
 #pragma unroll
     for (int a = kVals; a < kChunks * 16; ++a) x[a] = 0.f;
 #pragma unroll
     for (int p = 0; p < kPass; ++p) {
+      const int row = p * kScoreRowsPerPass + sub;
+      const bool live = ok && row < n;
+      const uint4 *v = reinterpret_cast<const uint4 *>(stage + row * kRowBytes) + part;
       float f[8], fh[8];
-      unpack8(v[p][0], f);
-      if (MM) unpack8(v[p][kVecs - 1], fh);
+      unpack8(live ? v[0] : make_uint4(0, 0, 0, 0), f);
+      if (MM) unpack8(live ? v[kVecPerRow * (kVecs - 1)] : make_uint4(0, 0, 0, 0), fh);
 #pragma unroll
       for (int j = 0; j < NQ; ++j) {
         float acc = 0.f;
@@ -212,33 +247,55 @@ __global__ void __launch_bounds__(kScoreThreads) k_score(const uint4 *__restrict
       float xs[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) xs[i] = x[ch * 16 + i];
-      const float r = butterfly16(xs, part);
+      const float s = butterfly16(xs, part);
       const int a = ch * 16 + part;
-      if (a < kVals) sc[a % NQ][(a / NQ) * kRowsPerPass + sub] = r;
+      if (a < kVals) out[(a % NQ) * kStageRows + (a / NQ) * kScoreRowsPerPass + sub] = s;
     }
-    __syncthreads();
-    for (int i = tid; i < NQ * kTile; i += kScoreThreads) {
-      const int j = i / kTile, cc = i - j * kTile;
-      const int c = c0 + cc;
-      if (c < C) scores[((int64_t)(b * NQ + j) * Hkv + g) * C + c] = sc[j][cc];
+    // stage rb consumed by every warp (and the scores of this stage are in
+    // `out`); a timed-out wait anywhere ends the CTA's loop on every thread
+    if (__syncthreads_or(!ok)) break;
+    if (tid == 0 && i_done < span) issue();
+    // the other half of the double-buffered `out` is written only after the
+    // next barrier, which every thread reaches after these stores
+    float *dst = scores + ((int64_t)(b * NQ) * Hkv + g) * C + c0;
+#pragma unroll
+    for (int i = tid; i < NQ * kStageRows; i += kScoreThreads) {
+      const int j = i / kStageRows, cc = i % kStageRows;
+      if (cc < n) dst[(int64_t)j * Hkv * C + cc] = out[i];
     }
-    __syncthreads();
-#pragma unroll
-    for (int p = 0; p < kPass; ++p)
-#pragma unroll
-      for (int e = 0; e < kVecs; ++e) v[p][e] = nv[p][e];
+    done += n;
+    c0 += n;
+    if (c0 == C) {
+      c0 = 0;
+      ++unit;
+      fresh = true;
+    }
   }
+  // after a timed-out wait: let the copies still in flight land (bounded) before the CTA exits
+  if (done < span && tid == 0)
+    for (int s2 = st + 1; s2 < st_issue; ++s2)
+      mbar_wait(smem_u32(&bar[s2 % kScoreStages]), (uint32_t)(s2 / kScoreStages) & 1u, status);
 }
 
 template <bool MM>
 static cudaError_t launch_score_t(const uint4 *q, const uint4 *lm, float *scores, int B, int n_q, int Hq, int Hkv,
-                                  int C, cudaStream_t s) {
-  if (B == 0) return cudaSuccess;
-  const int per_cta = score_tile(MM) * kTilesPerCta;
-  dim3 grid(B * Hkv, (C + per_cta - 1) / per_cta);
+                                  int C, int sm_count, int32_t *status, cudaStream_t s) {
+  const int64_t total = (int64_t)B * Hkv * C;
+  if (total == 0) return cudaSuccess;
+  constexpr int kStageRows = score_stage_rows(MM);
+  const int64_t stages = (total + kStageRows - 1) / kStageRows;
+  const int64_t ctas = sm_count > 0 ? (sm_count < stages ? sm_count : stages) : 1;
+  const int64_t per = (stages + ctas - 1) / ctas * kStageRows;   // rows per CTA, whole stages
+  const int grid = (int)((total + per - 1) / per);
+  const size_t smem = score_smem(n_q, MM);
   switch (n_q) {
-#define DD_SCORE_CASE(N) \
-  case N: return launch_k(k_score<N, MM>, grid, dim3(kScoreThreads), 0, s, q, lm, scores, Hq, Hkv, C);
+#define DD_SCORE_CASE(N)                                                                                         \
+  case N: {                                                                                                       \
+    cudaError_t e = cudaFuncSetAttribute(k_score<N, MM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    if (e != cudaSuccess) return e;                                                                               \
+    return launch_k(k_score<N, MM>, dim3(grid), dim3(kScoreThreads), smem, s, q, lm, scores, Hq, Hkv, C, total,   \
+                    per, status);                                                                                 \
+  }
     DD_SCORE_CASE(1) DD_SCORE_CASE(2) DD_SCORE_CASE(3) DD_SCORE_CASE(4)
     DD_SCORE_CASE(5) DD_SCORE_CASE(6) DD_SCORE_CASE(7) DD_SCORE_CASE(8)
 #undef DD_SCORE_CASE
@@ -247,13 +304,13 @@ static cudaError_t launch_score_t(const uint4 *q, const uint4 *lm, float *scores
 }
 
 cudaError_t launch_score(const uint4 *q, const uint4 *lm, float *scores, int B, int n_q, int Hq, int Hkv, int C,
-                         cudaStream_t s) {
-  return launch_score_t<false>(q, lm, scores, B, n_q, Hq, Hkv, C, s);
+                         int sm_count, int32_t *status, cudaStream_t s) {
+  return launch_score_t<false>(q, lm, scores, B, n_q, Hq, Hkv, C, sm_count, status, s);
 }
 
 cudaError_t launch_score_minmax(const uint4 *q, const uint4 *lm2, float *scores, int B, int n_q, int Hq, int Hkv,
-                                int C, cudaStream_t s) {
-  return launch_score_t<true>(q, lm2, scores, B, n_q, Hq, Hkv, C, s);
+                                int C, int sm_count, int32_t *status, cudaStream_t s) {
+  return launch_score_t<true>(q, lm2, scores, B, n_q, Hq, Hkv, C, sm_count, status, s);
 }
 
 }  // namespace dd

@@ -434,13 +434,12 @@ cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32
 }
 
 // ---------------------------------------------------------------------------
-// The whole selection of a step in one kernel, one CTA (512 threads) per
-// (b,g) unit, when a unit's n_q score rows fit in shared memory:
-//  a1  the unit's landmarks are scored for all queries exactly as k_score
-//      does (16 lanes per landmark row, same per-lane FMA order and
-//      butterfly, so the scores are the same bits), kept in shared memory;
-//  a2  the top-k of every row comes from one radix select over all rows at
-//      once (per-row histograms, warp j settles row j);
+// The selection of a step after scoring, in one kernel, one CTA (512
+// threads) per (b,g) unit, when a unit's n_q score rows fit in shared memory:
+//  a2  the unit's score rows (just written by the scoring kernel, so read
+//      from L2) become order keys in shared memory; the top-k of every row
+//      comes from one radix select over all rows at once (per-row
+//      histograms, warp j settles row j);
 //  a3  the union and residency lookup read the selections from shared
 //      memory; the global miss ordinals and union offsets (sums over the
 //      earlier units) come from a look-back: each CTA takes its unit from a
@@ -450,10 +449,9 @@ cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32
 //      bounded (DD_ERR_TIMEOUT).  The CTA then writes its union lists with
 //      global slots, its miss-list entries and its part of the attention
 //      plan; the last unit writes the totals.
-// Scores, selections and per-entry slots go to device memory only when asked for.
+// Selections and per-entry slots go to device memory only when asked for.
 // ---------------------------------------------------------------------------
 constexpr int kFusedThreads = 512;
-constexpr int kFusedRowsPerPass = kFusedThreads / 16;   // 32 landmarks per pass
 
 constexpr int kLookBatch = 8;   // look-back words per lane in flight (256 units per round)
 
@@ -466,185 +464,222 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
   return v;
 }
 
-constexpr int kRingMaxStages = 6;            // landmark ring: up to 6 x 32 KB in flight per SM
-constexpr int kRingStageBytes = 32 * 1024;
-constexpr size_t kSelectDynSmem = 208 * 1024; // dynamic shared memory the fused kernel may use
+constexpr size_t kSelectMaxSmem = 216 * 1024;   // dynamic shared memory (beside the static ~8 KB)
 
-// ring stages that fit beside a unit's score rows and selections (at least 4
-// whenever the fused kernel is used at all)
-__host__ __device__ inline int ring_stages(int n_q, int C, int k) {
-  const long long rest = (long long)kSelectDynSmem - (long long)n_q * C * 4 - (long long)n_q * k * 4;
-  const long long st = rest / kRingStageBytes;
-  return (int)(st > kRingMaxStages ? kRingMaxStages : st);
+// dynamic shared memory of the fused kernel: [union scratch, (NQ + 4) words
+// per 32 chunks][keys, NQ*C][selections, NQ*k]; 0 when it does not fit
+size_t fused_select_smem(int n_q, int C, int k) {
+  const size_t W = (size_t)(C + 31) / 32;
+  const size_t bytes = ((size_t)n_q + 4) * W * 4 + (size_t)n_q * C * 4 + (size_t)n_q * k * 4;
+  return bytes <= kSelectMaxSmem ? bytes : 0;
 }
 
-template <int NQ, bool MM>
-__global__ void __launch_bounds__(kFusedThreads) k_select_fused(const uint4 *__restrict__ q,
-                                                                const uint4 *__restrict__ lm, SelectOut o) {
-  constexpr int kVecs = MM ? 2 : 1;
-  constexpr int kRowBytes = 256 * kVecs;                          // one landmark (one or two vectors)
-  constexpr int kStageLm = kRingStageBytes / kRowBytes;           // 128 or 64 landmarks per stage
-  constexpr int kPass = kStageLm / kFusedRowsPerPass;             // landmarks per thread per stage
-  constexpr int kVals = kPass * NQ;
-  constexpr int kChunks = (kVals + 15) / 16;
-  // dynamic shared memory: [ring, then the union scratch][scores -> keys, NQ*C][selections, NQ*k]
+// The kernel asks for at least this much, so that no two of its CTAs share an
+// SM: a CTA that does would run at part speed, and every later unit waits for
+// it in the look-back.  (Launched early behind the scoring kernel, the CTAs
+// would otherwise crowd onto the few SMs that kernel leaves free.)
+constexpr size_t kSelectMinSmem = 120 * 1024;
+
+template <int NQ>
+__global__ void __launch_bounds__(kFusedThreads, 1) k_select_fused(SelectOut o) {
   extern __shared__ __align__(128) unsigned char fsm_raw[];
-  const int n_ring = ring_stages(NQ, o.C, o.k);
-  unsigned char *ring = fsm_raw;
-  uint32_t *fsm = reinterpret_cast<uint32_t *>(fsm_raw + n_ring * kRingStageBytes);
-  __shared__ __align__(8) uint64_t ring_bar[kRingMaxStages];
   __shared__ int hist[NQ][256];
   __shared__ int scratch[33];
-  __shared__ uint32_t s_prefix[NQ];
-  __shared__ int s_remaining[NQ];
   __shared__ int s_unit, s_uoff, s_moff;
+  __shared__ uint32_t s_epoch;
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __shared__ uint32_t s_epoch;
   if (tid == 0) {
     s_unit = atomicAdd(o.ticket, 1);                       // units in the order their CTAs start
     // this launch's look-back epoch; the previous launch's last CTA advanced it
     s_epoch = *reinterpret_cast<volatile uint32_t *>(o.ticket + 2);
-    for (int st = 0; st < n_ring; ++st) mbar_init(smem_u32(&ring_bar[st]), 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   const int unit = s_unit;
   const uint32_t epoch = s_epoch;
   const int C = o.C, k = o.k, Hkv = o.Hkv;
   const int b = unit / Hkv, g = unit - b * Hkv;
-  const int G = o.Hq / Hkv;
-  const int part = tid & 15, sub = tid >> 4;
-  float *sc = reinterpret_cast<float *>(fsm);
-  int32_t *sel_s = reinterpret_cast<int32_t *>(fsm + NQ * C);
-
-  // ---- a1: the unit's landmarks stream through the ring (one thread issues
-  // the bulk copies); every warp scores its rows of each stage from shared memory
-  const int n_st = (C + kStageLm - 1) / kStageLm;
-  const unsigned char *lm_unit = reinterpret_cast<const unsigned char *>(lm) + (int64_t)unit * C * kRowBytes;
-  auto issue = [&](int st) {
-    const int r0 = st * kStageLm;
-    const uint32_t bytes = (uint32_t)min(kStageLm, C - r0) * kRowBytes;
-    const uint32_t bar = smem_u32(&ring_bar[st % n_ring]);
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_load(smem_u32(ring + (st % n_ring) * kRingStageBytes), lm_unit + (int64_t)r0 * kRowBytes, bytes, bar);
-  };
-  if (tid == 0)
-    for (int st = 0; st < min(n_ring, n_st); ++st) issue(st);
-  float qs[NQ][8];
-#pragma unroll
-  for (int j = 0; j < NQ; ++j) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) qs[j][e] = 0.f;
-    for (int h = g * G; h < (g + 1) * G; ++h) {
-      float f[8];
-      unpack8(q[((int64_t)(b * NQ + j) * o.Hq + h) * kVecPerRow + part], f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qs[j][e] += f[e];
-    }
-  }
-  for (int st = 0; st < n_st; ++st) {
-    const int rb = st % n_ring;
-    mbar_wait(smem_u32(&ring_bar[rb]), (uint32_t)(st / n_ring) & 1u, o.status);
-    const unsigned char *stage = ring + rb * kRingStageBytes;
-    const int r0 = st * kStageLm;
-    float x[kChunks * 16];
-#pragma unroll
-    for (int a = kVals; a < kChunks * 16; ++a) x[a] = 0.f;
-#pragma unroll
-    for (int p = 0; p < kPass; ++p) {
-      const int row = p * kFusedRowsPerPass + sub;
-      const bool live = r0 + row < C;
-      const uint4 *src = reinterpret_cast<const uint4 *>(stage + row * kRowBytes) + part;
-      float f[8], fh[8];
-      unpack8(live ? src[0] : make_uint4(0, 0, 0, 0), f);
-      if (MM) unpack8(live ? src[kVecPerRow * (kVecs - 1)] : make_uint4(0, 0, 0, 0), fh);
-#pragma unroll
-      for (int j = 0; j < NQ; ++j) {
-        float acc = 0.f;
-        if (MM) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc += fmaxf(qs[j][e] * f[e], qs[j][e] * fh[e]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc = fmaf(qs[j][e], f[e], acc);
-        }
-        x[p * NQ + j] = acc;
-      }
-    }
-#pragma unroll
-    for (int ch = 0; ch < kChunks; ++ch) {
-      float xs[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) xs[i] = x[ch * 16 + i];
-      const float r = butterfly16(xs, part);
-      const int a = ch * 16 + part;
-      const int c = r0 + (a / NQ) * kFusedRowsPerPass + sub;
-      if (a < kVals && c < C) sc[(a % NQ) * C + c] = r;
-    }
-    __syncthreads();                                       // stage rb consumed by every warp
-    if (tid == 0 && st + n_ring < n_st) issue(st + n_ring);
-  }
-  // the ring is free from here on: the union scratch lives there
   const int W = (C + 31) >> 5;
-  uint32_t *qbits = reinterpret_cast<uint32_t *>(ring);     // [NQ][W]
-  uint32_t *ubw = qbits + NQ * kMaxWords, *mbw = ubw + kMaxWords;
-  int *upre = reinterpret_cast<int *>(mbw + kMaxWords), *mpre = upre + kMaxWords;
-  if (o.scores) {
-    for (int i = tid; i < NQ * C; i += kFusedThreads) {
-      const int j = i / C, c = i - j * C;
-      o.scores[((int64_t)(b * NQ + j) * Hkv + g) * C + c] = sc[i];
-    }
+  uint32_t *qbits = reinterpret_cast<uint32_t *>(fsm_raw);                   // [NQ][W]
+  uint32_t *ubw = qbits + NQ * W, *mbw = ubw + W;
+  int *upre = reinterpret_cast<int *>(mbw + W), *mpre = upre + W;
+  uint32_t *keys = reinterpret_cast<uint32_t *>(mpre + W);    // [NQ][C]
+  int32_t *sel_s = reinterpret_cast<int32_t *>(keys + NQ * C);   // [NQ][k]
+
+  // ---- a2: the top k of every row (score descending, lower chunk first among
+  // equal scores), as one bitmap per row.  The row is split into at least k
+  // aligned segments of S chunks (S a power of two, at most 32); the smallest
+  // segment maximum t is a lower bound on the row's k-th largest key, since
+  // every segment holds a key >= t.  Only keys >= t take part in a radix
+  // select whose 8-bit digits are taken relative to the low end of the
+  // current key range (first pass: [t, row maximum], digit width sized to
+  // it), so the few keys left spread over the bins.  A pass ends the row when
+  // the boundary bin holds exactly the keys still needed; after the last
+  // digit the remaining ties go to the lowest chunks.
+  // per row: the current key range [lo, lo + w], its digit shift, keys still needed
+  __shared__ uint32_t s_lo[NQ], s_hi[NQ], s_w[NQ];
+  __shared__ int s_shift[NQ], s_rem[NQ], s_state[NQ];   // state 0: running, 1: keys >= lo, 2: ties at lo
+  int S = 32;
+  while (S > 1 && (C + S - 1) / S < k) S >>= 1;
+  if (tid < NQ) {
+    s_lo[tid] = 0xFFFFFFFFu;
+    s_hi[tid] = 0u;
   }
-  // ---- a2: radix select of all NQ rows at once (scores become order keys in place)
-  uint32_t *keys = fsm;
-  for (int i = tid; i < NQ * C; i += kFusedThreads) keys[i] = order_key(sc[i]);
-  uint32_t prefix = 0, pmask = 0;   // of row `warp` (warps >= NQ carry no row)
-  int remaining = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < NQ * 256; i += kFusedThreads) (&hist[0][0])[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < NQ * C; i += kFusedThreads) {
-      const int j = i / C;
-      const uint32_t key = keys[i];
-      const uint32_t pj = shift == 24 ? 0u : s_prefix[j];
-      if ((key & pmask) == pj) atomicAdd(&hist[j][(key >> shift) & 255u], 1);
+  __syncthreads();
+  {
+    // every row's scores of a 4 x 512-chunk slab in flight at once
+    const float *rows = o.scores + ((int64_t)(b * NQ) * Hkv + g) * C;   // row j at + j * Hkv * C
+    uint32_t mn[NQ], mx[NQ];   // over the segments this lane leads
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+      mn[j] = 0xFFFFFFFFu;
+      mx[j] = 0u;
     }
-    __syncthreads();
-    if (warp < NQ) {
-      int cnt[8], s = 0;
+    for (int c0 = warp * 32; c0 < C; c0 += 4 * kFusedThreads) {   // warp-uniform
+      float v[NQ][4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        cnt[e] = hist[warp][255 - 8 * lane - e];
-        s += cnt[e];
-      }
-      const int incl = warp_incl_scan(s);
-      const int excl = incl - s;
-      if (excl < remaining && remaining <= incl) {
-        int r = remaining - excl;
+      for (int j = 0; j < NQ; ++j)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (r > 0 && r <= cnt[e]) {
-            s_prefix[warp] = prefix | ((uint32_t)(255 - 8 * lane - e) << shift);
-            s_remaining[warp] = r;
-            r = 0;
-          } else if (r > 0) {
-            r -= cnt[e];
+        for (int e = 0; e < 4; ++e) {
+          const int c = c0 + e * kFusedThreads + lane;
+          v[j][e] = c < C ? rows[(int64_t)j * Hkv * C + c] : 0.f;
+        }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (c0 + e * kFusedThreads >= C) break;   // warp-uniform
+        const int c = c0 + e * kFusedThreads + lane;
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+          const uint32_t key = c < C ? order_key(v[j][e]) : 0u;
+          if (c < C) keys[j * C + c] = key;
+          uint32_t m = key;
+          for (int off = 1; off < S; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+          if ((lane & (S - 1)) == 0 && c < C) {
+            mn[j] = min(mn[j], m);
+            mx[j] = max(mx[j], m);
           }
         }
       }
     }
-    __syncthreads();
-    if (warp < NQ) {
-      prefix = s_prefix[warp];
-      remaining = s_remaining[warp];
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        mn[j] = min(mn[j], __shfl_xor_sync(0xffffffffu, mn[j], off));
+        mx[j] = max(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], off));
+      }
+      if (lane == 0 && mx[j] >= mn[j]) {   // the warp led at least one segment
+        atomicMin(&s_lo[j], mn[j]);
+        atomicMax(&s_hi[j], mx[j]);
+      }
     }
-    pmask |= 0xFFu << shift;
+  }
+  __syncthreads();
+  if (tid < NQ) {
+    const uint32_t d = s_hi[tid] - s_lo[tid];
+    s_w[tid] = d;
+    s_shift[tid] = d ? max(0, 24 - __clz(d)) : 0;   // w >> shift < 256
+    s_rem[tid] = k;
+    s_state[tid] = 0;
+  }
+  for (int pass = 0; pass < 5; ++pass) {
+    for (int i = tid; i < NQ * 256; i += kFusedThreads) (&hist[0][0])[i] = 0;
+    __syncthreads();
+    for (int j = 0; j < NQ; ++j) {
+      if (s_state[j] != 0) continue;
+      const uint32_t lo = s_lo[j], w = s_w[j];
+      const int sh = s_shift[j];
+      for (int c = tid; c < C; c += kFusedThreads) {
+        const uint32_t key = keys[j * C + c];
+        if (key >= lo && key - lo <= w) atomicAdd(&hist[j][(key - lo) >> sh], 1);
+      }
+    }
+    __syncthreads();
+    if (warp < NQ && s_state[warp] == 0) {
+      // lane l owns bins 255-8l down to 248-8l (descending digit order)
+      int cnt[8], sum = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        cnt[e] = hist[warp][255 - 8 * lane - e];
+        sum += cnt[e];
+      }
+      const int incl = warp_incl_scan(sum);
+      const int rem = s_rem[warp];
+      int above = incl - sum;
+      if (above < rem && rem <= incl) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (above < rem && rem <= above + cnt[e]) {
+            const int sh = s_shift[warp];
+            const uint32_t lo = s_lo[warp] + ((uint32_t)(255 - 8 * lane - e) << sh);
+            const int r = rem - above;
+            s_lo[warp] = lo;
+            s_rem[warp] = r;
+            if (cnt[e] == r) {
+              s_state[warp] = 1;
+            } else if (sh == 0) {
+              s_state[warp] = 2;
+            } else {   // the boundary bin [lo, lo + 2^sh - 1] becomes the range
+              const uint32_t w = (1u << sh) - 1u;
+              s_w[warp] = w;
+              s_shift[warp] = max(0, 24 - __clz(w));
+            }
+          }
+          above += cnt[e];
+        }
+      }
+    }
+    __syncthreads();
+    bool more = false;
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) more |= s_state[j] == 0;
+    if (!more) break;
+  }
+  // bitmaps: every warp builds whole 32-chunk words with a ballot; a row with
+  // ties at its last key is walked in chunk order by warp 0
+  for (int j = 0; j < NQ; ++j) {
+    const uint32_t lo = s_lo[j];
+    if (s_state[j] == 1) {
+      for (int c0 = warp * 32; c0 < C; c0 += kFusedThreads) {
+        const int c = c0 + lane;
+        const unsigned w = __ballot_sync(0xffffffffu, c < C && keys[j * C + c] >= lo);
+        if (lane == 0) qbits[j * W + (c0 >> 5)] = w;
+      }
+    } else if (warp == 0) {
+      if (s_state[j] != 2 && lane == 0) set_status(o.status, DD_ERR_DEVICE_CHECK);
+      const int rem = s_rem[j];
+      int run = 0;
+      for (int c0 = 0; c0 < C; c0 += 32) {
+        const int c = c0 + lane;
+        const uint32_t key = c < C ? keys[j * C + c] : 0u;
+        const bool eq = c < C && key == lo;
+        const unsigned be = __ballot_sync(0xffffffffu, eq);
+        const bool take = key > lo || (eq && run + __popc(be & ((1u << lane) - 1u)) < rem);
+        const unsigned w = __ballot_sync(0xffffffffu, c < C && take);
+        if (lane == 0) qbits[j * W + (c0 >> 5)] = w;
+        run += __popc(be);
+      }
+    }
+  }
+  __syncthreads();
+  if (o.sel || o.attn_slot) {
+    // the selections in ascending chunk order, from the bitmaps (row j has k bits)
+    for (int j = 0; j < NQ; ++j) {
+      const uint32_t w = tid < W ? qbits[j * W + tid] : 0u;
+      int tot;
+      int pos = block_excl_scan(__popc(w), scratch, &tot);
+      uint32_t rest = w;
+      while (rest) {
+        const int bit = __ffs(rest) - 1;
+        rest &= rest - 1;
+        if (pos < k) sel_s[j * k + pos] = tid * 32 + bit;
+        ++pos;
+      }
+      if (tid == 0 && tot != k) set_status(o.status, DD_ERR_DEVICE_CHECK);
+    }
     __syncthreads();
   }
-  for (int j = 0; j < NQ; ++j) emit_topk(keys + j * C, C, s_prefix[j], s_remaining[j], scratch, sel_s + j * k);
-  __syncthreads();
   if (o.sel) {
     for (int i = tid; i < NQ * k; i += kFusedThreads) {
       const int j = i / k, r = i - j * k;
@@ -652,35 +687,42 @@ __global__ void __launch_bounds__(kFusedThreads) k_select_fused(const uint4 *__r
     }
   }
 
-  // ---- a3: union bitmaps, residency, one union word per thread (W <= 512)
-  for (int i = tid; i < NQ * W; i += kFusedThreads) qbits[i] = 0u;
-  __syncthreads();
-  for (int i = tid; i < NQ * k; i += kFusedThreads) {
-    const int j = i / k, c = sel_s[i];
-    if (c < 0 || c >= C) {
-      set_status(o.status, DD_ERR_DEVICE_CHECK);
-      continue;
-    }
-    atomicOr(&qbits[j * W + (c >> 5)], 1u << (c & 31));
+  // ---- a3: union words, then the residency of every union chunk (one
+  // lookup per chunk, all of them in flight at once, kept in shared memory
+  // where the keys were), then one union word per thread (W <= 512)
+  const int32_t *rs_unit = o.resident_slot + (int64_t)unit * C;
+  int32_t *rs_s = reinterpret_cast<int32_t *>(keys);   // [C], valid for union chunks
+  if (tid < W) {
+    uint32_t ub = 0;
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) ub |= qbits[j * W + tid];
+    ubw[tid] = ub;
+    mbw[tid] = 0u;
   }
   __syncthreads();
-  const int32_t *rs_unit = o.resident_slot + (int64_t)unit * C;
+  for (int c0 = tid; c0 < C; c0 += 4 * kFusedThreads) {
+    int32_t rs[4];
+    bool in[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = c0 + e * kFusedThreads;
+      in[e] = c < C && ((ubw[c >> 5] >> (c & 31)) & 1u);
+      rs[e] = in[e] ? rs_unit[c] : -1;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (!in[e]) continue;
+      const int c = c0 + e * kFusedThreads;
+      rs_s[c] = rs[e];
+      if (rs[e] >= o.hot_slots) set_status(o.status, DD_ERR_DEVICE_CHECK);
+      if (rs[e] < 0 || rs[e] >= o.hot_slots) atomicOr(&mbw[c >> 5], 1u << (c & 31));
+    }
+  }
+  __syncthreads();
   int cu = 0, cm = 0;
   if (tid < W) {
-    uint32_t ub = 0, mb = 0;
-    for (int j = 0; j < NQ; ++j) ub |= qbits[j * W + tid];
-    uint32_t rest = ub;
-    while (rest) {
-      const int bit = __ffs(rest) - 1;
-      rest &= rest - 1;
-      const int32_t rs = rs_unit[tid * 32 + bit];
-      if (rs >= o.hot_slots) set_status(o.status, DD_ERR_DEVICE_CHECK);
-      if (rs < 0 || rs >= o.hot_slots) mb |= 1u << bit;
-    }
-    ubw[tid] = ub;
-    mbw[tid] = mb;
-    cu = __popc(ub);
-    cm = __popc(mb);
+    cu = __popc(ubw[tid]);
+    cm = __popc(mbw[tid]);
   }
   int tot;
   const int ex = block_excl_scan((cu << 16) | cm, scratch, &tot);   // unions never exceed C <= 16384
@@ -760,7 +802,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_select_fused(const uint4 *__r
           qm = 0;
         }
       } else {
-        const int32_t rs = rs_unit[c];
+        const int32_t rs = rs_s[c];
         o.union_slot[ubase + up] = rs;
         row = rs * o.cs;
       }
@@ -776,7 +818,7 @@ __global__ void __launch_bounds__(kFusedThreads) k_select_fused(const uint4 *__r
         const int w = c >> 5;
         const uint32_t low = (1u << (c & 31)) - 1u;
         if ((mbw[w] >> (c & 31)) & 1u) val = -(int32_t)((int64_t)moff + mpre[w] + __popc(mbw[w] & low) + 1);
-        else val = rs_unit[c];
+        else val = rs_s[c];
       }
       o.attn_slot[((int64_t)(b * NQ + j) * Hkv + g) * k + r] = val;
     }
@@ -805,36 +847,24 @@ __global__ void __launch_bounds__(kFusedThreads) k_select_fused(const uint4 *__r
   }
 }
 
-// the fused kernel's dynamic shared memory; 0 when its ring would be shallower than 4 stages
-size_t fused_select_smem(int n_q, int C, int k) {
-  const int st = ring_stages(n_q, C, k);
-  if (st < 4) return 0;
-  return (size_t)st * kRingStageBytes + (size_t)n_q * C * 4 + (size_t)n_q * k * 4;
-}
-
-template <bool MM>
-static cudaError_t launch_select_fused_t(const uint4 *q, const uint4 *lm, const SelectOut &o, int n_q,
-                                         cudaStream_t s) {
-  const size_t smem = fused_select_smem(n_q, o.C, o.k);
+cudaError_t launch_select_fused(const SelectOut &o, int n_q, cudaStream_t s) {
+  if (o.units == 0) return cudaSuccess;
+  size_t smem = fused_select_smem(n_q, o.C, o.k);
+  if (smem == 0) return cudaErrorInvalidValue;
+  if (smem < kSelectMinSmem) smem = kSelectMinSmem;
   switch (n_q) {
 #define DD_FUSED_CASE(N)                                                                                      \
   case N: {                                                                                                    \
-    cudaError_t e = cudaFuncSetAttribute(k_select_fused<N, MM>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+    cudaError_t e = cudaFuncSetAttribute(k_select_fused<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
                                          (int)smem);                                                           \
     if (e != cudaSuccess) return e;                                                                            \
-    return launch_k(k_select_fused<N, MM>, dim3(o.units), dim3(kFusedThreads), smem, s, q, lm, o);            \
+    return launch_k(k_select_fused<N>, dim3(o.units), dim3(kFusedThreads), smem, s, o);                        \
   }
     DD_FUSED_CASE(1) DD_FUSED_CASE(2) DD_FUSED_CASE(3) DD_FUSED_CASE(4)
     DD_FUSED_CASE(5) DD_FUSED_CASE(6) DD_FUSED_CASE(7) DD_FUSED_CASE(8)
 #undef DD_FUSED_CASE
     default: return cudaErrorInvalidValue;
   }
-}
-
-cudaError_t launch_select_fused(bool minmax, const uint4 *q, const uint4 *lm, const SelectOut &o, int n_q,
-                                cudaStream_t s) {
-  if (o.units == 0) return cudaSuccess;
-  return minmax ? launch_select_fused_t<true>(q, lm, o, n_q, s) : launch_select_fused_t<false>(q, lm, o, n_q, s);
 }
 
 // ---------------------------------------------------------------------------
