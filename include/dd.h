@@ -198,10 +198,11 @@ dd_status dd_sparse_attn_decode(dd_ctx *ctx, const void *q, const void *Khot, co
  * for dd_create, and the other arguments are those of dd_sparse_attn_decode.
  * device_status: caller-owned device int32, zero before the call; a kernel
  * that finds an error writes its dd_status code there (first error wins).
- * The split-K partials live in one fixed 8 MiB device array inside the
+ * The split-K partials live in one fixed 16 MiB device array inside the
  * library, which every GPU that loads the library holds until the process
- * exits.  A shape whose partials (B*Hkv * segments * NQ * 130 floats) do not
- * fit is refused at once with DD_ERR_CAPACITY.  The first call on a device
+ * exits.  A shape whose partials ((2 * SM count + B*Hkv) slots * consumer
+ * warps per 16 query vectors * NQ * 130 floats, with NQ = n_q*Hq/Hkv) and
+ * chunk offsets do not fit is refused at once with DD_ERR_CAPACITY.  The first call on a device
  * looks up that array's device address (once per device); make that first
  * call before any stream capture.  Nothing in the array needs to start at
  * zero, but every call shares it: calls that overlap on the GPU (on any

@@ -9,20 +9,22 @@
 // pick are masked for that query (the chunk's query mask).
 //
 // Work split ("stream-K"): the unions of all (request, KV head) units are
-// laid end to end (chunk_off = exclusive prefix of the union sizes) and one
-// persistent CTA per SM takes an equal contiguous slice of that sequence.  A
+// laid end to end (chunk_off = exclusive prefix of the union sizes) and each
+// of two persistent CTAs per SM takes an equal contiguous slice of that
+// sequence (two CTAs so that one's producer issues copies while the other's
+// does its per-stage bookkeeping or waits on a fresh slice's tables).  A
 // slice covers a few units ("runs").  At the end of a run every consumer
 // warp writes its partial (running max, sum and accumulator of its rows) into
 // slot CTA + unit, sub-slot warp -- slices are ordered like the units, so no
 // two (CTA, unit) pairs share a slot and n_cta + units slots suffice -- and a
 // combine kernel merges the partials of every unit.
 //
-// Data movement: a producer warp streams 128-row tiles of K and V into shared
+// Data movement: a producer warp streams 64-row tiles of K and V into shared
 // memory with 2-D TMA loads (cp.async.bulk.tensor, 128-byte swizzle, one box
 // per chunk and 64-column half) and each run's query vectors with bulk
 // copies, all completing on mbarriers; it runs ahead across run boundaries
 // with kStages tiles in flight.  Math: consumer warps own 16 query vectors
-// (one m16 tile) and 16-row slices of each tile; S = Q.K^T and O += P.V run on
+// (one m16 tile) and 16- or 32-row slices of each tile; S = Q.K^T and O += P.V run on
 // the tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate) with an online
 // softmax in fp32; P is split into bf16 hi + lo parts so the PV product keeps
 // ~16 significant bits.  The work is HBM-bound: the MMAs only keep the
@@ -34,23 +36,27 @@
 
 namespace dd {
 
-constexpr int kStageRows = 128;
-constexpr int kHalfBytes = kStageRows * 128;          // 128 rows x 64 bf16
+constexpr int kAttnCtasPerSm = 2;
+constexpr int kStageRows = 64;
+constexpr int kHalfBytes = kStageRows * 128;          // 64 rows x 64 bf16
 constexpr int kStageBytes = 4 * kHalfBytes;           // K lo, K hi, V lo, V hi
 constexpr int kMaxChunksPerStage = kStageRows / 16;   // cs >= 16
 constexpr int kQStride = 272;                         // bytes per staged query vector (256 + pad)
-constexpr int kHostBatch = 8;                         // 16-byte host loads in flight per lane (fused gather)
+constexpr int kHostBatch = 4;                         // 16-byte host loads in flight per lane (fused gather)
 
-// Tiles in flight: three for one m-tile, two when the staged queries and the
-// merge buffers of more m-tiles need the room (227 KiB of shared memory).
+// Tiles in flight per CTA: three for one m-tile, two when the staged queries
+// of more m-tiles need the room (two CTAs share an SM's 228 KiB).
 __host__ __device__ constexpr int stages_for(int mt) { return mt == 1 ? 3 : 2; }
 
 enum : int32_t { kFirst = 1, kLast = 2, kEnd = 4 };
 
-struct StageMeta {
+// 16-byte aligned: the mbarriers that follow the per-stage records in shared
+// memory need 8-byte alignment whatever the number of chunks per stage
+struct alignas(16) StageMeta {
   int32_t unit, nch, flags, uoff, ucnt, pad;   // uoff/ucnt: the unit's range in the concatenated unions
   uint8_t qm[kMaxChunksPerStage];
 };
+static_assert(sizeof(StageMeta) % 8 == 0, "mbarriers follow the stage records");
 
 struct AttnParams {
   const uint16_t *q;          // bf16 [B,n_q,Hq,128]
@@ -132,18 +138,20 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
 
 
 // ----------------------------------------------------------------- the kernel
-// Registers per thread: the register file holds one CTA, whose warps are
-// charged in groups of four; at most 224 (no spills in the consumer loop).
+// Registers per thread: the register file holds kAttnCtasPerSm CTAs (their
+// threads rounded up to a multiple of 128); at most 224.
 __host__ __device__ constexpr int attn_max_regs(int threads) {
-  return (65536 / ((threads + 127) / 128 * 128)) / 8 * 8 > 224 ? 224
-                                                                : (65536 / ((threads + 127) / 128 * 128)) / 8 * 8;
+  return (65536 / ((kAttnCtasPerSm * threads + 127) / 128 * 128)) / 8 * 8 > 224
+             ? 224
+             : (65536 / ((kAttnCtasPerSm * threads + 127) / 128 * 128)) / 8 * 8;
 }
 
 // Producer warps: warp 0 issues metadata and TMA; both share the host copies
-// of the fused gather.  Measured on the 16-request 32K layer, the host link
-// moved the most with about 16 loads of 16 bytes in flight per producer lane
-// in total: 2 warps x 8 (402 us per layer) beat 1 x 16 (407), 2 x 16 (414),
-// 4 x 16 (477) and 1 x 4 (499).
+// of the fused gather.  Measured on the 16-request 32K layer with one CTA per
+// SM, the host link moved the most with about 16 loads of 16 bytes in flight
+// per producer lane pair: 2 warps x 8 (402 us per layer) beat 1 x 16 (407),
+// 2 x 16 (414), 4 x 16 (477) and 1 x 4 (499); with two CTAs per SM the same
+// depth per SM is 2 warps x 4 loads in each CTA (kHostBatch).
 __host__ __device__ constexpr int producers_for(int) { return 2; }
 
 template <int MT, int WPM>
@@ -154,8 +162,8 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
   constexpr int kConsumers = MT * WPM;
   constexpr int kProducers = producers_for(kConsumers);
   constexpr int kStages = stages_for(MT);
-  constexpr int kRowsPerWarp = kStageRows / WPM;      // 32, 64 or 128
-  constexpr int kBlocks = kRowsPerWarp / 32;
+  constexpr int kRowsPerWarp = kStageRows / WPM;      // 16, 32 or 64
+  constexpr int kBlocks = kRowsPerWarp >= 32 ? kRowsPerWarp / 32 : 1;   // 16-row warps: half A only
   constexpr int kQBytes = 16 * MT * kQStride;
 
   extern __shared__ uint8_t smem_raw[];
@@ -392,7 +400,7 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
       const int row0 = wq * kRowsPerWarp + blk * 32;
       const int ciA = row0 >> rows_per_chunk_shift, ciB = (row0 + 16) >> rows_per_chunk_shift;
       const uint32_t qmA = ciA < m_nch ? m_qm[ciA] : 0u;
-      const uint32_t qmB = ciB < m_nch ? m_qm[ciB] : 0u;
+      const uint32_t qmB = (kRowsPerWarp >= 32 && ciB < m_nch) ? m_qm[ciB] : 0u;
       if ((qmA | qmB) == 0) continue;
       const bool okA0 = (qmA >> j0) & 1u, okA1 = (qmA >> j1) & 1u;
       const bool okB0 = (qmB >> j0) & 1u, okB1 = (qmB >> j1) & 1u;
@@ -700,11 +708,11 @@ AttnShape attn_shape(int NQ) {
   return s;
 }
 
-// One persistent CTA per SM; partial slot CTA + unit for every (CTA, unit)
-// pair that shares chunks, one sub-slot per consumer warp of an m-tile.
+// kAttnCtasPerSm persistent CTAs per SM; partial slot CTA + unit for every
+// (CTA, unit) pair that shares chunks, one sub-slot per consumer warp of an m-tile.
 AttnPlan attn_plan(int units, int umax, int NQ, int sm_count) {
   AttnPlan pl;
-  pl.n_cta = sm_count > 0 ? sm_count : 1;
+  pl.n_cta = sm_count > 0 ? kAttnCtasPerSm * sm_count : 1;
   const int wpm = attn_shape(NQ).wpm;
   pl.part_o_floats = ((int64_t)pl.n_cta + units) * wpm * NQ * 128;
   pl.part_ml_floats = ((int64_t)pl.n_cta + units) * wpm * NQ * 2;

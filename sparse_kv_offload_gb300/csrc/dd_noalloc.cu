@@ -14,8 +14,8 @@
 
 namespace {
 
-// Largest scratch the allocation-free attention may use: 8 MiB.
-constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+// Largest scratch the allocation-free attention may use: 16 MiB.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 constexpr size_t kDummyPoolBytes = 64 * 128 * 2;   // a valid base address for unused TMA maps
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
