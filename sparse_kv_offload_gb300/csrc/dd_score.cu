@@ -118,9 +118,9 @@ cudaError_t launch_build_minmax(const uint4 *K, uint4 *lm2, int64_t n_chunks, in
 // value qsum . k can take over any key k inside the chunk's box).
 //
 // The landmarks of all (b,g) units lie end to end in HBM, and scoring reads
-// each of their bytes once, so the kernel is a stream: one CTA per SM takes an
-// equal contiguous span of landmark rows (a multiple of a ring stage) and
-// pulls it through a ring of kScoreStages 32 KB shared-memory stages with
+// each of their bytes once, so the kernel is a stream: two CTAs per SM each
+// take an equal contiguous span of landmark rows (a multiple of a ring stage)
+// and pull it through a ring of kScoreStages 32 KB shared-memory stages with
 // 1-D bulk copies (one thread issues; completion on an mbarrier per stage,
 // bounded waits).  A stage never crosses a unit boundary, so every stage
 // scores against one unit's group sums (rebuilt when the unit changes).
@@ -133,9 +133,10 @@ cudaError_t launch_build_minmax(const uint4 *K, uint4 *lm2, int64_t n_chunks, in
 // xor-8/4/2/1 tree over the 16 lanes.  A stage's scores are gathered in
 // shared memory and written out as contiguous runs of each query row.
 // ---------------------------------------------------------------------------
-constexpr int kScoreThreads = 512;
-constexpr int kScoreRowsPerPass = kScoreThreads / 16;     // 32 landmark rows per pass
-constexpr int kScoreStages = 6;
+constexpr int kScoreThreads = 256;
+constexpr int kScoreRowsPerPass = kScoreThreads / 16;     // 16 landmark rows per pass
+constexpr int kScoreStages = 3;
+constexpr int kScoreCtasPerSm = 2;   // two issuers per SM: one streams while the other scores
 constexpr int kScoreStageBytes = 32 * 1024;
 __host__ __device__ constexpr int score_stage_rows(bool mm) { return kScoreStageBytes / (mm ? 512 : 256); }
 __host__ __device__ constexpr size_t score_smem(int n_q, bool mm) {
@@ -143,14 +144,14 @@ __host__ __device__ constexpr size_t score_smem(int n_q, bool mm) {
 }
 
 template <int NQ, bool MM>
-__global__ void __launch_bounds__(kScoreThreads, 1) k_score(const uint4 *__restrict__ q, const uint4 *__restrict__ lm,
+__global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) k_score(const uint4 *__restrict__ q, const uint4 *__restrict__ lm,
                                                             float *__restrict__ scores, int Hq, int Hkv, int C,
                                                             int64_t total_rows, int64_t rows_per_cta,
                                                             int32_t *status) {
   constexpr int kVecs = MM ? 2 : 1;                       // vectors per landmark
   constexpr int kRowBytes = 256 * kVecs;
   constexpr int kStageRows = score_stage_rows(MM);       // 128 or 64
-  constexpr int kPass = kStageRows / kScoreRowsPerPass;   // rows per thread per stage: 4 or 2
+  constexpr int kPass = kStageRows / kScoreRowsPerPass;   // rows per thread per stage: 8 or 4
   constexpr int kVals = kPass * NQ;                       // partial dots per lane per stage
   constexpr int kChunks = (kVals + 15) / 16;
   extern __shared__ __align__(128) unsigned char ssm[];
@@ -284,7 +285,8 @@ static cudaError_t launch_score_t(const uint4 *q, const uint4 *lm, float *scores
   if (total == 0) return cudaSuccess;
   constexpr int kStageRows = score_stage_rows(MM);
   const int64_t stages = (total + kStageRows - 1) / kStageRows;
-  const int64_t ctas = sm_count > 0 ? (sm_count < stages ? sm_count : stages) : 1;
+  const int64_t slots = (int64_t)kScoreCtasPerSm * (sm_count > 0 ? sm_count : 1);
+  const int64_t ctas = slots < stages ? slots : stages;
   const int64_t per = (stages + ctas - 1) / ctas * kStageRows;   // rows per CTA, whole stages
   const int grid = (int)((total + per - 1) / per);
   const size_t smem = score_smem(n_q, MM);
