@@ -273,7 +273,8 @@ def config_of(w, gather_mode, world=1, landmarks="mean"):
                    "memcpy": "miss list to host, cudaMemcpyAsync per run of chunks"}.get(gather_mode, gather_mode)
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "L": w.L, "cs": w.cs, "k": w.k,
             "n_q": w.n_q, "residency": w.residency, "gather": gather_desc, "landmarks": landmarks,
-            "l2": f"inputs larger than L2 ({N_LAYERS} layers of landmarks and host KV cycled)",
+            "l2": (f"inputs larger than L2 ({N_LAYERS} layers of landmarks and host KV cycled)" if N_LAYERS >= 4 else
+                   f"{N_LAYERS} layer(s) cycled: inputs may stay in L2 between steps (profiling runs only)"),
             "host_pages": "every pinned host K/V page read once by the GPU before timing",
             "parallelism": f"independent batch per GPU x{world}"}
 
@@ -842,8 +843,14 @@ def main():
     ap.add_argument("--prefetch-ctas", type=int, default=2, help="pipelined mode: prefetch copy CTAs per SM")
     ap.add_argument("--pipeline", action="store_true",
                     help="decode steps over several layers with drifting queries and predictive prefetch")
+    ap.add_argument("--layers", type=int, default=N_LAYERS,
+                    help="layers whose inputs the steps cycle through (fewer than 4 only to hold less device "
+                         "memory under a profiler: one layer's inputs then stay in L2 between steps)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.layers < 1:
+        ap.error("--layers must be at least 1")
+    globals()["N_LAYERS"] = args.layers
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":
