@@ -179,7 +179,7 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   add(B * n_q * Hkv * k, 4);                   // attn_slot
   add(c->plan.part_o_floats, 4);               // part_o
   add(c->plan.part_ml_floats, 4);              // part_ml
-  add(units + 1, 4);                           // chunk_off
+  add(2 * units + 1, 4);                       // chunk_off + fix-up counters
   add(c->plan.flat_entries, 16);               // flat chunk table
   add(64 * 128, 2);                            // dummy pool (64 rows)
   add(units, 8);                               // look-back words
@@ -200,7 +200,7 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   c->attn_slot = carve<int32_t>(cur, B * n_q * Hkv * k);
   c->part_o = carve<float>(cur, c->plan.part_o_floats);
   c->part_ml = carve<float>(cur, c->plan.part_ml_floats);
-  c->chunk_off = carve<int32_t>(cur, units + 1);
+  c->chunk_off = carve<int32_t>(cur, 2 * units + 1);
   c->flat = carve<int4>(cur, c->plan.flat_entries);
   c->dummy_pool = carve<uint16_t>(cur, 64 * 128);
   c->lb_word = carve<unsigned long long>(cur, units);
@@ -448,7 +448,7 @@ static dd_status attn_impl(dd_ctx *c, const void *q, const void *Khot, const voi
   if (c->max_misses > 0 && (!Kst || !Vst || !aligned16(Kst) || !aligned16(Vst))) return DD_ERR_INVALID_ARG;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)kD);
   const dd_dims &d = c->dims;
-  c->launches += plan_ready ? 2 : 3;
+  c->launches += plan_ready ? 1 : 2;   // the attention (and its plan kernel)
   const dd::AttnScratch scr = {c->part_o, c->part_ml, c->chunk_off, c->flat, c->dummy_pool};
   return cuda_ok(dd::launch_attn(q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count, scale, out,
                                  c->plan, scr, plan_ready, kh_dev, vh_dev, c->status, d.B, d.n_q, d.Hq, d.Hkv, d.cs,

@@ -16,8 +16,10 @@
 // slice covers a few units ("runs").  At the end of a run every consumer
 // warp writes its partial (running max, sum and accumulator of its rows) into
 // slot CTA + unit, sub-slot warp -- slices are ordered like the units, so no
-// two (CTA, unit) pairs share a slot and n_cta + units slots suffice -- and a
-// combine kernel merges the partials of every unit.
+// two (CTA, unit) pairs share a slot and n_cta + units slots suffice -- and
+// the CTA counts itself in on the unit's arrival counter; the CTA that
+// arrives last merges all partials of the unit (stream-K fix-up), so the
+// outputs leave the same kernel.
 //
 // Data movement: a producer warp streams 64-row tiles of K and V into shared
 // memory with 2-D TMA loads (cp.async.bulk.tensor, 128-byte swizzle, one box
@@ -68,6 +70,8 @@ struct AttnParams {
   float *part_o;              // [gridDim + units, NQ, 128], slot = CTA + unit
   float *part_ml;             // [gridDim + units, NQ, 2]
   int32_t *status;
+  int32_t *arrive;            // [units] CTAs that have finished a part of each unit (zeroed by the planner)
+  const uint16_t *k_tail, *v_tail;   // bf16 [B,n_q,Hkv,128] the step's own new rows, or null
   int n_q, Hq, Hkv, G, NQ, cs, umax, units;
   float scale_log2;           // softmax scale * log2(e)
 };
@@ -137,6 +141,97 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
 }
 
 
+// ------------------------------------------------------------ stream-K fix-up
+// Run by the consumer warps of the CTA that finished the last part of `unit`
+// (every other CTA whose slice covered part of it has published its partials
+// before counting itself in).  Thread (query vector, 8 columns): merges the
+// partials of every consumer warp of CTAs c0..c1 in order, then, when the
+// step's own rows are given, its tail rows: query j of the unit also attends
+// to the new rows of tokens 0..j (DualDecoder §5.2: the tokens of a step
+// follow one another along the sequence under a causal mask).
+template <int WPM>
+__device__ __forceinline__ void fixup_unit(const AttnParams &p, int unit, int c0, int c1, int n_threads, int ctid) {
+  const int lane = threadIdx.x & 31;
+  const int n_parts = (c1 - c0 + 1) * WPM;
+  const int b = unit / p.Hkv, g = unit - b * p.Hkv;
+  for (int w0 = (ctid >> 5) * 32; w0 < p.NQ * 16; w0 += n_threads) {   // warp-uniform
+    const int w = w0 + lane;
+    const bool act = w < p.NQ * 16;
+    const int qv = act ? (w >> 4) : 0, cg = w & 15;
+    const int j = qv / p.G, h = g * p.G + (qv - j * p.G);
+    float M = -INFINITY, L = 0.f, acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int i0 = 0; i0 < n_parts; i0 += 4) {
+      float ms[4], ls[4];
+      float4 oa[4], ob[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int i = i0 + t;
+        const bool ok = act && i < n_parts;
+        const int64_t k = (((int64_t)c0 + i / WPM + unit) * WPM + i % WPM) * p.NQ + qv;
+        const float4 *src = reinterpret_cast<const float4 *>(p.part_o + k * 128 + cg * 8);
+        ms[t] = ok ? p.part_ml[k * 2] : -INFINITY;
+        ls[t] = ok ? p.part_ml[k * 2 + 1] : 0.f;
+        oa[t] = ok ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+        ob[t] = ok ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (ms[t] == -INFINITY) continue;
+        const float Mn = fmaxf(M, ms[t]);
+        const float a = M == -INFINITY ? 0.f : exp2f(M - Mn), wt = exp2f(ms[t] - Mn);
+        const float o8[8] = {oa[t].x, oa[t].y, oa[t].z, oa[t].w, ob[t].x, ob[t].y, ob[t].z, ob[t].w};
+        L = L * a + wt * ls[t];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = acc[e] * a + wt * o8[e];
+        M = Mn;
+      }
+    }
+    if (p.k_tail) {
+      float qf[8];
+      unpack8(act ? *reinterpret_cast<const uint4 *>(p.q + ((int64_t)(b * p.n_q + j) * p.Hq + h) * 128 + cg * 8)
+                  : make_uint4(0, 0, 0, 0),
+              qf);
+#pragma unroll
+      for (int t = 0; t < kMaxNq; ++t) {
+        const bool use = act && t <= j;
+        const int64_t trow = ((int64_t)(b * p.n_q + t) * p.Hkv + g) * 128 + cg * 8;
+        float x = 0.f;
+        if (use) {
+          float kf[8];
+          unpack8(*reinterpret_cast<const uint4 *>(p.k_tail + trow), kf);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x = fmaf(qf[e], kf[e], x);
+        }
+        // the 16 lanes of this query vector hold its 128 columns
+        x += __shfl_xor_sync(0xffffffffu, x, 8);
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        if (use) {
+          float vf[8];
+          unpack8(*reinterpret_cast<const uint4 *>(p.v_tail + trow), vf);
+          const float s2 = x * p.scale_log2;
+          const float Mn = fmaxf(M, s2);
+          const float a = M == -INFINITY ? 0.f : exp2f(M - Mn), wt = exp2f(s2 - Mn);
+          L = L * a + wt;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] = acc[e] * a + wt * vf[e];
+          M = Mn;
+        }
+      }
+    }
+    if (act) {
+      float4 *dst = reinterpret_cast<float4 *>(p.out + ((int64_t)(b * p.n_q + j) * p.Hq + h) * 128 + cg * 8);
+      dst[0] = make_float4(L > 0.f ? acc[0] / L : 0.f, L > 0.f ? acc[1] / L : 0.f, L > 0.f ? acc[2] / L : 0.f,
+                           L > 0.f ? acc[3] / L : 0.f);
+      dst[1] = make_float4(L > 0.f ? acc[4] / L : 0.f, L > 0.f ? acc[5] / L : 0.f, L > 0.f ? acc[6] / L : 0.f,
+                           L > 0.f ? acc[7] / L : 0.f);
+    }
+  }
+}
+
 // ----------------------------------------------------------------- the kernel
 // Registers per thread: the register file holds kAttnCtasPerSm CTAs (their
 // threads rounded up to a multiple of 128); at most 224.
@@ -174,6 +269,7 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
   StageMeta *meta = reinterpret_cast<StageMeta *>(qsm + kStages * kQBytes);  // [kStages]
   uint64_t *bars = reinterpret_cast<uint64_t *>(meta + kStages);             // full[kStages], empty[kStages]
 
+  __shared__ int s_fix;   // this CTA finished the last part of the unit whose run just ended
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
   if (tid == 0) {
@@ -186,7 +282,7 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
   __syncthreads();
   pdl_wait();
   pdl_trigger();
-  // self-planned slice of the concatenated unions (the same split the combine assumes)
+  // self-planned slice of the concatenated unions (the same split the fix-up assumes)
   const int total = p.chunk_off[p.units];
   const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x;
   const int lo = min(total, (int)blockIdx.x * per), hi = min(total, lo + per);
@@ -373,6 +469,7 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
     const int buf = s % kStages;
     if (!mbar_wait(full0 + 8 * buf, (s / kStages) & 1, p.status)) break;
     const int m_nch = meta[buf].nch, m_flags = meta[buf].flags, m_unit = meta[buf].unit;
+    const int m_uoff = meta[buf].uoff, m_ucnt = meta[buf].ucnt;
     const uint8_t *m_qm = meta[buf].qm;
     if (m_flags & kFirst) {
       // this run's query vectors from shared memory (padded rows: no bank conflicts)
@@ -520,7 +617,7 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
     if (m_flags & kLast) {
       // this warp's partial for the run: rows of its m-tile, straight from
       // registers into sub-slot wq of slot CTA + unit (no cross-warp merge;
-      // the combine kernel merges all partials of the unit)
+      // the fix-up below merges all partials of the unit)
       float lq0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
       lq0 += __shfl_xor_sync(0xffffffffu, lq0, 2);
       float lq1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -538,6 +635,26 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
         for (int i = 0; i < 16; ++i) *reinterpret_cast<float2 *>(dst + i * 8) = make_float2(o[i][2], o[i][3]);
         if (tq == 0) *reinterpret_cast<float2 *>(p.part_ml + (pbase + qv1) * 2) = make_float2(m1, lq1);
       }
+      // the run is over: the next stage starts a new one, which reloads the
+      // queries and restarts the accumulators, so none of them stays live
+      // through the fix-up below
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) qa[ks][0] = qa[ks][1] = qa[ks][2] = qa[ks][3] = 0u;
+      m0 = m1 = -INFINITY;
+      l0 = l1 = 0.f;
+      // stream-K fix-up: CTAs c0..c1 hold parts of the unit; the one that
+      // counts itself in last merges them (partials published first)
+      const int c0 = m_uoff / per, c1 = (m_uoff + m_ucnt - 1) / per;
+      __threadfence();
+      asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");   // consumer warps only
+      if (tid == 0) s_fix = atomicAdd(p.arrive + m_unit, 1) + 1 == c1 - c0 + 1;
+      asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
+      if (s_fix) {
+        __threadfence();
+        fixup_unit<WPM>(p, m_unit, c0, c1, kConsumers * 32, tid);
+      }
     }
     if (m_flags & kEnd) break;
   }
@@ -552,7 +669,9 @@ constexpr int kPlanThreads = 256;
 __global__ void __launch_bounds__(kPlanThreads) k_attn_plan(
     const int32_t *__restrict__ union_cnt, const int32_t *__restrict__ union_slot,
     const uint8_t *__restrict__ union_qmask, const int32_t *__restrict__ miss_count, AttnPlanOut po, float *out,
-    int units, int umax, int n_q, int Hq, int Hkv, int64_t hot_slots, int64_t max_misses, int cs, int32_t *status) {
+    int units, int umax, int n_q, int Hq, int Hkv, int64_t hot_slots, int64_t max_misses, int cs, int32_t *status,
+    const uint16_t *__restrict__ q, const uint16_t *__restrict__ k_tail, const uint16_t *__restrict__ v_tail,
+    float scale_log2) {
   __shared__ int scratch[33];
   pdl_wait();
   pdl_trigger();
@@ -574,95 +693,29 @@ __global__ void __launch_bounds__(kPlanThreads) k_attn_plan(
   attn_plan_unit(po, unit, units, off, U, total, union_slot + ubase, union_qmask + ubase, nullptr, 0,
                  min((int64_t)*miss_count, max_misses), hot_slots, cs, status);
   if (U == 0) {
+    // no slice visits this unit: its output is the attention over the tail
+    // rows alone (rows 0..j for query j), or zero without them
     const int G = Hq / Hkv, b = unit / Hkv, g = unit - b * Hkv;
     for (int e = threadIdx.x; e < n_q * G * 128; e += kPlanThreads) {
       const int qv = e >> 7, col = e & 127, j = qv / G, h = g * G + (qv - j * G);
-      out[((int64_t)(b * n_q + j) * Hq + h) * 128 + col] = 0.f;
-    }
-  }
-}
-
-// --------------------------------------------------------------- combine
-// One CTA per (unit, query vector): merges the partials of every warp of
-// every CTA whose slice covered part of the unit's union, then, when the
-// step's own tokens are given, their tail rows: query j of the unit also
-// attends to the new rows of tokens 0..j (DualDecoder §5.2: the tokens of a
-// step follow one another along the sequence under a causal mask).
-__global__ void __launch_bounds__(128) k_attn_combine(const float *__restrict__ part_o,
-                                                      const float *__restrict__ part_ml,
-                                                      const int32_t *__restrict__ chunk_off, int n_cta,
-                                                      float *__restrict__ out,
-                                                      const int32_t *status, int n_q, int Hq, int Hkv, int NQ,
-                                                      int wpm, const uint16_t *__restrict__ q,
-                                                      const uint16_t *__restrict__ k_tail,
-                                                      const uint16_t *__restrict__ v_tail, float scale_log2) {
-  __shared__ float red[4][kMaxNq];
-  pdl_wait();
-  pdl_trigger();
-  if (load_status(status) != 0) return;
-  const int unit = blockIdx.x, qv = blockIdx.y, col = threadIdx.x;
-  const int off = chunk_off[unit], U = chunk_off[unit + 1] - off;
-  const int per = (chunk_off[gridDim.x] + n_cta - 1) / n_cta;   // the attention kernel's split
-  const bool tail = k_tail != nullptr;
-  if ((U <= 0 || per <= 0) && !tail) return;
-  const int G = Hq / Hkv, b = unit / Hkv, g = unit - b * Hkv, j = qv / G, h = g * G + (qv - j * G);
-  float M = -INFINITY, L = 0.f, acc = 0.f;
-  if (U > 0 && per > 0) {
-    const int c0 = off / per, c1 = (off + U - 1) / per;
-    const int n = (c1 - c0 + 1) * wpm;   // partials: (CTA c0 + i / wpm, warp i % wpm)
-    for (int ib = 0; ib < n; ib += 4) {
-      float ms[4], ls[4], os[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int i = ib + t;
-        const int64_t k = (((int64_t)c0 + i / wpm + unit) * wpm + i % wpm) * NQ + qv;
-        const bool ok = i < n;
-        ms[t] = ok ? part_ml[k * 2] : -INFINITY;
-        ls[t] = ok ? part_ml[k * 2 + 1] : 0.f;
-        os[t] = ok ? part_o[k * 128 + col] : 0.f;
+      float M = -INFINITY, L = 0.f, acc = 0.f;
+      if (k_tail) {
+        const uint16_t *qr = q + ((int64_t)(b * n_q + j) * Hq + h) * 128;
+        for (int t = 0; t <= j; ++t) {
+          const int64_t trow = ((int64_t)(b * n_q + t) * Hkv + g) * 128;
+          float x = 0.f;
+          for (int c = 0; c < 128; ++c)
+            x = fmaf(__uint_as_float((uint32_t)qr[c] << 16), __uint_as_float((uint32_t)k_tail[trow + c] << 16), x);
+          const float s2 = x * scale_log2, Mn = fmaxf(M, s2);
+          const float a = M == -INFINITY ? 0.f : exp2f(M - Mn), w = exp2f(s2 - Mn);
+          L = L * a + w;
+          acc = acc * a + w * __uint_as_float((uint32_t)v_tail[trow + col] << 16);
+          M = Mn;
+        }
       }
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        if (ms[t] == -INFINITY) continue;
-        const float Mn = fmaxf(M, ms[t]);
-        const float a = M == -INFINITY ? 0.f : exp2f(M - Mn), w = exp2f(ms[t] - Mn);
-        L = L * a + w * ls[t];
-        acc = acc * a + w * os[t];
-        M = Mn;
-      }
+      out[((int64_t)(b * n_q + j) * Hq + h) * 128 + col] = L > 0.f ? acc / L : 0.f;
     }
   }
-  if (tail) {
-    // logits of tail rows 0..j: 128-lane dot products, reduced per warp, then across the 4 warps
-    const int lane = col & 31, warp = col >> 5;
-    const float qc = __uint_as_float((uint32_t)q[((int64_t)(b * n_q + j) * Hq + h) * 128 + col] << 16);
-    float z[kMaxNq];
-#pragma unroll
-    for (int t = 0; t < kMaxNq; ++t) {
-      float x = 0.f;
-      if (t <= j) x = qc * __uint_as_float((uint32_t)k_tail[((int64_t)(b * n_q + t) * Hkv + g) * 128 + col] << 16);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-      z[t] = x;
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int t = 0; t < kMaxNq; ++t) red[warp][t] = z[t];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int t = 0; t < kMaxNq; ++t) {
-      if (t > j) break;
-      const float s2 = (red[0][t] + red[1][t] + red[2][t] + red[3][t]) * scale_log2;
-      const float vt = __uint_as_float((uint32_t)v_tail[((int64_t)(b * n_q + t) * Hkv + g) * 128 + col] << 16);
-      const float Mn = fmaxf(M, s2);
-      const float a = M == -INFINITY ? 0.f : exp2f(M - Mn), w = exp2f(s2 - Mn);
-      L = L * a + w;
-      acc = acc * a + w * vt;
-      M = Mn;
-    }
-  }
-  out[((int64_t)(b * n_q + j) * Hq + h) * 128 + col] = L > 0.f ? acc / L : 0.f;
 }
 
 // --------------------------------------------------------------- host side
@@ -753,10 +806,15 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
     return cudaErrorInvalidValue;
 
   cudaError_t e = cudaSuccess;
+  const bool tail = k_tail && v_tail;
+  const uint16_t *kt = tail ? static_cast<const uint16_t *>(k_tail) : nullptr;
+  const uint16_t *vt = tail ? static_cast<const uint16_t *>(v_tail) : nullptr;
+  const float scale_log2 = softmax_scale * 1.4426950408889634f;
   if (!plan_ready) {
     const AttnPlanOut po = {scr.chunk_off, scr.flat};
     e = launch_k(k_attn_plan, dim3(units), dim3(kPlanThreads), 0, s, union_cnt, union_slot, union_qmask, miss_count,
-                 po, out, units, umax, n_q, Hq, Hkv, has_hot ? hot_slots : 0, has_st ? max_misses : 0, cs, status);
+                 po, out, units, umax, n_q, Hq, Hkv, has_hot ? hot_slots : 0, has_st ? max_misses : 0, cs, status,
+                 static_cast<const uint16_t *>(q), kt, vt, scale_log2);
     if (e != cudaSuccess) return e;
   }
 
@@ -773,8 +831,11 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
   p.part_o = scr.part_o;
   p.part_ml = scr.part_ml;
   p.status = status;
+  p.arrive = scr.chunk_off + units + 1;   // the planner zeroed these counters
+  p.k_tail = kt;
+  p.v_tail = vt;
   p.n_q = n_q; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.NQ = NQ; p.cs = cs; p.umax = umax; p.units = units;
-  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.scale_log2 = scale_log2;
 
   switch (sh.mt) {
     case 1: e = launch_attn_t<1, 4>(plan.n_cta, sh, tkh, tvh, tks, tvs, p, s); break;
@@ -783,12 +844,7 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
     case 4: e = launch_attn_t<4, 1>(plan.n_cta, sh, tkh, tvh, tks, tvs, p, s); break;
     default: return cudaErrorInvalidValue;
   }
-  if (e != cudaSuccess) return e;
-  const bool tail = k_tail && v_tail;
-  return launch_k(k_attn_combine, dim3(units, NQ), dim3(128), 0, s, scr.part_o, scr.part_ml, scr.chunk_off,
-                  plan.n_cta, out, status, n_q, Hq, Hkv, NQ, sh.wpm, static_cast<const uint16_t *>(q),
-                  tail ? static_cast<const uint16_t *>(k_tail) : nullptr,
-                  tail ? static_cast<const uint16_t *>(v_tail) : nullptr, p.scale_log2);
+  return e;
 }
 
 }  // namespace dd

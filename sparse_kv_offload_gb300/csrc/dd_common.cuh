@@ -231,7 +231,8 @@ __device__ __forceinline__ int block_sum(int v, int *scratch) {
 // from it: persistent CTA c takes chunks [c*per, (c+1)*per) with
 // per = ceil(chunk_off[units] / number of CTAs).
 struct AttnPlanOut {
-  int32_t *chunk_off;   // [units + 1] exclusive prefix of the union sizes
+  int32_t *chunk_off;   // [units + 1] exclusive prefix of the union sizes, then [units] arrival counters
+                        // of the attention's stream-K fix-up, which the planner zeroes
   int4 *flat;           // [units * umax] per chunk: {first pool row (hot) | -2 - row (staging) | -1, query mask,
                         //  host chunk (b*Hkv+g)*C + c for staging chunks | -1, 0}
 };
@@ -259,6 +260,7 @@ __device__ __forceinline__ void attn_plan_unit(const AttnPlanOut &po, int unit, 
   }
   if (tid == 0) {
     po.chunk_off[unit] = off;
+    po.chunk_off[units + 1 + unit] = 0;   // arrival counter of the attention's fix-up
     if (unit == units - 1) po.chunk_off[units] = total;
   }
 }
@@ -284,7 +286,7 @@ struct SelectOut {
   int32_t *union_idx, *union_slot;
   uint8_t *union_qmask;
   int32_t *union_cnt, *unit_miss, *miss_list, *miss_count;
-  int32_t *chunk_off;             // attention plan: [units + 1]
+  int32_t *chunk_off;             // attention plan: [units + 1], then [units] fix-up counters
   int4 *flat;                     // attention plan: [units * umax]
   unsigned long long *lb_word;    // look-back: [units] {epoch:30, union count:17, miss count:17}
   int32_t *ticket;                // [3] next unit, CTAs done, look-back epoch of the next launch (never 0)
@@ -313,7 +315,7 @@ struct AttnPlan {
 };
 struct AttnScratch {
   float *part_o, *part_ml;
-  int32_t *chunk_off;         // [units + 1]
+  int32_t *chunk_off;         // [units + 1], then [units] fix-up counters
   int4 *flat;                 // [units * umax]
   const void *dummy_pool;     // >= 64 rows x 256 B, a valid base for unused tensor maps
 };

@@ -5,7 +5,7 @@
 // loop whose device memory is already carved up by its own pool, or a host
 // engine that forbids cudaMalloc between decode steps because the call can
 // synchronise the device.  dd_sparse_attn_decode_noalloc runs the same
-// attention and combine kernels, with the partials in a fixed device array
+// attention kernel (and its plan kernel), with the partials in a fixed device array
 // that is part of the library image.  That array (kNoAllocScratchBytes) is
 // held by every GPU that loads the library until the process exits.
 #include <mutex>
@@ -76,7 +76,7 @@ extern "C" dd_status dd_sparse_attn_decode_noalloc(const dd_dims *dims, int64_t 
   const dd::AttnPlan plan = dd::attn_plan(units, umax, NQ, sms);
   const size_t o_bytes = round256((size_t)plan.part_o_floats * sizeof(float));
   const size_t ml_bytes = round256((size_t)plan.part_ml_floats * sizeof(float));
-  const size_t off_bytes = round256((size_t)(units + 1) * sizeof(int32_t));
+  const size_t off_bytes = round256((size_t)(2 * units + 1) * sizeof(int32_t));   // + fix-up counters
   const size_t flat_bytes = round256((size_t)plan.flat_entries * 16);
   if (o_bytes + ml_bytes + off_bytes + flat_bytes + kDummyPoolBytes > kNoAllocScratchBytes)
     return DD_ERR_CAPACITY;

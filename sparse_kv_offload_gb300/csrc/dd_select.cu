@@ -827,6 +827,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_select_fused(SelectOut o) 
     o.union_cnt[unit] = U;
     o.unit_miss[unit] = M;
     o.chunk_off[unit] = uoff;
+    o.chunk_off[o.units + 1 + unit] = 0;   // arrival counter of the attention's fix-up
     if (unit == o.units - 1) {
       o.chunk_off[o.units] = uoff + U;
       *o.miss_count = moff + M;
