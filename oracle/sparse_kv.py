@@ -336,6 +336,10 @@ def sparse_attn_decode(q, Khot, Vhot, Kst, Vst, attn_slot, cs: int, scale: float
     head floor(h/G); the rows of query j are those of the k chunks in
     ``attn_slot[b,j,g,:]``.
 
+    A query with no selected chunk attends to its tail rows alone; with no
+    rows at all its output is zero (the softmax over an empty set is
+    undefined; zero is the library's convention).
+
     Tail rows (optional): ``K_tail, V_tail`` bf16 [B, n_q, Hkv, d] are the
     keys and values of the step's own new tokens, token j being query j's.
     DualDecoder §5.2 places the tokens of a step one after the other along
@@ -355,11 +359,15 @@ def sparse_attn_decode(q, Khot, Vhot, Kst, Vst, attn_slot, cs: int, scale: float
         for j in range(n_q):
             for g in range(Hkv):
                 slots = [int(s) for s in attn_slot[b, j, g] if s != NO_SLOT]
-                Kr = bf16_decode(np.concatenate([_rows(Khot, Kst, s) for s in slots], axis=0))
-                Vr = bf16_decode(np.concatenate([_rows(Vhot, Vst, s) for s in slots], axis=0))
+                Kr = np.zeros((0, d)) if not slots else bf16_decode(
+                    np.concatenate([_rows(Khot, Kst, s) for s in slots], axis=0))
+                Vr = np.zeros((0, d)) if not slots else bf16_decode(
+                    np.concatenate([_rows(Vhot, Vst, s) for s in slots], axis=0))
                 if K_tail is not None:
                     Kr = np.concatenate([Kr, bf16_decode(K_tail[b, :j + 1, g])], axis=0)
                     Vr = np.concatenate([Vr, bf16_decode(V_tail[b, :j + 1, g])], axis=0)
+                if Kr.shape[0] == 0:
+                    continue        # nothing to attend to: the output stays zero (library convention)
                 for h in range(g * G, (g + 1) * G):
                     z = (Kr @ qf[b, j, h]) * scale
                     p = np.exp(z - z.max())

@@ -74,6 +74,35 @@ def test_attention_with_tail_rows_only_masks_later_tokens(dd):
     tl.check_attention(out.cpu().numpy().reshape(want.shape), want)
 
 
+@pytest.mark.parametrize("with_tail", [False, True], ids=["no_tail", "tail"])
+def test_attention_units_with_empty_unions(dd, with_tail):
+    # units whose union is empty: no attention CTA visits them, so the plan
+    # kernel writes their output (the tail rows alone, or zero)
+    import torch
+    w = Workload("empty_units", B=2, Hq=8, Hkv=2, d=128, L=1024, cs=16, k=8, n_q=2, spec_scale=(0.0, 0.3), seed=83)
+    x = tl.host_inputs(w)
+    res = oracle.resolve_union(oracle.select_topk(oracle.score_landmarks(x["q"], x["lm"]), w.k), x["slot"])
+    Kst, Vst = oracle.gather_kv(x["K"], x["V"], res["miss_list"], w.cs)
+    cnt = res["union_cnt"].copy()
+    attn_slot = res["attn_slot"].copy()
+    for b, g in ((0, 1), (1, 0)):                                      # two of the four units emptied
+        cnt[b, g] = 0
+        attn_slot[b, :, g] = oracle.NO_SLOT
+    kt, vt = _tails(w, 84) if with_tail else (None, None)
+    want = oracle.sparse_attn_decode(x["q"], x["Khot"], x["Vhot"], Kst, Vst, attn_slot, w.cs, K_tail=kt, V_tail=vt)
+    out = torch.full((w.B * w.n_q * w.Hq * w.d,), float("nan"), device="cuda")
+    tails = dict(K_tail=tl.to_bf16(kt), V_tail=tl.to_bf16(vt)) if with_tail else {}
+    with dd.Context(shape_of(w), max_misses=max(1, res["miss_count"])) as ctx:
+        ctx.sparse_attn_decode(tl.to_bf16(x["q"]), None, None, tl.to_bf16(Kst), tl.to_bf16(Vst),
+                               tl.to_i32(res["union_slot"]), torch.from_numpy(res["union_qmask"]).cuda(),
+                               tl.to_i32(cnt), tl.to_i32(np.array([res["miss_count"]])), out, **tails)
+        assert ctx.status() == 0
+    got = out.cpu().numpy().reshape(want.shape)
+    if not with_tail:
+        assert np.all(got[0, :, 4:] == 0) and np.all(got[1, :, :4] == 0)   # query heads of the emptied units
+    tl.check_attention(got, want)
+
+
 def test_tail_rows_need_both_tensors(dd):
     w = TINY
     x = tl.host_inputs(w)

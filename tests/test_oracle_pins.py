@@ -476,6 +476,27 @@ def test_attention_tail_row_of_a_later_token_is_masked():
     np.testing.assert_allclose(out[0, 1], 5.0, rtol=0, atol=1e-9)   # its own row dominates (logit 8*128/sqrt(128))
 
 
+def test_attention_with_no_selected_chunk_is_causal_sdpa_over_the_tail_rows():
+    # a query with no selected chunk attends to tail rows 0..j alone; with no tail either, zero
+    rng = np.random.default_rng(23)
+    B, n_q, Hq, Hkv, d, cs = 1, 3, 4, 2, 128, 16
+    G = Hq // Hkv
+    q = enc(rng.standard_normal((B, n_q, Hq, d)))
+    Kt = enc(rng.standard_normal((B, n_q, Hkv, d)))
+    Vt = enc(rng.standard_normal((B, n_q, Hkv, d)))
+    none = np.full((B, n_q, Hkv, 2), oracle.NO_SLOT, np.int32)
+    empty = np.zeros((0, cs, d), np.uint16)
+    out = oracle.sparse_attn_decode(q, empty, empty, empty, empty, none, cs, K_tail=Kt, V_tail=Vt)
+    qf, Ktf, Vtf = (torch.from_numpy(synth.bf16_to_f32(x).astype(np.float64)) for x in (q, Kt, Vt))
+    Kseq = Ktf.permute(0, 2, 1, 3).repeat_interleave(G, dim=1)           # [B, Hq, n_q, d]
+    Vseq = Vtf.permute(0, 2, 1, 3).repeat_interleave(G, dim=1)
+    mask = torch.arange(n_q)[None, :] <= torch.arange(n_q)[:, None]      # query j sees tokens 0..j
+    want = torch.nn.functional.scaled_dot_product_attention(qf.permute(0, 2, 1, 3), Kseq, Vseq, attn_mask=mask,
+                                                            scale=1 / math.sqrt(d))
+    np.testing.assert_allclose(out, want.permute(0, 2, 1, 3).numpy(), rtol=1e-10, atol=1e-12)
+    assert np.all(oracle.sparse_attn_decode(q, empty, empty, empty, empty, none, cs) == 0)
+
+
 # ---------------------------------------------------------------- residency update (delta selection, capped LRU)
 
 def _res_step(state, union, step_id, cap, cs=1, d=2):
