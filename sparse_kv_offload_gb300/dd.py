@@ -394,7 +394,7 @@ def sparse_attn_decode_noalloc(shape: Shape, hot_slots, max_misses, q, Khot, Vho
                                stream=None):
     """dd_sparse_attn_decode without a context, for callers that cannot
     allocate device memory: its split-K partials sit in the library's fixed
-    8 MiB device array.  ``device_status`` is a zeroed device int32 tensor that
+    16 MiB device array.  ``device_status`` is a zeroed device int32 tensor that
     receives a device-detected dd_status code.  Calls that overlap on the GPU
     share that array and race; serialise them."""
     s = shape
