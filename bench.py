@@ -269,8 +269,12 @@ def profiled_traffic(stage: str, workload: str):
 
 
 def config_of(w, gather_mode, world=1, landmarks="mean"):
+    base, _, auto = gather_mode.partition(" ")
     gather_desc = {"zerocopy": "zero-copy, fused into the attention kernel",
-                   "memcpy": "miss list to host, cudaMemcpyAsync per run of chunks"}.get(gather_mode, gather_mode)
+                   "kernel": "zero-copy gather kernel into staging, then the attention",
+                   "memcpy": "miss list to host, cudaMemcpyAsync per run of chunks"}.get(base, base) + (
+        " (chosen automatically: " + ("a hot pool exists" if base == "kernel" else "no hot pool") + ")"
+        if auto else "")
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "L": w.L, "cs": w.cs, "k": w.k,
             "n_q": w.n_q, "residency": w.residency, "gather": gather_desc, "landmarks": landmarks,
             "l2": (f"inputs larger than L2 ({N_LAYERS} layers of landmarks and host KV cycled)" if N_LAYERS >= 4 else
@@ -289,6 +293,7 @@ class LayerData:
     def __init__(self, dd, shape, w, layer, rank, lm_vectors=1):
         import torch
         seed = rank_seed(w.seed, rank)
+        self.seed = seed
         self.q = torch.empty(w.B * w.n_q * w.Hq * w.d, dtype=torch.bfloat16, device="cuda")
         dd.synth_queries(shape, seed, layer, w.spec_scale, self.q)
         bias = u_hat = None
@@ -308,7 +313,9 @@ class LayerData:
         dd.synth_kv(shape, seed, synth.tensor_id(synth.TID_K, layer), self.Kh, bias, u_hat)
         dd.synth_kv(shape, seed, synth.tensor_id(synth.TID_V, layer), self.Vh)
         self.lm = torch.empty(w.B * w.Hkv * w.C * lm_vectors * w.d, dtype=torch.bfloat16, device="cuda")
-        self.Khot = self.Vhot = None   # an HBM copy of K / V when every chunk is resident
+        self.bias, self.u_hat = bias, u_hat
+        self.Khot = self.Vhot = None   # HBM pool of the resident chunks (slot order)
+        self.slot = None               # residency map [B*Hkv*C]: pool slot, or -1 (host)
         self.q_host = torch.empty(self.q.numel(), dtype=torch.bfloat16, pin_memory=True)
         torch.cuda.synchronize()
         self.q_host.copy_(self.q)
@@ -366,33 +373,81 @@ def run_ours(args, world, rank, local):
     from sparse_kv_offload_gb300 import dd
     w = BY_NAME[args.workload]
     shape = dd.Shape(w.B, w.Hq, w.Hkv, w.d, w.L, w.cs, w.k, w.n_q)
-    mode = dd.GATHER_MEMCPY if args.mode == "memcpy" else dd.GATHER_ZEROCOPY
+    mode = {"memcpy": dd.GATHER_MEMCPY, "kernel": dd.GATHER_KERNEL, "auto": dd.GATHER_AUTO}.get(args.mode,
+                                                                                              dd.GATHER_ZEROCOPY)
     cap = w.max_misses
 
     minmax = args.landmarks == "minmax"
     lm_kind = dd.LM_MINMAX if minmax else dd.LM_MEAN
     layers = [LayerData(dd, shape, w, l, rank, 2 if minmax else 1) for l in range(N_LAYERS)]
     resident_all = args.residency == "all"
+    own_residency = args.residency == "workload" and w.residency in ("uniform", "carry")
     if resident_all:
         # every chunk resident: the layers' K and V also live in an HBM pool, in the
         # host layout ([B*Hkv*C] chunks of cs rows), and the residency map is the identity
         for L_ in layers:
             L_.Khot = L_.Kh.to("cuda")
             L_.Vhot = L_.Vh.to("cuda")
-    ctx = dd.Context(shape, max_misses=cap, hot_slots=w.B * w.Hkv * w.C if resident_all else 0)
     touch = torch.empty(w.B * w.Hkv * w.C * w.d, dtype=torch.bfloat16, device="cuda")
-    for L_ in layers:
-        if minmax:
-            ctx.build_landmarks_minmax(L_.Kh, L_.lm)
-        else:
-            ctx.build_landmarks(L_.Kh, L_.lm)
-        # the GPU's first access to a pinned host page pays for its address
-        # translation; read every V page once too (K was just read in full),
-        # so that the timed steps see the steady state
-        ctx.build_landmarks(L_.Vh, touch)
-    del touch
-    slot = (torch.arange(w.B * w.Hkv * w.C, dtype=torch.int32, device="cuda") if resident_all
-            else torch.full((w.B * w.Hkv * w.C,), -1, dtype=torch.int32, device="cuda"))
+    with dd.Context(shape, max_misses=cap) as ctx0:
+        for L_ in layers:
+            if minmax:
+                ctx0.build_landmarks_minmax(L_.Kh, L_.lm)
+            else:
+                ctx0.build_landmarks(L_.Kh, L_.lm)
+            # the GPU's first access to a pinned host page pays for its address
+            # translation; read every V page once too (K was just read in full),
+            # so that the timed steps see the steady state
+            ctx0.build_landmarks(L_.Vh, touch)
+        del touch
+        maps = []
+        for l, L_ in enumerate(layers):
+            if resident_all or not own_residency:
+                maps.append(None)
+                continue
+            if w.residency == "uniform":
+                res = synth.uniform_residency(L_.seed, w.B, w.Hkv, w.C, w.resident_frac, l)
+            else:
+                # temporal locality: this layer's union, taken from one untimed step with
+                # nothing resident, stands in for the previous step's; a seeded share of
+                # it is resident
+                uidx = torch.empty(w.B * w.Hkv * shape.umax, dtype=torch.int32, device="cuda")
+                ucnt = torch.empty(w.B * w.Hkv, dtype=torch.int32, device="cuda")
+                Kst0 = [torch.empty(cap * w.cs * w.d, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+                Vst0 = [torch.empty(cap * w.cs * w.d, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+                out0 = torch.empty(w.B * w.n_q * w.Hq * w.d, dtype=torch.float32, device="cuda")
+                none = torch.full((w.B * w.Hkv * w.C,), -1, dtype=torch.int32, device="cuda")
+                ctx0.step(0, L_.q, L_.lm, L_.Kh, L_.Vh, none, None, None, Kst0, Vst0, out0, lm_kind=lm_kind,
+                          intermediates={"union_idx": uidx, "union_cnt": ucnt})
+                ui = uidx.cpu().numpy().reshape(w.B * w.Hkv, shape.umax)
+                uc = ucnt.cpu().numpy()
+                sets = [set(ui[u, :uc[u]].tolist()) for u in range(w.B * w.Hkv)]
+                res = synth.carried_residency(L_.seed, sets, w.B, w.Hkv, w.C, w.resident_frac, l)
+                del Kst0, Vst0, out0, none
+            maps.append(res.reshape(-1))
+        # one pool size for every layer (the context checks each step's pools against it)
+        n_pool = max([int((m >= 0).sum()) for m in maps if m is not None] + [0])
+        for l, L_ in enumerate(layers):
+            m = maps[l]
+            if resident_all:
+                L_.slot = torch.arange(w.B * w.Hkv * w.C, dtype=torch.int32, device="cuda")
+            elif m is None:
+                L_.slot = torch.full((w.B * w.Hkv * w.C,), -1, dtype=torch.int32, device="cuda")
+            else:
+                n_hot = int((m >= 0).sum())
+                chunk_map = np.empty(n_hot, np.int32)
+                chunk_map[m[m >= 0]] = np.nonzero(m >= 0)[0]
+                L_.Khot = torch.empty(max(1, n_pool) * w.cs * w.d, dtype=torch.bfloat16, device="cuda")
+                L_.Vhot = torch.empty(max(1, n_pool) * w.cs * w.d, dtype=torch.bfloat16, device="cuda")
+                if n_hot:
+                    cm = torch.from_numpy(chunk_map).cuda()
+                    dd.synth_kv(shape, L_.seed, synth.tensor_id(synth.TID_K, l), L_.Khot, L_.bias, L_.u_hat,
+                                chunk_map=cm)
+                    dd.synth_kv(shape, L_.seed, synth.tensor_id(synth.TID_V, l), L_.Vhot, chunk_map=cm)
+                L_.slot = torch.from_numpy(m.astype(np.int32)).cuda()
+        torch.cuda.synchronize()
+    hot_slots = w.B * w.Hkv * w.C if resident_all else n_pool
+    ctx = dd.Context(shape, max_misses=cap, hot_slots=hot_slots)
     ns = cap * w.cs * w.d
     Kst = [torch.empty(ns, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     Vst = [torch.empty(ns, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
@@ -409,7 +464,9 @@ def run_ours(args, world, rank, local):
     # (the fused gather + attention, or the gather in memcpy mode): an event
     # between two kernels stops the next one from launching early.  The
     # per-stage breakdown comes from separate steps with all six events.
-    fused = args.mode == "zerocopy"   # the attention kernel gathers the missing chunks itself
+    # the gather the step runs (auto: the separate gather kernel when there is a hot pool)
+    gather_used = args.mode if args.mode != "auto" else ("kernel" if hot_slots > 0 else "zerocopy")
+    fused = gather_used == "zerocopy"   # the attention kernel gathers the missing chunks itself
     dom_marks = (4, 5) if fused else (3, 4)
     n_stage = min(K, 200)
 
@@ -426,7 +483,7 @@ def run_ours(args, world, rank, local):
 
     def step(i, layer, events=None, inter=None):
         d_ = layers[layer % N_LAYERS]
-        ctx.step(layer, d_.q, d_.lm, d_.Kh, d_.Vh, slot, d_.Khot, d_.Vhot, Kst, Vst, out, mode=mode,
+        ctx.step(layer, d_.q, d_.lm, d_.Kh, d_.Vh, d_.slot, d_.Khot, d_.Vhot, Kst, Vst, out, mode=mode,
                  intermediates=inter, stage_events=events, lm_kind=lm_kind, mass_gamma=args.mass_gamma,
                  softmax_scale=args.softmax_scale)
 
@@ -480,15 +537,24 @@ def run_ours(args, world, rank, local):
     # the dominant kernel's duration is the one measured inside the timed region
     t_dom = (dom_ms_timed if dom == dom_timed else stage_ms[dom]) * 1e-3
     traffic = profiled_traffic(dom, w.name)
-    if fused and dom == "attention" and M == 0:
-        roof = {"bound": "hbm", "achieved": attn_b / t_dom / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                "peak_kind": hbm_kind, "traffic": None,
-                "kernel": "k_attn (every chunk resident: K and V by TMA from the HBM pool)"}
-    elif fused and dom == "attention":
-        roof = {"bound": "host_link", "achieved": gather_b / t_dom / 1e9, "peak": link_memcpy, "unit": "GB/s",
-                "peak_kind": "pinned H2D cudaMemcpyAsync, best of 10 x 1 GiB, measured in this run",
-                "traffic": traffic, "kernel": "k_attn (gather fused: missing chunks read over the host link)",
-                "hbm_achieved": attn_b / t_dom / 1e9}
+    wl_name = w.name + "_all_resident" if resident_all else w.name
+    if fused and dom == "attention":
+        # the kernel reads the hot pool over HBM and the misses over the host
+        # link at once: its bound is whichever would take longer at its peak
+        t_link = gather_b / (link_memcpy * 1e9) if (M > 0 and link_memcpy) else 0.0
+        t_hbm = attn_b / (hbm_peak * 1e9)
+        if t_link >= t_hbm:
+            roof = {"bound": "host_link", "achieved": gather_b / t_dom / 1e9, "peak": link_memcpy, "unit": "GB/s",
+                    "peak_kind": "pinned H2D cudaMemcpyAsync, best of 10 x 1 GiB, measured in this run",
+                    "traffic": profiled_traffic("attention", wl_name),
+                    "kernel": "k_attn (gather fused: missing chunks read over the host link)",
+                    "hbm_achieved": attn_b / t_dom / 1e9}
+        else:
+            roof = {"bound": "hbm", "achieved": attn_b / t_dom / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                    "peak_kind": hbm_kind, "traffic": profiled_traffic("attention", wl_name),
+                    "kernel": ("k_attn (every chunk resident: K and V by TMA from the HBM pool)" if M == 0 else
+                               "k_attn (resident chunks by TMA from the HBM pool, misses over the host link)"),
+                    "host_link_achieved": gather_b / t_dom / 1e9}
     elif dom == "gather":
         roof = {"bound": "host_link", "achieved": gather_b / t_dom / 1e9, "peak": link_memcpy, "unit": "GB/s",
                 "peak_kind": "pinned H2D cudaMemcpyAsync, best of 10 x 1 GiB, measured in this run",
@@ -497,32 +563,33 @@ def run_ours(args, world, rank, local):
                                 "staging writes stay in L2"}
     else:
         roof = {"bound": "hbm", "achieved": stage_bytes[dom] / t_dom / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                "peak_kind": hbm_kind, "traffic": traffic, "kernel": KERNEL_SOURCE[dom][0]}
+                "peak_kind": hbm_kind, "traffic": profiled_traffic(dom, wl_name if dom == "attention" else w.name),
+                "kernel": KERNEL_SOURCE[dom][0] + (" (every chunk from HBM: the hot pool and the staging buffer)"
+                                                   if dom == "attention" else "")}
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["peak"] else None
-    if fused:
-        # attention is bound by the host link here; the HBM-bound kernel is the scoring pass
-        roof_hbm = {"bound": "hbm",
-                    "kernels": "k_score (the landmark stream; bytes: the landmark and query reads and the score "
-                               "rows)",
-                    "achieved": score_b / (stage_ms["score"] * 1e-3) / 1e9,
-                    "peak": hbm_peak, "unit": "GB/s", "peak_kind": hbm_kind,
-                    "traffic": {"score": profiled_traffic("score", w.name)}}
-    else:
-        t_sa = (stage_ms["score"] + stage_ms["attention"]) * 1e-3
-        roof_hbm = {"bound": "hbm", "kernels": "score + attention", "achieved": (score_b + attn_b) / t_sa / 1e9,
-                    "peak": hbm_peak, "unit": "GB/s", "peak_kind": hbm_kind,
-                    "traffic": {"score": profiled_traffic("score", w.name),
-                                "attention": profiled_traffic("attention", w.name)}}
+    # the scoring pass is HBM-bound in every mode; when the attention reads its
+    # chunks from HBM too (a separate gather into staging, or every chunk
+    # resident), scoring + attention is also reported against the HBM peak
+    roof_hbm = {"bound": "hbm",
+                "kernels": "k_score (the landmark stream; bytes: the landmark and query reads and the score rows)",
+                "achieved": score_b / (stage_ms["score"] * 1e-3) / 1e9,
+                "peak": hbm_peak, "unit": "GB/s", "peak_kind": hbm_kind,
+                "traffic": {"score": profiled_traffic("score", w.name)}}
     roof_hbm["frac"] = roof_hbm["achieved"] / hbm_peak
+    if not fused or M == 0:
+        t_sa = (stage_ms["score"] + stage_ms["attention"]) * 1e-3
+        roof_hbm["score_plus_attention"] = {
+            "kernels": "k_score + k_attn (bytes: landmarks, queries and scores + the union's K and V, each read once)",
+            "achieved": (score_b + attn_b) / t_sa / 1e9, "frac": (score_b + attn_b) / t_sa / 1e9 / hbm_peak}
 
     # the same steps captured in a CUDA graph (one capture of all layers) and replayed
     graph = None
-    if mode == dd.GATHER_ZEROCOPY:
+    if mode != dd.GATHER_MEMCPY:
         gs = torch.cuda.Stream()
         with torch.cuda.stream(gs):
             for l in range(N_LAYERS):          # warm-up on the capture stream
                 d_ = layers[l]
-                ctx.step(l, d_.q, d_.lm, d_.Kh, d_.Vh, slot, d_.Khot, d_.Vhot, Kst, Vst, out, mode=mode,
+                ctx.step(l, d_.q, d_.lm, d_.Kh, d_.Vh, d_.slot, d_.Khot, d_.Vhot, Kst, Vst, out, mode=mode,
                          lm_kind=lm_kind, stream=gs, mass_gamma=args.mass_gamma,
                          softmax_scale=args.softmax_scale)
         torch.cuda.synchronize()
@@ -530,7 +597,7 @@ def run_ours(args, world, rank, local):
         with torch.cuda.graph(cg, stream=gs, capture_error_mode="relaxed"):
             for l in range(N_LAYERS):
                 d_ = layers[l]
-                ctx.step(l, d_.q, d_.lm, d_.Kh, d_.Vh, slot, d_.Khot, d_.Vhot, Kst, Vst, out, mode=mode,
+                ctx.step(l, d_.q, d_.lm, d_.Kh, d_.Vh, d_.slot, d_.Khot, d_.Vhot, Kst, Vst, out, mode=mode,
                          lm_kind=lm_kind, stream=gs, mass_gamma=args.mass_gamma,
                          softmax_scale=args.softmax_scale)
         reps = max(1, K // N_LAYERS)
@@ -584,12 +651,19 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": world * K / t_max, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": 1e3 * t_max / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(config_of(w, args.mode, world, args.landmarks),
+        "config": dict(config_of(w, gather_used + (" (auto)" if args.mode == "auto" else ""), world,
+                                 args.landmarks),
                        **({"selection": f"coverage budgets: gamma {args.mass_gamma}, at most k chunks",
                            "softmax_scale": args.softmax_scale or 1 / math.sqrt(w.d)}
                           if args.mass_gamma > 0 else {}),
                        **({"residency": "all: every chunk in an HBM pool, no host reads",
-                           "workload": w.name + "_all_resident"} if resident_all else {})),
+                           "workload": w.name + "_all_resident"} if resident_all else
+                          {"residency": "none: every chunk read from host memory",
+                           "workload": w.name + "_all_host"} if (args.residency == "none" and w.residency != "none")
+                          else {"residency": (f"carry: {w.resident_frac:.0%} of each unit's union (taken from an "
+                                              f"untimed step) resident in an HBM pool" if w.residency == "carry" else
+                                              f"uniform: {w.resident_frac:.0%} of all chunks resident in an HBM pool")}
+                          if own_residency else {})),
         "roofline": roof, "roofline_hbm": roof_hbm,
         "stages_us": {n: 1e3 * v for n, v in stage_ms.items()},
         "stages_note": f"stages_us: mean over {n_stage} further steps with an event at every stage boundary "
@@ -832,13 +906,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=LLAMA8B_32K.name, choices=sorted(BY_NAME))
-    ap.add_argument("--mode", choices=("zerocopy", "memcpy"), default="zerocopy")
+    ap.add_argument("--mode", choices=("auto", "zerocopy", "kernel", "memcpy"), default="auto",
+                    help="gather: auto (the library's choice: the separate gather kernel when there is a hot pool, "
+                         "else fused into the attention), zerocopy (fused), kernel (separate), memcpy")
     ap.add_argument("--landmarks", choices=("mean", "minmax"), default="mean")
     ap.add_argument("--mass-gamma", type=float, default=0.0,
                     help="> 0: coverage budgets (smallest chunk set reaching this attention mass, at most k)")
     ap.add_argument("--softmax-scale", type=float, default=0.0, help="<= 0: 1/sqrt(d)")
-    ap.add_argument("--residency", choices=("none", "all"), default="none",
-                    help="all: the whole KV also in an HBM pool (no misses; attention bound by HBM)")
+    ap.add_argument("--residency", choices=("workload", "none", "all"), default="workload",
+                    help="workload: the workload's own residency (none, a carried share of the union, or a "
+                         "uniform share of all chunks in an HBM pool); none: every chunk read from host memory; "
+                         "all: the whole KV also in an HBM pool (no misses; attention bound by HBM)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefetch-ctas", type=int, default=2, help="pipelined mode: prefetch copy CTAs per SM")
     ap.add_argument("--pipeline", action="store_true",

@@ -74,9 +74,20 @@ typedef struct {
 } dd_dims;
 
 typedef enum {
-  DD_GATHER_ZEROCOPY = 0,   /* a kernel loads the host chunks over the host link (no host sync) */
-  DD_GATHER_MEMCPY = 1      /* miss list read back to the host, one cudaMemcpyAsync per run of
+  DD_GATHER_ZEROCOPY = 0,   /* a kernel loads the host chunks over the host link (no host sync); in
+                               dd_step that kernel is the attention itself, which reads each missing
+                               chunk when its tile comes up */
+  DD_GATHER_MEMCPY = 1,     /* miss list read back to the host, one cudaMemcpyAsync per run of
                                consecutive chunks on the context's copy stream (host sync) */
+  DD_GATHER_KERNEL = 2,     /* a separate zero-copy gather kernel copies every missing chunk into
+                               the staging buffer with all SMs' loads in flight, then the attention
+                               reads staging like the hot pool; for steps where most chunks are
+                               resident and the misses are few and scattered */
+  DD_GATHER_AUTO = 3        /* dd_step only: DD_GATHER_KERNEL when the context has a hot pool
+                               (hot_slots > 0), else DD_GATHER_ZEROCOPY.  Measured on one GB300:
+                               with 10-50% of the union missing the separate gather kernel keeps the
+                               host link at 84-93% of its peak where the fused one reaches 31-53%;
+                               with every chunk missing the fused gather is 2-3% faster */
 } dd_gather_mode;
 
 typedef struct dd_ctx dd_ctx;
@@ -247,8 +258,8 @@ typedef struct {
   int32_t *sel_cnt;              /* with mass_gamma: optional int32 [B,n_q,Hkv] row lengths */
 } dd_step_args;
 
-/* dd_step may be captured into a CUDA graph (zero-copy mode; the memcpy
- * mode reads the miss list on the host): it keeps no per-call state on the
+/* dd_step may be captured into a CUDA graph (zero-copy, kernel and auto
+ * gather modes; the memcpy mode reads the miss list on the host): it keeps no per-call state on the
  * host that a replay would repeat wrongly.  While the stream is capturing, the
  * release events of the staging buffers are left alone -- the graph orders
  * its own steps -- so a caller that replays such a graph and also runs steps

@@ -38,9 +38,11 @@ struct dd_ctx {
   cudaEvent_t ready = nullptr;                    // miss list available to the copy stream / copies done
   bool used[2] = {false, false};
   int64_t launches = 0;
-  // cached host -> device pointer translations for pinned host memory
-  const void *kh_host = nullptr, *vh_host = nullptr;
-  const void *kh_dev = nullptr, *vh_dev = nullptr;
+  // recent host -> device pointer translations for pinned host memory
+  static constexpr int kViews = 16;
+  const void *view_host[kViews] = {};
+  const void *view_dev[kViews] = {};
+  int view_next = 0;
 };
 
 namespace {
@@ -98,18 +100,24 @@ dd_status device_view(const void *p, const void **out) {
   return DD_ERR_INVALID_ARG;
 }
 
-dd_status host_kv_views(dd_ctx *c, const void *Kh, const void *Vh, const void **kd, const void **vd) {
-  if (Kh != c->kh_host) {
-    DD_TRY(device_view(Kh, &c->kh_dev));
-    c->kh_host = Kh;
-  }
-  if (Vh != c->vh_host) {
-    DD_TRY(device_view(Vh, &c->vh_dev));
-    c->vh_host = Vh;
-  }
-  *kd = c->kh_dev;
-  *vd = c->vh_dev;
+// Device view of a pinned host pointer, from the context's small cache of
+// recent translations (a decode loop cycles through a few layers' K and V).
+dd_status cached_view(dd_ctx *c, const void *h, const void **d) {
+  for (int i = 0; i < dd_ctx::kViews; ++i)
+    if (c->view_host[i] == h && h != nullptr) {
+      *d = c->view_dev[i];
+      return DD_OK;
+    }
+  DD_TRY(device_view(h, d));
+  c->view_host[c->view_next] = h;
+  c->view_dev[c->view_next] = *d;
+  c->view_next = (c->view_next + 1) % dd_ctx::kViews;
   return DD_OK;
+}
+
+dd_status host_kv_views(dd_ctx *c, const void *Kh, const void *Vh, const void **kd, const void **vd) {
+  DD_TRY(cached_view(c, Kh, kd));
+  return cached_view(c, Vh, vd);
 }
 
 template <typename T>
@@ -381,7 +389,7 @@ static dd_status gather_memcpy(dd_ctx *c, const void *Kh, const void *Vh, const 
 dd_status dd_gather_kv(dd_ctx *c, const void *Kh, const void *Vh, const int32_t *miss_list, const int32_t *miss_count,
                        void *Kst, void *Vst, dd_gather_mode mode, dd_stream_t stream) {
   if (!c) return DD_ERR_INVALID_ARG;
-  if (mode != DD_GATHER_ZEROCOPY && mode != DD_GATHER_MEMCPY) return DD_ERR_INVALID_ARG;
+  if (mode != DD_GATHER_ZEROCOPY && mode != DD_GATHER_MEMCPY && mode != DD_GATHER_KERNEL) return DD_ERR_INVALID_ARG;
   if (c->units == 0) return DD_OK;
   if (!Kh || !Vh || !miss_list || !miss_count) return DD_ERR_INVALID_ARG;
   if (c->max_misses > 0 && (!Kst || !Vst || !aligned16(Kst) || !aligned16(Vst))) return DD_ERR_INVALID_ARG;
@@ -582,12 +590,14 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   const bool captured = capturing != cudaStreamCaptureStatusNone;
   if (!captured && c->used[p] && c->released_on[p] != s) DD_CUDA(cudaStreamWaitEvent(s, c->released[p], 0));
   const void *kh_dev = nullptr, *vh_dev = nullptr;
-  if (a->mode == DD_GATHER_ZEROCOPY) {
+  const dd_gather_mode gmode =
+      a->mode == DD_GATHER_AUTO ? (c->hot_slots > 0 ? DD_GATHER_KERNEL : DD_GATHER_ZEROCOPY) : a->mode;
+  if (gmode == DD_GATHER_ZEROCOPY) {
     // the attention kernel itself copies the missing chunks from host memory
     // into its tiles and into staging buffer p (one pass over the host link)
     if (c->max_misses > 0) DD_TRY(host_kv_views(c, a->Kh, a->Vh, &kh_dev, &vh_dev));
   } else {
-    DD_TRY(dd_gather_kv(c, a->Kh, a->Vh, miss_list, miss_count, a->Kst[p], a->Vst[p], a->mode, stream));
+    DD_TRY(dd_gather_kv(c, a->Kh, a->Vh, miss_list, miss_count, a->Kst[p], a->Vst[p], gmode, stream));
   }
   // memcpy mode: dd_gather_kv made this stream wait for the copy stream
   DD_TRY(mark(4));

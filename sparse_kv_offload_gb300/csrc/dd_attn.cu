@@ -32,6 +32,7 @@
 // ~16 significant bits.  The work is HBM-bound: the MMAs only keep the
 // arithmetic under the memory time.
 #include <cuda.h>
+#include <mutex>
 #include <cudaTypedefs.h>
 
 #include "dd_common.cuh"
@@ -720,22 +721,42 @@ __global__ void __launch_bounds__(kPlanThreads) k_attn_plan(
 
 // --------------------------------------------------------------- host side
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     cudaDriverEntryPointQueryResult q;
     void *f = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
-// A [rows, 128] bf16 pool viewed as 2-D, boxes of cs rows x 64 columns.
+// A [rows, 128] bf16 pool viewed as 2-D, boxes of cs rows x 64 columns.  A
+// descriptor depends on nothing but (base, rows, cs), so the last few are
+// kept: a decode loop cycles through the same pools step after step.
 static bool make_pool_map(CUtensorMap *map, const void *base, int64_t rows, int cs) {
+  struct Entry {
+    const void *base;
+    int64_t rows;
+    int cs;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry cache[32];
+  static int n = 0, next = 0;
+  if (base == nullptr || rows <= 0) return false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+      if (cache[i].base == base && cache[i].rows == rows && cache[i].cs == cs) {
+        *map = cache[i].map;
+        return true;
+      }
+  }
   auto enc = tensor_map_encoder();
-  if (!enc || base == nullptr || rows <= 0) return false;
+  if (!enc) return false;
   cuuint64_t dims[2] = {128, (cuuint64_t)rows};
   cuuint64_t strides[1] = {256};
   cuuint32_t box[2] = {64, (cuuint32_t)cs};
@@ -743,7 +764,12 @@ static bool make_pool_map(CUtensorMap *map, const void *base, int64_t rows, int 
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  cache[next] = {base, rows, cs, *map};
+  next = (next + 1) % 32;
+  if (n < 32) ++n;
+  return true;
 }
 
 struct AttnShape {
@@ -776,7 +802,7 @@ AttnPlan attn_plan(int units, int umax, int NQ, int sm_count) {
 template <int MT, int WPM>
 static cudaError_t launch_attn_t(int n_cta, const AttnShape &sh, const CUtensorMap &a, const CUtensorMap &b,
                                  const CUtensorMap &c, const CUtensorMap &d, const AttnParams &p, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(k_attn<MT, WPM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
+  cudaError_t e = set_dyn_smem((const void *)k_attn<MT, WPM>, sh.smem);
   if (e != cudaSuccess) return e;
   return launch_k(k_attn<MT, WPM>, dim3(n_cta), dim3(sh.threads), sh.smem, s, a, b, c, d, p);
 }

@@ -293,7 +293,7 @@ static cudaError_t launch_score_t(const uint4 *q, const uint4 *lm, float *scores
   switch (n_q) {
 #define DD_SCORE_CASE(N)                                                                                         \
   case N: {                                                                                                       \
-    cudaError_t e = cudaFuncSetAttribute(k_score<N, MM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    cudaError_t e = set_dyn_smem((const void *)k_score<N, MM>, smem);                                         \
     if (e != cudaSuccess) return e;                                                                               \
     return launch_k(k_score<N, MM>, dim3(grid), dim3(kScoreThreads), smem, s, q, lm, scores, Hq, Hkv, C, total,   \
                     per, status);                                                                                 \

@@ -130,7 +130,7 @@ cudaError_t launch_topk(const float *scores, int32_t *sel, int rows, int C, int 
   if (rows == 0) return cudaSuccess;
   const size_t smem = (size_t)C * sizeof(uint32_t);
   if (smem > 48 * 1024) {   // the opt-in is per device, so ask on every launch that needs it
-    cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_dyn_smem((const void *)k_topk, smem);
     if (e != cudaSuccess) return e;
   }
   return launch_k(k_topk, dim3(rows), dim3(kTopkThreads), smem, s, scores, sel, C, k);
@@ -317,7 +317,7 @@ cudaError_t launch_topk_mass(const float *scores, int32_t *sel, int32_t *sel_cnt
   while (k_pow < k_max) k_pow <<= 1;
   const size_t smem = (size_t)k_pow * 8 + (size_t)C * 4 + (size_t)k_max * 4 + (size_t)((C + 31) / 32) * 4;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_topk_mass, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_dyn_smem((const void *)k_topk_mass, smem);
     if (e != cudaSuccess) return e;
   }
   return launch_k(k_topk_mass, dim3(rows), dim3(kTopkThreads), smem, s, scores, sel, sel_cnt, C, k_max, k_min,
@@ -856,8 +856,7 @@ cudaError_t launch_select_fused(const SelectOut &o, int n_q, cudaStream_t s) {
   switch (n_q) {
 #define DD_FUSED_CASE(N)                                                                                      \
   case N: {                                                                                                    \
-    cudaError_t e = cudaFuncSetAttribute(k_select_fused<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
-                                         (int)smem);                                                           \
+    cudaError_t e = set_dyn_smem((const void *)k_select_fused<N>, smem);                                                           \
     if (e != cudaSuccess) return e;                                                                            \
     return launch_k(k_select_fused<N>, dim3(o.units), dim3(kFusedThreads), smem, s, o);                        \
   }

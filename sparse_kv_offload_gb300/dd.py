@@ -19,7 +19,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libdd.so")
 
 DD_OK, DD_ERR_INVALID_ARG, DD_ERR_CUDA, DD_ERR_CAPACITY, DD_ERR_TIMEOUT, DD_ERR_DEVICE_CHECK = range(6)
-GATHER_ZEROCOPY, GATHER_MEMCPY = 0, 1
+GATHER_ZEROCOPY, GATHER_MEMCPY, GATHER_KERNEL, GATHER_AUTO = 0, 1, 2, 3
 LM_MEAN, LM_MINMAX = 0, 1
 
 EXPORTED = (

@@ -75,7 +75,7 @@ def test_minmax_scores_within_fp32_bound(dd, w):
 
 
 @pytest.mark.parametrize("w", [TINY, V_HOT, V_CARRY, V_5Q, V_ZIPF], ids=lambda w: w.name)
-@pytest.mark.parametrize("mode", [0, 1], ids=["zerocopy", "memcpy"])
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["zerocopy", "memcpy", "kernel"])
 def test_step_with_minmax_landmarks_matches_oracle(dd, w, mode):
     x = tl.host_inputs(w)
     lm2 = oracle.build_minmax_landmarks(x["K"], w.cs)

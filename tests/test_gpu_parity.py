@@ -217,7 +217,7 @@ def test_resolve_capacity_and_range_errors(dd):
 
 # ------------------------------------------------------------------ a4 gather
 
-@pytest.mark.parametrize("mode", ["zerocopy", "memcpy"])
+@pytest.mark.parametrize("mode", ["zerocopy", "memcpy", "kernel"])
 @pytest.mark.parametrize("cs", [16, 64])
 def test_gather_bytes_exact(dd, mode, cs):
     import torch
@@ -236,7 +236,8 @@ def test_gather_bytes_exact(dd, mode, cs):
     Vst = torch.full((cap * cs * w.d,), 7, dtype=torch.int16, device="cuda").view(torch.bfloat16)
     with dd.Context(shape_of(w), max_misses=cap) as ctx:
         ctx.gather_kv(tl.to_bf16(Kh, "cpu", pin=True), tl.to_bf16(Vh, "cpu", pin=True), tl.to_i32(miss),
-                      tl.to_i32(np.array([M])), Kst, Vst, dd.GATHER_ZEROCOPY if mode == "zerocopy" else dd.GATHER_MEMCPY)
+                      tl.to_i32(np.array([M])), Kst, Vst,
+                      {"zerocopy": dd.GATHER_ZEROCOPY, "kernel": dd.GATHER_KERNEL, "memcpy": dd.GATHER_MEMCPY}[mode])
         assert ctx.status() == 0
     wk, wv = oracle.gather_kv(Kh, Vh, miss, cs)
     gk = tl.from_bf16(Kst).reshape(cap, cs, w.d)

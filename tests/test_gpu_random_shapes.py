@@ -60,7 +60,7 @@ def _inputs(w):
     return _INPUTS[w.name]
 
 
-@pytest.mark.parametrize("mode", [0, 1], ids=["zerocopy", "memcpy"])
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["zerocopy", "memcpy", "kernel"])
 @pytest.mark.parametrize("w", CASES, ids=lambda w: f"{w.name}_B{w.B}_G{w.G}_nq{w.n_q}_C{w.C}_k{w.k}_cs{w.cs}")
 def test_random_shape_step_matches_oracle(dd, w, mode):
     x, want = _inputs(w)

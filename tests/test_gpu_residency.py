@@ -33,7 +33,7 @@ def _tails(w, seed):
 
 
 @pytest.mark.parametrize("w", [TINY, V_HOT, V_5Q, V_NQ64, V_ONEQ], ids=lambda w: w.name)
-@pytest.mark.parametrize("mode", [0, 1], ids=["zerocopy", "memcpy"])
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["zerocopy", "memcpy", "kernel"])
 def test_step_with_tail_rows_matches_oracle(dd, w, mode):
     x = tl.host_inputs(w)
     kt, vt = _tails(w, w.seed)

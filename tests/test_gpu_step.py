@@ -62,7 +62,7 @@ class StepBuffers:
 
 
 @pytest.mark.parametrize("w", STEP_CASES, ids=lambda w: w.name)
-@pytest.mark.parametrize("mode", [0, 1], ids=["zerocopy", "memcpy"])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3], ids=["zerocopy", "memcpy", "kernel", "auto"])
 def test_step_matches_oracle(dd, w, mode):
     x = tl.host_inputs(w)
     want = oracle.step(x["q"], x["lm"], x["K"], x["V"], x["slot"], x["Khot"], x["Vhot"], w.k, w.cs)
