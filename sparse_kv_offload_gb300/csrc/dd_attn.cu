@@ -10,9 +10,10 @@
 //
 // Work split ("stream-K"): the unions of all (request, KV head) units are
 // laid end to end (chunk_off = exclusive prefix of the union sizes) and each
-// of two persistent CTAs per SM takes an equal contiguous slice of that
-// sequence (two CTAs so that one's producer issues copies while the other's
-// does its per-stage bookkeeping or waits on a fresh slice's tables).  A
+// persistent CTA (two per SM for up to 16 query vectors per KV head, so that
+// one's producer issues copies while the other's does its per-stage
+// bookkeeping or waits on a fresh slice's tables) takes an equal contiguous
+// slice of that sequence.  A
 // slice covers a few units ("runs").  At the end of a run every consumer
 // warp writes its partial (running max, sum and accumulator of its rows) into
 // slot CTA + unit, sub-slot warp -- slices are ordered like the units, so no
@@ -39,7 +40,10 @@
 
 namespace dd {
 
-constexpr int kAttnCtasPerSm = 2;
+// Persistent CTAs per SM: two for one m-tile (16 query vectors), one for
+// more, whose consumers need the registers of a whole SM (two CTAs would cap
+// them at 128 per thread and spill).
+__host__ __device__ constexpr int ctas_per_sm(int mt) { return mt == 1 ? 2 : 1; }
 constexpr int kStageRows = 64;
 constexpr int kHalfBytes = kStageRows * 128;          // 64 rows x 64 bf16
 constexpr int kStageBytes = 4 * kHalfBytes;           // K lo, K hi, V lo, V hi
@@ -47,9 +51,9 @@ constexpr int kMaxChunksPerStage = kStageRows / 16;   // cs >= 16
 constexpr int kQStride = 272;                         // bytes per staged query vector (256 + pad)
 constexpr int kHostBatch = 4;                         // 16-byte host loads in flight per lane (fused gather)
 
-// Tiles in flight per CTA: three for one m-tile, two when the staged queries
-// of more m-tiles need the room (two CTAs share an SM's 228 KiB).
-__host__ __device__ constexpr int stages_for(int mt) { return mt == 1 ? 3 : 2; }
+// Tiles in flight per CTA: three for one m-tile (two CTAs share an SM's
+// 228 KiB), four for more (one CTA per SM, beside its staged queries).
+__host__ __device__ constexpr int stages_for(int mt) { return mt == 1 ? 3 : 4; }
 
 enum : int32_t { kFirst = 1, kLast = 2, kEnd = 4 };
 
@@ -234,12 +238,12 @@ __device__ __forceinline__ void fixup_unit(const AttnParams &p, int unit, int c0
 }
 
 // ----------------------------------------------------------------- the kernel
-// Registers per thread: the register file holds kAttnCtasPerSm CTAs (their
-// threads rounded up to a multiple of 128); at most 224.
-__host__ __device__ constexpr int attn_max_regs(int threads) {
-  return (65536 / ((kAttnCtasPerSm * threads + 127) / 128 * 128)) / 8 * 8 > 224
+// Registers per thread: the register file holds `ctas` CTAs (their threads
+// rounded up to a multiple of 128); at most 224.
+__host__ __device__ constexpr int attn_max_regs(int threads, int ctas) {
+  return (65536 / ((ctas * threads + 127) / 128 * 128)) / 8 * 8 > 224
              ? 224
-             : (65536 / ((kAttnCtasPerSm * threads + 127) / 128 * 128)) / 8 * 8;
+             : (65536 / ((ctas * threads + 127) / 128 * 128)) / 8 * 8;
 }
 
 // Producer warps: warp 0 issues metadata and TMA; both share the host copies
@@ -251,7 +255,7 @@ __host__ __device__ constexpr int attn_max_regs(int threads) {
 __host__ __device__ constexpr int producers_for(int) { return 2; }
 
 template <int MT, int WPM>
-__global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) * 32))
+__global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) * 32, ctas_per_sm(MT)))
     k_attn(const __grid_constant__ CUtensorMap tm_khot, const __grid_constant__ CUtensorMap tm_vhot,
            const __grid_constant__ CUtensorMap tm_kst, const __grid_constant__ CUtensorMap tm_vst,
            const AttnParams p) {
@@ -787,11 +791,11 @@ AttnShape attn_shape(int NQ) {
   return s;
 }
 
-// kAttnCtasPerSm persistent CTAs per SM; partial slot CTA + unit for every
+// ctas_per_sm persistent CTAs per SM; partial slot CTA + unit for every
 // (CTA, unit) pair that shares chunks, one sub-slot per consumer warp of an m-tile.
 AttnPlan attn_plan(int units, int umax, int NQ, int sm_count) {
   AttnPlan pl;
-  pl.n_cta = sm_count > 0 ? kAttnCtasPerSm * sm_count : 1;
+  pl.n_cta = sm_count > 0 ? ctas_per_sm(attn_shape(NQ).mt) * sm_count : 1;
   const int wpm = attn_shape(NQ).wpm;
   pl.part_o_floats = ((int64_t)pl.n_cta + units) * wpm * NQ * 128;
   pl.part_ml_floats = ((int64_t)pl.n_cta + units) * wpm * NQ * 2;
