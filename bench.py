@@ -478,14 +478,21 @@ def run_ours(args, world, rank, local):
         return ev_
     ev = events(K)
     ev_stage = events(n_stage)
+    # per traced step, the kernels' own first-start / last-end %globaltimer stamps
+    # (scoring, selection, attention): their durations inside the step, with no
+    # event between them to stop a kernel from starting early (steps of their
+    # own, after the timed ones, so the timed steps carry no extra host work)
+    n_trace = min(K, 200)
+    trace = torch.zeros((n_trace, 3, 2, dd.TRACE_SLOTS), dtype=torch.int64, device="cuda")
+    trace[:, :, 0] = -1                    # UINT64_MAX: the per-SM start words (atomic min)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
 
-    def step(i, layer, events=None, inter=None):
+    def step(i, layer, events=None, inter=None, trace=None):
         d_ = layers[layer % N_LAYERS]
         ctx.step(layer, d_.q, d_.lm, d_.Kh, d_.Vh, d_.slot, d_.Khot, d_.Vhot, Kst, Vst, out, mode=mode,
                  intermediates=inter, stage_events=events, lm_kind=lm_kind, mass_gamma=args.mass_gamma,
-                 softmax_scale=args.softmax_scale)
+                 softmax_scale=args.softmax_scale, trace=trace)
 
     sampler = ClockSampler(local) if rank == 0 else None
     for i in range(args.warmup):
@@ -517,6 +524,8 @@ def run_ours(args, world, rank, local):
     dom_ms_timed = float(np.mean([ev[i][dom_marks[0]].elapsed_time(ev[i][dom_marks[1]]) for i in range(K)]))
     for i in range(n_stage):
         step(i, args.warmup + K + i, ev_stage[i])
+    for i in range(n_trace):
+        step(i, args.warmup + K + n_stage + i, trace=trace[i])
     torch.cuda.synchronize()
     if ctx.status() != 0:
         raise RuntimeError("device status after the stage-breakdown steps is not OK")
@@ -576,11 +585,31 @@ def run_ours(args, world, rank, local):
                 "peak": hbm_peak, "unit": "GB/s", "peak_kind": hbm_kind,
                 "traffic": {"score": profiled_traffic("score", w.name)}}
     roof_hbm["frac"] = roof_hbm["achieved"] / hbm_peak
+    # the same fraction inside steps without events, from the kernels' own stamps
+    tr_raw = trace.cpu().numpy().view(np.uint64)
+    starts = tr_raw[:, :, 0].min(axis=2).astype(np.float64)         # [K, kernel]: the earliest CTA start
+    ends = tr_raw[:, :, 1].max(axis=2).astype(np.float64)           # the latest CTA end
+    in_step = {}
+    for j, name in enumerate(("score", "select", "attention")):
+        ok = (starts[:, j] < 2.0 ** 63) & (ends[:, j] > 0)
+        in_step[name] = float(np.median(ends[ok, j] - starts[ok, j])) * 1e-3 if ok.any() else None
+    ok = (starts[:, 0] < 2.0 ** 63) & (ends[:, 2] > 0)
+    in_step["score_start_to_attention_end"] = float(np.median(ends[ok, 2] - starts[ok, 0])) * 1e-3 if ok.any() else None
+    if in_step["score"]:
+        roof_hbm["in_step"] = {"score_us": in_step["score"], "achieved": score_b / (in_step["score"] * 1e-6) / 1e9,
+                               "frac": score_b / (in_step["score"] * 1e-6) / 1e9 / hbm_peak,
+                               "note": "k_score from the end of the kernel before it (its dependency wait) to its last "
+                                       "CTA's end, stamped by the kernel (%globaltimer) in 200 further steps with no "
+                                       "events between the kernels; its first landmark requests come before that "
+                                       "wait, so this is the time scoring adds to the step; median over the steps"}
     if not fused or M == 0:
         t_sa = (stage_ms["score"] + stage_ms["attention"]) * 1e-3
         roof_hbm["score_plus_attention"] = {
             "kernels": "k_score + k_attn (bytes: landmarks, queries and scores + the union's K and V, each read once)",
             "achieved": (score_b + attn_b) / t_sa / 1e9, "frac": (score_b + attn_b) / t_sa / 1e9 / hbm_peak}
+        if in_step["score"] and in_step["attention"]:
+            t_in = (in_step["score"] + in_step["attention"]) * 1e-6
+            roof_hbm["score_plus_attention"]["in_step_frac"] = (score_b + attn_b) / t_in / 1e9 / hbm_peak
 
     # the same steps captured in a CUDA graph (one capture of all layers) and replayed
     graph = None
@@ -666,10 +695,14 @@ def run_ours(args, world, rank, local):
                           if own_residency else {})),
         "roofline": roof, "roofline_hbm": roof_hbm,
         "stages_us": {n: 1e3 * v for n, v in stage_ms.items()},
+        "in_step_us": in_step,
         "stages_note": f"stages_us: mean over {n_stage} further steps with an event at every stage boundary "
                        f"('score' is the scoring kernel; with the fused selection 'topk' is the one kernel for "
                        f"top-k, union, residency, ordinals and plan, and 'resolve' and 'gather' are empty); "
-                       f"{dom_timed}: {1e3 * dom_ms_timed:.1f} us inside the timed region",
+                       f"{dom_timed}: {1e3 * dom_ms_timed:.1f} us inside the timed region; in_step_us: median "
+                       f"over {n_trace} further steps with no events, from the kernels' own %globaltimer stamps "
+                       f"(from the end of the kernel before, or for the attention from its first copy, to the last "
+                       f"CTA's end)",
         "per_step": {"union_chunks": U, "missing_chunks": M, "gather_bytes": gather_b,
                      "host_link_gbs": gather_b / (dom_ms_timed * 1e-3) / 1e9},
         "host_link_peaks_gbs": {"memcpy_h2d": link_memcpy, "zero_copy_gather_sequential": link_zc},

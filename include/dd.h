@@ -92,6 +92,8 @@ typedef enum {
 
 typedef struct dd_ctx dd_ctx;
 
+#define DD_TRACE_SLOTS 256   /* per-SM slots of dd_step_args.trace */
+
 /* Create a context for one shape.  max_misses: capacity of each staging
  * buffer in chunks (M_cap); B*Hkv*Umax guarantees DD_ERR_CAPACITY never
  * occurs.  hot_slots: number of chunk slots of the caller's hot pool (0 when
@@ -256,6 +258,20 @@ typedef struct {
   float mass_gamma;              /* > 0: coverage budgets (dd_select_topk_mass) instead of a fixed k */
   int32_t mass_k_min;            /* with mass_gamma: the shortest row */
   int32_t *sel_cnt;              /* with mass_gamma: optional int32 [B,n_q,Hkv] row lengths */
+  /* optional in-step timing, device uint64 [3][2][DD_TRACE_SLOTS] or NULL:
+   * for the scoring, selection and attention kernels (i = 0, 1, 2), every
+   * CTA records when its wait for the kernel before it returned (attention:
+   * when it issues its first copy; the scoring kernel's first landmark
+   * requests come before that wait and are not counted) with an
+   * atomic min into trace[i][0][s] and when it finished with an atomic max
+   * into trace[i][1][s], s = the SM it ran on (%smid mod DD_TRACE_SLOTS; ns of
+   * %globaltimer).  The kernel's window is the minimum of row 0 and the
+   * maximum of row 1.  The caller sets every trace[i][0][s] to UINT64_MAX and
+   * every trace[i][1][s] to 0 before the step.  Unlike events between the
+   * kernels it leaves their overlap in place, and one pair of words per SM
+   * keeps the atomics from contending.  Fused selection and attention only
+   * (the stage kernels of the other paths record nothing). */
+  uint64_t *trace;
 } dd_step_args;
 
 /* dd_step may be captured into a CUDA graph (zero-copy, kernel and auto

@@ -120,6 +120,23 @@ dd_status host_kv_views(dd_ctx *c, const void *Kh, const void *Vh, const void **
   return cached_view(c, Vh, vd);
 }
 
+// Landmark scoring of all n_q queries (mean or min/max landmarks), with the
+// step's optional timing words.
+dd_status score_impl(dd_ctx *c, const void *q, const void *lm, float *scores, bool minmax,
+                     unsigned long long *trace, dd_stream_t stream) {
+  if (!c) return DD_ERR_INVALID_ARG;
+  if (c->units == 0) return DD_OK;
+  if (!q || !lm || !scores || !aligned16(q) || !aligned16(lm)) return DD_ERR_INVALID_ARG;
+  c->launches += 1;
+  const dd_dims &d = c->dims;
+  return cuda_ok(minmax ? dd::launch_score_minmax(static_cast<const uint4 *>(q), static_cast<const uint4 *>(lm),
+                                                  scores, d.B, d.n_q, d.Hq, d.Hkv, c->C, c->sm_count, c->status,
+                                                  (cudaStream_t)stream, trace)
+                        : dd::launch_score(static_cast<const uint4 *>(q), static_cast<const uint4 *>(lm), scores, d.B,
+                                           d.n_q, d.Hq, d.Hkv, c->C, c->sm_count, c->status, (cudaStream_t)stream,
+                                           trace));
+}
+
 template <typename T>
 T *carve(uint8_t *&cur, int64_t n) {
   T *p = reinterpret_cast<T *>(cur);
@@ -271,13 +288,7 @@ dd_status dd_build_landmarks(dd_ctx *c, const void *K, void *lm, dd_stream_t str
 }
 
 dd_status dd_score_landmarks(dd_ctx *c, const void *q, const void *lm, float *scores, dd_stream_t stream) {
-  if (!c) return DD_ERR_INVALID_ARG;
-  if (c->units == 0) return DD_OK;
-  if (!q || !lm || !scores || !aligned16(q) || !aligned16(lm)) return DD_ERR_INVALID_ARG;
-  c->launches += 1;
-  return cuda_ok(dd::launch_score(static_cast<const uint4 *>(q), static_cast<const uint4 *>(lm), scores, c->dims.B,
-                                  c->dims.n_q, c->dims.Hq, c->dims.Hkv, c->C, c->sm_count, c->status,
-                                  (cudaStream_t)stream));
+  return score_impl(c, q, lm, scores, false, nullptr, stream);
 }
 
 dd_status dd_build_landmarks_minmax(dd_ctx *c, const void *K, void *lm2, dd_stream_t stream) {
@@ -292,13 +303,7 @@ dd_status dd_build_landmarks_minmax(dd_ctx *c, const void *K, void *lm2, dd_stre
 }
 
 dd_status dd_score_landmarks_minmax(dd_ctx *c, const void *q, const void *lm2, float *scores, dd_stream_t stream) {
-  if (!c) return DD_ERR_INVALID_ARG;
-  if (c->units == 0) return DD_OK;
-  if (!q || !lm2 || !scores || !aligned16(q) || !aligned16(lm2)) return DD_ERR_INVALID_ARG;
-  c->launches += 1;
-  return cuda_ok(dd::launch_score_minmax(static_cast<const uint4 *>(q), static_cast<const uint4 *>(lm2), scores,
-                                         c->dims.B, c->dims.n_q, c->dims.Hq, c->dims.Hkv, c->C, c->sm_count,
-                                         c->status, (cudaStream_t)stream));
+  return score_impl(c, q, lm2, scores, true, nullptr, stream);
 }
 
 dd_status dd_select_topk(dd_ctx *c, const float *scores, int32_t *sel, dd_stream_t stream) {
@@ -446,7 +451,7 @@ static dd_status attn_impl(dd_ctx *c, const void *q, const void *Khot, const voi
                            const void *Vst, const int32_t *union_slot, const uint8_t *union_qmask,
                            const int32_t *union_cnt, const int32_t *miss_count, float softmax_scale, float *out,
                            bool plan_ready, const void *kh_dev, const void *vh_dev, const void *k_tail,
-                           const void *v_tail, dd_stream_t stream) {
+                           const void *v_tail, dd_stream_t stream, unsigned long long *trace = nullptr) {
   if (!c) return DD_ERR_INVALID_ARG;
   if (c->units == 0) return DD_OK;
   if ((k_tail == nullptr) != (v_tail == nullptr)) return DD_ERR_INVALID_ARG;
@@ -460,7 +465,8 @@ static dd_status attn_impl(dd_ctx *c, const void *q, const void *Khot, const voi
   const dd::AttnScratch scr = {c->part_o, c->part_ml, c->chunk_off, c->flat, c->dummy_pool};
   return cuda_ok(dd::launch_attn(q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count, scale, out,
                                  c->plan, scr, plan_ready, kh_dev, vh_dev, c->status, d.B, d.n_q, d.Hq, d.Hkv, d.cs,
-                                 c->umax, c->hot_slots, c->max_misses, (cudaStream_t)stream, k_tail, v_tail));
+                                 c->umax, c->hot_slots, c->max_misses, (cudaStream_t)stream, k_tail, v_tail,
+                                 trace));
 }
 
 dd_status dd_sparse_attn_decode(dd_ctx *c, const void *q, const void *Khot, const void *Vhot, const void *Kst,
@@ -511,6 +517,7 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   const int p = a->layer & 1;
   if (c->max_misses > 0 && (!a->Kst[p] || !a->Vst[p])) return DD_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
+  unsigned long long *trace = reinterpret_cast<unsigned long long *>(a->trace);
   float *scores = a->scores ? a->scores : c->scores;
   int32_t *sel = a->sel ? a->sel : c->sel;
   int32_t *union_idx = a->union_idx ? a->union_idx : c->union_idx;
@@ -531,9 +538,9 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   // (b,g) when a unit's score rows fit in shared memory (fixed k only), and as
   // separate stage kernels otherwise
   if (a->lm_kind == DD_LM_MINMAX) {
-    DD_TRY(dd_score_landmarks_minmax(c, a->q, a->lm, scores, stream));
+    DD_TRY(score_impl(c, a->q, a->lm, scores, true, trace, stream));
   } else {
-    DD_TRY(dd_score_landmarks(c, a->q, a->lm, scores, stream));
+    DD_TRY(score_impl(c, a->q, a->lm, scores, false, trace, stream));
   }
   DD_TRY(mark(1));
   const bool fused = a->mass_gamma <= 0.f && dd::fused_select_smem(d.n_q, c->C, d.k) > 0;
@@ -564,6 +571,7 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
     o.hot_slots = c->hot_slots;
     o.max_misses = c->max_misses;
     o.status = c->status;
+    o.trace = trace ? trace + 2 * dd::kTraceSlots : nullptr;
     DD_CUDA(dd::launch_select_fused(o, d.n_q, s));
     DD_TRY(mark(2));
     c->launches += 1;
@@ -602,7 +610,8 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   // memcpy mode: dd_gather_kv made this stream wait for the copy stream
   DD_TRY(mark(4));
   DD_TRY(attn_impl(c, a->q, a->Khot, a->Vhot, a->Kst[p], a->Vst[p], union_slot, union_qmask, union_cnt, miss_count,
-                   a->softmax_scale, a->out, true, kh_dev, vh_dev, a->K_tail, a->V_tail, stream));
+                   a->softmax_scale, a->out, true, kh_dev, vh_dev, a->K_tail, a->V_tail, stream,
+                   trace ? trace + 4 * dd::kTraceSlots : nullptr));
   DD_TRY(mark(5));
   if (!captured) {
     DD_CUDA(cudaEventRecord(c->released[p], s));

@@ -76,6 +76,7 @@ struct AttnParams {
   float *part_ml;             // [gridDim + units, NQ, 2]
   int32_t *status;
   int32_t *arrive;            // [units] CTAs that have finished a part of each unit (zeroed by the planner)
+  unsigned long long *trace;  // optional [2][kTraceSlots]: per-SM earliest start, latest end (ns)
   const uint16_t *k_tail, *v_tail;   // bf16 [B,n_q,Hkv,128] the step's own new rows, or null
   int n_q, Hq, Hkv, G, NQ, cs, umax, units;
   float scale_log2;           // softmax scale * log2(e)
@@ -310,6 +311,7 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
     int4 nxt = (x0 + 32 + lane < hi) ? p.flat[x0 + 32 + lane] : make_int4(-1, 0, -1, 0);
     const bool fused = p.kh != nullptr;
     const int pw = warp - kConsumers;
+    if (p.trace && pw == 0 && lane == 0) trace_start(p.trace);   // before this CTA's first copy
     if (pw > 0 && !fused) return;
     int s = 0, u = u0, x = lo;
     bool first = true, alive = true;
@@ -663,6 +665,10 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
     }
     if (m_flags & kEnd) break;
   }
+  if (p.trace) {
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");   // every consumer warp is done
+    if (tid == 0) trace_end(p.trace);
+  }
 }
 
 // --------------------------------------------------------------- plan
@@ -816,7 +822,8 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
                         const int32_t *miss_count, float softmax_scale, float *out, const AttnPlan &plan,
                         const AttnScratch &scr, bool plan_ready, const void *kh_dev, const void *vh_dev,
                         int32_t *status, int B, int n_q, int Hq, int Hkv, int cs, int umax, int64_t hot_slots,
-                        int64_t max_misses, cudaStream_t s, const void *k_tail, const void *v_tail) {
+                        int64_t max_misses, cudaStream_t s, const void *k_tail, const void *v_tail,
+                        unsigned long long *trace) {
   const int units = B * Hkv;
   if (units == 0) return cudaSuccess;
   const int G = Hq / Hkv, NQ = n_q * G;
@@ -864,6 +871,7 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
   p.arrive = scr.chunk_off + units + 1;   // the planner zeroed these counters
   p.k_tail = kt;
   p.v_tail = vt;
+  p.trace = trace;
   p.n_q = n_q; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.NQ = NQ; p.cs = cs; p.umax = umax; p.units = units;
   p.scale_log2 = scale_log2;
 

@@ -142,6 +142,24 @@ __device__ __forceinline__ unsigned long long wait_published(const unsigned long
   return w;
 }
 
+// Optional in-step timing (dd_step_args.trace): one pair of words per SM so
+// that only the CTAs sharing an SM contend; the reader takes the minimum of
+// the starts and the maximum of the ends over the kTraceSlots slots.
+constexpr int kTraceSlots = DD_TRACE_SLOTS;
+__device__ __forceinline__ int trace_slot() {
+  uint32_t id;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(id));
+  return (int)(id & (kTraceSlots - 1));
+}
+// Out of line: called once per CTA, they should not add to the register
+// pressure of the kernels' main loops.
+static __device__ __noinline__ void trace_start(unsigned long long *t) {   // t: this kernel's [2][kTraceSlots]
+  atomicMin(t + trace_slot(), (unsigned long long)globaltimer_ns());
+}
+static __device__ __noinline__ void trace_end(unsigned long long *t) {
+  atomicMax(t + kTraceSlots + trace_slot(), (unsigned long long)globaltimer_ns());
+}
+
 // 1-D bulk copy global -> shared, completion counted on an mbarrier (16-byte
 // aligned addresses, size a multiple of 16)
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
@@ -274,10 +292,11 @@ struct Ctx;
 cudaError_t set_dyn_smem(const void *func, size_t bytes);
 cudaError_t launch_build_landmarks(const uint4 *K, uint4 *lm, int64_t n_chunks, int cs, cudaStream_t s);
 cudaError_t launch_score(const uint4 *q, const uint4 *lm, float *scores, int B, int n_q, int Hq, int Hkv,
-                         int C, int sm_count, int32_t *status, cudaStream_t s);
+                         int C, int sm_count, int32_t *status, cudaStream_t s, unsigned long long *trace = nullptr);
 cudaError_t launch_build_minmax(const uint4 *K, uint4 *lm2, int64_t n_chunks, int cs, cudaStream_t s);
 cudaError_t launch_score_minmax(const uint4 *q, const uint4 *lm2, float *scores, int B, int n_q, int Hq, int Hkv,
-                                int C, int sm_count, int32_t *status, cudaStream_t s);
+                                int C, int sm_count, int32_t *status, cudaStream_t s,
+                                unsigned long long *trace = nullptr);
 cudaError_t launch_topk(const float *scores, int32_t *sel, int rows, int C, int k, cudaStream_t s);
 // outputs and state of the fused selection kernel (dd_select.cu)
 struct SelectOut {
@@ -295,6 +314,7 @@ struct SelectOut {
   int units, Hq, Hkv, C, k, umax, cs;
   int64_t hot_slots, max_misses;
   int32_t *status;
+  unsigned long long *trace;      // optional [2][kTraceSlots]: per-SM earliest start, latest end (ns)
 };
 size_t fused_select_smem(int n_q, int C, int k);
 cudaError_t launch_select_fused(const SelectOut &o, int n_q, cudaStream_t s);
@@ -328,7 +348,7 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
                         const AttnScratch &scr, bool plan_ready, const void *kh_dev, const void *vh_dev,
                         int32_t *status, int B, int n_q, int Hq, int Hkv, int cs, int umax, int64_t hot_slots,
                         int64_t max_misses, cudaStream_t s, const void *k_tail = nullptr,
-                        const void *v_tail = nullptr);
+                        const void *v_tail = nullptr, unsigned long long *trace = nullptr);
 cudaError_t launch_update_residency(int32_t step, int32_t cap, int S, int units, const int32_t *union_idx,
                                     const int32_t *union_slot, const int32_t *union_cnt, const int32_t *miss_count,
                                     int64_t max_misses, const uint4 *Kst, const uint4 *Vst, int32_t *resident_slot,

@@ -147,7 +147,7 @@ template <int NQ, bool MM>
 __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) k_score(const uint4 *__restrict__ q, const uint4 *__restrict__ lm,
                                                             float *__restrict__ scores, int Hq, int Hkv, int C,
                                                             int64_t total_rows, int64_t rows_per_cta,
-                                                            int32_t *status) {
+                                                            int32_t *status, unsigned long long *trace) {
   constexpr int kVecs = MM ? 2 : 1;                       // vectors per landmark
   constexpr int kRowBytes = 256 * kVecs;
   constexpr int kStageRows = score_stage_rows(MM);       // 128 or 64
@@ -192,6 +192,8 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) k_score(const 
     while (st_issue < kScoreStages && i_done < span) issue();
   pdl_wait();
   pdl_trigger();
+  // the step's critical path: from the end of the kernel before this one
+  if (trace && tid == 0) trace_start(trace);
 
   const int part = tid & 15, sub = tid >> 4;
   const int G = Hq / Hkv;
@@ -276,11 +278,15 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) k_score(const 
   if (done < span && tid == 0)
     for (int s2 = st + 1; s2 < st_issue; ++s2)
       mbar_wait(smem_u32(&bar[s2 % kScoreStages]), (uint32_t)(s2 / kScoreStages) & 1u, status);
+  if (trace) {
+    __syncthreads();
+    if (tid == 0) trace_end(trace);
+  }
 }
 
 template <bool MM>
 static cudaError_t launch_score_t(const uint4 *q, const uint4 *lm, float *scores, int B, int n_q, int Hq, int Hkv,
-                                  int C, int sm_count, int32_t *status, cudaStream_t s) {
+                                  int C, int sm_count, int32_t *status, unsigned long long *trace, cudaStream_t s) {
   const int64_t total = (int64_t)B * Hkv * C;
   if (total == 0) return cudaSuccess;
   constexpr int kStageRows = score_stage_rows(MM);
@@ -296,7 +302,7 @@ static cudaError_t launch_score_t(const uint4 *q, const uint4 *lm, float *scores
     cudaError_t e = set_dyn_smem((const void *)k_score<N, MM>, smem);                                         \
     if (e != cudaSuccess) return e;                                                                               \
     return launch_k(k_score<N, MM>, dim3(grid), dim3(kScoreThreads), smem, s, q, lm, scores, Hq, Hkv, C, total,   \
-                    per, status);                                                                                 \
+                    per, status, trace);                                                                          \
   }
     DD_SCORE_CASE(1) DD_SCORE_CASE(2) DD_SCORE_CASE(3) DD_SCORE_CASE(4)
     DD_SCORE_CASE(5) DD_SCORE_CASE(6) DD_SCORE_CASE(7) DD_SCORE_CASE(8)
@@ -306,13 +312,13 @@ static cudaError_t launch_score_t(const uint4 *q, const uint4 *lm, float *scores
 }
 
 cudaError_t launch_score(const uint4 *q, const uint4 *lm, float *scores, int B, int n_q, int Hq, int Hkv, int C,
-                         int sm_count, int32_t *status, cudaStream_t s) {
-  return launch_score_t<false>(q, lm, scores, B, n_q, Hq, Hkv, C, sm_count, status, s);
+                         int sm_count, int32_t *status, cudaStream_t s, unsigned long long *trace) {
+  return launch_score_t<false>(q, lm, scores, B, n_q, Hq, Hkv, C, sm_count, status, trace, s);
 }
 
 cudaError_t launch_score_minmax(const uint4 *q, const uint4 *lm2, float *scores, int B, int n_q, int Hq, int Hkv,
-                                int C, int sm_count, int32_t *status, cudaStream_t s) {
-  return launch_score_t<true>(q, lm2, scores, B, n_q, Hq, Hkv, C, sm_count, status, s);
+                                int C, int sm_count, int32_t *status, cudaStream_t s, unsigned long long *trace) {
+  return launch_score_t<true>(q, lm2, scores, B, n_q, Hq, Hkv, C, sm_count, status, trace, s);
 }
 
 }  // namespace dd

@@ -491,6 +491,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_select_fused(SelectOut o) 
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
+    if (o.trace) trace_start(o.trace);
     s_unit = atomicAdd(o.ticket, 1);                       // units in the order their CTAs start
     // this launch's look-back epoch; the previous launch's last CTA advanced it
     s_epoch = *reinterpret_cast<volatile uint32_t *>(o.ticket + 2);
@@ -845,6 +846,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_select_fused(SelectOut o) 
       o.ticket[2] = (int32_t)(next == 0u ? 1u : next);
       __threadfence();
     }
+  }
+  if (o.trace) {
+    __syncthreads();
+    if (tid == 0) trace_end(o.trace);
   }
 }
 

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libdd.so")
 
 DD_OK, DD_ERR_INVALID_ARG, DD_ERR_CUDA, DD_ERR_CAPACITY, DD_ERR_TIMEOUT, DD_ERR_DEVICE_CHECK = range(6)
 GATHER_ZEROCOPY, GATHER_MEMCPY, GATHER_KERNEL, GATHER_AUTO = 0, 1, 2, 3
+TRACE_SLOTS = 256          # per-SM slots of a step's timing words (DD_TRACE_SLOTS)
 LM_MEAN, LM_MINMAX = 0, 1
 
 EXPORTED = (
@@ -61,6 +62,7 @@ class StepArgs(ctypes.Structure):
         ("mass_gamma", ctypes.c_float),
         ("mass_k_min", ctypes.c_int32),
         ("sel_cnt", _vp),
+        ("trace", _vp),
     ]
 
 
@@ -338,7 +340,7 @@ class Context:
 
     def step(self, layer, q, lm, Kh, Vh, resident_slot, Khot, Vhot, Kst_pair, Vst_pair, out,
              mode=GATHER_ZEROCOPY, softmax_scale=0.0, intermediates=None, stage_events=None, stream=None,
-             lm_kind=LM_MEAN, K_tail=None, V_tail=None, mass_gamma=0.0, mass_k_min=1, sel_cnt=None):
+             lm_kind=LM_MEAN, K_tail=None, V_tail=None, mass_gamma=0.0, mass_k_min=1, sel_cnt=None, trace=None):
         """One layer; ``intermediates`` optionally maps names of dd_step_args' optional
         outputs (scores, sel, union_idx, union_slot, union_qmask, union_cnt, miss_list,
         miss_count, attn_slot) to caller tensors; ``stage_events`` optionally gives six
@@ -352,6 +354,8 @@ class Context:
         a.mass_gamma = float(mass_gamma)
         a.mass_k_min = int(mass_k_min)
         a.sel_cnt = _ptr(sel_cnt, torch.int32, s.B * s.n_q * s.Hkv, name="sel_cnt", allow_none=True)
+        # int64 tensor of 3 * 2 * TRACE_SLOTS (uint64 bits): see dd_step_args.trace
+        a.trace = _ptr(trace, torch.int64, 6 * TRACE_SLOTS, name="trace", allow_none=True)
         a.K_tail = _ptr(K_tail, torch.bfloat16, s.B * s.n_q * s.Hkv * s.d, name="K_tail", allow_none=True)
         a.V_tail = _ptr(V_tail, torch.bfloat16, s.B * s.n_q * s.Hkv * s.d, name="V_tail", allow_none=True)
         a.lm = _ptr(lm, torch.bfloat16, s.B * s.Hkv * s.C * s.d * (2 if lm_kind == LM_MINMAX else 1), name="lm")

@@ -8,7 +8,7 @@ from sparse_kv_offload_gb300 import synth
 from sparse_kv_offload_gb300.workloads import TINY, Workload
 
 import dd_testlib as tl
-from test_gpu_parity import STEP_CASES, shape_of
+from test_gpu_parity import STEP_CASES, V_HOT, shape_of
 
 pytestmark = pytest.mark.gpu
 
@@ -207,7 +207,7 @@ def test_step_replays_in_a_cuda_graph(dd):
     # wrongly (the look-back epoch lives on the device), so a captured step
     # replays correctly, also after its inputs change in place
     import torch
-    from test_gpu_parity import V_HOT
+
     w = V_HOT
     x = tl.host_inputs(w)
     buf = StepBuffers(w, x)
@@ -248,3 +248,28 @@ def test_step_replays_in_a_cuda_graph(dd):
         torch.cuda.synchronize()
         assert ctx.status() == 0
         check(want2)
+
+
+def test_step_trace_orders_the_kernels(dd):
+    # the kernels' own timing words: a non-empty window per kernel, each kernel
+    # starting after the one before it has finished (each waits for it before
+    # its work), and the step's results unchanged
+    import torch
+    w = V_HOT
+    x = tl.host_inputs(w)
+    want = oracle.step(x["q"], x["lm"], x["K"], x["V"], x["slot"], x["Khot"], x["Vhot"], w.k, w.cs)
+    buf = StepBuffers(w, x)
+    trace = torch.zeros((3, 2, dd.TRACE_SLOTS), dtype=torch.int64, device="cuda")
+    trace[:, 0] = -1
+    with dd.Context(shape_of(w), max_misses=buf.cap, hot_slots=buf.hot) as ctx:
+        ctx.step(0, buf.q, buf.lm, buf.Kh, buf.Vh, buf.slot, buf.Khot, buf.Vhot, buf.Kst, buf.Vst, buf.out,
+                 trace=trace)
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+    raw = trace.cpu().numpy().view(np.uint64)
+    start, end = raw[:, 0].min(axis=1), raw[:, 1].max(axis=1)
+    for j in range(3):
+        assert 0 < start[j] < end[j] < np.uint64(2 ** 63), f"kernel {j}: window {start[j]}..{end[j]}"
+    assert end[0] <= start[1] and end[1] <= start[2]
+    assert np.all((raw[:, 0] == np.uint64(2 ** 64 - 1)) == (raw[:, 1] == 0))   # an SM either ran CTAs or not
+    tl.check_attention(buf.out.cpu().numpy().reshape(want["out"].shape), want["out"])
