@@ -75,8 +75,10 @@ typedef struct {
 
 typedef enum {
   DD_GATHER_ZEROCOPY = 0,   /* a kernel loads the host chunks over the host link (no host sync); in
-                               dd_step that kernel is the attention itself, which reads each missing
-                               chunk when its tile comes up */
+                               dd_step that kernel is the attention itself: one warp per CTA copies
+                               the missing chunks of the CTA's slice into staging, in slice order and
+                               as far ahead as the link allows, while another streams every tile
+                               (hot pool or staging) by TMA */
   DD_GATHER_MEMCPY = 1,     /* miss list read back to the host, one cudaMemcpyAsync per run of
                                consecutive chunks on the context's copy stream (host sync) */
   DD_GATHER_KERNEL = 2,     /* a separate zero-copy gather kernel copies every missing chunk into
@@ -86,8 +88,9 @@ typedef enum {
   DD_GATHER_AUTO = 3        /* dd_step only: DD_GATHER_KERNEL when the context has a hot pool
                                (hot_slots > 0), else DD_GATHER_ZEROCOPY.  Measured on one GB300:
                                with 10-50% of the union missing the separate gather kernel keeps the
-                               host link at 84-93% of its peak where the fused one reaches 31-53%;
-                               with every chunk missing the fused gather is 2-3% faster */
+                               host link at 84-93% of its peak where the fused one reaches 51-69%
+                               (the misses fall unevenly on the attention's slices); with every
+                               chunk missing the fused gather is 3% faster */
 } dd_gather_mode;
 
 typedef struct dd_ctx dd_ctx;

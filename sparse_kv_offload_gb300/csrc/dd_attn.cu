@@ -276,14 +276,16 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
   uint64_t *bars = reinterpret_cast<uint64_t *>(meta + kStages);             // full[kStages], empty[kStages]
 
   __shared__ int s_fix;   // this CTA finished the last part of the unit whose run just ended
+  __shared__ int s_ready; // fused gather: missing chunks of this slice already in staging, in slice order
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full0 + 8 * s, p.kh != nullptr ? 1 + kProducers : 1);
+      mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kConsumers);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_ready = 0;
   }
   __syncthreads();
   pdl_wait();
@@ -297,9 +299,79 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
 
   if (warp >= kConsumers) {
     // ------------------------------------------------------------ producers
-    // streams the flat chunk table of this slice in batches of 32 (the next
-    // batch already in flight) and cuts it into stages that never cross a
-    // unit boundary; lane i of `bnd` holds the end of unit ubase + i
+    const bool fused = p.kh != nullptr;
+    const int pw = warp - kConsumers;
+    if (pw > 0) {
+      if (fused && pw == 1) {
+        // fused gather, copier warp: every missing chunk of the slice, in
+        // slice order, from pinned host memory into its staging rows, as far
+        // ahead of the issuing warp as the link allows.  The batch's missing
+        // chunks are numbered k = 0..n-1 (lane k holds chunk k's host index
+        // and staging row) and their elements walked as one sequence,
+        // kCopyBatch loads per lane in flight.  Whenever chunks complete, all
+        // lanes fence (GPU scope, then the generic -> async proxy fence, as
+        // the issuing warp reads staging by TMA) and lane 0 publishes how
+        // many of the slice's misses are in place (s_ready, release).
+        constexpr int kCopyBatch = 2 * kHostBatch;
+        const int vec = p.cs * 16;   // uint4 per chunk, K or V
+        int done = 0;                // misses of the slice copied so far
+        for (int xb = lo; xb < hi; xb += 32) {
+          const int4 e = (xb + lane < hi) ? p.flat[xb + lane] : make_int4(-1, 0, -1, 0);
+          const unsigned mm = __ballot_sync(0xffffffffu, e.x < -1 && e.y != 0 && e.z >= 0);
+          const int n_miss = __popc(mm);
+          if (n_miss == 0) continue;
+          int my_pos = 0;   // batch position of missing chunk number `lane`
+          {
+            unsigned m2 = mm;
+            for (int k = 0; k < lane && m2; ++k) m2 &= m2 - 1;
+            my_pos = m2 ? __ffs(m2) - 1 : 0;
+          }
+          const int my_host = __shfl_sync(0xffffffffu, e.z, my_pos);
+          const int my_row = __shfl_sync(0xffffffffu, e.x, my_pos);
+          const int total_e = n_miss * 2 * vec;
+          int published = 0;
+#pragma unroll 1
+          for (int e0 = 0; e0 < total_e; e0 += 32 * kCopyBatch) {
+            uint4 v[kCopyBatch];
+#pragma unroll
+            for (int t = 0; t < kCopyBatch; ++t) {
+              const int eu = e0 + t * 32;                       // warp-uniform
+              const int k = eu / (2 * vec);
+              const int host = __shfl_sync(0xffffffffu, my_host, k & 31);
+              const int el = eu - k * 2 * vec + lane;           // within the chunk: K then V
+              const uint4 *src = el >= vec ? p.vh + (int64_t)host * vec + (el - vec) : p.kh + (int64_t)host * vec + el;
+              v[t] = eu < total_e ? ldg_nc(src) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int t = 0; t < kCopyBatch; ++t) {
+              const int eu = e0 + t * 32;
+              const int k = eu / (2 * vec);
+              const int row = __shfl_sync(0xffffffffu, my_row, k & 31);
+              if (eu >= total_e) continue;
+              const int el = eu - k * 2 * vec + lane;
+              const int kv = el >= vec, r = kv ? el - vec : el;
+              (kv ? p.vst : p.kst)[(int64_t)(-2 - row) * 16 + r] = v[t];   // -2 - row: first staging row
+            }
+            // chunks whose every element precedes e0 + 32 * kCopyBatch are complete
+            const int complete = min(n_miss, (e0 + 32 * kCopyBatch) / (2 * vec));
+            if (complete > published) {
+              __threadfence();
+              asm volatile("fence.proxy.async.global;" ::: "memory");
+              __syncwarp();
+              if (lane == 0)
+                asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_u32(&s_ready)), "r"(done + complete)
+                             : "memory");
+              published = complete;
+            }
+          }
+          done += n_miss;
+        }
+      }
+      return;
+    }
+    // issuing warp: streams the flat chunk table of this slice in batches of
+    // 32 (the next batch already in flight) and cuts it into stages that never
+    // cross a unit boundary; lane i of `bnd` holds the end of unit ubase + i
     const int chunks_per_stage = kStageRows / p.cs;
     const uint32_t box_bytes = (uint32_t)p.cs * 128u;
     const int u0 = unit_of_chunk_warp(p.chunk_off, p.units, lo);
@@ -309,10 +381,8 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
     int x0 = lo;
     int4 cur = (x0 + lane < hi) ? p.flat[x0 + lane] : make_int4(-1, 0, -1, 0);
     int4 nxt = (x0 + 32 + lane < hi) ? p.flat[x0 + 32 + lane] : make_int4(-1, 0, -1, 0);
-    const bool fused = p.kh != nullptr;
-    const int pw = warp - kConsumers;
-    if (p.trace && pw == 0 && lane == 0) trace_start(p.trace);   // before this CTA's first copy
-    if (pw > 0 && !fused) return;
+    if (p.trace && lane == 0) trace_start(p.trace);   // before this CTA's first copy
+    int missed = 0;   // fused gather: missing chunks met so far, in slice order (lane 0)
     int s = 0, u = u0, x = lo;
     bool first = true, alive = true;
     while (x < hi && alive) {
@@ -342,9 +412,7 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
             hosts[i] = __shfl_sync(0xffffffffu, cur.z, (x - x0 + i) & 31);
           }
           const int buf = s % kStages;
-          if (lane == 0 && pw > 0) {
-            if (s >= kStages && !mbar_wait(empty0 + 8 * buf, ((s / kStages) - 1) & 1, p.status)) alive = false;
-          } else if (lane == 0) {
+          if (lane == 0) {
             if (s >= kStages && !mbar_wait(empty0 + 8 * buf, ((s / kStages) - 1) & 1, p.status)) {
               alive = false;
             } else {
@@ -359,8 +427,7 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
               for (int i = 0; i < kMaxChunksPerStage; ++i) {
                 const uint8_t q8 = (i < nch && rows[i] != -1) ? (uint8_t)qms[i] : 0;
                 m.qm[i] = q8;
-                // chunks the warp copies from host memory arrive by stores, not by TMA
-                if (q8 && !(fused && rows[i] < -1)) bytes += 4 * box_bytes;
+                if (q8) bytes += 4 * box_bytes;
               }
               const uint32_t bar = full0 + 8 * buf;
               mbar_arrive_expect_tx(bar, bytes);
@@ -375,7 +442,24 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
 #pragma unroll
               for (int i = 0; i < kMaxChunksPerStage; ++i) {
                 if (i >= nch || rows[i] == -1 || qms[i] == 0) continue;
-                if (fused && rows[i] < -1) continue;
+                if (fused && rows[i] < -1 && hosts[i] >= 0) {
+                  // a missing chunk: staged by the copier warp; wait until it is in place (bounded)
+                  const int ord = missed++;
+                  const uint64_t t0 = globaltimer_ns();
+                  for (uint32_t it = 0;; ++it) {
+                    int ready;
+                    asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(ready) : "r"(smem_u32(&s_ready))
+                                 : "memory");
+                    if (ready > ord) break;
+                    if ((it & 63u) == 63u && globaltimer_ns() - t0 > 2000000000ull) {
+                      set_status(p.status, DD_ERR_TIMEOUT);
+                      alive = false;
+                      break;
+                    }
+                  }
+                  if (!alive) break;
+                  asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
                 const bool hot = rows[i] >= 0;
                 const CUtensorMap *mk = hot ? &tm_khot : &tm_kst;
                 const CUtensorMap *mv = hot ? &tm_vhot : &tm_vst;
@@ -390,62 +474,6 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
           }
           alive = __shfl_sync(0xffffffffu, alive, 0);
           if (!alive) break;
-          if (fused) {
-            // missing chunks: 16-byte loads over the host link by all lanes,
-            // stored swizzled into the tile and written back to staging.  The
-            // stage's missing chunks are numbered k = 0..n-1 (lane k holds
-            // chunk k's host index, staging row and tile position) and their
-            // elements are walked as one sequence, kHostBatch loads per lane
-            // in flight.
-            const uint32_t sbase = smem_u32(stages + buf * kStageBytes);
-            const int vec = p.cs * 16;   // uint4 per chunk, K or V
-            uint32_t mask = 0;
-#pragma unroll
-            for (int i = 0; i < kMaxChunksPerStage; ++i)
-              if (i < nch && rows[i] < -1 && qms[i] != 0 && hosts[i] >= 0) mask |= 1u << i;
-            const int n_miss = __popc(mask);
-            int my_i = 0;   // stage position of missing chunk number `lane`
-            {
-              uint32_t m2 = mask;
-              for (int k = 0; k < lane && m2; ++k) m2 &= m2 - 1;
-              my_i = m2 ? __ffs(m2) - 1 : 0;
-            }
-            const int my_host = __shfl_sync(0xffffffffu, cur.z, (x - x0 + my_i) & 31);
-            const int my_row = __shfl_sync(0xffffffffu, cur.x, (x - x0 + my_i) & 31);
-            const int n_mine = (n_miss + kProducers - 1 - pw) / kProducers;   // chunks pw, pw+kProducers, ...
-            const int total_e = n_mine * 2 * vec;
-#pragma unroll 1
-            for (int e0 = 0; e0 < total_e; e0 += 32 * kHostBatch) {
-              uint4 v[kHostBatch];
-#pragma unroll
-              for (int u = 0; u < kHostBatch; ++u) {
-                const int eu = e0 + u * 32;                      // warp-uniform
-                const int kk = eu / (2 * vec), k = kk * kProducers + pw;
-                const int host = __shfl_sync(0xffffffffu, my_host, k & 31);
-                const int e = eu - kk * 2 * vec + lane;          // within the chunk: K then V
-                const uint4 *src = e >= vec ? p.vh + (int64_t)host * vec + (e - vec) : p.kh + (int64_t)host * vec + e;
-                v[u] = eu < total_e ? ldg_nc(src) : make_uint4(0, 0, 0, 0);
-              }
-#pragma unroll
-              for (int u = 0; u < kHostBatch; ++u) {
-                const int eu = e0 + u * 32;
-                const int kk = eu / (2 * vec), k = kk * kProducers + pw;
-                const int si = __shfl_sync(0xffffffffu, my_i, k & 31);
-                const int row = __shfl_sync(0xffffffffu, my_row, k & 31);
-                if (eu >= total_e) continue;
-                const int e = eu - kk * 2 * vec + lane;
-                const int kv = e >= vec, r = kv ? e - vec : e;
-                const int t = r >> 4, cg = r & 15;
-                const uint32_t dst = sbase + (kv ? 2 * kHalfBytes : 0) + swz(si * p.cs + t, cg);
-                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v[u].x), "r"(v[u].y),
-                             "r"(v[u].z), "r"(v[u].w) : "memory");
-                const int64_t mrow = -2 - row;                   // first staging row of the chunk
-                (kv ? p.vst : p.kst)[mrow * 16 + r] = v[u];
-              }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full0 + 8 * buf);
-          }
           first = false;
           ++s;
       }
