@@ -49,7 +49,7 @@ constexpr int kHalfBytes = kStageRows * 128;          // 64 rows x 64 bf16
 constexpr int kStageBytes = 4 * kHalfBytes;           // K lo, K hi, V lo, V hi
 constexpr int kMaxChunksPerStage = kStageRows / 16;   // cs >= 16
 constexpr int kQStride = 272;                         // bytes per staged query vector (256 + pad)
-constexpr int kHostBatch = 4;                         // 16-byte host loads in flight per lane (fused gather)
+constexpr int kCopyBatch = 8;                         // fused gather: 16-byte host loads in flight per copier lane
 
 // Tiles in flight per CTA: three for one m-tile (two CTAs share an SM's
 // 228 KiB), four for more (one CTA per SM, beside its staged queries).
@@ -247,12 +247,12 @@ __host__ __device__ constexpr int attn_max_regs(int threads, int ctas) {
              : (65536 / ((ctas * threads + 127) / 128 * 128)) / 8 * 8;
 }
 
-// Producer warps: warp 0 issues metadata and TMA; both share the host copies
-// of the fused gather.  Measured on the 16-request 32K layer with one CTA per
-// SM, the host link moved the most with about 16 loads of 16 bytes in flight
-// per producer lane pair: 2 warps x 8 (402 us per layer) beat 1 x 16 (407),
-// 2 x 16 (414), 4 x 16 (477) and 1 x 4 (499); with two CTAs per SM the same
-// depth per SM is 2 warps x 4 loads in each CTA (kHostBatch).
+// Producer warps: warp 0 issues the stages' metadata and every tile copy
+// (TMA); in the fused gather warp 1 copies the slice's missing chunks from
+// host memory into staging ahead of it.  Measured on the 16-request 32K
+// layer, the host link moved the most with about 16 KB of 16-byte loads in
+// flight per SM (2 x 8 per lane of one warp in each of two CTAs now; with
+// one CTA per SM, 2 warps x 8 beat 1 x 16, 2 x 16, 4 x 16 and 1 x 4).
 __host__ __device__ constexpr int producers_for(int) { return 2; }
 
 template <int MT, int WPM>
@@ -312,7 +312,6 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
         // lanes fence (GPU scope, then the generic -> async proxy fence, as
         // the issuing warp reads staging by TMA) and lane 0 publishes how
         // many of the slice's misses are in place (s_ready, release).
-        constexpr int kCopyBatch = 2 * kHostBatch;
         const int vec = p.cs * 16;   // uint4 per chunk, K or V
         int done = 0;                // misses of the slice copied so far
         for (int xb = lo; xb < hi; xb += 32) {
