@@ -253,7 +253,6 @@ def profiled_traffic(stage: str, workload: str):
     """DRAM bytes per launch of the stage's main kernel from the committed ncu
     summary, or None when there is none or the kernel source has changed since
     the counters were taken."""
-    import hashlib
     import re
     kernel, src = KERNEL_SOURCE[stage]
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
@@ -261,11 +260,22 @@ def profiled_traffic(stage: str, workload: str):
         return None
     text = open(path).read()
     t = re.search(r"^traffic_bytes_per_launch: (\d+)$", text, re.M)
-    h = re.search(r"^source_sha256_prefix: ([0-9a-f]+)$", text, re.M)
+    h = re.search(r"^code_sha256_prefix: ([0-9a-f]+)$", text, re.M)
     if not t or not h:
         return None
-    cur = hashlib.sha256(open(os.path.join(ROOT, "sparse_kv_offload_gb300", "csrc", src), "rb").read()).hexdigest()
+    cur = code_hash(os.path.join(ROOT, "sparse_kv_offload_gb300", "csrc", src))
     return int(t.group(1)) if cur.startswith(h.group(1)) else None
+
+
+def code_hash(path: str) -> str:
+    """sha256 of a CUDA source with its comments and whitespace removed: a
+    profile stays valid across comment edits, not across code changes."""
+    import hashlib
+    import re
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()
 
 
 def config_of(w, gather_mode, world=1, landmarks="mean"):

@@ -10,28 +10,30 @@
 //
 // Work split ("stream-K"): the unions of all (request, KV head) units are
 // laid end to end (chunk_off = exclusive prefix of the union sizes) and each
-// persistent CTA (two per SM for up to 16 query vectors per KV head, so that
-// one's producer issues copies while the other's does its per-stage
-// bookkeeping or waits on a fresh slice's tables) takes an equal contiguous
-// slice of that sequence.  A
-// slice covers a few units ("runs").  At the end of a run every consumer
-// warp writes its partial (running max, sum and accumulator of its rows) into
-// slot CTA + unit, sub-slot warp -- slices are ordered like the units, so no
-// two (CTA, unit) pairs share a slot and n_cta + units slots suffice -- and
-// the CTA counts itself in on the unit's arrival counter; the CTA that
-// arrives last merges all partials of the unit (stream-K fix-up), so the
-// outputs leave the same kernel.
+// persistent CTA takes an equal contiguous slice of that sequence (two CTAs
+// per SM for up to 16 query vectors per KV head, so that one's producer
+// issues copies while the other's does its per-stage bookkeeping or waits on
+// a fresh slice's tables).  A slice covers a few units ("runs").  At the end
+// of a run every consumer warp writes its partial (running max, sum and
+// accumulator of its rows) into slot CTA + unit, sub-slot warp -- slices are
+// ordered like the units, so no two (CTA, unit) pairs share a slot and
+// n_cta + units slots suffice -- and the CTA counts itself in on the unit's
+// arrival counter; the CTA that arrives last merges all partials of the unit
+// (stream-K fix-up), so the outputs leave the same kernel.
 //
-// Data movement: a producer warp streams 64-row tiles of K and V into shared
-// memory with 2-D TMA loads (cp.async.bulk.tensor, 128-byte swizzle, one box
-// per chunk and 64-column half) and each run's query vectors with bulk
-// copies, all completing on mbarriers; it runs ahead across run boundaries
-// with kStages tiles in flight.  Math: consumer warps own 16 query vectors
-// (one m16 tile) and 16- or 32-row slices of each tile; S = Q.K^T and O += P.V run on
-// the tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate) with an online
-// softmax in fp32; P is split into bf16 hi + lo parts so the PV product keeps
-// ~16 significant bits.  The work is HBM-bound: the MMAs only keep the
-// arithmetic under the memory time.
+// Data movement: the issuing producer warp streams 64-row tiles of K and V
+// into shared memory with 2-D TMA loads (cp.async.bulk.tensor, 128-byte
+// swizzle, one box per chunk and 64-column half) from the hot pool or the
+// staging buffer, and each run's query vectors with bulk copies, all
+// completing on mbarriers; it runs ahead across run boundaries with kStages
+// tiles in flight.  When the gather is fused in, the other producer warp
+// copies the slice's missing chunks from pinned host memory into staging
+// ahead of it.  Math: consumer warps own 16 query vectors (one m16 tile) and
+// 16- or 32-row slices of each tile; S = Q.K^T and O += P.V run on the tensor
+// cores (mma.sync m16n8k16 bf16, fp32 accumulate) with an online softmax in
+// fp32; P is split into bf16 hi + lo parts so the PV product keeps ~16
+// significant bits.  The work is bound by HBM or the host link: the MMAs only
+// keep the arithmetic under the memory time.
 #include <cuda.h>
 #include <mutex>
 #include <cudaTypedefs.h>
