@@ -14,12 +14,13 @@
 // per SM for up to 16 query vectors per KV head, so that one's producer
 // issues copies while the other's does its per-stage bookkeeping or waits on
 // a fresh slice's tables).  A slice covers a few units ("runs").  At the end
-// of a run every consumer warp writes its partial (running max, sum and
-// accumulator of its rows) into slot CTA + unit, sub-slot warp -- slices are
-// ordered like the units, so no two (CTA, unit) pairs share a slot and
-// n_cta + units slots suffice -- and the CTA counts itself in on the unit's
-// arrival counter; the CTA that arrives last merges all partials of the unit
-// (stream-K fix-up), so the outputs leave the same kernel.
+// of a run the consumer warps that share an m-tile merge their states in
+// shared memory, and the CTA writes one partial (running max, sum and
+// accumulator per query vector) into slot CTA + unit -- slices are ordered
+// like the units, so no two (CTA, unit) pairs share a slot and n_cta + units
+// slots suffice -- and counts itself in on the unit's arrival counter; the
+// CTA that arrives last merges the unit's partials (stream-K fix-up), so the
+// outputs leave the same kernel.  A unit inside one slice skips the count.
 //
 // Data movement: the issuing producer warp streams 64-row tiles of K and V
 // into shared memory with 2-D TMA loads (cp.async.bulk.tensor, 128-byte
@@ -52,6 +53,7 @@ constexpr int kStageBytes = 4 * kHalfBytes;           // K lo, K hi, V lo, V hi
 constexpr int kMaxChunksPerStage = kStageRows / 16;   // cs >= 16
 constexpr int kQStride = 272;                         // bytes per staged query vector (256 + pad)
 constexpr int kCopyBatch = 8;                         // fused gather: 16-byte host loads in flight per copier lane
+constexpr int kMergeFloats = 68;                       // a lane's run state: 64 accumulator elements, m0, m1, l0, l1
 
 // Tiles in flight per CTA: three for one m-tile (two CTAs share an SM's
 // 228 KiB), four for more (one CTA per SM, beside its staged queries).
@@ -153,14 +155,13 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
 // Run by the consumer warps of the CTA that finished the last part of `unit`
 // (every other CTA whose slice covered part of it has published its partials
 // before counting itself in).  Thread (query vector, 8 columns): merges the
-// partials of every consumer warp of CTAs c0..c1 in order, then, when the
+// partials of CTAs c0..c1 in order, then, when the
 // step's own rows are given, its tail rows: query j of the unit also attends
 // to the new rows of tokens 0..j (DualDecoder §5.2: the tokens of a step
 // follow one another along the sequence under a causal mask).
-template <int WPM>
 __device__ __forceinline__ void fixup_unit(const AttnParams &p, int unit, int c0, int c1, int n_threads, int ctid) {
   const int lane = threadIdx.x & 31;
-  const int n_parts = (c1 - c0 + 1) * WPM;
+  const int n_parts = c1 - c0 + 1;
   const int b = unit / p.Hkv, g = unit - b * p.Hkv;
   for (int w0 = (ctid >> 5) * 32; w0 < p.NQ * 16; w0 += n_threads) {   // warp-uniform
     const int w = w0 + lane;
@@ -177,7 +178,7 @@ __device__ __forceinline__ void fixup_unit(const AttnParams &p, int unit, int c0
       for (int t = 0; t < 4; ++t) {
         const int i = i0 + t;
         const bool ok = act && i < n_parts;
-        const int64_t k = (((int64_t)c0 + i / WPM + unit) * WPM + i % WPM) * p.NQ + qv;
+        const int64_t k = ((int64_t)c0 + i + unit) * p.NQ + qv;
         const float4 *src = reinterpret_cast<const float4 *>(p.part_o + k * 128 + cg * 8);
         ms[t] = ok ? p.part_ml[k * 2] : -INFINITY;
         ls[t] = ok ? p.part_ml[k * 2 + 1] : 0.f;
@@ -647,33 +648,81 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * buf);
-
     if (m_flags & kLast) {
-      // this warp's partial for the run: rows of its m-tile, straight from
-      // registers into sub-slot wq of slot CTA + unit (no cross-warp merge;
-      // the fix-up below merges all partials of the unit)
-      float lq0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
-      lq0 += __shfl_xor_sync(0xffffffffu, lq0, 2);
-      float lq1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
-      lq1 += __shfl_xor_sync(0xffffffffu, lq1, 2);
-      const int64_t pbase = (((int64_t)blockIdx.x + m_unit) * WPM + wq) * p.NQ;
-      if (qv0 < p.NQ) {
-        float *dst = p.part_o + (pbase + qv0) * 128 + 2 * tq;
+      // the run is over: first merge the WPM warps of each m-tile, which hold
+      // the same query rows over different key rows, into warp wq = 0.  Lane
+      // l of partner warps holds the same (row, column) elements, so each
+      // round is elementwise: warps [h, 2h) put their state into slots of the
+      // stage just consumed (released only after the last round), warps
+      // [0, h) rescale both to the larger maximum and add.
+      if constexpr (WPM > 1) {
+        static_assert(MT * (WPM / 2) * kMergeFloats * 32 * 4 <= kStageBytes, "merge slots exceed a stage");
+        float *xs = reinterpret_cast<float *>(stages + buf * kStageBytes);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) *reinterpret_cast<float2 *>(dst + i * 8) = make_float2(o[i][0], o[i][1]);
-        if (tq == 0) *reinterpret_cast<float2 *>(p.part_ml + (pbase + qv0) * 2) = make_float2(m0, lq0);
-      }
-      if (qv1 < p.NQ) {
-        float *dst = p.part_o + (pbase + qv1) * 128 + 2 * tq;
+        for (int h = WPM / 2; h >= 1; h /= 2) {
+          // every warp is done with the stage's tiles (first round) or with the last round's slots
+          asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
+          if (wq >= h && wq < 2 * h) {
+            float *d = xs + (mt * h + wq - h) * (kMergeFloats * 32) + lane;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) *reinterpret_cast<float2 *>(dst + i * 8) = make_float2(o[i][2], o[i][3]);
-        if (tq == 0) *reinterpret_cast<float2 *>(p.part_ml + (pbase + qv1) * 2) = make_float2(m1, lq1);
+            for (int i = 0; i < 16; ++i)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) d[(4 * i + e) * 32] = o[i][e];
+            d[64 * 32] = m0;
+            d[65 * 32] = m1;
+            d[66 * 32] = l0;
+            d[67 * 32] = l1;
+          }
+          asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
+          if (wq < h) {
+            const float *d = xs + (mt * h + wq) * (kMergeFloats * 32) + lane;
+            const float mb0 = d[64 * 32], mb1 = d[65 * 32];
+            const float M0 = fmaxf(m0, mb0), M1 = fmaxf(m1, mb1);
+            const float sa0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M0), sb0 = mb0 == -INFINITY ? 0.f : exp2f(mb0 - M0);
+            const float sa1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M1), sb1 = mb1 == -INFINITY ? 0.f : exp2f(mb1 - M1);
+            l0 = l0 * sa0 + d[66 * 32] * sb0;
+            l1 = l1 * sa1 + d[67 * 32] * sb1;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              o[i][0] = o[i][0] * sa0 + d[(4 * i + 0) * 32] * sb0;
+              o[i][1] = o[i][1] * sa0 + d[(4 * i + 1) * 32] * sb0;
+              o[i][2] = o[i][2] * sa1 + d[(4 * i + 2) * 32] * sb1;
+              o[i][3] = o[i][3] * sa1 + d[(4 * i + 3) * 32] * sb1;
+            }
+            m0 = M0;
+            m1 = M1;
+          }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");   // the slots are read
+        // order the slots' generic writes before the tile copies that refill the stage
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
-      // the run is over: the next stage starts a new one, which reloads the
-      // queries and restarts the accumulators, so none of them stays live
-      // through the fix-up below
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * buf);
+      // the CTA's partial for the run: rows of each m-tile, from warp wq = 0
+      // into slot CTA + unit
+      if (wq == 0) {
+        float lq0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+        lq0 += __shfl_xor_sync(0xffffffffu, lq0, 2);
+        float lq1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+        lq1 += __shfl_xor_sync(0xffffffffu, lq1, 2);
+        const int64_t pbase = ((int64_t)blockIdx.x + m_unit) * p.NQ;
+        if (qv0 < p.NQ) {
+          float *dst = p.part_o + (pbase + qv0) * 128 + 2 * tq;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) *reinterpret_cast<float2 *>(dst + i * 8) = make_float2(o[i][0], o[i][1]);
+          if (tq == 0) *reinterpret_cast<float2 *>(p.part_ml + (pbase + qv0) * 2) = make_float2(m0, lq0);
+        }
+        if (qv1 < p.NQ) {
+          float *dst = p.part_o + (pbase + qv1) * 128 + 2 * tq;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) *reinterpret_cast<float2 *>(dst + i * 8) = make_float2(o[i][2], o[i][3]);
+          if (tq == 0) *reinterpret_cast<float2 *>(p.part_ml + (pbase + qv1) * 2) = make_float2(m1, lq1);
+        }
+      }
+      // the next stage starts a new run, which reloads the queries and
+      // restarts the accumulators, so none of them stays live through the
+      // fix-up below
 #pragma unroll
       for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 #pragma unroll
@@ -681,16 +730,27 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
       m0 = m1 = -INFINITY;
       l0 = l1 = 0.f;
       // stream-K fix-up: CTAs c0..c1 hold parts of the unit; the one that
-      // counts itself in last merges them (partials published first)
+      // counts itself in last merges them.  The barrier orders the CTA's
+      // partial before thread 0's fence and count (a unit inside one CTA
+      // needs no count)
       const int c0 = m_uoff / per, c1 = (m_uoff + m_ucnt - 1) / per;
-      __threadfence();
       asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");   // consumer warps only
-      if (tid == 0) s_fix = atomicAdd(p.arrive + m_unit, 1) + 1 == c1 - c0 + 1;
+      if (tid == 0) {
+        if (c0 == c1) {
+          s_fix = 1;
+        } else {
+          __threadfence();
+          s_fix = atomicAdd(p.arrive + m_unit, 1) + 1 == c1 - c0 + 1;
+        }
+      }
       asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
       if (s_fix) {
         __threadfence();
-        fixup_unit<WPM>(p, m_unit, c0, c1, kConsumers * 32, tid);
+        fixup_unit(p, m_unit, c0, c1, kConsumers * 32, tid);
       }
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * buf);
     }
     if (m_flags & kEnd) break;
   }
@@ -827,13 +887,12 @@ AttnShape attn_shape(int NQ) {
 }
 
 // ctas_per_sm persistent CTAs per SM; partial slot CTA + unit for every
-// (CTA, unit) pair that shares chunks, one sub-slot per consumer warp of an m-tile.
+// (CTA, unit) pair that shares chunks.
 AttnPlan attn_plan(int units, int umax, int NQ, int sm_count) {
   AttnPlan pl;
   pl.n_cta = sm_count > 0 ? ctas_per_sm(attn_shape(NQ).mt) * sm_count : 1;
-  const int wpm = attn_shape(NQ).wpm;
-  pl.part_o_floats = ((int64_t)pl.n_cta + units) * wpm * NQ * 128;
-  pl.part_ml_floats = ((int64_t)pl.n_cta + units) * wpm * NQ * 2;
+  pl.part_o_floats = ((int64_t)pl.n_cta + units) * NQ * 128;
+  pl.part_ml_floats = ((int64_t)pl.n_cta + units) * NQ * 2;
   pl.flat_entries = (int64_t)units * umax;
   return pl;
 }
