@@ -216,8 +216,9 @@ dd_status dd_sparse_attn_decode(dd_ctx *ctx, const void *q, const void *Khot, co
  * that finds an error writes its dd_status code there (first error wins).
  * The split-K partials live in one fixed 16 MiB device array inside the
  * library, which every GPU that loads the library holds until the process
- * exits.  A shape whose partials ((2 * SM count + B*Hkv) slots * consumer
- * warps per 16 query vectors * NQ * 130 floats, with NQ = n_q*Hq/Hkv) and
+ * exits.  A shape whose partials ((CTAs + B*Hkv) slots * NQ * 130 floats,
+ * with NQ = n_q*Hq/Hkv and CTAs = 2 * SM count for NQ <= 16, else the SM
+ * count), chunk table (16 bytes per union chunk, B*Hkv*min(C, n_q*k)) and
  * chunk offsets do not fit is refused at once with DD_ERR_CAPACITY.  The first call on a device
  * looks up that array's device address (once per device); make that first
  * call before any stream capture.  Nothing in the array needs to start at
