@@ -57,3 +57,35 @@ def test_host_checks_answer_without_a_gpu(lib_path):
     if not torch.cuda.is_available():
         good = dd.Dims(1, 8, 2, 128, 1024, 16, 8, 2)
         assert lib.dd_create(ctypes.byref(good), ctypes.c_int64(4), ctypes.c_int64(0), ctypes.byref(h)) == dd.DD_ERR_CUDA
+
+
+# (B, Hq, Hkv, d, L, cs, k, n_q), max_misses, hot_slots: each breaks one rule dd_create checks on the host
+BAD_SHAPES = {
+    "negative_batch": ((-1, 8, 2, 128, 1024, 16, 8, 2), 4, 0),
+    "heads_not_grouped": ((1, 6, 4, 128, 1024, 16, 8, 2), 4, 0),
+    "no_kv_heads": ((1, 8, 0, 128, 1024, 16, 8, 2), 4, 0),
+    "chunk_size_8": ((1, 8, 2, 128, 1024, 8, 8, 2), 4, 0),
+    "chunk_size_128": ((1, 8, 2, 128, 1024, 128, 4, 2), 4, 0),
+    "ragged_context": ((1, 8, 2, 128, 1000, 16, 8, 2), 4, 0),
+    "k_zero": ((1, 8, 2, 128, 1024, 16, 0, 2), 4, 0),
+    "more_chunks_than_supported": ((1, 8, 2, 128, 16384 * 16 + 16, 16, 8, 2), 4, 0),
+    "no_query": ((1, 8, 2, 128, 1024, 16, 8, 0), 4, 0),
+    "nine_queries": ((1, 8, 2, 128, 1024, 16, 8, 9), 4, 0),
+    "65_query_vectors": ((1, 72, 8, 128, 1024, 16, 8, 8), 4, 0),     # n_q * G = 72
+    "negative_staging": ((1, 8, 2, 128, 1024, 16, 8, 2), -1, 0),
+    "staging_rows_overflow_int32": ((1, 8, 2, 128, 1024, 16, 8, 2), 1 << 27, 0),
+    "hot_rows_overflow_int32": ((1, 8, 2, 128, 1024, 16, 8, 2), 4, 1 << 27),
+}
+
+
+@pytest.mark.parametrize("case", sorted(BAD_SHAPES))
+def test_create_refuses_each_unsupported_shape(lib_path, case):
+    from sparse_kv_offload_gb300 import dd
+    dims, max_misses, hot_slots = BAD_SHAPES[case]
+    lib = ctypes.CDLL(lib_path)
+    lib.dd_create.restype = ctypes.c_int32
+    h = ctypes.c_void_p(1)
+    d = dd.Dims(*dims)
+    r = lib.dd_create(ctypes.byref(d), ctypes.c_int64(max_misses), ctypes.c_int64(hot_slots), ctypes.byref(h))
+    assert r == dd.DD_ERR_INVALID_ARG
+    assert h.value is None                     # no context handed out
