@@ -34,7 +34,11 @@
  *     dd_destroy.
  *   - Device pointers must be 16-byte aligned.  "Host" K/V pointers must be
  *     page-locked (cudaHostAlloc, cudaMallocHost or cudaHostRegister); the
- *     kernels read them in place over the host link.
+ *     kernels read them in place over the host link.  A context remembers the
+ *     device-side address of the last few host K/V pointers it was given, keyed
+ *     by the host address, so a host K/V buffer must stay allocated and pinned
+ *     while the context lives: a buffer freed or unregistered and another
+ *     placed at the same address needs a new context.
  *   - Every call is asynchronous on the stream it is given (NULL = the legacy
  *     default stream) and returns DD_ERR_INVALID_ARG / DD_ERR_CUDA at once for
  *     errors the host can see.  Errors found on the device (an index out of

@@ -371,14 +371,17 @@ static dd_status gather_memcpy(dd_ctx *c, const void *Kh, const void *Vh, const 
   DD_CUDA(cudaStreamSynchronize(s));
   const int64_t chunk_bytes = (int64_t)c->dims.cs * kD * 2;
   const int64_t n_total = (int64_t)c->units * c->C;
+  const int32_t *ml = c->h_miss + 1;
+  // the whole list is checked before the first copy is queued, so an error
+  // leaves nothing in flight on the copy stream
+  for (int64_t i = 0; i < M; ++i)
+    if (ml[i] < 0 || ml[i] >= n_total) return DD_ERR_DEVICE_CHECK;
   DD_CUDA(cudaEventRecord(c->ready, s));
   DD_CUDA(cudaStreamWaitEvent(c->copy_stream, c->ready, 0));
-  const int32_t *ml = c->h_miss + 1;
   int64_t m = 0;
   while (m < M) {
     int64_t run = 1;
     while (m + run < M && ml[m + run] == ml[m] + run) ++run;
-    if (ml[m] < 0 || ml[m] + run > n_total) return DD_ERR_DEVICE_CHECK;
     const int64_t src = (int64_t)ml[m] * chunk_bytes, dst = m * chunk_bytes;
     DD_CUDA(cudaMemcpyAsync(static_cast<uint8_t *>(Kst) + dst, static_cast<const uint8_t *>(Kh) + src,
                             (size_t)(run * chunk_bytes), cudaMemcpyDefault, c->copy_stream));

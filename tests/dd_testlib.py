@@ -107,3 +107,67 @@ def selection_rows_match(gpu_sel: np.ndarray, scores64: np.ndarray, oracle_sel: 
         assert must <= gset, f"row {r}: GPU dropped a chunk clearly above the k-th score"
         assert not (gset & never), f"row {r}: GPU kept a chunk clearly below the (k+1)-th score"
     return same.reshape(gpu_sel.shape[:-1])
+
+
+# ------------------------------------------------ a3-a5 on the GPU's selection
+
+# How often the step-level checks took the tie path: units whose GPU selection
+# differs from the oracle's inside the tie band, so that the oracle's union,
+# gather and attention were re-run on the GPU's own selection.  Printed in the
+# terminal summary of every run (tests/conftest.py).
+TIE_TALLY = {"checks": 0, "units": 0, "tie_units": 0, "tie_rows": 0}
+
+
+def follow_gpu_selection(gpu_sel, want, q, K, V, slot, Khot, Vhot, cs, scale=None, K_tail=None, V_tail=None):
+    """The oracle's a3-a5 driven by the GPU's own selection.
+
+    A selection may differ from the oracle's only inside the tie band (the
+    k-th and (k+1)-th scores within TIE_REL), and the caller has checked that
+    with ``selection_rows_match`` (or the coverage rule's own check).  The
+    union, the residency lookup, the miss ordinals, the staging layout and
+    the attention are exact functions of the selection, so they are compared
+    bit-exact (attention within the tolerances) against the oracle run on the
+    GPU's rows.  Where every row agrees this is the oracle's own step.
+    Returns (reference dict, tie-unit mask [B, Hkv])."""
+    gpu_sel = np.asarray(gpu_sel).reshape(want["sel"].shape)
+    diff_rows = np.any(gpu_sel != want["sel"], axis=-1)          # [B, n_q, Hkv]
+    tie_units = diff_rows.any(axis=1)                            # [B, Hkv]
+    TIE_TALLY["checks"] += 1
+    TIE_TALLY["units"] += int(tie_units.size)
+    TIE_TALLY["tie_units"] += int(tie_units.sum())
+    TIE_TALLY["tie_rows"] += int(diff_rows.sum())
+    if not tie_units.any():
+        return want, tie_units
+    ref = oracle.resolve_union(gpu_sel, slot)
+    Kst, Vst = oracle.gather_kv(K, V, ref["miss_list"], cs)
+    ref["out"] = oracle.sparse_attn_decode(q, Khot, Vhot, Kst, Vst, ref["attn_slot"], cs, scale, K_tail, V_tail)
+    ref.update(Kst=Kst, Vst=Vst, sel=gpu_sel, scores=want["scores"])
+    return ref, tie_units
+
+
+def check_layout(g: dict, ref: dict, B: int, Hkv: int, umax: int, Kst=None, Vst=None):
+    """Every unit's union, query mask, slots, the miss list, the per-entry slots
+    and (when the staging buffer is given) the staged bytes, bit-exact.
+    ``g`` holds the step's intermediates as numpy arrays; absent keys are skipped."""
+    M = int(g["miss_count"][0]) if "miss_count" in g else None
+    if M is not None:
+        assert M == ref["miss_count"], f"miss count {M} != {ref['miss_count']}"
+    if "union_cnt" in g:
+        cnt = g["union_cnt"].reshape(B, Hkv)
+        assert np.array_equal(cnt, ref["union_cnt"]), "union sizes differ"
+        for name in ("union_idx", "union_slot", "union_qmask"):
+            if name not in g:
+                continue
+            a = g[name].reshape(B, Hkv, umax)
+            for b in range(B):
+                for h in range(Hkv):
+                    n = cnt[b, h]
+                    assert np.array_equal(a[b, h, :n], ref[name][b, h, :n]), f"{name} of unit ({b},{h}) differs"
+    if "miss_list" in g and M is not None:
+        assert np.array_equal(g["miss_list"][:M], ref["miss_list"]), "miss lists differ"
+    if "attn_slot" in g:
+        assert np.array_equal(g["attn_slot"].reshape(ref["attn_slot"].shape), ref["attn_slot"]), "attn_slot differs"
+    if Kst is not None and M is not None:
+        gk = from_bf16(Kst).reshape(-1, ref["Kst"].shape[1], ref["Kst"].shape[2])[:M]
+        gv = from_bf16(Vst).reshape(-1, ref["Vst"].shape[1], ref["Vst"].shape[2])[:M]
+        assert np.array_equal(gk, ref["Kst"]) and np.array_equal(gv, ref["Vst"]), "staged bytes differ"

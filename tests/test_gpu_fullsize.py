@@ -162,9 +162,15 @@ def test_full_size_step_on_sampled_units(dd, w):
         got_s = scores[b, :, g].astype(np.float64)
         assert np.abs(got_s - s_u[0, :, 0]).max() <= 1e-4 * max(1.0, np.abs(s_u).max())
         sel_u = oracle.select_topk(s_u, w.k)
-        same = tl.selection_rows_match(sel[b:b + 1, :, g:g + 1], s_u, sel_u, w.k)
-        if not same.all():
-            continue   # a tie inside the band: the rest of this unit follows the GPU's own choice
+        gsel_u = sel[b:b + 1, :, g:g + 1]
+        tl.selection_rows_match(gsel_u, s_u, sel_u, w.k)
+        # the rest of the unit follows the GPU's own selection (the oracle's where they agree)
+        tie = not np.array_equal(gsel_u, sel_u)
+        tl.TIE_TALLY["checks"] += 1
+        tl.TIE_TALLY["units"] += 1
+        tl.TIE_TALLY["tie_units"] += int(tie)
+        tl.TIE_TALLY["tie_rows"] += int(np.any(gsel_u != sel_u, axis=-1).sum())
+        sel_u = np.ascontiguousarray(gsel_u)
         U = oracle.union_of_query_selections(sel_u, 0, 0)
         assert cnt[u] == len(U) and np.array_equal(uidx[u, :cnt[u]], U)
         want_qm = [sum(1 << j for j in range(w.n_q) if c in set(sel_u[0, j, 0].tolist())) for c in U]

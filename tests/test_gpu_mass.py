@@ -126,17 +126,13 @@ def test_step_with_coverage_budget_matches_oracle(dd, w, scale, gamma):
     same = check_mass_rows(sel, cnt.cpu().numpy().reshape(want["sel_cnt"].shape), want["scores"], w.k, gamma,
                            scale / G)
     assert len(set(want["sel_cnt"].reshape(-1).tolist())) > 1          # the budgets do vary
-    unit_ok = same.all(axis=1)
-    assert unit_ok.mean() > 0.8
-    if unit_ok.all():
-        M = int(buf.inter["miss_count"].item())
-        assert M == want["miss_count"]
-        assert np.array_equal(buf.inter["miss_list"].cpu().numpy()[:M], want["miss_list"])
-        assert np.array_equal(buf.inter["attn_slot"].cpu().numpy().reshape(want["attn_slot"].shape),
-                              want["attn_slot"])
-    out = buf.out.cpu().numpy().reshape(want["out"].shape)
-    mask = np.broadcast_to(unit_ok[:, None, :, None], (w.B, w.n_q, w.Hkv, G)).reshape(w.B, w.n_q, w.Hq)
-    tl.check_attention(out, want["out"], mask)
+    # union, miss list, slots, staging bytes and attention of every unit, on the GPU's own
+    # rows where a row's count or chunks took the gamma boundary or the tie band
+    g = {k: v.cpu().numpy() for k, v in buf.inter.items()}
+    ref, _ = tl.follow_gpu_selection(sel, want, x["q"], x["K"], x["V"], x["slot"], x["Khot"], x["Vhot"], w.cs,
+                                     scale=scale)
+    tl.check_layout(g, ref, w.B, w.Hkv, w.max_union, buf.Kst[0], buf.Vst[0])
+    tl.check_attention(buf.out.cpu().numpy().reshape(ref["out"].shape), ref["out"])
 
 
 def test_coverage_budget_rejects_bad_arguments(dd):

@@ -1,9 +1,9 @@
 """The allocation-free attention entry point, for callers that cannot
 allocate device memory (their device memory is owned by their own pool, or
 they may not call cudaMalloc between decode steps because it can synchronise
-the device): its output must equal the context-based dd_sparse_attn_decode's,
-within the attention tolerance of the other tests, on two calls in a row that
-share the library's fixed scratch array.
+the device): its output must equal the context-based dd_sparse_attn_decode's
+and the oracle's, within the attention tolerance of the other tests, on two
+calls in a row that share the library's fixed scratch array.
 
 Collected last on purpose, so that a run stopping at the first failure has
 already run every other test; it also passes alone in a fresh process."""
@@ -42,6 +42,10 @@ def test_noalloc_attention_equals_context_attention_twice(dd, w):
     import torch
     x = tl.host_inputs(w)
     sel = oracle.select_topk(oracle.score_landmarks(x["q"], x["lm"]), w.k)
+    # the oracle's attention on this selection, from its own union and gather
+    res = oracle.resolve_union(sel, x["slot"])
+    Ks, Vs = oracle.gather_kv(x["K"], x["V"], res["miss_list"], w.cs)
+    want_oracle = oracle.sparse_attn_decode(x["q"], x["Khot"], x["Vhot"], Ks, Vs, res["attn_slot"], w.cs)
     shape = dd.Shape(w.B, w.Hq, w.Hkv, w.d, w.L, w.cs, w.k, w.n_q)
     cap, hot = w.max_misses, x["Khot"].shape[0]
     nu = w.B * w.Hkv * w.max_union
@@ -65,6 +69,7 @@ def test_noalloc_attention_equals_context_attention_twice(dd, w):
         ctx.sparse_attn_decode(q, Khot, Vhot, Kst, Vst, union_slot, union_qmask, union_cnt, miss_count, ref)
         assert ctx.status() == 0
         want = ref.cpu().numpy().reshape(w.B, w.n_q, w.Hq, w.d)
+        tl.check_attention(want, want_oracle)
         for call in range(2):
             out = torch.full_like(ref, float("nan"))
             status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -72,13 +77,19 @@ def test_noalloc_attention_equals_context_attention_twice(dd, w):
                                           union_cnt, miss_count, out, status)
             torch.cuda.synchronize()
             assert int(status.item()) == 0, f"call {call}: device status {int(status.item())}"
-            tl.check_attention(out.cpu().numpy().reshape(want.shape), want)
+            got = out.cpu().numpy().reshape(want.shape)
+            tl.check_attention(got, want)
+            tl.check_attention(got, want_oracle)
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch(dd):
-    # the 32B-class, five-query layer at 64 requests needs about 19 MB of
-    # partials and chunk table on a 152-SM GPU: more than the 16 MiB array
-    big = dd.Dims(64, 64, 8, 128, 32768, 16, 128, 5)
+    # the 32B-class, five-query layer at 128 requests: its per-unit partials
+    # alone (units x 40 query vectors x 128 fp32) exceed the 16 MiB array,
+    # whatever the GPU's SM count adds for the per-CTA partials
+    B, Hq, Hkv, L, cs, k, n_q = 128, 64, 8, 32768, 16, 128, 5
+    per_unit_partials = B * Hkv * (n_q * Hq // Hkv) * 128 * 4
+    assert per_unit_partials > 16 << 20
+    big = dd.Dims(B, Hq, Hkv, 128, L, cs, k, n_q)
     lib = ctypes.CDLL(dd.LIB_PATH)
     fn = lib.dd_sparse_attn_decode_noalloc
     fn.restype = ctypes.c_int32
