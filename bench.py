@@ -1,20 +1,27 @@
 #!/usr/bin/env python3
 """Benchmark of one layer of the sparse-KV decode step on GB300.
 
-A step is one ``dd_step`` over one layer of the Llama-3-8B-shaped workload
-(16 requests, 32 query / 8 KV heads, head dim 128, 32K context in chunks of
-16, top-64 chunks per KV head, one real + one speculative query, all KV in
-pinned host memory): score -> top-k -> union/resolve -> gather -> attention.
-Four layers of independent data are cycled so that no step finds its inputs
-in L2.  Prints one JSON line (see the keys below).
+A step is one ``dd_step`` over one layer: score -> top-k -> union/resolve ->
+gather -> attention.  The default (headline) workload is the 32B-class GQA
+layer: 32 requests, 64 query / 8 KV heads, head dim 128, 32K context in
+chunks of 16, top-128 chunks per KV head, one real + four draft queries per
+request sharing one deduplicated gather, all KV in pinned host memory.  Four
+layers of independent data are cycled so that no step finds its inputs in L2.
+Prints one JSON line (see the keys below).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--mode zerocopy|memcpy] [--landmarks mean|minmax]
-                    [--pipeline [--prefetch-ctas N]]
+                    [--workload NAME] [--mode auto|zerocopy|kernel|memcpy] [--landmarks mean|minmax]
+                    [--residency workload|none|all] [--pipeline [--prefetch-ctas N] [--layer-gap-us T]]
 
-``--impl reference`` times the CPU oracle instead (a bounded sample of the
-same workload per step).  The default line also reports the oracle on one
-core and on every host core (independent units, one process per core).
+At N=1 the headline line carries ``per_config``: every other workload (with
+its own residency) and the fully resident lines of the Llama-3-8B-shaped and
+32B-class layers, each measured the same way in a child process run before
+the headline (so that one process holds its pinned host KV at a time).  It
+also carries ``landmark_build_us``, the landmark build (prefill) timed on its
+own from pinned host memory and from HBM.
+``--impl reference`` times the CPU oracle instead, on whole steps of the same
+workload spread over the host cores.  The default line also reports the oracle
+on one core (a bounded sample) and on every host core.
 ``--pipeline`` runs several layers with drifting queries: predictive prefetch
 on a low-priority stream, the same steps serialized, and the same steps with
 the capped LRU residency update.  Under torchrun every rank runs its own independent
@@ -42,7 +49,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from sparse_kv_offload_gb300 import synth                      # noqa: E402
-from sparse_kv_offload_gb300.workloads import BY_NAME, LLAMA8B_32K  # noqa: E402
+from sparse_kv_offload_gb300.workloads import (BY_NAME, GQA32B_5Q, LLAMA8B_32K, QWEN8B_128K,  # noqa: E402
+                                               STRESS_512K, TINY)
 
 METRIC = "sparse decode steps/s per layer; HBM GB/s and host-gather GB/s vs roofline"
 UNIT = "steps/s"
@@ -60,21 +68,49 @@ def peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    """nvidia-smi sampled every 50 ms for the whole GPU arm; each sample keeps
+    the driver's timestamp, so that the clocks can be summarised over the GPU
+    work and over each timed block (``window``)."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, device_index: int):
         self.proc = None
-        self.lines = []
+        self.windows = []            # (name, t0, t1) in time.time() seconds
         try:
             import torch
             uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", uuid, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+
+    def window(self, name, t0, t1):
+        self.windows.append((name, t0, t1))
+
+    @staticmethod
+    def _parse(out):
+        import datetime
+        rows = []
+        for r in out.strip().splitlines():
+            f = [x.strip() for x in r.split(",")]
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[1]), float(f[2]),
+                             {n for n, v in zip(ClockSampler.REASONS, f[4:8]) if v.lower() == "active"}))
+            except (ValueError, IndexError):
+                continue
+        return rows
+
+    @staticmethod
+    def _summary(rows):
+        if not rows:
+            return {"samples": 0}
+        return {"sm_mhz": float(np.median([r[1] for r in rows])), "sm_max_mhz": max(r[2] for r in rows),
+                "reasons": sorted(set().union(*[r[3] for r in rows])), "samples": len(rows)}
 
     def stop(self):
         if not self.proc:
@@ -85,22 +121,18 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
-        sm, mx, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for r in rows:
-            try:
-                sm.append(float(r[0]))
-                mx.append(float(r[1]))
-                for n, v in zip(names, r[3:7]):
-                    if v.strip().lower() == "active":
-                        reasons.add(n)
-            except (ValueError, IndexError):
-                continue
-        if not sm:
+        rows = self._parse(out)
+        if not rows:
             return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        # samples inside the windows of GPU work (timed and untimed blocks); all samples when none fell inside
+        inside = [r for r in rows if any(t0 - 0.025 <= r[0] <= t1 + 0.025 for _, t0, t1 in self.windows)]
+        res = self._summary(inside or rows)
+        res["scope"] = ("samples taken while the GPU arm's kernels ran (every timed and untimed block)" if inside
+                        else "every sample of the GPU arm")
+        res["samples_all"] = len(rows)
+        res["blocks"] = {name: self._summary([r for r in rows if t0 - 0.025 <= r[0] <= t1 + 0.025])
+                         for name, t0, t1 in self.windows}
+        return res
 
 
 # ------------------------------------------------------------------ distributed
@@ -218,26 +250,56 @@ def cpu_baseline_all_cores(w, budget_s=8.0, landmarks="mean"):
                       f"{budget_s:.0f} s; steps/s = sum of units/s / {w.units}"}
 
 
+_REF_SAMPLE = None
+
+
+def _ref_init(wname, landmarks, heads_q):
+    """A reference-arm process: the inputs of one of request 0's KV heads."""
+    global _REF_SAMPLE
+    _REF_SAMPLE = OracleSample(BY_NAME[wname], landmarks, heads=[heads_q.get()])
+    _REF_SAMPLE.run_units(1)
+
+
+def _ref_run(n):
+    return _REF_SAMPLE.run_units(n)
+
+
 def run_reference(args, world, rank):
+    """The oracle on whole steps: each step evaluates all B*Hkv (request, KV
+    head) units, spread over one process per host core (units are independent
+    through every stage, so the numerics are the oracle's own)."""
     if rank != 0:
         return 0
+    import multiprocessing as mp
     w = BY_NAME[args.workload]
-    s = OracleSample(w, args.landmarks)
-    t_unit = s.run_units(1)
-    # size each step's sample so that the whole run stays near two minutes
-    per_step = min(2.0, 120.0 / (args.steps + args.warmup))
-    n = int(max(1, min(w.Hkv, per_step // max(t_unit, 1e-6))))
-    for _ in range(args.warmup):
-        s.run_units(n)
-    spent = sum(s.run_units(n) for _ in range(args.steps))
-    value = args.steps * n / (w.units * spent)
+    n_proc = max(1, min(os.cpu_count() or 1, w.units))
+    ctx = mp.get_context("spawn")
+    heads_q = ctx.Queue()
+    for i in range(n_proc):
+        heads_q.put(i % w.Hkv)
+    per_task = max(1, w.units // (4 * n_proc))
+    tasks = [per_task] * (w.units // per_task) + ([w.units % per_task] if w.units % per_task else [])
+    with ctx.Pool(n_proc, initializer=_ref_init, initargs=(w.name, args.landmarks, heads_q)) as pool:
+        for _ in range(args.warmup):
+            pool.map(_ref_run, tasks, chunksize=1)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            pool.map(_ref_run, tasks, chunksize=1)
+        spent = time.perf_counter() - t0
+    value = args.steps / spent
+    sample = (f"whole steps: each step runs the oracle (numpy fp64) on all {w.units} (request, KV head) units of "
+              f"the workload, {per_task} units per task over {n_proc} processes (one per host core); each process "
+              f"holds the host inputs of one of request 0's {w.Hkv} KV heads, and every unit of a step is "
+              f"evaluated on those inputs (units have the same shape; generating all {w.B} requests' host KV in "
+              f"numpy would take minutes)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * spent / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, "oracle", landmarks=args.landmarks),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": s.describe(n)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": n_proc, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": spent,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -375,12 +437,52 @@ def host_link_peaks(dd, shape):
     return best, zc
 
 
-def run_ours(args, world, rank, local):
+def landmark_build_times(dd, shape, w, L_, lm_kind, sampler, reps=5):
+    """The landmark build (prefill, off the decode path) timed on its own, from
+    the pinned host K (read over the host link) and from a device copy of the
+    same K (read from HBM): median of ``reps`` launches after two warm-ups."""
+    import torch
+    minmax = lm_kind == dd.LM_MINMAX
+    vec = 2 if minmax else 1
+    lm = torch.empty(w.B * w.Hkv * w.C * vec * w.d, dtype=torch.bfloat16, device="cuda")
+    k_bytes = w.B * w.Hkv * w.L * w.d * 2
+    lm_bytes = lm.numel() * 2
+    res = {"bytes_read": k_bytes, "bytes_written": lm_bytes,
+           "kernel": "k_build_minmax" if minmax else "k_build_landmarks"}
+    with dd.Context(shape, max_misses=1) as c:
+        build = c.build_landmarks_minmax if minmax else c.build_landmarks
+        for src_name, K in (("pinned_host", L_.Kh), ("device", None)):
+            if K is None:
+                K = L_.Kh.to("cuda")
+            for _ in range(2):
+                build(K, lm)
+            torch.cuda.synchronize()
+            t_wall = time.time()
+            times = []
+            for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                build(K, lm)
+                b.record()
+                b.synchronize()
+                times.append(a.elapsed_time(b) * 1e3)
+            if sampler:
+                sampler.window(f"landmark build ({src_name})", t_wall, time.time())
+            us = float(np.median(times))
+            res[src_name] = {"us": us, "gbs": (k_bytes + lm_bytes) / (us * 1e-6) / 1e9}
+            del K
+        if c.status() != 0:
+            raise RuntimeError("device status after the landmark builds is not OK")
+    return res
+
+
+def run_ours(args, world, rank, local, per_config=None):
     import torch
     torch.cuda.set_device(local)
     from sparse_kv_offload_gb300 import build
     build.build()
     from sparse_kv_offload_gb300 import dd
+    sampler = ClockSampler(local) if rank == 0 else None
     w = BY_NAME[args.workload]
     shape = dd.Shape(w.B, w.Hq, w.Hkv, w.d, w.L, w.cs, w.k, w.n_q)
     mode = {"memcpy": dd.GATHER_MEMCPY, "kernel": dd.GATHER_KERNEL, "auto": dd.GATHER_AUTO}.get(args.mode,
@@ -504,7 +606,6 @@ def run_ours(args, world, rank, local):
                  intermediates=inter, stage_events=events, lm_kind=lm_kind, mass_gamma=args.mass_gamma,
                  softmax_scale=args.softmax_scale, trace=trace)
 
-    sampler = ClockSampler(local) if rank == 0 else None
     for i in range(args.warmup):
         step(i, i)
     torch.cuda.synchronize()
@@ -512,6 +613,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     launches0 = ctx.launch_count()
     t0 = time.perf_counter()
+    t0_wall = time.time()
     t_start.record()
     for i in range(K):
         marks = [ev[i][m] if m in dom_marks else None for m in range(6)]
@@ -519,10 +621,11 @@ def run_ours(args, world, rank, local):
     t_end.record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    if sampler:
+        sampler.window("timed steps", t0_wall, time.time())
     barrier(world)
     torch.cuda.synchronize()
     launches = ctx.launch_count() - launches0
-    clocks = sampler.stop() if sampler else None
     st = ctx.status()
     if st != 0:
         raise RuntimeError(f"device status after the timed steps: {dd.status_str(st)}")
@@ -532,11 +635,14 @@ def run_ours(args, world, rank, local):
     names = ("score", "topk", "resolve", "gather", "attention")
     dom_timed = names[dom_marks[0]]
     dom_ms_timed = float(np.mean([ev[i][dom_marks[0]].elapsed_time(ev[i][dom_marks[1]]) for i in range(K)]))
+    t1_wall = time.time()
     for i in range(n_stage):
         step(i, args.warmup + K + i, ev_stage[i])
     for i in range(n_trace):
         step(i, args.warmup + K + n_stage + i, trace=trace[i])
     torch.cuda.synchronize()
+    if sampler:
+        sampler.window("stage-breakdown and traced steps", t1_wall, time.time())
     if ctx.status() != 0:
         raise RuntimeError("device status after the stage-breakdown steps is not OK")
     stage_ms = {n: float(np.mean([ev_stage[i][s].elapsed_time(ev_stage[i][s + 1]) for i in range(n_stage)]))
@@ -645,11 +751,14 @@ def run_ours(args, world, rank, local):
             for _ in range(3):
                 cg.replay()
             torch.cuda.synchronize()
+            tg_wall = time.time()
             ga.record(gs)
             for _ in range(reps):
                 cg.replay()
             gb.record(gs)
         torch.cuda.synchronize()
+        if sampler:
+            sampler.window("graph replay", tg_wall, time.time())
         if ctx.status() != 0:
             raise RuntimeError("device status after the graph replays is not OK")
         g_s = max_over_ranks(ga.elapsed_time(gb) * 1e-3, world)
@@ -668,6 +777,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    te_wall = time.time()
     a.record()
     for i in range(K):
         layer = args.warmup + i
@@ -677,8 +787,12 @@ def run_ours(args, world, rank, local):
         out_host.copy_(out, non_blocking=True)
     b.record()
     torch.cuda.synchronize()
+    if sampler:
+        sampler.window("e2e steps", te_wall, time.time())
     e2e_s = max_over_ranks(a.elapsed_time(b) * 1e-3, world)
     barrier(world)
+    lm_times = landmark_build_times(dd, shape, w, layers[0], lm_kind, sampler) if args.landmark_timing else None
+    clocks = sampler.stop() if sampler else None
 
     cpu = cpu_baseline(w, landmarks=args.landmarks) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     cpu_all = (cpu_baseline_all_cores(w, landmarks=args.landmarks)
@@ -725,13 +839,116 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "cpu_baseline_all_cores": cpu_all,
     }
+    if lm_times:
+        hbm_peak_, _ = peaks()
+        lm_times["pinned_host"]["frac_of_host_link"] = lm_times["pinned_host"]["gbs"] / link_memcpy
+        lm_times["device"]["frac_of_hbm"] = lm_times["device"]["gbs"] / hbm_peak_
+        line["landmark_build_us"] = lm_times
+    if per_config is not None:
+        line["per_config"] = per_config
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ------------------------------------------------------------------ the other workloads, one process each
+PER_CONFIG = (
+    (TINY.name, "workload"), (LLAMA8B_32K.name, "workload"), (QWEN8B_128K.name, "workload"),
+    (STRESS_512K.name, "workload"), (LLAMA8B_32K.name, "all"), (GQA32B_5Q.name, "all"),
+)
+
+
+def _compact(line):
+    """The figures of one workload's line that go into the headline's per_config."""
+    keep = ("value", "ms_per_step", "steps", "warmup", "graph_replay", "e2e", "roofline", "per_step",
+            "in_step_us", "stages_us", "gpu_launches", "clocks", "host_link_peaks_gbs")
+    out = {"workload": line["config"]["workload"], "residency": line["config"]["residency"],
+           "gather": line["config"]["gather"]}
+    out.update({k: line.get(k) for k in keep})
+    rh = line.get("roofline_hbm") or {}
+    out["score"] = {"achieved_gbs": rh.get("achieved"), "frac": rh.get("frac"),
+                    "in_step": rh.get("in_step")}
+    if "score_plus_attention" in rh:
+        out["score_plus_attention"] = rh["score_plus_attention"]
+    if isinstance(out.get("clocks"), dict):
+        out["clocks"] = {k: out["clocks"].get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")}
+    return out
+
+
+def run_per_config(args):
+    """Every other workload (and the fully resident lines) through this same
+    script, one child process each (each frees its pinned host KV at exit):
+    warm-up, timed steps, stage breakdown, graph replay and e2e as in the
+    headline line, no CPU baseline."""
+    steps = max(20, min(args.steps, 300))
+    out = []
+    for name, residency in PER_CONFIG:
+        if name == args.workload and residency == args.residency:
+            continue
+        cmd = [sys.executable, os.path.abspath(__file__), "--workload", name, "--residency", residency,
+               "--steps", str(steps), "--warmup", str(args.warmup), "--no-cpu-baseline", "--no-per-config",
+               "--mode", args.mode]
+        t0 = time.perf_counter()
+        try:
+            r = subprocess.run(cmd, capture_output=True, text=True, timeout=900)
+            lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+            if r.returncode != 0 or not lines:
+                out.append({"workload": name, "residency": residency, "error":
+                            f"rc {r.returncode}: " + (r.stderr.strip().splitlines() or ["no output"])[-1][-300:]})
+                continue
+            item = _compact(json.loads(lines[-1]))
+        except subprocess.TimeoutExpired:
+            item = {"workload": name, "residency": residency, "error": "timed out after 900 s"}
+        item["child_wall_s"] = time.perf_counter() - t0
+        out.append(item)
+    return out
 
 
 # ------------------------------------------------------------------ pipelined decode (predictive prefetch)
 DRIFT_T, SIGMA_DRIFT, SIGMA_SPEC = 8, 0.3, 0.1
 RES_SLOTS_PER_K, RES_CAP_PER_K = 4, 4     # hot pool of 4k slots per (b,g); admit up to k/2 per step
+
+
+class LayerGap:
+    """Stand-in for the rest of a layer (projections and MLP) between two
+    layers' sparse steps: one bf16 GEMM of the step's tokens against a weight
+    matrix streamed from HBM, sized so that it takes about ``us``
+    microseconds (a decode GEMM with few rows is bound by the weight reads)."""
+
+    def __init__(self, us, tokens, d_model=4096):
+        import torch
+        self.us = us
+        self.x = None
+        if us <= 0:
+            self.measured_us = 0.0
+            return
+        self.x = torch.randn(tokens, d_model, dtype=torch.bfloat16, device="cuda")
+        n = max(256, int(us * 1e-6 * 6.0e12 / (2 * d_model)) // 256 * 256)
+        for _ in range(3):                      # calibrate the width against the measured time
+            self.W = torch.randn(d_model, n, dtype=torch.bfloat16, device="cuda")
+            t = self._time()
+            n = max(256, int(n * us / t) // 256 * 256)
+        self.W = torch.randn(d_model, n, dtype=torch.bfloat16, device="cuda")
+        self.measured_us = self._time()
+        self.shape = (tokens, d_model, n)
+
+    def _time(self, reps=20):
+        import torch
+        for _ in range(3):
+            self.run()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            self.run()
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b) * 1e3 / reps
+
+    def run(self, stream=None):
+        import torch
+        if self.x is None:
+            return
+        with torch.cuda.stream(stream or torch.cuda.current_stream()):
+            torch.matmul(self.x, self.W)
 
 
 def run_pipeline(args, world, rank, local):
@@ -786,6 +1003,8 @@ def run_pipeline(args, world, rank, local):
     ev_pf = [torch.cuda.Event() for _ in range(N)]
     torch.cuda.synchronize()
     link_memcpy, _ = host_link_peaks(dd, shape)
+    gap = LayerGap(args.layer_gap_us, w.B * w.n_q)
+    pf_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(K * N)]
 
     def q_of(i, l):
         return qs[l][i % T]
@@ -798,8 +1017,13 @@ def run_pipeline(args, world, rank, local):
             count = pfc[n_rec[0]:n_rec[0] + 1]
             n_rec[0] += 1
         L_ = layers[t]
+        timed = count is not None
+        if timed:
+            pf_ev[n_rec[0] - 1][0].record(lo)
         ctx_lo.prefetch_kv(sel_store[t], w.n_q - 1, L_.Kh, L_.Vh, Kpf[p], Vpf[p], pf_map[p], pf_count=count,
                            ctas_per_sm=args.prefetch_ctas, stream=lo, sel_rows=w.n_q, first_row=1)
+        if timed:
+            pf_ev[n_rec[0] - 1][1].record(lo)
         ev_pf[t].record(lo)
 
     def pipelined(i, rec=None):
@@ -815,12 +1039,14 @@ def run_pipeline(args, world, rank, local):
             t = (l + 2) % N
             lo.wait_event(ev_step[l])
             prefetch(t, p, record=rec is not None)
+            gap.run(hi)
 
-    def serialized(i):
+    def serialized(i, events=None):
         for l in range(N):
             L_ = layers[l]
             ctx_hi.step(i * N + l, q_of(i, l), L_.lm, L_.Kh, L_.Vh, none_res, Kpf[0], Vpf[0], Kurg, Vurg, out,
-                        stream=hi)
+                        stream=hi, stage_events=None if events is None else events[l])
+            gap.run(hi)
 
     # prime: one step of every layer without prediction fills the selections, then the
     # prefetches of layers 0 and 1 for the first pipelined step
@@ -862,8 +1088,74 @@ def run_pipeline(args, world, rank, local):
     torch.cuda.synchronize()
     t_ser = a2.elapsed_time(b2) * 1e-3
     assert ctx_hi.status() == 0
+
+    # OasisKV eq. (4) terms, each on its own: T_pred = the step's scoring + selection
+    # (the predicted rows are the speculative rows of the step's own selection),
+    # T_select = resolving the predicted rows into a transfer plan (union, ordinals),
+    # T_transfer = copying the planned chunks from pinned host memory
+    n_ev = min(K, 20)
+    st_ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(N)] for _ in range(n_ev)]
+    for row in st_ev:
+        for evs in row:
+            for e in evs:
+                e.record()                  # creates the event handles the step records into
+    with torch.cuda.stream(hi):
+        for i in range(n_ev):
+            serialized(args.warmup + i, st_ev[i])
+    torch.cuda.synchronize()
+    t_pred = float(np.mean([st_ev[i][l][0].elapsed_time(st_ev[i][l][2]) for i in range(n_ev) for l in range(N)]))
+    shape_p = dd.Shape(w.B, w.Hq, w.Hkv, w.d, w.L, w.cs, w.k, w.n_q - 1)
+    t_sel, t_xfer = [], []
+    with dd.Context(shape_p, max_misses=cap) as ctx_p:
+        ui = torch.empty(units * shape_p.umax, dtype=torch.int32, device="cuda")
+        us_ = torch.empty_like(ui)
+        uq = torch.empty(units * shape_p.umax, dtype=torch.uint8, device="cuda")
+        uc = torch.empty(units, dtype=torch.int32, device="cuda")
+        ml = torch.empty(cap, dtype=torch.int32, device="cuda")
+        mc = torch.empty(1, dtype=torch.int32, device="cuda")
+        for r in range(3 + n_ev):
+            for l in range(N):
+                pred = sel_store[l].view(w.B, w.n_q, w.Hkv, w.k)[:, 1:].contiguous()
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e[0].record()
+                ctx_p.resolve_union(pred, none_res, ui, us_, uq, uc, ml, mc)
+                e[1].record()
+                ctx_p.gather_kv(layers[l].Kh, layers[l].Vh, ml, mc, Kpf[0], Vpf[0], mode=dd.GATHER_KERNEL)
+                e[2].record()
+                torch.cuda.synchronize()
+                if r >= 3:
+                    t_sel.append(e[0].elapsed_time(e[1]))
+                    t_xfer.append(e[1].elapsed_time(e[2]))
+        assert ctx_p.status() == 0
     ctx_hi.close()
     ctx_lo.close()
+
+    # lower bound: the same steps (and gaps) with every chunk of every layer resident in an HBM pool
+    ctx_a = dd.Context(shape, max_misses=cap, hot_slots=units * w.C)
+    ident = torch.arange(units * w.C, dtype=torch.int32, device="cuda")
+    pools_all = [(L_.Kh.to("cuda"), L_.Vh.to("cuda")) for L_ in layers]
+
+    def resident(i):
+        for l in range(N):
+            L_ = layers[l]
+            ctx_a.step(i * N + l, q_of(i, l), L_.lm, L_.Kh, L_.Vh, ident, pools_all[l][0], pools_all[l][1], Kurg,
+                       Vurg, out, stream=hi)
+            gap.run(hi)
+
+    with torch.cuda.stream(hi):
+        for i in range(args.warmup):
+            resident(i)
+    torch.cuda.synchronize()
+    a4, b4 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a4.record(hi)
+    for i in range(K):
+        resident(args.warmup + i)
+    b4.record(hi)
+    torch.cuda.synchronize()
+    t_all = a4.elapsed_time(b4) * 1e-3
+    assert ctx_a.status() == 0
+    ctx_a.close()
+    del pools_all
 
     # the same drifting steps with a per-(b,g) hot pool kept by the capped LRU
     # residency update after every step (OasisKV delta selection)
@@ -893,6 +1185,7 @@ def run_pipeline(args, world, rank, local):
             ctx_r.update_residency(i + 1, cap_r, S, Kurg[g_ & 1], Vurg[g_ & 1], P_["rs"], P_["sc"], P_["lu"],
                                    P_["K"], P_["V"], union_idx=inter["union_idx"], union_slot=inter["union_slot"],
                                    union_cnt=inter["union_cnt"], miss_count=inter["miss_count"], stream=hi)
+            gap.run(hi)
 
     for i in range(max(args.warmup, 2 * T)):       # fill the pools
         with_residency(i)
@@ -928,7 +1221,28 @@ def run_pipeline(args, world, rank, local):
                            "prediction_hit_rate": 1.0 - M / U if U else None,
                            "urgent_bytes": M * chunk_b, "prefetch_bytes": P * chunk_b,
                            "host_link_gbs": (M + P) * chunk_b * steps / t_pipe / 1e9},
+        "layer_gap": {"requested_us": args.layer_gap_us, "measured_us": gap.measured_us,
+                      "what": ("between layers, a bf16 GEMM of the step's tokens against a weight matrix read from "
+                               f"HBM (shape {getattr(gap, 'shape', None)}), standing in for projections and MLP")
+                      if args.layer_gap_us > 0 else "none: the sparse path alone, layer after layer"},
         "serialized_same_steps": {"value": steps / t_ser, "unit": UNIT, "ms_per_step": 1e3 * t_ser / steps},
+        "all_resident_same_steps": {"value": steps / t_all, "unit": UNIT, "ms_per_step": 1e3 * t_all / steps,
+                                    "note": "every chunk of every layer in an HBM pool: no host transfer at all"},
+        "exposed_gather_us_per_layer_step": {
+            "pipelined": 1e6 * (t_pipe - t_all) / steps, "serialized": 1e6 * (t_ser - t_all) / steps,
+            "note": "time per layer-step above the same steps with every chunk resident (gaps included in both)"},
+        "eq4": {"T_pred_us": 1e3 * t_pred, "T_select_us": 1e3 * float(np.mean(t_sel)),
+                "T_transfer_us": 1e3 * float(np.mean(t_xfer)),
+                "T_pipe_us": 1e3 * max(t_pred, float(np.mean(t_sel)), float(np.mean(t_xfer))),
+                "delta_prefetch_us": 1e6 * t_pipe / steps,
+                "holds": max(t_pred, float(np.mean(t_sel)), float(np.mean(t_xfer))) * 1e-3 <= t_pipe / steps,
+                "prefetch_in_pipeline_us": float(np.mean([e0.elapsed_time(e1) for e0, e1 in pf_ev[:n_rec[0]]]))
+                * 1e3 if n_rec[0] else None,
+                "note": "OasisKV eq. (4): T_pipe = max(T_pred, T_select, T_transfer) <= Delta_prefetch = T_step / "
+                        "N_layer. T_pred: the step's scoring + selection (its speculative rows are the prediction); "
+                        "T_select: union and ordinals of the predicted rows (k_union + k_assign); T_transfer: the "
+                        "zero-copy gather of the planned chunks (k_gather); each timed on its own, mean over the "
+                        "layers; Delta_prefetch: the pipelined time per layer-step"},
         "residency_same_steps": {"value": steps / t_res, "unit": UNIT, "ms_per_step": 1e3 * t_res / steps,
                                  "slots_per_unit": S, "cap_per_unit_and_step": cap_r,
                                  "missing_chunks_per_layer_step": M_res,
@@ -948,7 +1262,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default=LLAMA8B_32K.name, choices=sorted(BY_NAME))
+    ap.add_argument("--workload", default=GQA32B_5Q.name, choices=sorted(BY_NAME))
     ap.add_argument("--mode", choices=("auto", "zerocopy", "kernel", "memcpy"), default="auto",
                     help="gather: auto (the library's choice: the separate gather kernel when there is a hot pool, "
                          "else fused into the attention), zerocopy (fused), kernel (separate), memcpy")
@@ -961,7 +1275,13 @@ def main():
                          "uniform share of all chunks in an HBM pool); none: every chunk read from host memory; "
                          "all: the whole KV also in an HBM pool (no misses; attention bound by HBM)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other workloads' lines (per_config; run only at N=1 with the default workload)")
+    ap.add_argument("--no-landmark-timing", action="store_true", help="skip the separate landmark-build timing")
     ap.add_argument("--prefetch-ctas", type=int, default=2, help="pipelined mode: prefetch copy CTAs per SM")
+    ap.add_argument("--layer-gap-us", type=float, default=0.0,
+                    help="pipelined mode: microseconds of other per-layer work (a weight-streaming GEMM) between "
+                         "two layers' sparse steps")
     ap.add_argument("--pipeline", action="store_true",
                     help="decode steps over several layers with drifting queries and predictive prefetch")
     ap.add_argument("--layers", type=int, default=N_LAYERS,
@@ -978,7 +1298,12 @@ def main():
             return run_reference(args, world, rank)
         if args.pipeline:
             return run_pipeline(args, world, rank, local)
-        return run_ours(args, world, rank, local)
+        args.landmark_timing = not args.no_landmark_timing and not args.no_per_config
+        per_config = None
+        if world == 1 and not args.no_per_config:
+            # the other workloads first, in child processes, while this process holds no GPU memory
+            per_config = run_per_config(args)
+        return run_ours(args, world, rank, local, per_config)
     finally:
         if world > 1:
             import torch.distributed as dist

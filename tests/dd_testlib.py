@@ -171,3 +171,40 @@ def check_layout(g: dict, ref: dict, B: int, Hkv: int, umax: int, Kst=None, Vst=
         gk = from_bf16(Kst).reshape(-1, ref["Kst"].shape[1], ref["Kst"].shape[2])[:M]
         gv = from_bf16(Vst).reshape(-1, ref["Vst"].shape[1], ref["Vst"].shape[2])[:M]
         assert np.array_equal(gk, ref["Kst"]) and np.array_equal(gv, ref["Vst"]), "staged bytes differ"
+
+
+def _bf16_bits(v: float) -> int:
+    return int(synth.f32_to_bf16(np.array([v], np.float32))[0])
+
+
+def tie_band_inputs():
+    """A small step whose selections tie in fp32 but not in fp64.
+
+    Per (request, KV head): k-1 chunks score far above the rest, and two
+    chunks B < A (by index) come next.  The real query is 1 in coordinates 0
+    and 1 (every head), so its score is G*2^16 + G*2^-9 for A and G*2^16 for
+    B; 2^-7 is below half an fp32 ulp at 2^18, so fp32 sums see a tie (the
+    lower index, B, wins) where fp64 keeps A.  The speculative query is 1 in
+    coordinates 0 and 2, so it scores A and B exactly equal (both keep B).
+    Returns (workload, host inputs, q, lm)."""
+    w = Workload("tie_band", B=2, Hq=8, Hkv=2, d=128, L=1024, cs=16, k=8, n_q=2, spec_scale=(0.0, 0.3), seed=91,
+                 residency="uniform", resident_frac=0.3)
+    x = host_inputs(w)
+    one = _bf16_bits(1.0)
+    q = np.zeros((w.B, w.n_q, w.Hq, w.d), np.uint16)
+    q[:, 0, :, 0] = q[:, 0, :, 1] = one                      # real query: coordinates 0 and 1
+    q[:, 1, :, 0] = q[:, 1, :, 2] = one                      # speculative query: coordinates 0 and 2
+    rng = np.random.default_rng(5)
+    lm = synth.f32_to_bf16(rng.uniform(-1, 1, (w.B, w.Hkv, w.C, w.d)).astype(np.float32) * np.float32(0.01))
+    lm[..., 0] = _bf16_bits(0.5)
+    for b in range(w.B):
+        for g in range(w.Hkv):
+            perm = rng.permutation(w.C)
+            big = perm[:w.k - 1]
+            lo, hi = sorted(int(c) for c in perm[w.k - 1:w.k + 1])   # B = lo, A = hi
+            lm[b, g, big, 0] = _bf16_bits(2.0 ** 17)
+            lm[b, g, [lo, hi], :] = 0
+            lm[b, g, [lo, hi], 0] = _bf16_bits(2.0 ** 16)
+            lm[b, g, hi, 1] = _bf16_bits(2.0 ** -9)
+    x["q"], x["lm"] = q, lm
+    return w, x, q, lm

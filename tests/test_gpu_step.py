@@ -271,26 +271,7 @@ def test_step_follows_the_gpu_selection_in_the_tie_band(dd, mode):
     # scores A and B exactly equal (both keep B), so the oracle's union has one
     # chunk more than the GPU's.  The step must then match the oracle's union,
     # miss list, staging bytes and attention on the GPU's own selection.
-    w = Workload("tie_band", B=2, Hq=8, Hkv=2, d=128, L=1024, cs=16, k=8, n_q=2, spec_scale=(0.0, 0.3), seed=91,
-                 residency="uniform", resident_frac=0.3)
-    x = tl.host_inputs(w)
-    one = np.uint16(0x3F80)                                  # bf16 1.0
-    q = np.zeros((w.B, w.n_q, w.Hq, w.d), np.uint16)
-    q[:, 0, :, 0] = q[:, 0, :, 1] = one                      # real query: coordinates 0 and 1
-    q[:, 1, :, 0] = q[:, 1, :, 2] = one                      # speculative query: coordinates 0 and 2
-    rng = np.random.default_rng(5)
-    lm = synth.f32_to_bf16(rng.uniform(-1, 1, (w.B, w.Hkv, w.C, w.d)).astype(np.float32) * np.float32(0.01))
-    lm[..., 0] = synth.f32_to_bf16(np.float32(0.5))
-    for b in range(w.B):
-        for g in range(w.Hkv):
-            perm = rng.permutation(w.C)
-            big = perm[:w.k - 1]
-            lo, hi = sorted(perm[w.k - 1:w.k + 1])           # B = lo, A = hi
-            lm[b, g, big, 0] = synth.f32_to_bf16(np.float32(2.0 ** 17))
-            lm[b, g, [lo, hi], :] = 0
-            lm[b, g, [lo, hi], 0] = synth.f32_to_bf16(np.float32(2.0 ** 16))
-            lm[b, g, hi, 1] = synth.f32_to_bf16(np.float32(2.0 ** -9))
-    x["q"], x["lm"] = q, lm
+    w, x, q, lm = tl.tie_band_inputs()
     want = oracle.step(q, lm, x["K"], x["V"], x["slot"], x["Khot"], x["Vhot"], w.k, w.cs)
     buf = StepBuffers(w, x)
     with dd.Context(shape_of(w), max_misses=buf.cap, hot_slots=buf.hot) as ctx:
