@@ -909,17 +909,29 @@ RES_SLOTS_PER_K, RES_CAP_PER_K = 4, 4     # hot pool of 4k slots per (b,g); admi
 
 
 class LayerGap:
-    """Stand-in for the rest of a layer (projections and MLP) between two
-    layers' sparse steps: one bf16 GEMM of the step's tokens against a weight
-    matrix streamed from HBM, sized so that it takes about ``us``
-    microseconds (a decode GEMM with few rows is bound by the weight reads)."""
+    """Stand-in for the rest of a layer between two layers' sparse steps.
+    ``gemm``: the projections and MLP, one bf16 GEMM of the step's tokens
+    against a weight matrix streamed from HBM, sized so that it takes about
+    ``us`` microseconds (a decode GEMM with few rows is bound by the weight
+    reads; it occupies every SM).  ``idle``: work that leaves the SMs free
+    (one thread spinning for ``us``), such as a wait on another device."""
 
-    def __init__(self, us, tokens, d_model=4096):
+    def __init__(self, us, tokens, d_model=4096, kind="gemm"):
         import torch
         self.us = us
+        self.kind = kind
         self.x = None
+        self.cycles = 0
         if us <= 0:
             self.measured_us = 0.0
+            return
+        if kind == "idle":
+            self.cycles = max(1, int(us * 2000.0))     # a first guess at 2 GHz, then calibrated by timing
+            for _ in range(2):
+                t = self._time()
+                self.cycles = max(1, int(self.cycles * us / t))
+            self.measured_us = self._time()
+            self.shape = None
             return
         self.x = torch.randn(tokens, d_model, dtype=torch.bfloat16, device="cuda")
         n = max(256, int(us * 1e-6 * 6.0e12 / (2 * d_model)) // 256 * 256)
@@ -945,6 +957,10 @@ class LayerGap:
 
     def run(self, stream=None):
         import torch
+        if self.cycles:
+            with torch.cuda.stream(stream or torch.cuda.current_stream()):
+                torch.cuda._sleep(self.cycles)
+            return
         if self.x is None:
             return
         with torch.cuda.stream(stream or torch.cuda.current_stream()):
@@ -1003,7 +1019,7 @@ def run_pipeline(args, world, rank, local):
     ev_pf = [torch.cuda.Event() for _ in range(N)]
     torch.cuda.synchronize()
     link_memcpy, _ = host_link_peaks(dd, shape)
-    gap = LayerGap(args.layer_gap_us, w.B * w.n_q)
+    gap = LayerGap(args.layer_gap_us, w.B * w.n_q, kind=args.layer_gap_kind)
     pf_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(K * N)]
 
     def q_of(i, l):
@@ -1221,10 +1237,12 @@ def run_pipeline(args, world, rank, local):
                            "prediction_hit_rate": 1.0 - M / U if U else None,
                            "urgent_bytes": M * chunk_b, "prefetch_bytes": P * chunk_b,
                            "host_link_gbs": (M + P) * chunk_b * steps / t_pipe / 1e9},
-        "layer_gap": {"requested_us": args.layer_gap_us, "measured_us": gap.measured_us,
-                      "what": ("between layers, a bf16 GEMM of the step's tokens against a weight matrix read from "
-                               f"HBM (shape {getattr(gap, 'shape', None)}), standing in for projections and MLP")
-                      if args.layer_gap_us > 0 else "none: the sparse path alone, layer after layer"},
+        "layer_gap": {"requested_us": args.layer_gap_us, "measured_us": gap.measured_us, "kind": args.layer_gap_kind,
+                      "what": ("none: the sparse path alone, layer after layer" if args.layer_gap_us <= 0 else
+                               "between layers, one thread spinning (the SMs stay free), standing in for a wait"
+                               if args.layer_gap_kind == "idle" else
+                               "between layers, a bf16 GEMM of the step's tokens against a weight matrix read from "
+                               f"HBM (shape {getattr(gap, 'shape', None)}), standing in for projections and MLP")},
         "serialized_same_steps": {"value": steps / t_ser, "unit": UNIT, "ms_per_step": 1e3 * t_ser / steps},
         "all_resident_same_steps": {"value": steps / t_all, "unit": UNIT, "ms_per_step": 1e3 * t_all / steps,
                                     "note": "every chunk of every layer in an HBM pool: no host transfer at all"},
@@ -1279,6 +1297,8 @@ def main():
                     help="skip the other workloads' lines (per_config; run only at N=1 with the default workload)")
     ap.add_argument("--no-landmark-timing", action="store_true", help="skip the separate landmark-build timing")
     ap.add_argument("--prefetch-ctas", type=int, default=2, help="pipelined mode: prefetch copy CTAs per SM")
+    ap.add_argument("--layer-gap-kind", choices=("gemm", "idle"), default="gemm",
+                    help="pipelined mode: the gap's work (a weight-streaming GEMM on every SM, or one spinning thread)")
     ap.add_argument("--layer-gap-us", type=float, default=0.0,
                     help="pipelined mode: microseconds of other per-layer work (a weight-streaming GEMM) between "
                          "two layers' sparse steps")
@@ -1287,8 +1307,18 @@ def main():
     ap.add_argument("--layers", type=int, default=N_LAYERS,
                     help="layers whose inputs the steps cycle through (fewer than 4 only to hold less device "
                          "memory under a profiler: one layer's inputs then stay in L2 between steps)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="> 0: the workload with this many requests instead of its own (a smaller case of the same "
+                         "kernels for profiler captures; named <workload>_b<B>)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.batch > 0:
+        w = BY_NAME[args.workload]
+        ws = w.scaled(name=f"{w.name}_b{args.batch}", B=args.batch)
+        BY_NAME[ws.name] = ws
+        args.workload = ws.name
+        args.no_per_config = True
+        args.no_cpu_baseline = True   # the oracle's worker processes know the named workloads only
     if args.layers < 1:
         ap.error("--layers must be at least 1")
     globals()["N_LAYERS"] = args.layers

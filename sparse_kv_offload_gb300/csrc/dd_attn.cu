@@ -15,12 +15,17 @@
 // issues copies while the other's does its per-stage bookkeeping or waits on
 // a fresh slice's tables).  A slice covers a few units ("runs").  At the end
 // of a run the consumer warps that share an m-tile merge their states in
-// shared memory, and the CTA writes one partial (running max, sum and
-// accumulator per query vector) into slot CTA + unit -- slices are ordered
-// like the units, so no two (CTA, unit) pairs share a slot and n_cta + units
-// slots suffice -- and counts itself in on the unit's arrival counter; the
-// CTA that arrives last merges the unit's partials (stream-K fix-up), so the
-// outputs leave the same kernel.  A unit inside one slice skips the count.
+// shared memory.  A unit that lies inside one slice is then complete and its
+// outputs are written at once.  For a unit shared by several CTAs the CTA
+// writes one partial (running max, sum and accumulator per query vector) into
+// slot CTA + unit -- slices are ordered like the units, so no two (CTA, unit)
+// pairs share a slot and n_cta + units slots suffice -- and counts itself in
+// on the unit's arrival counter; the CTA that arrives last merges the unit's
+// partials (stream-K fix-up), so the outputs leave the same kernel.  Only a
+// slice's first run can continue a unit begun earlier without being its last
+// run; when the gather is not fused, that run's count (and merge) is left to
+// the otherwise idle second producer warp, so the consumers never wait on a
+// GPU-scope round trip in the middle of their slice.
 //
 // Data movement: the issuing producer warp streams 64-row tiles of K and V
 // into shared memory with 2-D TMA loads (cp.async.bulk.tensor, 128-byte
@@ -143,6 +148,16 @@ __device__ __forceinline__ uint32_t swz(int row, int cg) {
   return (uint32_t)((cg >> 3) * kHalfBytes + row * 128 + ((((cg & 7) ^ (row & 7))) << 4));
 }
 
+// Stream-K arrival count: adds one with release (the CTA's published
+// partials, ordered before it by a barrier, become visible with it) and
+// acquire (the other CTAs' partials are visible to whoever reads them after
+// this thread, through a barrier) semantics at GPU scope.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t *p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // two fp32 -> packed bf16x2 (round to nearest even), lo in the low half
 __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -252,7 +267,8 @@ __host__ __device__ constexpr int attn_max_regs(int threads, int ctas) {
 
 // Producer warps: warp 0 issues the stages' metadata and every tile copy
 // (TMA); in the fused gather warp 1 copies the slice's missing chunks from
-// host memory into staging ahead of it.  Measured on the 16-request 32K
+// host memory into staging ahead of it, otherwise it counts the first run's
+// partial in (the finisher).  Measured on the 16-request 32K
 // layer, the host link moved the most with about 16 KB of 16-byte loads in
 // flight per SM (2 x 8 per lane of one warp in each of two CTAs now; with
 // one CTA per SM, 2 warps x 8 beat 1 x 16, 2 x 16, 4 x 16 and 1 x 4).
@@ -280,6 +296,7 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
 
   __shared__ int s_fix;   // this CTA finished the last part of the unit whose run just ended
   __shared__ int s_ready; // fused gather: missing chunks of this slice already in staging, in slice order
+  __shared__ int s_pub;   // partials the consumers handed to the finisher warp (one per m-tile and run)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
   if (tid == 0) {
@@ -289,6 +306,7 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_ready = 0;
+    s_pub = 0;
   }
   __syncthreads();
   pdl_wait();
@@ -305,6 +323,39 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
     const bool fused = p.kh != nullptr;
     const int pw = warp - kConsumers;
     if (pw > 0) {
+      if (!fused && pw == 1) {
+        // finisher warp (the gather is not fused, so this warp copies
+        // nothing): the stream-K count of the slice's first run when that run
+        // continues a unit begun by an earlier CTA and is not the slice's last
+        // run.  Only the first run can be such a run (every later one starts
+        // inside the slice).  The consumers publish that run's partial and go
+        // on with the next run; this warp counts the CTA in on the unit and,
+        // when it arrives last, merges the unit, off the consumers' path.
+        const int u = unit_of_chunk_warp(p.chunk_off, p.units, lo);
+        const int off_u = p.chunk_off[u], end_u = p.chunk_off[u + 1];
+        if (off_u < lo && end_u < hi) {
+          const int c0 = off_u / per, c1 = (end_u - 1) / per;
+          bool ok = true;
+          const uint64_t t0 = globaltimer_ns();
+          for (uint32_t it = 0;; ++it) {   // the partials of every m-tile, published with release
+            int n;
+            asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(n) : "r"(smem_u32(&s_pub)) : "memory");
+            if (n >= MT) break;
+            __nanosleep(64);
+            if ((it & 15u) == 15u && globaltimer_ns() - t0 > 2000000000ull) {
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) {
+            if (lane == 0) set_status(p.status, DD_ERR_TIMEOUT);
+            return;
+          }
+          int last = 0;
+          if (lane == 0) last = atom_add_acq_rel_gpu(p.arrive + u, 1) + 1 == c1 - c0 + 1;
+          if (__shfl_sync(0xffffffffu, last, 0)) fixup_unit(p, u, c0, c1, 32, lane);
+        }
+      }
       if (fused && pw == 1) {
         // fused gather, copier warp: every missing chunk of the slice, in
         // slice order, from pinned host memory into its staging rows, as far
@@ -699,25 +750,59 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * buf);
-      // the CTA's partial for the run: rows of each m-tile, from warp wq = 0
-      // into slot CTA + unit
+      // CTAs c0..c1 hold parts of the unit.  A unit inside this slice (c0 ==
+      // c1) is complete here: without tail rows its rows of each m-tile are
+      // written straight from warp wq = 0.  Otherwise warp wq = 0 publishes
+      // the CTA's partial into slot CTA + unit, and the CTA counts itself in
+      // on the unit's arrival counter: here, or -- for the slice's first run
+      // when it continues an earlier CTA's unit and is not the slice's last run
+      // and the gather is not fused -- by the finisher warp, so that these
+      // warps go straight on with the next run.
+      const int c0 = m_uoff / per, c1 = (m_uoff + m_ucnt - 1) / per;
+      const bool direct = c0 == c1 && p.k_tail == nullptr;
+      const bool handoff = c0 != c1 && p.kh == nullptr && m_uoff < lo && !(m_flags & kEnd);
       if (wq == 0) {
         float lq0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
         lq0 += __shfl_xor_sync(0xffffffffu, lq0, 2);
         float lq1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
         lq1 += __shfl_xor_sync(0xffffffffu, lq1, 2);
-        const int64_t pbase = ((int64_t)blockIdx.x + m_unit) * p.NQ;
-        if (qv0 < p.NQ) {
-          float *dst = p.part_o + (pbase + qv0) * 128 + 2 * tq;
+        if (direct) {
+          const int b = m_unit / p.Hkv, g = m_unit - b * p.Hkv;
+          if (qv0 < p.NQ) {
+            const int h = g * p.G + (qv0 - j0 * p.G);
+            const float inv = lq0 > 0.f ? 1.f / lq0 : 0.f;
+            float *dst = p.out + ((int64_t)(b * p.n_q + j0) * p.Hq + h) * 128 + 2 * tq;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) *reinterpret_cast<float2 *>(dst + i * 8) = make_float2(o[i][0], o[i][1]);
-          if (tq == 0) *reinterpret_cast<float2 *>(p.part_ml + (pbase + qv0) * 2) = make_float2(m0, lq0);
-        }
-        if (qv1 < p.NQ) {
-          float *dst = p.part_o + (pbase + qv1) * 128 + 2 * tq;
+            for (int i = 0; i < 16; ++i)
+              *reinterpret_cast<float2 *>(dst + i * 8) = make_float2(o[i][0] * inv, o[i][1] * inv);
+          }
+          if (qv1 < p.NQ) {
+            const int h = g * p.G + (qv1 - j1 * p.G);
+            const float inv = lq1 > 0.f ? 1.f / lq1 : 0.f;
+            float *dst = p.out + ((int64_t)(b * p.n_q + j1) * p.Hq + h) * 128 + 2 * tq;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) *reinterpret_cast<float2 *>(dst + i * 8) = make_float2(o[i][2], o[i][3]);
-          if (tq == 0) *reinterpret_cast<float2 *>(p.part_ml + (pbase + qv1) * 2) = make_float2(m1, lq1);
+            for (int i = 0; i < 16; ++i)
+              *reinterpret_cast<float2 *>(dst + i * 8) = make_float2(o[i][2] * inv, o[i][3] * inv);
+          }
+        } else {
+          const int64_t pbase = ((int64_t)blockIdx.x + m_unit) * p.NQ;
+          if (qv0 < p.NQ) {
+            float *dst = p.part_o + (pbase + qv0) * 128 + 2 * tq;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) *reinterpret_cast<float2 *>(dst + i * 8) = make_float2(o[i][0], o[i][1]);
+            if (tq == 0) *reinterpret_cast<float2 *>(p.part_ml + (pbase + qv0) * 2) = make_float2(m0, lq0);
+          }
+          if (qv1 < p.NQ) {
+            float *dst = p.part_o + (pbase + qv1) * 128 + 2 * tq;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) *reinterpret_cast<float2 *>(dst + i * 8) = make_float2(o[i][2], o[i][3]);
+            if (tq == 0) *reinterpret_cast<float2 *>(p.part_ml + (pbase + qv1) * 2) = make_float2(m1, lq1);
+          }
+          if (handoff) {
+            // the m-tile's partial is written: hand it to the finisher warp
+            __syncwarp();
+            if (lane == 0) asm volatile("red.release.cta.shared.add.u32 [%0], 1;" ::"r"(smem_u32(&s_pub)) : "memory");
+          }
         }
       }
       // the next stage starts a new run, which reloads the queries and
@@ -729,24 +814,15 @@ __global__ void __maxnreg__(attn_max_regs((MT * WPM + producers_for(MT * WPM)) *
       for (int ks = 0; ks < 8; ++ks) qa[ks][0] = qa[ks][1] = qa[ks][2] = qa[ks][3] = 0u;
       m0 = m1 = -INFINITY;
       l0 = l1 = 0.f;
-      // stream-K fix-up: CTAs c0..c1 hold parts of the unit; the one that
-      // counts itself in last merges them.  The barrier orders the CTA's
-      // partial before thread 0's fence and count (a unit inside one CTA
-      // needs no count)
-      const int c0 = m_uoff / per, c1 = (m_uoff + m_ucnt - 1) / per;
-      asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");   // consumer warps only
-      if (tid == 0) {
-        if (c0 == c1) {
-          s_fix = 1;
-        } else {
-          __threadfence();
-          s_fix = atomicAdd(p.arrive + m_unit, 1) + 1 == c1 - c0 + 1;
-        }
-      }
-      asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
-      if (s_fix) {
-        __threadfence();
-        fixup_unit(p, m_unit, c0, c1, kConsumers * 32, tid);
+      if (!direct && !handoff) {
+        // stream-K fix-up: the CTA that counts itself in last merges the
+        // unit's partials (a unit inside one CTA needs no count).  The
+        // barrier orders the CTA's partial before thread 0's count, and
+        // thread 0's acquire before every thread's reads of the partials.
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");   // consumer warps only
+        if (tid == 0) s_fix = c0 == c1 || atom_add_acq_rel_gpu(p.arrive + m_unit, 1) + 1 == c1 - c0 + 1;
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
+        if (s_fix) fixup_unit(p, m_unit, c0, c1, kConsumers * 32, tid);
       }
     } else {
       __syncwarp();
