@@ -306,9 +306,16 @@ def run_reference(args, world, rank):
 
 
 # the step scores in one streaming kernel (k_score), then runs top-k and the
-# resolver as one kernel (k_select_fused)
-KERNEL_SOURCE = {"gather": ("k_gather", "dd_gather.cu"), "attention": ("k_attn", "dd_attn.cu"),
-                 "score": ("k_score", "dd_score.cu"), "topk": ("k_select_fused", "dd_select.cu")}
+# resolver as one kernel (k_select_fused); the attention is k_attn (mma.sync)
+# up to 16 query vectors per KV head and k_attn_tc (tcgen05) above
+KERNEL_SOURCE = {"gather": ("k_gather", ("dd_gather.cu",)), "attention": ("k_attn", ("dd_attn.cu", "dd_attn.cuh")),
+                 "attention_tc": ("k_attn_tc", ("dd_attn_tc.cu", "dd_attn.cuh")),
+                 "score": ("k_score", ("dd_score.cu",)), "topk": ("k_select_fused", ("dd_select.cu",))}
+
+
+def attention_stage(w) -> str:
+    """The attention kernel the workload runs: tcgen05 above 16 query vectors per KV head."""
+    return "attention_tc" if w.n_q * w.G > 16 else "attention"
 
 
 def profiled_traffic(stage: str, workload: str):
@@ -316,7 +323,7 @@ def profiled_traffic(stage: str, workload: str):
     summary, or None when there is none or the kernel source has changed since
     the counters were taken."""
     import re
-    kernel, src = KERNEL_SOURCE[stage]
+    kernel, srcs = KERNEL_SOURCE[stage]
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
@@ -325,19 +332,23 @@ def profiled_traffic(stage: str, workload: str):
     h = re.search(r"^code_sha256_prefix: ([0-9a-f]+)$", text, re.M)
     if not t or not h:
         return None
-    cur = code_hash(os.path.join(ROOT, "sparse_kv_offload_gb300", "csrc", src))
+    cur = code_hash(*[os.path.join(ROOT, "sparse_kv_offload_gb300", "csrc", f) for f in srcs])
     return int(t.group(1)) if cur.startswith(h.group(1)) else None
 
 
-def code_hash(path: str) -> str:
-    """sha256 of a CUDA source with its comments and whitespace removed: a
-    profile stays valid across comment edits, not across code changes."""
+def code_hash(*paths: str) -> str:
+    """sha256 of the CUDA sources of a kernel with their comments and whitespace
+    removed: a profile stays valid across comment edits, not across code
+    changes."""
     import hashlib
     import re
-    text = open(path).read()
-    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-    text = re.sub(r"//[^\n]*", " ", text)
-    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()
+    parts = []
+    for path in paths:
+        text = open(path).read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        parts.append(" ".join(text.split()))
+    return hashlib.sha256("\n".join(parts).encode()).hexdigest()
 
 
 def config_of(w, gather_mode, world=1, landmarks="mean"):
@@ -663,6 +674,8 @@ def run_ours(args, world, rank, local, per_config=None):
     t_dom = (dom_ms_timed if dom == dom_timed else stage_ms[dom]) * 1e-3
     traffic = profiled_traffic(dom, w.name)
     wl_name = w.name + "_all_resident" if resident_all else w.name
+    att = attention_stage(w)
+    att_kernel = KERNEL_SOURCE[att][0]
     if fused and dom == "attention":
         # the kernel reads the hot pool over HBM and the misses over the host
         # link at once: its bound is whichever would take longer at its peak
@@ -671,14 +684,14 @@ def run_ours(args, world, rank, local, per_config=None):
         if t_link >= t_hbm:
             roof = {"bound": "host_link", "achieved": gather_b / t_dom / 1e9, "peak": link_memcpy, "unit": "GB/s",
                     "peak_kind": "pinned H2D cudaMemcpyAsync, best of 10 x 1 GiB, measured in this run",
-                    "traffic": profiled_traffic("attention", wl_name),
-                    "kernel": "k_attn (gather fused: missing chunks read over the host link)",
+                    "traffic": profiled_traffic(att, wl_name),
+                    "kernel": att_kernel + " (gather fused: missing chunks read over the host link)",
                     "hbm_achieved": attn_b / t_dom / 1e9}
         else:
             roof = {"bound": "hbm", "achieved": attn_b / t_dom / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                    "peak_kind": hbm_kind, "traffic": profiled_traffic("attention", wl_name),
-                    "kernel": ("k_attn (every chunk resident: K and V by TMA from the HBM pool)" if M == 0 else
-                               "k_attn (resident chunks by TMA from the HBM pool, misses over the host link)"),
+                    "peak_kind": hbm_kind, "traffic": profiled_traffic(att, wl_name),
+                    "kernel": att_kernel + (" (every chunk resident: K and V by TMA from the HBM pool)" if M == 0 else
+                                            " (resident chunks by TMA from the HBM pool, misses over the host link)"),
                     "host_link_achieved": gather_b / t_dom / 1e9}
     elif dom == "gather":
         roof = {"bound": "host_link", "achieved": gather_b / t_dom / 1e9, "peak": link_memcpy, "unit": "GB/s",
@@ -688,9 +701,10 @@ def run_ours(args, world, rank, local, per_config=None):
                                 "staging writes stay in L2"}
     else:
         roof = {"bound": "hbm", "achieved": stage_bytes[dom] / t_dom / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                "peak_kind": hbm_kind, "traffic": profiled_traffic(dom, wl_name if dom == "attention" else w.name),
-                "kernel": KERNEL_SOURCE[dom][0] + (" (every chunk from HBM: the hot pool and the staging buffer)"
-                                                   if dom == "attention" else "")}
+                "peak_kind": hbm_kind,
+                "traffic": profiled_traffic(att, wl_name) if dom == "attention" else profiled_traffic(dom, w.name),
+                "kernel": (att_kernel + " (every chunk from HBM: the hot pool and the staging buffer)"
+                           if dom == "attention" else KERNEL_SOURCE[dom][0])}
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["peak"] else None
     # the scoring pass is HBM-bound in every mode; when the attention reads its
     # chunks from HBM too (a separate gather into staging, or every chunk

@@ -66,14 +66,14 @@ def test_traffic_counts_only_for_the_captured_code(bench, monkeypatch):
     checked = 0
     for path, text, prefix in _summaries():
         name = os.path.basename(path)[:-3]
-        kernel = next((k for k in by_kernel if name.startswith(k + "_")), None)
+        kernel = max((k for k in by_kernel if name.startswith(k + "_")), key=len, default=None)
         if kernel is None:
             continue
         workload = name[len(kernel) + 1:]
         want = int(re.search(r"^traffic_bytes_per_launch: (\d+)$", text, re.M).group(1))
-        monkeypatch.setattr(bench, "code_hash", lambda p, pre=prefix: pre + "0" * 8)
+        monkeypatch.setattr(bench, "code_hash", lambda *p, pre=prefix: pre + "0" * 8)
         assert bench.profiled_traffic(by_kernel[kernel], workload) == want, name
-        monkeypatch.setattr(bench, "code_hash", lambda p, pre=prefix: ("f" if pre[0] != "f" else "0") + pre[1:])
+        monkeypatch.setattr(bench, "code_hash", lambda *p, pre=prefix: ("f" if pre[0] != "f" else "0") + pre[1:])
         assert bench.profiled_traffic(by_kernel[kernel], workload) is None, name
         checked += 1
     assert checked >= 1
