@@ -201,14 +201,19 @@ __device__ __forceinline__ void fixup_unit(const AttnParams &p, int unit, int c0
 // the fused gather, or the finisher when the gather is not fused).  The tile
 // ring has kStages stages of kStageBytes, each run's query vectors go to a
 // q_bytes slot per stage (kQStride bytes per vector), and the finisher waits
-// for n_pub hand-offs of the consumers' partial.
+// for n_pub hand-offs of the consumers' partial.  With n_issue > 1 issuing
+// warps, each walks the whole slice and issues the stages s with
+// s % n_issue == issue_idx: a stage costs its issuing warp a few thousand
+// cycles (the record, the mbarrier and one TMA instruction per 2 KiB box),
+// which one warp cannot hide behind the stages of a single CTA per SM.  The
+// fused gather keeps one issuing warp (it meets the misses in slice order).
 template <int kStages>
 __device__ __forceinline__ void attn_producer_warp(const AttnParams &p, const CUtensorMap *tm_khot,
                                                    const CUtensorMap *tm_vhot, const CUtensorMap *tm_kst,
                                                    const CUtensorMap *tm_vst, int lo, int hi, int per, int pw,
                                                    uint8_t *stages, uint8_t *qsm, int q_bytes, StageMeta *meta,
                                                    uint32_t full0, uint32_t empty0, int *s_ready, int *s_pub,
-                                                   int n_pub) {
+                                                   int n_pub, int issue_idx = 0, int n_issue = 1) {
   const int lane = threadIdx.x & 31;
   const bool fused = p.kh != nullptr;
   if (pw > 0) {
@@ -323,7 +328,7 @@ __device__ __forceinline__ void attn_producer_warp(const AttnParams &p, const CU
   int x0 = lo;
   int4 cur = (x0 + lane < hi) ? p.flat[x0 + lane] : make_int4(-1, 0, -1, 0);
   int4 nxt = (x0 + 32 + lane < hi) ? p.flat[x0 + 32 + lane] : make_int4(-1, 0, -1, 0);
-  if (p.trace && lane == 0) trace_start(p.trace);   // before this CTA's first copy
+  if (p.trace && lane == 0 && issue_idx == 0) trace_start(p.trace);   // before this CTA's first copy
   int missed = 0;   // fused gather: missing chunks met so far, in slice order
   int s = 0, u = u0, x = lo;
   bool first = true, alive = true;
@@ -344,7 +349,10 @@ __device__ __forceinline__ void attn_producer_warp(const AttnParams &p, const CU
     const bool last = x + nch == min(end_u, hi);
     const bool end = x + nch == hi;
     const int b = u / p.Hkv, g = u - b * p.Hkv;
-    {
+    if (s % n_issue != issue_idx) {   // another issuing warp's stage
+      first = false;
+      ++s;
+    } else {
         int32_t rows[kMaxChunksPerStage];   // the stage's chunks, for its record (lane 0)
         uint32_t qms[kMaxChunksPerStage];
 #pragma unroll

@@ -37,7 +37,7 @@ namespace dd {
 namespace {
 
 constexpr int kTcSoftmaxWarps = 8;                                 // two per tensor-memory lane quarter
-constexpr int kTcThreads = (kTcSoftmaxWarps + 3) * 32;             // + issuing warp, copier / finisher, MMA warp
+constexpr int kTcThreads = (kTcSoftmaxWarps + 4) * 32;             // + 2 issuing warps, copier / finisher, MMA warp
 constexpr int kTcM = 64;                                           // query vectors per MMA (M)
 constexpr int kTcTmemCols = 256;                                   // S: 2 x 64 columns, O: 128 columns
 constexpr int kTcTileBytes = kTcM * 128;                           // a 64-row, 128-byte-row swizzled tile
@@ -201,10 +201,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem_o = tmem + 2 * kTcM;   // O: columns 128..255
 
   if (warp >= kTcSoftmaxWarps) {
+    // warps 8 and 9 issue the stages alternately and warp 10 finishes; when
+    // the gather is fused, warp 8 issues every stage and warp 9 copies (warp
+    // 10 has nothing to do).  Warp 11 issues the MMAs.
     const int pw = warp - kTcSoftmaxWarps;
-    if (pw < 2) {
-      attn_producer_warp<kStages>(p, &tm_khot, &tm_vhot, &tm_kst, &tm_vst, lo, hi, per, pw, stages, qsm, q_bytes, meta,
-                                  full0, empty0, &s_ready, &s_pub, 1);
+    if (pw < 3) {
+      const bool fused = p.kh != nullptr;
+      if (pw == 0 || (pw == 1 && !fused))
+        attn_producer_warp<kStages>(p, &tm_khot, &tm_vhot, &tm_kst, &tm_vst, lo, hi, per, 0, stages, qsm, q_bytes,
+                                    meta, full0, empty0, &s_ready, &s_pub, 1, pw, fused ? 1 : 2);
+      else if (pw == (fused ? 1 : 2))
+        attn_producer_warp<kStages>(p, &tm_khot, &tm_vhot, &tm_kst, &tm_vst, lo, hi, per, 1, stages, qsm, q_bytes,
+                                    meta, full0, empty0, &s_ready, &s_pub, 1);
       return;
     }
     // ---------------------------------------------------------------- MMA warp

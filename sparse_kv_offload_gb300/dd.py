@@ -115,8 +115,11 @@ def _chk(status: int, what: str):
 
 
 def _stream(stream) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return s.cuda_stream
+    # the current stream's raw handle without building a torch.cuda.Stream
+    # object (a tenth of the host time of torch.cuda.current_stream())
+    if stream is not None:
+        return stream.cuda_stream
+    return torch._C._cuda_getCurrentRawStream(torch._C._cuda_getDevice())
 
 
 def _ptr(t, dtype=None, numel=None, device=True, name="tensor", allow_none=False):
