@@ -550,6 +550,45 @@ static bool make_pool_map(CUtensorMap *map, const void *base, int64_t rows, int 
   return true;
 }
 
+// The queries [B, n_q, Hq, 128] bf16 viewed as 4-D, boxes of 64 columns x G
+// heads x n_q queries x 1 request: one box is half of the query vectors of a
+// (request, KV head) unit, rows j * G + h, in the 128B-swizzled layout the
+// tcgen05 attention's A operand takes.  Cached like the pool maps.
+static bool make_q_map(CUtensorMap *map, const void *q, int B, int n_q, int Hq, int G) {
+  struct Entry {
+    const void *q;
+    int B, n_q, Hq, G;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry cache[16];
+  static int n = 0, next = 0;
+  if (q == nullptr) return false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+      if (cache[i].q == q && cache[i].B == B && cache[i].n_q == n_q && cache[i].Hq == Hq && cache[i].G == G) {
+        *map = cache[i].map;
+        return true;
+      }
+  }
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {128, (cuuint64_t)Hq, (cuuint64_t)n_q, (cuuint64_t)B};
+  cuuint64_t strides[3] = {256, (cuuint64_t)Hq * 256, (cuuint64_t)n_q * Hq * 256};
+  cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)n_q, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  cache[next] = {q, B, n_q, Hq, G, *map};
+  next = (next + 1) % 16;
+  if (n < 16) ++n;
+  return true;
+}
+
 struct AttnShape {
   int mt, wpm, threads;
   size_t smem;
@@ -646,7 +685,9 @@ cudaError_t launch_attn(const void *q, const void *Khot, const void *Vhot, const
   // more: tcgen05 with the accumulators in tensor memory, one CTA per SM
   if (sh.mt == 1) return launch_attn_t<1, 4>(plan.n_cta, sh, tkh, tvh, tks, tvs, p, s);
   if (sh.mt > 4) return cudaErrorInvalidValue;
-  return launch_attn_tc(plan.n_cta, NQ, tkh, tvh, tks, tvs, p, s);
+  CUtensorMap tq;
+  if (!make_q_map(&tq, q, B, n_q, Hq, G)) return cudaErrorInvalidValue;
+  return launch_attn_tc(plan.n_cta, tkh, tvh, tks, tvs, tq, p, s);
 }
 
 }  // namespace dd

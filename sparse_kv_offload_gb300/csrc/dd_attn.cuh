@@ -89,6 +89,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, int w,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
+// 2^x by the PTX ex2.approx instruction (results below 2^-126 flushed to 0;
+// 2^-inf = 0); the attention tests hold it to the oracle's tolerance
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Stream-K arrival count: adds one with release (the CTA's published
 // partials, ordered before it by a barrier, become visible with it) and
 // acquire (the other CTAs' partials are visible to whoever reads them after
@@ -201,7 +218,14 @@ __device__ __forceinline__ void fixup_unit(const AttnParams &p, int unit, int c0
 // the fused gather, or the finisher when the gather is not fused).  The tile
 // ring has kStages stages of kStageBytes, each run's query vectors go to a
 // q_bytes slot per stage (kQStride bytes per vector), and the finisher waits
-// for n_pub hand-offs of the consumers' partial.  With n_issue > 1 issuing
+// for n_pub hand-offs of the consumers' partial.  With a query tensor map
+// (tm_q: q viewed as [B][n_q][Hq][128] bf16, boxes of 64 x G x n_q), a run's
+// query vectors come instead by two TMA boxes straight into the 128B-swizzled
+// query tile of the run's parity at qsm (2 x kHalfBytes each, rows j*G + h);
+// before the tile of run r >= 2 is overwritten, the issuing warp waits on
+// q_free[r & 1], which the MMA issuer arrives on (tcgen05.commit) when run
+// r - 1 begins, i.e. once every MMA that read run r - 2's queries is done.
+// With n_issue > 1 issuing
 // warps, each walks the whole slice and issues the stages s with
 // s % n_issue == issue_idx: a stage costs its issuing warp a few thousand
 // cycles (the record, the mbarrier and one TMA instruction per 2 KiB box),
@@ -213,7 +237,8 @@ __device__ __forceinline__ void attn_producer_warp(const AttnParams &p, const CU
                                                    const CUtensorMap *tm_vst, int lo, int hi, int per, int pw,
                                                    uint8_t *stages, uint8_t *qsm, int q_bytes, StageMeta *meta,
                                                    uint32_t full0, uint32_t empty0, int *s_ready, int *s_pub,
-                                                   int n_pub, int issue_idx = 0, int n_issue = 1) {
+                                                   int n_pub, int issue_idx = 0, int n_issue = 1,
+                                                   const CUtensorMap *tm_q = nullptr, uint32_t qfree0 = 0) {
   const int lane = threadIdx.x & 31;
   const bool fused = p.kh != nullptr;
   if (pw > 0) {
@@ -331,6 +356,7 @@ __device__ __forceinline__ void attn_producer_warp(const AttnParams &p, const CU
   if (p.trace && lane == 0 && issue_idx == 0) trace_start(p.trace);   // before this CTA's first copy
   int missed = 0;   // fused gather: missing chunks met so far, in slice order
   int s = 0, u = u0, x = lo;
+  int run = 0;   // runs begun before this stage
   bool first = true, alive = true;
   while (x < hi && alive) {
     if (u - ubase >= 32) {
@@ -350,6 +376,7 @@ __device__ __forceinline__ void attn_producer_warp(const AttnParams &p, const CU
     const bool end = x + nch == hi;
     const int b = u / p.Hkv, g = u - b * p.Hkv;
     if (s % n_issue != issue_idx) {   // another issuing warp's stage
+      run += first;
       first = false;
       ++s;
     } else {
@@ -400,7 +427,18 @@ __device__ __forceinline__ void attn_producer_warp(const AttnParams &p, const CU
         if (lane == 0) mbar_arrive_expect_tx(bar, bytes);   // the record is written; no copy has been issued yet
         // the copies themselves, spread over the lanes: the run's query vectors,
         // and lane i the four boxes of the stage's chunk i
-        if (first) {
+        if (first && tm_q != nullptr) {
+          if (lane == 0) {
+            if (run >= 2 && !mbar_wait(qfree0 + 8 * (run & 1), ((run >> 1) - 1) & 1, p.status)) alive = false;
+            if (alive) {
+              const uint32_t qdst = smem_u32(qsm) + (uint32_t)(run & 1) * 2u * kHalfBytes;
+              tma_load_4d(qdst, tm_q, 0, g * p.G, 0, b, bar);
+              tma_load_4d(qdst + kHalfBytes, tm_q, 64, g * p.G, 0, b, bar);
+            }
+          }
+          alive = __shfl_sync(0xffffffffu, alive, 0);
+          if (!alive) break;
+        } else if (first) {
           const uint32_t qdst = smem_u32(qsm + buf * q_bytes);
           for (int qv = lane; qv < p.NQ; qv += 32) {
             const int j = qv / p.G, h = g * p.G + (qv - j * p.G);
@@ -445,6 +483,7 @@ __device__ __forceinline__ void attn_producer_warp(const AttnParams &p, const CU
         }
         alive = __all_sync(0xffffffffu, ok);
         if (!alive) break;
+        run += first;
         first = false;
         ++s;
     }
@@ -460,8 +499,8 @@ __device__ __forceinline__ void attn_producer_warp(const AttnParams &p, const CU
 
 // tcgen05 attention (dd_attn_tc.cu) for more than 16 query vectors per KV
 // head: one persistent CTA per SM of attn_tc_threads() threads.
-cudaError_t launch_attn_tc(int n_cta, int NQ, const CUtensorMap &khot, const CUtensorMap &vhot,
-                           const CUtensorMap &kst, const CUtensorMap &vst, const AttnParams &p, cudaStream_t s);
+cudaError_t launch_attn_tc(int n_cta, const CUtensorMap &khot, const CUtensorMap &vhot, const CUtensorMap &kst,
+                           const CUtensorMap &vst, const CUtensorMap &q, const AttnParams &p, cudaStream_t s);
 int attn_tc_threads();
 
 }  // namespace dd

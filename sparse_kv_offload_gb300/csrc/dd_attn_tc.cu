@@ -127,34 +127,32 @@ __device__ __forceinline__ void tmem_st32_split(uint32_t taddr, const float *v) 
 
 // Shared-memory plan, 1024-byte aligned parts:
 //   tile ring  [kStages][32 KiB]  K lo, K hi, V lo, V hi halves of 64 rows
-//   Q tile     [2 halves][64 rows][128 B]   the run's query vectors (A of S)
+//   Q tiles    [2 runs][2 halves][64 rows][128 B]   the queries of runs of
+//              each parity (A of S), written by TMA with the 128-byte swizzle
 //   P          [2 buffers][hi, lo][64 rows][128 B]   (A of O += P V)
-//   Q slots    [kStages][NQ][272 B]   the producer's bulk copies of each run's queries
 //   stage records, then the mbarriers:
-//     full[kStages], empty[kStages], s_full[2], pv_done[2], p_ready, q_ready, mma_done
-size_t tc_smem_bytes(int stages, int NQ) {
-  return 1024 + (size_t)stages * kStageBytes + 2 * kTcTileBytes + 4 * kTcTileBytes + (size_t)stages * NQ * kQStride +
-         (size_t)stages * sizeof(StageMeta) + (size_t)(2 * stages + 7) * 8;
+//     full[kStages], empty[kStages], s_full[2], pv_done[2], p_ready, q_free[2], mma_done
+size_t tc_smem_bytes(int stages) {
+  return 1024 + (size_t)stages * kStageBytes + 4 * kTcTileBytes + 4 * kTcTileBytes +
+         (size_t)stages * sizeof(StageMeta) + (size_t)(2 * stages + 8) * 8;
 }
 
 template <int kStages>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tm_khot, const __grid_constant__ CUtensorMap tm_vhot,
               const __grid_constant__ CUtensorMap tm_kst, const __grid_constant__ CUtensorMap tm_vst,
-              const AttnParams p) {
+              const __grid_constant__ CUtensorMap tm_q, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *stages = smem;
   uint8_t *qtile = stages + kStages * kStageBytes;
-  uint8_t *pbuf = qtile + 2 * kTcTileBytes;
-  uint8_t *qsm = pbuf + 4 * kTcTileBytes;
-  const int q_bytes = p.NQ * kQStride;
-  StageMeta *meta = reinterpret_cast<StageMeta *>(qsm + kStages * q_bytes);
+  uint8_t *pbuf = qtile + 4 * kTcTileBytes;
+  StageMeta *meta = reinterpret_cast<StageMeta *>(pbuf + 4 * kTcTileBytes);
   uint64_t *bars = reinterpret_cast<uint64_t *>(meta + kStages);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
   const uint32_t sfull0 = smem_u32(bars + 2 * kStages), pvdone0 = smem_u32(bars + 2 * kStages + 2);
-  const uint32_t pready = smem_u32(bars + 2 * kStages + 4), qready = smem_u32(bars + 2 * kStages + 5);
-  const uint32_t mmadone = smem_u32(bars + 2 * kStages + 6);
+  const uint32_t pready = smem_u32(bars + 2 * kStages + 4), qfree0 = smem_u32(bars + 2 * kStages + 5);
+  const uint32_t mmadone = smem_u32(bars + 2 * kStages + 7);
 
   __shared__ int s_fix, s_ready, s_pub;
   __shared__ uint32_t s_tmem;
@@ -173,7 +171,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);   // released by the commit after the stage's PV
     }
-    for (int i = 2 * kStages; i < 2 * kStages + 7; ++i) mbar_init(smem_u32(bars + i), 1);
+    for (int i = 2 * kStages; i < 2 * kStages + 8; ++i) mbar_init(smem_u32(bars + i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_ready = 0;
     s_pub = 0;
@@ -208,11 +206,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (pw < 3) {
       const bool fused = p.kh != nullptr;
       if (pw == 0 || (pw == 1 && !fused))
-        attn_producer_warp<kStages>(p, &tm_khot, &tm_vhot, &tm_kst, &tm_vst, lo, hi, per, 0, stages, qsm, q_bytes,
-                                    meta, full0, empty0, &s_ready, &s_pub, 1, pw, fused ? 1 : 2);
+        attn_producer_warp<kStages>(p, &tm_khot, &tm_vhot, &tm_kst, &tm_vst, lo, hi, per, 0, stages, qtile, 0, meta,
+                                    full0, empty0, &s_ready, &s_pub, 1, pw, fused ? 1 : 2, &tm_q, qfree0);
       else if (pw == (fused ? 1 : 2))
-        attn_producer_warp<kStages>(p, &tm_khot, &tm_vhot, &tm_kst, &tm_vst, lo, hi, per, 1, stages, qsm, q_bytes,
-                                    meta, full0, empty0, &s_ready, &s_pub, 1);
+        attn_producer_warp<kStages>(p, &tm_khot, &tm_vhot, &tm_kst, &tm_vst, lo, hi, per, 1, stages, qtile, 0, meta,
+                                    full0, empty0, &s_ready, &s_pub, 1);
       return;
     }
     // ---------------------------------------------------------------- MMA warp
@@ -239,17 +237,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return true;
       };
       int run = 0, pend = -1;
+      uint32_t qrun = qt;
       bool pend_first = false, ok = true;
       for (int s = 0; ok; ++s) {
         const int b = s % kStages;
         if (!mbar_wait(full0 + 8 * b, (s / kStages) & 1, p.status)) break;
         const int flags = meta[b].flags;
         if (flags & kFirst) {
-          // a new run: the previous stage's PV goes first (the softmax warps
-          // read the finished O before they stage the new queries)
-          if (pend >= 0 && !(ok = issue_pv(pend, pend_first))) break;
-          pend = -1;
-          if (!mbar_wait(qready, run & 1, p.status)) break;
+          // a new run, its queries in the Q tile of its parity (they came with
+          // this stage); every MMA issued so far, among them the last that
+          // read the previous run's queries, frees that run's tile once done
+          if (run > 0) tc_commit(qfree0 + 8 * ((run - 1) & 1));
+          qrun = qt + (uint32_t)(run & 1) * 2u * kTcTileBytes;
           ++run;
         }
         tc_fence_after();
@@ -258,7 +257,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-          tc_mma(tmem + (s & 1) * kTcM, smem_desc_sw128(qt + (ks >> 2) * kTcTileBytes + (ks & 3) * 32, 16, 1024),
+          tc_mma(tmem + (s & 1) * kTcM, smem_desc_sw128(qrun + (ks >> 2) * kTcTileBytes + (ks & 3) * 32, 16, 1024),
                  smem_desc_sw128(kb + off, 16, 1024), id_s, ks > 0);
         }
         tc_commit(sfull0 + 8 * (s & 1));
@@ -302,17 +301,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t qm4 = 0;   // the stage's four query masks, one byte each
 #pragma unroll
     for (int i = 0; i < kMaxChunksPerStage; ++i) qm4 |= (uint32_t)meta[b].qm[i] << (8 * i);
-    if (m_flags & kFirst) {
-      // the run's query vectors into the swizzled Q tile
-      const uint8_t *qs = qsm + b * q_bytes;
-      for (int e = tid; e < p.NQ * 16; e += kTcSoftmaxWarps * 32) {
-        const int qv = e >> 4, cg = e & 15;
-        const uint4 v = *reinterpret_cast<const uint4 *>(qs + qv * kQStride + cg * 16);
-        *reinterpret_cast<uint4 *>(qtile + (cg >> 3) * kTcTileBytes + qv * 128 + ((((cg & 7) ^ (qv & 7))) << 4)) = v;
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      asm volatile("bar.sync 1, %0;" ::"r"(kTcSoftmaxWarps * 32) : "memory");
-      if (tid == 0) mbar_arrive(qready);
+    if (m_flags & kFirst) {   // a new run (its queries came by TMA with the stage)
       m_ref = -INFINITY;
       l = 0.f;
     }
@@ -322,10 +311,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tmem_ld16_split<16>(tmem + lane_base + (s & 1) * kTcM + 32 * wh, x);
     // the stage's rows query j sees (loaded and picked)
     const uint32_t cm = active ? (uint32_t)(meta[b].rows_of[j] >> col0) & 0xFFFFu : 0u;
+    // (raw scores here; the scale is applied to the maximum and inside the
+    // exponent: x -> x * scale is increasing, so max(x) * scale is the maximum
+    // of the scaled scores exactly)
 #pragma unroll
-    for (int t = 0; t < 16; ++t) x[t] = ((cm >> t) & 1u) ? x[t] * sl2 : -INFINITY;
+    for (int t = 0; t < 16; ++t) x[t] = ((cm >> t) & 1u) ? x[t] : -INFINITY;
     float pm = fmaxf(fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7]))),
                      fmaxf(fmaxf(fmaxf(x[8], x[9]), fmaxf(x[10], x[11])), fmaxf(fmaxf(x[12], x[13]), fmaxf(x[14], x[15]))));
+    pm *= sl2;
     pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));   // this warp's half of the row
     if (sub == 0) s_pmax[wh][row] = pm;
     // One barrier with an OR reduction both exchanges the halves' maxima and
@@ -366,7 +359,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // top 8 significant bits, lo = p - hi (exact in fp32) the next 8, so
       // hi + lo carries p to ~2^-14 relative
       uint8_t *ph = pbuf + (s & 1) * 2 * kTcTileBytes + row * 128;
-      const float base = m_ref == -INFINITY ? INFINITY : m_ref;   // an all-masked row: every p is 0
+      const float nbase = m_ref == -INFINITY ? -INFINITY : -m_ref;   // an all-masked row: every p is 0
       float gsum[2];
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
@@ -374,7 +367,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t hb[8], lb[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          e[i] = exp2f(x[c2 * 8 + i] - base);
+          e[i] = ex2_approx(fmaf(x[c2 * 8 + i], sl2, nbase));
           hb[i] = __float_as_uint(e[i]) & 0xFFFF0000u;
           lb[i] = __float_as_uint(e[i] - __uint_as_float(hb[i]));
         }
@@ -471,16 +464,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }  // namespace
 
 
-cudaError_t launch_attn_tc(int n_cta, int NQ, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
-                           const CUtensorMap &d, const AttnParams &p, cudaStream_t s) {
-  // dynamic plus the kernel's ~1 KB of static shared memory within 227 KiB
-  const bool four = tc_smem_bytes(4, NQ) + 2048 <= 227 * 1024;
-  const size_t smem = tc_smem_bytes(four ? 4 : 3, NQ);
-  const void *fn = four ? (const void *)k_attn_tc<4> : (const void *)k_attn_tc<3>;
+cudaError_t launch_attn_tc(int n_cta, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
+                           const CUtensorMap &d, const CUtensorMap &tq, const AttnParams &p, cudaStream_t s) {
+  // five stages when they fit beside the kernel's static shared memory in the
+  // per-block limit, else four
+  static int five = -1;
+  if (five < 0) {
+    int dev = 0, optin = 0;
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, (const void *)k_attn_tc<5>);
+    if (e != cudaSuccess) return e;
+    five = tc_smem_bytes(5) + fa.sharedSizeBytes <= (size_t)optin ? 1 : 0;
+  }
+  const size_t smem = tc_smem_bytes(five ? 5 : 4);
+  const void *fn = five ? (const void *)k_attn_tc<5> : (const void *)k_attn_tc<4>;
   cudaError_t e = set_dyn_smem(fn, smem);
   if (e != cudaSuccess) return e;
-  return four ? launch_k(k_attn_tc<4>, dim3(n_cta), dim3(kTcThreads), smem, s, a, b, c, d, p)
-              : launch_k(k_attn_tc<3>, dim3(n_cta), dim3(kTcThreads), smem, s, a, b, c, d, p);
+  return five ? launch_k(k_attn_tc<5>, dim3(n_cta), dim3(kTcThreads), smem, s, a, b, c, d, tq, p)
+              : launch_k(k_attn_tc<4>, dim3(n_cta), dim3(kTcThreads), smem, s, a, b, c, d, tq, p);
 }
 
 int attn_tc_threads() { return kTcThreads; }
