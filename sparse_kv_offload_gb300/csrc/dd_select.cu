@@ -475,13 +475,16 @@ size_t fused_select_smem(int n_q, int C, int k) {
 }
 
 // The kernel asks for at least this much, so that no two of its CTAs share an
-// SM: a CTA that does would run at part speed, and every later unit waits for
-// it in the look-back.  (Launched early behind the scoring kernel, the CTAs
-// would otherwise crowd onto the few SMs that kernel leaves free.)
+// SM while there are SMs enough for one unit each: a CTA that shares one runs
+// at part speed, and every later unit waits for it in the look-back.
+// (Launched early behind the scoring kernel, the CTAs would otherwise crowd
+// onto the few SMs that kernel leaves free.)  With more units than SMs, two
+// CTAs per SM (kSelectMinSmem2 each) run all units in one wave instead of two.
 constexpr size_t kSelectMinSmem = 120 * 1024;
+constexpr size_t kSelectMinSmem2 = 100 * 1024;
 
 template <int NQ>
-__global__ void __launch_bounds__(kFusedThreads, 1) k_select_fused(SelectOut o) {
+__global__ void __launch_bounds__(kFusedThreads, 2) k_select_fused(SelectOut o) {
   extern __shared__ __align__(128) unsigned char fsm_raw[];
   __shared__ int hist[NQ][256];
   __shared__ int scratch[33];
@@ -857,7 +860,8 @@ cudaError_t launch_select_fused(const SelectOut &o, int n_q, cudaStream_t s) {
   if (o.units == 0) return cudaSuccess;
   size_t smem = fused_select_smem(n_q, o.C, o.k);
   if (smem == 0) return cudaErrorInvalidValue;
-  if (smem < kSelectMinSmem) smem = kSelectMinSmem;
+  const size_t floor_bytes = o.units > o.sm_count ? kSelectMinSmem2 : kSelectMinSmem;
+  if (smem < floor_bytes) smem = floor_bytes;
   switch (n_q) {
 #define DD_FUSED_CASE(N)                                                                                      \
   case N: {                                                                                                    \
