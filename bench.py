@@ -308,9 +308,10 @@ def run_reference(args, world, rank):
 # the step scores in one streaming kernel (k_score), then runs top-k and the
 # resolver as one kernel (k_select_fused); the attention is k_attn (mma.sync)
 # up to 16 query vectors per KV head and k_attn_tc (tcgen05) above
-KERNEL_SOURCE = {"gather": ("k_gather", ("dd_gather.cu",)), "attention": ("k_attn", ("dd_attn.cu", "dd_attn.cuh")),
-                 "attention_tc": ("k_attn_tc", ("dd_attn_tc.cu", "dd_attn.cuh")),
-                 "score": ("k_score", ("dd_score.cu",)), "topk": ("k_select_fused", ("dd_select.cu",))}
+KERNEL_SOURCE = {"gather": ("k_gather", ("dd_gather.cu",)),
+                 "attention": ("k_attn", ("dd_attn.cu", "dd_attn.cuh", "dd_tc.cuh")),
+                 "attention_tc": ("k_attn_tc", ("dd_attn_tc.cu", "dd_attn.cuh", "dd_tc.cuh")),
+                 "score": ("k_score_tc", ("dd_score_tc.cu", "dd_tc.cuh")), "topk": ("k_select_fused", ("dd_select.cu",))}
 
 
 def attention_stage(w) -> str:

@@ -7,10 +7,7 @@
 #ifndef DD_ATTN_CUH_
 #define DD_ATTN_CUH_
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include "dd_common.cuh"
+#include "dd_tc.cuh"
 
 namespace dd {
 
@@ -82,22 +79,6 @@ __device__ __forceinline__ int unit_of_chunk_warp(const int32_t *off, int units,
 
 
 // ----------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, int w,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
-      "[%6];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
-      : "memory");
-}
-
 // 2^x by the PTX ex2.approx instruction (results below 2^-126 flushed to 0;
 // 2^-inf = 0); the attention tests hold it to the oracle's tolerance
 __device__ __forceinline__ float ex2_approx(float x) {

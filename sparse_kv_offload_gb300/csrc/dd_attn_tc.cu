@@ -43,36 +43,6 @@ constexpr int kTcTmemCols = 256;                                   // S: 2 x 64 
 constexpr int kTcTileBytes = kTcM * 128;                           // a 64-row, 128-byte-row swizzled tile
 constexpr float kRescaleLog2 = 8.f;                                // lazy rescale threshold (log2 units)
 
-// tcgen05 shared-memory matrix descriptor: start address, leading and stride
-// byte offsets (16-byte units), descriptor version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, A and B
-// major-ness (0 = K-major, 1 = MN-major), N >> 3, M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, int accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// arrives on the mbarrier once every tcgen05 operation this thread issued before has completed
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
 // 16x32bx2 tensor-memory access, 32 columns per thread: threads 0-15 of the
 // warp read lanes 0-15 of its lane quarter at columns [c, c + 32), threads
 // 16-31 the same lanes at columns [c + kSplit, c + kSplit + 32).

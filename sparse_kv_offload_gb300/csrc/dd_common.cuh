@@ -291,6 +291,8 @@ struct Ctx;
 // dynamic shared-memory opt-in of a kernel on the current device, cached (dd_host.cu)
 cudaError_t set_dyn_smem(const void *func, size_t bytes);
 cudaError_t launch_build_landmarks(const uint4 *K, uint4 *lm, int64_t n_chunks, int cs, cudaStream_t s);
+cudaError_t launch_score_tc(const void *q, const void *lm, float *scores, int B, int n_q, int Hq, int Hkv, int C,
+                            int sm_count, int32_t *status, cudaStream_t s, unsigned long long *trace);
 cudaError_t launch_score(const uint4 *q, const uint4 *lm, float *scores, int B, int n_q, int Hq, int Hkv,
                          int C, int sm_count, int32_t *status, cudaStream_t s, unsigned long long *trace = nullptr);
 cudaError_t launch_build_minmax(const uint4 *K, uint4 *lm2, int64_t n_chunks, int cs, cudaStream_t s);

@@ -112,10 +112,13 @@ cudaError_t launch_build_minmax(const uint4 *K, uint4 *lm2, int64_t n_chunks, in
 }
 
 // ---------------------------------------------------------------------------
-// a1: scores[b,j,g,c] = qsum[b,j,g,:] . lm[b,g,c,:] with qsum the fp32 sum of
-// the group's G query heads (mean landmarks), or
-// sum_i max(qsum_i * min_i, qsum_i * max_i) (min/max landmarks: the largest
-// value qsum . k can take over any key k inside the chunk's box).
+// a1 on the CUDA cores, for min/max landmarks: scores[b,j,g,c] =
+// sum_i max(qsum_i * min_i, qsum_i * max_i) with qsum the fp32 sum of the
+// group's G query heads (the largest value qsum . k can take over any key k
+// inside the chunk's box), which is not a product the tensor cores can take.
+// (The kernel also holds the mean-landmark form qsum . lm, which mean
+// landmarks no longer use: they are scored on the tensor cores,
+// dd_score_tc.cu.)
 //
 // The landmarks of all (b,g) units lie end to end in HBM, and scoring reads
 // each of their bytes once, so the kernel is a stream: two CTAs per SM each
@@ -311,9 +314,11 @@ static cudaError_t launch_score_t(const uint4 *q, const uint4 *lm, float *scores
   }
 }
 
+// mean landmarks: a product of the landmark rows with the query vectors, on
+// the tensor cores (dd_score_tc.cu)
 cudaError_t launch_score(const uint4 *q, const uint4 *lm, float *scores, int B, int n_q, int Hq, int Hkv, int C,
                          int sm_count, int32_t *status, cudaStream_t s, unsigned long long *trace) {
-  return launch_score_t<false>(q, lm, scores, B, n_q, Hq, Hkv, C, sm_count, status, trace, s);
+  return launch_score_tc(q, lm, scores, B, n_q, Hq, Hkv, C, sm_count, status, s, trace);
 }
 
 cudaError_t launch_score_minmax(const uint4 *q, const uint4 *lm2, float *scores, int B, int n_q, int Hq, int Hkv,
