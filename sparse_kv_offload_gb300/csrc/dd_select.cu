@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) k_select_fused(SelectOut o) 
   {
     // every row's scores of a 4 x 512-chunk slab in flight at once
     const float *rows = o.scores + ((int64_t)(b * NQ) * Hkv + g) * C;   // row j at + j * Hkv * C
-    uint32_t mn[NQ], mx[NQ];   // over the segments this lane leads
+    uint32_t mn[NQ], mx[NQ];   // over the segments this thread takes
 #pragma unroll
     for (int j = 0; j < NQ; ++j) {
       mn[j] = 0xFFFFFFFFu;
@@ -551,21 +551,32 @@ __global__ void __launch_bounds__(kFusedThreads, 2) k_select_fused(SelectOut o) 
         }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        if (c0 + e * kFusedThreads >= C) break;   // warp-uniform
         const int c = c0 + e * kFusedThreads + lane;
 #pragma unroll
-        for (int j = 0; j < NQ; ++j) {
-          const uint32_t key = c < C ? order_key(v[j][e]) : 0u;
-          if (c < C) keys[j * C + c] = key;
-          uint32_t m = key;
-          for (int off = 1; off < S; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-          if ((lane & (S - 1)) == 0 && c < C) {
-            mn[j] = min(mn[j], m);
-            mx[j] = max(mx[j], m);
-          }
-        }
+        for (int j = 0; j < NQ; ++j)
+          if (c < C) keys[j * C + c] = order_key(v[j][e]);
       }
     }
+    __syncthreads();
+    // segment maxima from shared memory, one segment of S keys per thread and
+    // row (independent loads instead of a shuffle chain per key; the read
+    // order is rotated by the thread so that a warp's 32 segments hit
+    // different banks)
+    const int nseg = (C + S - 1) / S;
+#pragma unroll
+    for (int j = 0; j < NQ; ++j)
+      for (int sg = tid; sg < nseg; sg += kFusedThreads) {
+        const uint32_t *kr = keys + j * C + sg * S;
+        uint32_t m = 0u;
+        if (sg * S + S <= C) {
+#pragma unroll 8
+          for (int i = 0; i < S; ++i) m = max(m, kr[(i + tid) & (S - 1)]);
+        } else {
+          for (int i = 0; i < C - sg * S; ++i) m = max(m, kr[i]);
+        }
+        mn[j] = min(mn[j], m);
+        mx[j] = max(mx[j], m);
+      }
 #pragma unroll
     for (int j = 0; j < NQ; ++j) {
 #pragma unroll
@@ -594,9 +605,13 @@ __global__ void __launch_bounds__(kFusedThreads, 2) k_select_fused(SelectOut o) 
       if (s_state[j] != 0) continue;
       const uint32_t lo = s_lo[j], w = s_w[j];
       const int sh = s_shift[j];
-      for (int c = tid; c < C; c += kFusedThreads) {
-        const uint32_t key = keys[j * C + c];
-        if (key >= lo && key - lo <= w) atomicAdd(&hist[j][(key - lo) >> sh], 1);
+      for (int c0 = tid; c0 < C; c0 += 4 * kFusedThreads) {   // four keys in flight
+        uint32_t kk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) kk[e] = c0 + e * kFusedThreads < C ? keys[j * C + c0 + e * kFusedThreads] : 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (c0 + e * kFusedThreads < C && kk[e] >= lo && kk[e] - lo <= w) atomicAdd(&hist[j][(kk[e] - lo) >> sh], 1);
       }
     }
     __syncthreads();
