@@ -36,7 +36,12 @@ namespace dd {
 
 namespace {
 
-constexpr int kTcSoftmaxWarps = 8;                                 // two per tensor-memory lane quarter
+// Eight softmax warps, two per tensor-memory lane quarter.  (Sixteen, four
+// per quarter with half the columns each, ran the fully resident 32B-class
+// layer's attention at 151 us against 121: at 640 threads a thread gets 96
+// registers and the kernel spills.)
+constexpr int kTcSoftmaxWarps = 8;
+constexpr int kTcColGroups = kTcSoftmaxWarps / 4;                  // warps sharing a lane quarter: column groups
 constexpr int kTcThreads = (kTcSoftmaxWarps + 4) * 32;             // + 2 issuing warps, copier / finisher, MMA warp
 constexpr int kTcM = 64;                                           // query vectors per MMA (M)
 constexpr int kTcTmemCols = 256;                                   // S: 2 x 64 columns, O: 128 columns
@@ -92,6 +97,43 @@ __device__ __forceinline__ void tmem_st32_split(uint32_t taddr, const float *v) 
       "n"(kSplit), DD_W32(r)
       : "memory");
 }
+template <int kSplit>
+__device__ __forceinline__ void tmem_ld8_split(uint32_t taddr, float *v) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr), "n"(kSplit));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int kSplit>
+__device__ __forceinline__ void tmem_st16_split(uint32_t taddr, const float *v) {
+  uint32_t r[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(v[i]);
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17};"
+      ::"r"(taddr), "n"(kSplit), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+      "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// A thread's columns of S (kCols = 16 or 8) or O (32 or 16), in the 16x32bx2
+// layout: threads 0-15 at [c, c + kCols), threads 16-31 at [c + kCols, c + 2 kCols).
+template <int kCols>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float *v) {
+  if constexpr (kCols == 32) tmem_ld32_split<32>(taddr, v);
+  else if constexpr (kCols == 16) tmem_ld16_split<16>(taddr, v);
+  else tmem_ld8_split<8>(taddr, v);
+}
+template <int kCols>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float *v) {
+  if constexpr (kCols == 32) tmem_st32_split<32>(taddr, v);
+  else tmem_st16_split<16>(taddr, v);
+}
 #undef DD_R32
 #undef DD_W32
 
@@ -126,7 +168,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   __shared__ int s_fix, s_ready, s_pub;
   __shared__ uint32_t s_tmem;
-  __shared__ float s_pmax[2][kTcM], s_lsum[2][kTcM];   // the two column halves of each row
+  // per column group of each row: the stage maxima, and at a run end the row
+  // sums (the same words: a run end reads the sums before a barrier that every
+  // thread passes before it writes the next stage's maxima)
+  __shared__ float s_red[kTcColGroups][kTcM];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   // The V halves of the tile ring start zeroed: rows of chunk slots that a
@@ -250,13 +295,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 
   // -------------------------------------------------------------- softmax warps
-  // Row r = 16 * (warp & 3) + (lane & 15) is query vector r.  Warps w and w + 4
-  // read the same tensor-memory lane quarter and take the left and right
-  // halves of each row; inside a warp the 16x32bx2 access gives lanes t and
-  // t + 16 the two quarters of that half: 16 columns of S and 32 of O each.
-  const int wq = warp & 3, wh = warp >> 2, sub = lane >> 4;
+  // Row r = 16 * (warp & 3) + (lane & 15) is query vector r.  The
+  // kTcColGroups warps w, w + 4, ... read the same tensor-memory lane quarter
+  // and take the row's columns in as many groups (warp >> 2); inside a warp
+  // the 16x32bx2 access gives lanes t and t + 16 the two halves of a group:
+  // kSCols columns of S and kOCols of O each.
+  constexpr int kSCols = kTcM / (2 * kTcColGroups), kOCols = 128 / (2 * kTcColGroups);
+  const int wq = warp & 3, wc = warp >> 2, sub = lane >> 4;
   const int row = 16 * wq + (lane & 15);
-  const int col0 = 32 * wh + 16 * sub;           // this thread's S columns [col0, col0 + 16)
+  const int col0 = (2 * wc + sub) * kSCols;      // this thread's S columns [col0, col0 + kSCols)
+  const int ocol = (2 * wc + sub) * kOCols;      // and O columns
   const bool active = row < p.NQ;
   const int j = active ? row / p.G : 0;
   const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
@@ -277,20 +325,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (!mbar_wait(sfull0 + 8 * (s & 1), (s >> 1) & 1, p.status)) break;
     tc_fence_after();
-    float x[16];
-    tmem_ld16_split<16>(tmem + lane_base + (s & 1) * kTcM + 32 * wh, x);
+    float x[kSCols];
+    tmem_ld_cols<kSCols>(tmem + lane_base + (s & 1) * kTcM + 2 * kSCols * wc, x);
     // the stage's rows query j sees (loaded and picked)
-    const uint32_t cm = active ? (uint32_t)(meta[b].rows_of[j] >> col0) & 0xFFFFu : 0u;
+    const uint32_t cm = active ? (uint32_t)(meta[b].rows_of[j] >> col0) & ((1u << kSCols) - 1u) : 0u;
     // (raw scores here; the scale is applied to the maximum and inside the
     // exponent: x -> x * scale is increasing, so max(x) * scale is the maximum
     // of the scaled scores exactly)
 #pragma unroll
-    for (int t = 0; t < 16; ++t) x[t] = ((cm >> t) & 1u) ? x[t] : -INFINITY;
-    float pm = fmaxf(fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7]))),
-                     fmaxf(fmaxf(fmaxf(x[8], x[9]), fmaxf(x[10], x[11])), fmaxf(fmaxf(x[12], x[13]), fmaxf(x[14], x[15]))));
+    for (int t = 0; t < kSCols; ++t) x[t] = ((cm >> t) & 1u) ? x[t] : -INFINITY;
+    float pm = x[0];
+#pragma unroll
+    for (int t = 1; t < kSCols; ++t) pm = fmaxf(pm, x[t]);
     pm *= sl2;
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));   // this warp's half of the row
-    if (sub == 0) s_pmax[wh][row] = pm;
+    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));   // this warp's group of the row
+    if (sub == 0) s_red[wc][row] = pm;
     // One barrier with an OR reduction both exchanges the halves' maxima and
     // takes the group's vote on a rescale (a row's maximum exceeds its
     // reference by more than 2^8 iff one of its halves does).  Before P(s)
@@ -304,7 +353,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         : "=r"(group_rescale)
         : "r"((uint32_t)(pm > m_ref + kRescaleLog2)), "r"(kTcSoftmaxWarps * 32)
         : "memory");
-    const float mx = fmaxf(pm, s_pmax[wh ^ 1][row]);
+    float mx = pm;
+#pragma unroll
+    for (int c = 0; c < kTcColGroups; ++c) mx = fmaxf(mx, s_red[c][row]);
     float factor = 1.f;
     if (mx > m_ref + kRescaleLog2) {
       if (m_ref != -INFINITY) factor = exp2f(m_ref - mx);
@@ -315,12 +366,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     if (__any_sync(0xffffffffu, factor != 1.f)) {
       // the accumulator moves to the new reference, before PV(s): this
-      // thread's 32 columns of O
-      float o[32];
-      tmem_ld32_split<32>(tmem_o + lane_base + 64 * wh, o);
+      // thread's columns of O
+      float o[kOCols];
+      tmem_ld_cols<kOCols>(tmem_o + lane_base + 2 * kOCols * wc, o);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] *= factor;
-      tmem_st32_split<32>(tmem_o + lane_base + 64 * wh, o);
+      for (int i = 0; i < kOCols; ++i) o[i] *= factor;
+      tmem_st_cols<kOCols>(tmem_o + lane_base + 2 * kOCols * wc, o);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       l *= factor;
     }
@@ -330,9 +381,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // hi + lo carries p to ~2^-14 relative
       uint8_t *ph = pbuf + (s & 1) * 2 * kTcTileBytes + row * 128;
       const float nbase = m_ref == -INFINITY ? -INFINITY : -m_ref;   // an all-masked row: every p is 0
-      float gsum[2];
+      float gsum[kSCols / 8];
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
+      for (int c2 = 0; c2 < kSCols / 8; ++c2) {
         float e[8];
         uint32_t hb[8], lb[8];
 #pragma unroll
@@ -351,7 +402,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         *reinterpret_cast<uint4 *>(ph + off) = h;
         *reinterpret_cast<uint4 *>(ph + kTcTileBytes + off) = lw;
       }
-      l += gsum[0] + gsum[1];
+#pragma unroll
+      for (int c2 = 0; c2 < kSCols / 8; ++c2) l += gsum[c2];
     }
     // V rows of chunk slots this stage did not load: zero (their P is 0)
     if (!(m_flags & kFull))
@@ -373,16 +425,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!mbar_wait(pvdone0 + 8 * (s & 1), (s >> 1) & 1, p.status)) break;
       tc_fence_after();
       const float lh = l + __shfl_xor_sync(0xffffffffu, l, 16);
-      if (sub == 0) s_lsum[wh][row] = lh;
+      if (sub == 0) s_red[wc][row] = lh;
       asm volatile("bar.sync 1, %0;" ::"r"(kTcSoftmaxWarps * 32) : "memory");
-      const float lrow = s_lsum[0][row] + s_lsum[1][row];
+      float lrow = 0.f;
+#pragma unroll
+      for (int c = 0; c < kTcColGroups; ++c) lrow += s_red[c][row];
+      asm volatile("bar.sync 1, %0;" ::"r"(kTcSoftmaxWarps * 32) : "memory");   // the sums are read
       const int c0 = m_uoff / per, c1 = (m_uoff + m_ucnt - 1) / per;
       const bool direct = c0 == c1 && p.k_tail == nullptr;
       const bool handoff = c0 != c1 && p.kh == nullptr && m_uoff < lo && !(m_flags & kEnd);
       const int bb = m_unit / p.Hkv, g = m_unit - bb * p.Hkv;
       float *dst = nullptr;
       float inv = 1.f;
-      const int ocol = 64 * wh + 32 * sub;   // this thread's 32 columns of O
       if (active) {
         if (direct) {
           const int h = g * p.G + (row - j * p.G);
@@ -391,15 +445,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         } else {
           const int64_t k = ((int64_t)blockIdx.x + m_unit) * p.NQ + row;
           dst = p.part_o + k * 128 + ocol;
-          if (wh == 0 && sub == 0) *reinterpret_cast<float2 *>(p.part_ml + k * 2) = make_float2(m_ref, lrow);
+          if (wc == 0 && sub == 0) *reinterpret_cast<float2 *>(p.part_ml + k * 2) = make_float2(m_ref, lrow);
         }
       }
       {
-        float o[32];
-        tmem_ld32_split<32>(tmem_o + lane_base + 64 * wh, o);
+        float o[kOCols];
+        tmem_ld_cols<kOCols>(tmem_o + lane_base + 2 * kOCols * wc, o);
         if (active) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
+          for (int i = 0; i < kOCols; i += 4)
             *reinterpret_cast<float4 *>(dst + i) = make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
         }
       }
