@@ -104,7 +104,22 @@ def test_landmarks_bit_exact(dd, w, where):
 
 # ------------------------------------------------------------------ a1 scores
 
-@pytest.mark.parametrize("w", [TINY, V_5Q, V_NQ64, V_ZIPF], ids=lambda w: w.name)
+# the tensor-core scoring's instantiations: N = NQ rounded up to 16 (16, 32,
+# 48, 64) with the group size unrolled (G = 4, 8) or generic (G = 1, 2, 6,
+# 16); C = 1000 leaves a ragged last tile of 104 landmark rows, and several
+# units share a CTA's span of tiles
+def _sc(name, Hq, Hkv, n_q, B=3, L=16000, seed=0):
+    return Workload(name, B=B, Hq=Hq, Hkv=Hkv, d=128, L=L, cs=16, k=8, n_q=n_q,
+                    spec_scale=(0.0,) + (0.2,) * (n_q - 1), seed=300 + seed)
+
+
+SCORE_TC_CASES = [_sc("g1_nq3", 8, 8, 3, seed=1), _sc("g2_nq16", 8, 4, 8, seed=2), _sc("g16_nq64", 32, 2, 4, seed=3),
+                  _sc("g16_nq32", 32, 2, 2, seed=4), _sc("g6_nq48", 12, 2, 8, seed=5),
+                  _sc("g8_nq16", 64, 8, 2, seed=6), _sc("g8_nq24", 64, 8, 3, seed=7),
+                  _sc("g4_nq32", 32, 8, 8, seed=8), _sc("g4_nq20", 32, 8, 5, seed=9)]
+
+
+@pytest.mark.parametrize("w", [TINY, V_5Q, V_NQ64, V_ZIPF] + SCORE_TC_CASES, ids=lambda w: w.name)
 def test_scores_within_fp32_bound(dd, w):
     import torch
     q = synth.queries(w.seed, w.B, w.n_q, w.Hq, w.d, w.spec_scale)
