@@ -576,6 +576,7 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
     o.status = c->status;
     o.trace = trace ? trace + 2 * dd::kTraceSlots : nullptr;
     o.sm_count = c->sm_count;
+    o.after_tc_score = a->lm_kind == DD_LM_MEAN;
     DD_CUDA(dd::launch_select_fused(o, d.n_q, s));
     DD_TRY(mark(2));
     c->launches += 1;

@@ -318,6 +318,7 @@ struct SelectOut {
   int32_t *status;
   unsigned long long *trace;      // optional [2][kTraceSlots]: per-SM earliest start, latest end (ns)
   int sm_count;                   // SMs of the device (two CTAs per SM when the units outnumber them)
+  bool after_tc_score;            // launched behind the tensor-core scoring kernel (one CTA on every SM)
 };
 size_t fused_select_smem(int n_q, int C, int k);
 cudaError_t launch_select_fused(const SelectOut &o, int n_q, cudaStream_t s);

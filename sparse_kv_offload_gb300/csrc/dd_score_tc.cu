@@ -56,7 +56,7 @@ constexpr size_t kScSmem = 1024 + (size_t)kScStages * kScTile + 4 * (size_t)kScQ
 template <int NQP, int GT>
 __global__ void __launch_bounds__(kScThreads, 1)
     k_score_tc(const __grid_constant__ CUtensorMap tm_lm, const __grid_constant__ CUtensorMap tm_q,
-               float *__restrict__ scores, int n_q, int G, int Hkv, int C, int64_t total_tiles, int64_t per_cta,
+               float *__restrict__ scores, int n_q, int G, int Hkv, int C, int64_t total_tiles,
                int32_t *status, unsigned long long *trace) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -69,8 +69,11 @@ __global__ void __launch_bounds__(kScThreads, 1)
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tpu = (C + kScRows - 1) / kScRows;   // tiles per unit
-  const int64_t t0 = (int64_t)blockIdx.x * per_cta;
-  const int64_t t1 = t0 + per_cta < total_tiles ? t0 + per_cta : total_tiles;
+  // CTA c takes tiles [c T / n, (c + 1) T / n) of all T: spans differ by one
+  // tile at most, and every SM holds one CTA (a selection CTA launched early
+  // then finds room for exactly one of its own beside it on each SM)
+  const int64_t t0 = (int64_t)blockIdx.x * total_tiles / gridDim.x;
+  const int64_t t1 = ((int64_t)blockIdx.x + 1) * total_tiles / gridDim.x;
   if (t0 >= t1) return;
   const int n = (int)(t1 - t0);
   const int NQ = n_q * G;
@@ -239,16 +242,14 @@ cudaError_t launch_score_tc(const void *q, const void *lm, float *scores, int B,
   CUtensorMap tlm, tq;
   if (!make_pool_map(&tlm, lm, units * C, kScRows) || !make_q_map(&tq, q, B, n_q, Hq, G)) return cudaErrorInvalidValue;
   const int64_t total = units * ((C + kScRows - 1) / kScRows);
-  const int64_t ctas = sm_count > 0 && sm_count < total ? sm_count : total;
-  const int64_t per = (total + ctas - 1) / ctas;
-  const int grid = (int)((total + per - 1) / per);
+  const int grid = (int)(sm_count > 0 && sm_count < total ? sm_count : total);
   const int P = (NQ + 15) / 16;
 #define DD_SCORE_TC(NQP, GT)                                                                                   \
   do {                                                                                                          \
     cudaError_t e = set_dyn_smem((const void *)k_score_tc<NQP, GT>, kScSmem);                                  \
     if (e != cudaSuccess) return e;                                                                             \
     return launch_k(k_score_tc<NQP, GT>, dim3(grid), dim3(kScThreads), kScSmem, s, tlm, tq, scores, n_q, G,     \
-                    Hkv, C, total, per, status, trace);                                                         \
+                    Hkv, C, total, status, trace);                                                              \
   } while (0)
   // the common group sizes with their column sums unrolled, any other G generically
   if (G == 8) {

@@ -474,14 +474,19 @@ size_t fused_select_smem(int n_q, int C, int k) {
   return bytes <= kSelectMaxSmem ? bytes : 0;
 }
 
-// The kernel asks for at least this much, so that no two of its CTAs share an
-// SM while there are SMs enough for one unit each: a CTA that shares one runs
-// at part speed, and every later unit waits for it in the look-back.
-// (Launched early behind the scoring kernel, the CTAs would otherwise crowd
-// onto the few SMs that kernel leaves free.)  With more units than SMs, two
-// CTAs per SM (kSelectMinSmem2 each) run all units in one wave instead of two.
+// No two of the kernel's CTAs should share an SM while there are SMs enough
+// for one unit each: a CTA that shares one runs at part speed, and every later
+// unit waits for it in the look-back.  Behind the tensor-core scoring, which
+// holds one CTA and ~198 KB of shared memory on every SM, a CTA of up to
+// kSelectCoSmem bytes launched early fits beside it once per SM and no
+// twice: it then waits at its dependency wait, already resident, and starts
+// the moment the scores are in.  Otherwise (larger rows, or behind the
+// min/max scoring) it asks for kSelectMinSmem, one CTA per SM.  With more
+// units than SMs, two CTAs per SM (kSelectMinSmem2 each) run all units in one
+// wave instead of two.
 constexpr size_t kSelectMinSmem = 120 * 1024;
 constexpr size_t kSelectMinSmem2 = 100 * 1024;
+constexpr size_t kSelectCoSmem = 20 * 1024;
 
 template <int NQ>
 __global__ void __launch_bounds__(kFusedThreads, 2) k_select_fused(SelectOut o) {
@@ -876,7 +881,8 @@ cudaError_t launch_select_fused(const SelectOut &o, int n_q, cudaStream_t s) {
   size_t smem = fused_select_smem(n_q, o.C, o.k);
   if (smem == 0) return cudaErrorInvalidValue;
   const size_t floor_bytes = o.units > o.sm_count ? kSelectMinSmem2 : kSelectMinSmem;
-  if (smem < floor_bytes) smem = floor_bytes;
+  if (!(o.units <= o.sm_count && o.after_tc_score && smem <= kSelectCoSmem) && smem < floor_bytes)
+    smem = floor_bytes;
   switch (n_q) {
 #define DD_FUSED_CASE(N)                                                                                      \
   case N: {                                                                                                    \
