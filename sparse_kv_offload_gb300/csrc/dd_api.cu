@@ -9,7 +9,7 @@
 
 #include <vector>
 
-#include "dd_common.cuh"
+#include "dd_tc.cuh"
 
 struct dd_ctx {
   dd_dims dims;
@@ -536,19 +536,22 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   };
   DD_TRY(mark(0));
   const dd_dims &d = c->dims;
-  // scoring streams every landmark once over all SMs; then top-k, union,
-  // residency, global ordinals and the attention plan run in one kernel per
-  // (b,g) when a unit's score rows fit in shared memory (fixed k only), and as
-  // separate stage kernels otherwise
-  if (a->lm_kind == DD_LM_MINMAX) {
-    DD_TRY(score_impl(c, a->q, a->lm, scores, true, trace, stream));
-  } else {
-    DD_TRY(score_impl(c, a->q, a->lm, scores, false, trace, stream));
-  }
-  DD_TRY(mark(1));
+  // Top-k, union, residency, global ordinals and the attention plan run in
+  // one kernel per (b,g) when a unit's score rows fit in shared memory (fixed
+  // k only), and as separate stage kernels otherwise.  The scoring streams
+  // every landmark once over all SMs before it, except when mean landmarks'
+  // units fill most SMs in one wave: the selection kernel then streams and
+  // scores its own unit on the tensor cores.
   const bool fused = a->mass_gamma <= 0.f && dd::fused_select_smem(d.n_q, c->C, d.k) > 0;
+  const int ss_stages = fused && a->lm_kind == DD_LM_MEAN && a->q && a->lm && aligned16(a->q) && aligned16(a->lm)
+                            ? dd::score_select_stages(c->units, c->sm_count, d.n_q, c->C, d.k)
+                            : 0;
+  if (ss_stages == 0) {
+    DD_TRY(score_impl(c, a->q, a->lm, scores, a->lm_kind == DD_LM_MINMAX, trace, stream));
+    DD_TRY(mark(1));
+  }
   if (fused) {
-    dd::SelectOut o;
+    dd::SelectOut o{};
     o.scores = scores;
     o.sel = a->sel;
     o.attn_slot = a->attn_slot;
@@ -577,7 +580,16 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
     o.trace = trace ? trace + 2 * dd::kTraceSlots : nullptr;
     o.sm_count = c->sm_count;
     o.after_tc_score = a->lm_kind == DD_LM_MEAN;
-    DD_CUDA(dd::launch_select_fused(o, d.n_q, s));
+    if (ss_stages > 0) {
+      if (!dd::make_pool_map(&o.tm_lm, a->lm, (int64_t)c->units * c->C, 128)) return DD_ERR_CUDA;
+      o.q16 = static_cast<const uint16_t *>(a->q);
+      o.scores_out = a->scores;
+      o.trace_score = trace;
+      DD_CUDA(dd::launch_score_select(o, d.n_q, ss_stages, s));
+      DD_TRY(mark(1));
+    } else {
+      DD_CUDA(dd::launch_select_fused(o, d.n_q, s));
+    }
     DD_TRY(mark(2));
     c->launches += 1;
   } else {

@@ -1,6 +1,7 @@
 // Shared device helpers of libdd (CUDA path only).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -319,9 +320,20 @@ struct SelectOut {
   unsigned long long *trace;      // optional [2][kTraceSlots]: per-SM earliest start, latest end (ns)
   int sm_count;                   // SMs of the device (two CTAs per SM when the units outnumber them)
   bool after_tc_score;            // launched behind the tensor-core scoring kernel (one CTA on every SM)
+  // scoring folded in (mean landmarks): the landmarks as a 2-D tensor map
+  // ([units * C, 128] bf16, boxes of 128 rows x 64 columns), the queries, the
+  // score rows when asked for, the scoring phase's timing words
+  CUtensorMap tm_lm;
+  const uint16_t *q16;
+  float *scores_out;
+  unsigned long long *trace_score;
 };
 size_t fused_select_smem(int n_q, int C, int k);
 cudaError_t launch_select_fused(const SelectOut &o, int n_q, cudaStream_t s);
+// the ring stages of the kernel with the scoring folded in for this step (0:
+// the two-kernel path: units not filling one wave of SMs, or too large)
+int score_select_stages(int units, int sm_count, int n_q, int C, int k);
+cudaError_t launch_score_select(const SelectOut &o, int n_q, int stages, cudaStream_t s);
 cudaError_t launch_selftest_wait(int kind, const unsigned long long *word, int32_t *status, cudaStream_t s);
 cudaError_t launch_topk_mass(const float *scores, int32_t *sel, int32_t *sel_cnt, int rows, int C, int k_max,
                              int k_min, float gamma, float tau_log2e, cudaStream_t s);

@@ -5,7 +5,9 @@
 // of all queries of a request are resolved together (hot pool first, host for
 // the rest), so a chunk wanted by several queries crosses the host link a
 // single time; attention still uses each query's own top-k.
-#include "dd_common.cuh"
+#include <algorithm>
+
+#include "dd_tc.cuh"
 
 namespace dd {
 
@@ -488,33 +490,231 @@ constexpr size_t kSelectMinSmem = 120 * 1024;
 constexpr size_t kSelectMinSmem2 = 100 * 1024;
 constexpr size_t kSelectCoSmem = 20 * 1024;
 
+// ---------------------------------------------------------------------------
+// Scoring folded into the selection, on the tensor cores (mean landmarks;
+// taken when the units fill most SMs in one wave, one CTA per SM).  The CTA
+// streams its own unit's C landmark rows through a ring of 128-row tiles (two
+// 2-D TMA boxes a tile, the first stages requested before the dependency
+// wait) and scores them as a product with the unit's n_q group-summed
+// queries, each fp32 group sum split into three bf16 parts (hi + mid + lo
+// equals it exactly, so each part's product is exact in fp32 and the three
+// add up to the fp32 dot product within fp32 accumulation): M = 128
+// landmarks, N = 3 n_q rounded up to 16, K = 128, fp32 accumulators in
+// tensor memory (two buffers).  Warps 0-3 read their lane (one landmark) and
+// write the order keys straight into the key rows; warp 4 issues the tile
+// copies, warp 5 the MMAs, warps 6-15 build the query tile.  The kernel
+// boundary, the round trip of the score rows through L2 and the rows' load
+// disappear from the step; the selection then runs as below.
+// ---------------------------------------------------------------------------
+constexpr int kFsRows = 128;                 // landmark rows per tile (M)
+constexpr int kFsHalf = kFsRows * 128;       // a 64-column half of a tile, 16 KiB
+constexpr int kFsTile = 2 * kFsHalf;         // 32 KiB
+constexpr int kFsMaxStages = 5;
+constexpr int kFsQHalf = 32 * 128;           // a 64-column half of the query tile (3 n_q <= 24 rows, 32 kept)
+constexpr int kFsTmemCols = 64;              // two accumulators of up to 32 columns
+
+// where the kernel with scoring folded in keeps its parts: the key rows and
+// selections, then (1024-aligned) the query tile and the ring, which the
+// selection's union scratch reuses once the scores are in
+__host__ __device__ inline size_t fs_head_bytes(int nq, int C, int k) {
+  return (((size_t)nq * C + (size_t)nq * k) * 4 + 1023) & ~(size_t)1023;
+}
+size_t score_select_tc_smem(int n_q, int C, int k, int stages) {
+  const size_t W = (size_t)(C + 31) / 32;
+  const size_t tail = std::max((size_t)2 * kFsQHalf + (size_t)stages * kFsTile, ((size_t)n_q + 4) * W * 4);
+  return 1024 + fs_head_bytes(n_q, C, k) + tail;   // + the alignment of the dynamic base
+}
+
+// bf16 of x rounded to nearest even, and its value as a float
+__device__ __forceinline__ uint16_t bf16_rn_bits(float x) {
+  uint16_t h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(x));
+  return h;
+}
+
 template <int NQ>
-__global__ void __launch_bounds__(kFusedThreads, 2) k_select_fused(SelectOut o) {
+__device__ __forceinline__ void fused_tc_score(const SelectOut &o, int unit, int b, int g, uint32_t *keys,
+                                               uint8_t *qtile, uint8_t *ring, uint64_t *bars, uint32_t tmem,
+                                               int n_stages) {
+  constexpr int NB = 3 * NQ;                           // B rows: the hi, mid, lo parts of each query's sum
+  constexpr int NQP = NB <= 16 ? 16 : 32;              // N of the MMA
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int C = o.C, Hq = o.Hq, Hkv = o.Hkv, G = Hq / Hkv;
+  const int nt = (C + kFsRows - 1) / kFsRows;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kFsMaxStages);
+  const uint32_t afull0 = smem_u32(bars + 2 * kFsMaxStages), aempty0 = smem_u32(bars + 2 * kFsMaxStages + 2);
+  const uint32_t mmadone = smem_u32(bars + 2 * kFsMaxStages + 4);
+  const int row_base = unit * C;
+  const int pre = nt < n_stages ? nt : n_stages;
+  if (warp == 4 && lane == 0) {
+    // the landmarks are not written by the kernels this one may overlap: the
+    // first stages go out before the dependency wait (bytes expected now,
+    // the arrivals after it)
+    for (int s = 0; s < pre; ++s) {
+      const uint32_t bar = full0 + 8 * s, dst = smem_u32(ring + s * kFsTile);
+      mbar_expect_tx(bar, (uint32_t)kFsTile);
+      tma_load_2d(dst, &o.tm_lm, 0, row_base + s * kFsRows, bar);
+      tma_load_2d(dst + kFsHalf, &o.tm_lm, 64, row_base + s * kFsRows, bar);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (o.trace_score && tid == 0) trace_start(o.trace_score);
+  if (warp >= 6) {
+    // ------------------------------------------------ the query tile (B)
+    // row 3j + p: part p of query j's fp32 group sum (heads in order);
+    // column i at the 128-byte-swizzled place of a K-major tile
+    for (int e = tid - 192; e < NQP * 128; e += kFusedThreads - 192) {
+      const int r = e >> 7, i = e & 127;
+      uint16_t v = 0;
+      if (r < NB) {
+        const int j = r / 3, part = r - 3 * j;
+        float sum = 0.f;
+        for (int h = g * G; h < (g + 1) * G; ++h)
+          sum += __uint_as_float((uint32_t)o.q16[((int64_t)(b * NQ + j) * Hq + h) * 128 + i] << 16);
+        const uint16_t hi = bf16_rn_bits(sum);
+        const float r1 = sum - __uint_as_float((uint32_t)hi << 16);
+        const uint16_t mid = bf16_rn_bits(r1);
+        const float r2 = r1 - __uint_as_float((uint32_t)mid << 16);
+        v = part == 0 ? hi : (part == 1 ? mid : bf16_rn_bits(r2));
+      }
+      const int half = i >> 6, cc = i & 63;
+      *reinterpret_cast<uint16_t *>(qtile + half * kFsQHalf + r * 128 + ((((cc >> 3) ^ (r & 7))) << 4) + (cc & 7) * 2) = v;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("bar.arrive 3, %0;" ::"r"(kFusedThreads - 160) : "memory");   // warps 5-15
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA
+    asm volatile("bar.sync 3, %0;" ::"r"(kFusedThreads - 160) : "memory");   // the query tile is written
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kFsRows, NQP, 0, 0), qb = smem_u32(qtile);
+      for (int s = 0; s < nt; ++s) {
+        const int slot = s % n_stages, buf = s & 1;
+        if (!mbar_wait(full0 + 8 * slot, (s / n_stages) & 1, o.status)) break;
+        if (s >= 2 && !mbar_wait(aempty0 + 8 * buf, ((s >> 1) - 1) & 1, o.status)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(ring + slot * kFsTile);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          tc_mma(tmem + buf * 32, smem_desc_sw128(a0 + (ks >> 2) * kFsHalf + (ks & 3) * 32, 16, 1024),
+                 smem_desc_sw128(qb + (ks >> 2) * kFsQHalf + (ks & 3) * 32, 16, 1024), idesc, ks > 0);
+        tc_commit(empty0 + 8 * slot);
+        tc_commit(afull0 + 8 * buf);
+      }
+      tc_commit(mmadone);
+      mbar_wait(mmadone, 0, o.status);
+    }
+    __syncwarp();
+  } else if (warp == 4) {
+    // ------------------------------------------------------- tile copies
+    if (lane == 0)
+      for (int s = 0; s < nt; ++s) {
+        const int slot = s % n_stages;
+        if (s >= n_stages && !mbar_wait(empty0 + 8 * slot, ((s / n_stages) - 1) & 1, o.status)) break;
+        const uint32_t bar = full0 + 8 * slot;
+        if (s < pre) {
+          mbar_arrive(bar);
+        } else {
+          const uint32_t dst = smem_u32(ring + slot * kFsTile);
+          mbar_arrive_expect_tx(bar, (uint32_t)kFsTile);
+          tma_load_2d(dst, &o.tm_lm, 0, row_base + s * kFsRows, bar);
+          tma_load_2d(dst + kFsHalf, &o.tm_lm, 64, row_base + s * kFsRows, bar);
+        }
+      }
+  } else {
+    // ---------------------------------------------- epilogue, warps 0-3
+    const int row = 32 * warp + lane;   // this thread's tensor-memory lane: landmark row of a tile
+    for (int s = 0; s < nt; ++s) {
+      const int buf = s & 1;
+      if (!mbar_wait(afull0 + 8 * buf, (s >> 1) & 1, o.status)) break;
+      tc_fence_after();
+      float v[NQP];
+#pragma unroll
+      for (int c = 0; c < NQP / 16; ++c) tmem_ld32x32b_x16(tmem + ((uint32_t)(32 * warp) << 16) + buf * 32 + 16 * c, v + 16 * c);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(aempty0 + 8 * buf);
+      const int c = s * kFsRows + row;
+      if (c < C) {
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+          const float sc = (v[3 * j] + v[3 * j + 1]) + v[3 * j + 2];
+          keys[j * C + c] = order_key(sc);
+          if (o.scores_out) o.scores_out[((int64_t)(b * NQ + j) * Hkv + g) * C + c] = sc;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();   // every key row is in place; the tensor memory is no longer read
+  if (warp == 5) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kFsTmemCols) : "memory");
+  }
+  if (o.trace_score && tid == 0) trace_end(o.trace_score);
+}
+
+template <int NQ, bool kScore>
+__global__ void __launch_bounds__(kFusedThreads, kScore ? 1 : 2)
+    k_select_fused(const __grid_constant__ SelectOut o, int n_stages) {
   extern __shared__ __align__(128) unsigned char fsm_raw[];
   __shared__ int hist[NQ][256];
   __shared__ int scratch[33];
   __shared__ int s_unit, s_uoff, s_moff;
   __shared__ uint32_t s_epoch;
-  pdl_wait();
-  pdl_trigger();
+  __shared__ __align__(8) uint64_t s_bars[2 * kFsMaxStages + 5];   // scoring folded in: full, empty, acc full/empty, done
+  __shared__ uint32_t s_tmem;
+  // With the scoring folded in, the ticket and the first landmark stages come
+  // before the dependency wait (the selection launched two kernels earlier
+  // has finished: the kernel in between waited for it before it released
+  // this one, so the counters are reset); everything it writes comes after.
+  if (!kScore) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
-    if (o.trace) trace_start(o.trace);
+    if (o.trace && !kScore) trace_start(o.trace);
     s_unit = atomicAdd(o.ticket, 1);                       // units in the order their CTAs start
     // this launch's look-back epoch; the previous launch's last CTA advanced it
     s_epoch = *reinterpret_cast<volatile uint32_t *>(o.ticket + 2);
+    if (kScore) {
+      for (int i = 0; i < 2 * kFsMaxStages + 5; ++i)
+        mbar_init(smem_u32(&s_bars[i]), i == 2 * kFsMaxStages + 2 || i == 2 * kFsMaxStages + 3 ? 4 : 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
   }
+  if (kScore && warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(kFsTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (kScore) tc_fence_before();
   __syncthreads();
+  if (kScore) tc_fence_after();
   const int unit = s_unit;
   const uint32_t epoch = s_epoch;
   const int C = o.C, k = o.k, Hkv = o.Hkv;
   const int b = unit / Hkv, g = unit - b * Hkv;
   const int W = (C + 31) >> 5;
-  uint32_t *qbits = reinterpret_cast<uint32_t *>(fsm_raw);                   // [NQ][W]
+  uint32_t *keys, *qbits;
+  int32_t *sel_s;
+  uint8_t *tail = nullptr;
+  if (kScore) {
+    uint8_t *base = fsm_raw + ((1024u - (smem_u32(fsm_raw) & 1023u)) & 1023u);
+    keys = reinterpret_cast<uint32_t *>(base);                       // [NQ][C]
+    sel_s = reinterpret_cast<int32_t *>(keys + NQ * C);              // [NQ][k]
+    tail = base + fs_head_bytes(NQ, C, k);                           // query tile + ring, then the union scratch
+    qbits = reinterpret_cast<uint32_t *>(tail);
+  } else {
+    qbits = reinterpret_cast<uint32_t *>(fsm_raw);                   // [NQ][W]
+    keys = qbits + (NQ + 4) * W;
+    sel_s = reinterpret_cast<int32_t *>(keys + NQ * C);
+  }
   uint32_t *ubw = qbits + NQ * W, *mbw = ubw + W;
   int *upre = reinterpret_cast<int *>(mbw + W), *mpre = upre + W;
-  uint32_t *keys = reinterpret_cast<uint32_t *>(mpre + W);    // [NQ][C]
-  int32_t *sel_s = reinterpret_cast<int32_t *>(keys + NQ * C);   // [NQ][k]
 
   // ---- a2: the top k of every row (score descending, lower chunk first among
   // equal scores), as one bitmap per row.  The row is split into at least k
@@ -536,15 +736,20 @@ __global__ void __launch_bounds__(kFusedThreads, 2) k_select_fused(SelectOut o) 
     s_hi[tid] = 0u;
   }
   __syncthreads();
+  if (kScore) {
+    fused_tc_score<NQ>(o, unit, b, g, keys, tail, tail + 2 * kFsQHalf, s_bars, s_tmem, n_stages);
+    if (o.trace && tid == 0) trace_start(o.trace);
+  }
   {
     // every row's scores of a 4 x 512-chunk slab in flight at once
-    const float *rows = o.scores + ((int64_t)(b * NQ) * Hkv + g) * C;   // row j at + j * Hkv * C
+    const float *rows = kScore ? nullptr : o.scores + ((int64_t)(b * NQ) * Hkv + g) * C;   // row j at + j * Hkv * C
     uint32_t mn[NQ], mx[NQ];   // over the segments this thread takes
 #pragma unroll
     for (int j = 0; j < NQ; ++j) {
       mn[j] = 0xFFFFFFFFu;
       mx[j] = 0u;
     }
+    if (!kScore)   // with the scoring folded in the key rows are written already
     for (int c0 = warp * 32; c0 < C; c0 += 4 * kFusedThreads) {   // warp-uniform
       float v[NQ][4];
 #pragma unroll
@@ -886,13 +1091,44 @@ cudaError_t launch_select_fused(const SelectOut &o, int n_q, cudaStream_t s) {
   switch (n_q) {
 #define DD_FUSED_CASE(N)                                                                                      \
   case N: {                                                                                                    \
-    cudaError_t e = set_dyn_smem((const void *)k_select_fused<N>, smem);                                                           \
+    cudaError_t e = set_dyn_smem((const void *)k_select_fused<N, false>, smem);                               \
     if (e != cudaSuccess) return e;                                                                            \
-    return launch_k(k_select_fused<N>, dim3(o.units), dim3(kFusedThreads), smem, s, o);                        \
+    return launch_k(k_select_fused<N, false>, dim3(o.units), dim3(kFusedThreads), smem, s, o, 0);             \
   }
     DD_FUSED_CASE(1) DD_FUSED_CASE(2) DD_FUSED_CASE(3) DD_FUSED_CASE(4)
     DD_FUSED_CASE(5) DD_FUSED_CASE(6) DD_FUSED_CASE(7) DD_FUSED_CASE(8)
 #undef DD_FUSED_CASE
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Folding the scoring in pays when one CTA per SM streams one unit and the
+// units fill most SMs in one wave (3/4 of them or more): a unit's landmarks
+// then stream at one SM's share of HBM, and the scoring kernel's boundary,
+// the score rows' round trip and their load leave the step.  With fewer
+// units the idle SMs' share of the bandwidth is lost, with more a second wave
+// follows; the scoring kernel then streams over every SM instead.
+int score_select_stages(int units, int sm_count, int n_q, int C, int k) {
+  if (units > sm_count || 4 * units < 3 * sm_count) return 0;
+  for (int st = kFsMaxStages; st >= 3; --st)
+    if (score_select_tc_smem(n_q, C, k, st) <= kSelectMaxSmem) return st;
+  return 0;
+}
+
+cudaError_t launch_score_select(const SelectOut &o, int n_q, int stages, cudaStream_t s) {
+  if (o.units == 0) return cudaSuccess;
+  if (stages < 1 || stages > kFsMaxStages) return cudaErrorInvalidValue;
+  const size_t smem = score_select_tc_smem(n_q, o.C, o.k, stages);
+  switch (n_q) {
+#define DD_SS_CASE(N)                                                                                         \
+  case N: {                                                                                                    \
+    cudaError_t e = set_dyn_smem((const void *)k_select_fused<N, true>, smem);                                \
+    if (e != cudaSuccess) return e;                                                                            \
+    return launch_k(k_select_fused<N, true>, dim3(o.units), dim3(kFusedThreads), smem, s, o, stages);         \
+  }
+    DD_SS_CASE(1) DD_SS_CASE(2) DD_SS_CASE(3) DD_SS_CASE(4)
+    DD_SS_CASE(5) DD_SS_CASE(6) DD_SS_CASE(7) DD_SS_CASE(8)
+#undef DD_SS_CASE
     default: return cudaErrorInvalidValue;
   }
 }

@@ -33,7 +33,16 @@ V_ONEQ = Workload("one_query", B=3, Hq=16, Hkv=4, d=128, L=2048, cs=32, k=7, n_q
 # C = 1000: a ragged last landmark stage, union words not a multiple of 32, three queries
 V_ODD = Workload("odd_c", B=3, Hq=12, Hkv=3, d=128, L=16000, cs=16, k=37, n_q=3, spec_scale=(0.0, 0.2, 0.4),
                  seed=83, residency="uniform", resident_frac=0.3)
-STEP_CASES = [TINY, V_HOT, V_CARRY, V_5Q, V_ZIPF, V_NQ64, V_ALL, V_ONEQ, V_ODD]
+# 128 (request, KV head) units fill most of the 152 SMs in one wave: the step
+# then scores inside the selection kernel on the tensor cores (C = 200: a
+# ragged second landmark tile; 2, 5 and 8 queries, N = 16 and 32)
+V_FOLD2 = Workload("fold_nq2", B=16, Hq=32, Hkv=8, d=128, L=3200, cs=16, k=16, n_q=2, spec_scale=(0.0, 0.3),
+                   seed=91, residency="uniform", resident_frac=0.4)
+V_FOLD5 = Workload("fold_nq5", B=16, Hq=64, Hkv=8, d=128, L=4096, cs=16, k=24, n_q=5,
+                   spec_scale=(0.0, 0.2, 0.4, 0.6, 0.8), seed=92)
+V_FOLD8 = Workload("fold_nq8", B=16, Hq=32, Hkv=8, d=128, L=2048, cs=16, k=8, n_q=8,
+                   spec_scale=(0.0,) + (0.1,) * 7, seed=93, residency="uniform", resident_frac=0.5)
+STEP_CASES = [TINY, V_HOT, V_CARRY, V_5Q, V_ZIPF, V_NQ64, V_ALL, V_ONEQ, V_ODD, V_FOLD2, V_FOLD5, V_FOLD8]
 
 
 @pytest.fixture(scope="module")
