@@ -513,11 +513,12 @@ constexpr int kFsMaxStages = 5;
 constexpr int kFsQHalf = 32 * 128;           // a 64-column half of the query tile (3 n_q <= 24 rows, 32 kept)
 constexpr int kFsTmemCols = 64;              // two accumulators of up to 32 columns
 
-// where the kernel with scoring folded in keeps its parts: the key rows and
-// selections, then (1024-aligned) the query tile and the ring, which the
-// selection's union scratch reuses once the scores are in
+// where the kernel with scoring folded in keeps its parts: the key rows,
+// selections and the unit's residency row, then (1024-aligned) the query tile
+// and the ring, which the selection's union scratch reuses once the scores
+// are in
 __host__ __device__ inline size_t fs_head_bytes(int nq, int C, int k) {
-  return (((size_t)nq * C + (size_t)nq * k) * 4 + 1023) & ~(size_t)1023;
+  return (((size_t)nq * C + (size_t)nq * k + (size_t)C) * 4 + 1023) & ~(size_t)1023;   // + the residency row
 }
 size_t score_select_tc_smem(int n_q, int C, int k, int stages) {
   const size_t W = (size_t)(C + 31) / 32;
@@ -532,10 +533,15 @@ __device__ __forceinline__ uint16_t bf16_rn_bits(float x) {
   return h;
 }
 
+// Besides the key rows, the epilogue warps take the segment maxima of the
+// selection's lower bound as the keys go by (segments of S chunks: lanes of a
+// warp hold 32 consecutive chunks) into s_lo / s_hi, and warps 6-15, once the
+// query tile is built, load the unit's residency row into rs_all.
 template <int NQ>
 __device__ __forceinline__ void fused_tc_score(const SelectOut &o, int unit, int b, int g, uint32_t *keys,
                                                uint8_t *qtile, uint8_t *ring, uint64_t *bars, uint32_t tmem,
-                                               int n_stages) {
+                                               int n_stages, int S, uint32_t *s_lo, uint32_t *s_hi,
+                                               int32_t *rs_all) {
   constexpr int NB = 3 * NQ;                           // B rows: the hi, mid, lo parts of each query's sum
   constexpr int NQP = NB <= 16 ? 16 : 32;              // N of the MMA
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -583,6 +589,8 @@ __device__ __forceinline__ void fused_tc_score(const SelectOut &o, int unit, int
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("bar.arrive 3, %0;" ::"r"(kFusedThreads - 160) : "memory");   // warps 5-15
+    const int32_t *rs_unit = o.resident_slot + (int64_t)unit * C;
+    for (int c = tid - 192; c < C; c += kFusedThreads - 192) rs_all[c] = rs_unit[c];
   } else if (warp == 5) {
     // ---------------------------------------------------------------- MMA
     asm volatile("bar.sync 3, %0;" ::"r"(kFusedThreads - 160) : "memory");   // the query tile is written
@@ -624,6 +632,12 @@ __device__ __forceinline__ void fused_tc_score(const SelectOut &o, int unit, int
   } else {
     // ---------------------------------------------- epilogue, warps 0-3
     const int row = 32 * warp + lane;   // this thread's tensor-memory lane: landmark row of a tile
+    uint32_t mn[NQ], mx[NQ];            // over the segments this lane leads
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+      mn[j] = 0xFFFFFFFFu;
+      mx[j] = 0u;
+    }
     for (int s = 0; s < nt; ++s) {
       const int buf = s & 1;
       if (!mbar_wait(afull0 + 8 * buf, (s >> 1) & 1, o.status)) break;
@@ -636,13 +650,32 @@ __device__ __forceinline__ void fused_tc_score(const SelectOut &o, int unit, int
       __syncwarp();
       if (lane == 0) mbar_arrive(aempty0 + 8 * buf);
       const int c = s * kFsRows + row;
-      if (c < C) {
 #pragma unroll
-        for (int j = 0; j < NQ; ++j) {
-          const float sc = (v[3 * j] + v[3 * j + 1]) + v[3 * j + 2];
-          keys[j * C + c] = order_key(sc);
+      for (int j = 0; j < NQ; ++j) {
+        const float sc = (v[3 * j] + v[3 * j + 1]) + v[3 * j + 2];
+        const uint32_t key = c < C ? order_key(sc) : 0u;
+        if (c < C) {
+          keys[j * C + c] = key;
           if (o.scores_out) o.scores_out[((int64_t)(b * NQ + j) * Hkv + g) * C + c] = sc;
         }
+        uint32_t m = key;
+        for (int off = 1; off < S; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if ((lane & (S - 1)) == 0 && c < C) {
+          mn[j] = min(mn[j], m);
+          mx[j] = max(mx[j], m);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        mn[j] = min(mn[j], __shfl_xor_sync(0xffffffffu, mn[j], off));
+        mx[j] = max(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], off));
+      }
+      if (lane == 0 && mx[j] >= mn[j]) {   // the warp led at least one segment
+        atomicMin(&s_lo[j], mn[j]);
+        atomicMax(&s_hi[j], mx[j]);
       }
     }
   }
@@ -737,7 +770,8 @@ __global__ void __launch_bounds__(kFusedThreads, kScore ? 1 : 2)
   }
   __syncthreads();
   if (kScore) {
-    fused_tc_score<NQ>(o, unit, b, g, keys, tail, tail + 2 * kFsQHalf, s_bars, s_tmem, n_stages);
+    fused_tc_score<NQ>(o, unit, b, g, keys, tail, tail + 2 * kFsQHalf, s_bars, s_tmem, n_stages, S, s_lo, s_hi,
+                       sel_s + NQ * k);
     if (o.trace && tid == 0) trace_start(o.trace);
   }
   {
@@ -771,8 +805,8 @@ __global__ void __launch_bounds__(kFusedThreads, kScore ? 1 : 2)
     // segment maxima from shared memory, one segment of S keys per thread and
     // row (independent loads instead of a shuffle chain per key; the read
     // order is rotated by the thread so that a warp's 32 segments hit
-    // different banks)
-    const int nseg = (C + S - 1) / S;
+    // different banks); with the scoring folded in they were taken already
+    const int nseg = kScore ? 0 : (C + S - 1) / S;
 #pragma unroll
     for (int j = 0; j < NQ; ++j)
       for (int sg = tid; sg < nseg; sg += kFusedThreads) {
@@ -919,8 +953,9 @@ __global__ void __launch_bounds__(kFusedThreads, kScore ? 1 : 2)
   // ---- a3: union words, then the residency of every union chunk (one
   // lookup per chunk, all of them in flight at once, kept in shared memory
   // where the keys were), then one union word per thread (W <= 512)
-  const int32_t *rs_unit = o.resident_slot + (int64_t)unit * C;
-  int32_t *rs_s = reinterpret_cast<int32_t *>(keys);   // [C], valid for union chunks
+  // (with the scoring folded in the whole row is in shared memory already)
+  const int32_t *rs_unit = kScore ? sel_s + NQ * k : o.resident_slot + (int64_t)unit * C;
+  int32_t *rs_s = kScore ? sel_s + NQ * k : reinterpret_cast<int32_t *>(keys);   // [C], valid for union chunks
   if (tid < W) {
     uint32_t ub = 0;
 #pragma unroll
