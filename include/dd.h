@@ -259,7 +259,8 @@ typedef struct {
   uint8_t *union_qmask;
   /* optional instrumentation: cudaEvent_t handles (NULL entries skipped)
    * recorded on the stream before scoring and after scoring, top-k, resolve,
-   * gather and attention */
+   * gather and attention (with the scoring folded into the selection kernel,
+   * see dd_step_folds_scoring, "after scoring" follows that one kernel) */
   void *stage_events[6];
   dd_landmark_kind lm_kind;      /* DD_LM_MEAN (0) or DD_LM_MINMAX: how lm is laid out and scored */
   const void *K_tail, *V_tail;   /* bf16 [B,n_q,Hkv,d] device or NULL: the step's own tokens (causal) */
@@ -278,7 +279,10 @@ typedef struct {
    * every trace[i][1][s] to 0 before the step.  Unlike events between the
    * kernels it leaves their overlap in place, and one pair of words per SM
    * keeps the atomics from contending.  Fused selection and attention only
-   * (the stage kernels of the other paths record nothing). */
+   * (the stage kernels of the other paths record nothing).  With the scoring
+   * folded into the selection kernel, i = 0 is that kernel's scoring phase
+   * (from its dependency wait to its last CTA's last key row) and i = 1 its
+   * selection phase (from the first CTA done scoring to the last CTA's end). */
   uint64_t *trace;
 } dd_step_args;
 
@@ -289,6 +293,16 @@ typedef struct {
  * its own steps -- so a caller that replays such a graph and also runs steps
  * on another stream orders the two itself. */
 dd_status dd_step(dd_ctx *ctx, const dd_step_args *args, dd_stream_t stream);
+
+/* Whether dd_step scores the landmarks inside its selection kernel, for a
+ * context of these dimensions on a device of sm_count SMs: with mean
+ * landmarks, a fixed k and (request, KV head) units filling 3/4 of the SMs or
+ * more in one wave, each selection CTA streams its own unit's landmarks and
+ * scores them on the tensor cores (one kernel fewer per step, the score rows
+ * never leave the SM).  Returns the depth of its landmark ring (3-5), or 0
+ * when the step runs the scoring kernel first (then also for invalid
+ * dimensions).  Host only: no device call. */
+int32_t dd_step_folds_scoring(const dd_dims *dims, int32_t sm_count, dd_landmark_kind lm_kind, float mass_gamma);
 
 /* Predictive prefetch of a layer's predicted selection into its transfer
  * buffer (DualDecoder §4.1-§4.2: the selection computed from the speculative

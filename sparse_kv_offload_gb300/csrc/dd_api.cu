@@ -509,6 +509,13 @@ dd_status dd_selftest_bounded_wait(dd_ctx *c, int32_t kind, dd_stream_t stream) 
   return cuda_ok(dd::launch_selftest_wait(kind, c->diag_word, c->status, (cudaStream_t)stream));
 }
 
+int32_t dd_step_folds_scoring(const dd_dims *d, int32_t sm_count, dd_landmark_kind lm_kind, float mass_gamma) {
+  if (!d || check_dims(d) != DD_OK || lm_kind != DD_LM_MEAN || !(mass_gamma <= 0.f)) return 0;
+  const int C = d->L / d->cs;
+  if (dd::fused_select_smem(d->n_q, C, d->k) == 0) return 0;
+  return dd::score_select_stages(d->B * d->Hkv, sm_count, d->n_q, C, d->k);
+}
+
 dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   if (!c || !a || a->layer < 0) return DD_ERR_INVALID_ARG;
   if (a->lm_kind != DD_LM_MEAN && a->lm_kind != DD_LM_MINMAX) return DD_ERR_INVALID_ARG;
@@ -543,8 +550,8 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
   // units fill most SMs in one wave: the selection kernel then streams and
   // scores its own unit on the tensor cores.
   const bool fused = a->mass_gamma <= 0.f && dd::fused_select_smem(d.n_q, c->C, d.k) > 0;
-  const int ss_stages = fused && a->lm_kind == DD_LM_MEAN && a->q && a->lm && aligned16(a->q) && aligned16(a->lm)
-                            ? dd::score_select_stages(c->units, c->sm_count, d.n_q, c->C, d.k)
+  const int ss_stages = a->q && a->lm && aligned16(a->q) && aligned16(a->lm)
+                            ? dd_step_folds_scoring(&d, c->sm_count, a->lm_kind, a->mass_gamma)
                             : 0;
   if (ss_stages == 0) {
     DD_TRY(score_impl(c, a->q, a->lm, scores, a->lm_kind == DD_LM_MINMAX, trace, stream));

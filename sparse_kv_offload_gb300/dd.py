@@ -28,7 +28,7 @@ EXPORTED = (
     "dd_resolve_union", "dd_gather_kv", "dd_sparse_attn_decode", "dd_step", "dd_get_status",
     "dd_launch_count", "dd_status_str", "dd_last_cuda_error", "dd_synth_kv", "dd_synth_queries", "dd_sparse_attn_decode_noalloc",
     "dd_build_landmarks_minmax", "dd_score_landmarks_minmax", "dd_update_residency",
-    "dd_prefetch_kv", "dd_select_topk_mass", "dd_selftest_bounded_wait",
+    "dd_prefetch_kv", "dd_select_topk_mass", "dd_selftest_bounded_wait", "dd_step_folds_scoring",
 )
 
 
@@ -89,6 +89,7 @@ def _load():
         "dd_prefetch_kv": (i32, [_vp, _vp, i32, i32, i32, _vp, _vp, _vp, _vp, _vp, _vp, i32, _vp]),
         "dd_get_status": (i32, [_vp, ctypes.POINTER(i32)]),
         "dd_launch_count": (i64, [_vp]),
+        "dd_step_folds_scoring": (i32, [ctypes.POINTER(Dims), i32, ctypes.c_int, f32]),
         "dd_status_str": (ctypes.c_char_p, [i32]),
         "dd_last_cuda_error": (ctypes.c_char_p, []),
         "dd_synth_kv": (i32, [ctypes.POINTER(Dims), ctypes.c_uint64, i32, _vp, _vp, _vp, i64, _vp, _vp]),
@@ -167,6 +168,13 @@ class Shape:
 
     def dims(self) -> Dims:
         return Dims(self.B, self.Hq, self.Hkv, self.d, self.L, self.cs, self.k, self.n_q)
+
+
+def step_folds_scoring(shape: "Shape", sm_count: int, lm_kind: int = 0, mass_gamma: float = 0.0) -> int:
+    """Ring depth of the selection kernel that scores its own unit inside dd_step
+    (0: the step runs the scoring kernel first); host only."""
+    d = shape.dims()
+    return int(_lib.dd_step_folds_scoring(ctypes.byref(d), int(sm_count), int(lm_kind), float(mass_gamma)))
 
 
 class Context:
