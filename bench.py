@@ -308,8 +308,9 @@ def run_reference(args, world, rank):
 # the step scores in one streaming kernel (k_score), then runs top-k and the
 # resolver as one kernel (k_select_fused); the attention is k_attn (mma.sync)
 # up to 16 query vectors per KV head and k_attn_tc (tcgen05) above
-# timed steps per CUDA-event bracket of the dominant kernel (see run_ours)
-EV_EVERY = 8
+# timed steps per CUDA-event bracket of the dominant kernel (see run_ours);
+# prime to the N_LAYERS layers cycled, so the bracketed steps cover every layer
+EV_EVERY = 7
 
 KERNEL_SOURCE = {"gather": ("k_gather", ("dd_gather.cu",)),
                  "attention": ("k_attn", ("dd_attn.cu", "dd_attn.cuh", "dd_tc.cuh")),
@@ -858,7 +859,7 @@ def run_ours(args, world, rank, local, per_config=None):
                        f"('score' is the scoring kernel; with the fused selection 'topk' is the one kernel for "
                        f"top-k, union, residency, ordinals and plan, and 'resolve' and 'gather' are empty); "
                        f"{dom_timed}: {1e3 * dom_ms_timed:.1f} us inside the timed region (CUDA events around it "
-                       f"on {len(ev_steps)} of the {K} timed steps, every {EV_EVERY}th); in_step_us: median "
+                       f"on {len(ev_steps)} of the {K} timed steps, every {EV_EVERY}th, all layers); in_step_us: median "
                        f"over {n_trace} further steps with no events, from the kernels' own %globaltimer stamps "
                        f"(from the end of the kernel before, or for the attention from its first copy, to the last "
                        f"CTA's end)",
