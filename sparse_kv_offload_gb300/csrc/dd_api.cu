@@ -26,6 +26,7 @@ struct dd_ctx {
   int32_t *chunk_off = nullptr;
   int4 *flat = nullptr;
   unsigned long long *lb_word = nullptr;        // fused selection: look-back words, ticket
+  unsigned long long *lb_pref = nullptr;        // fused selection: offsets by the last CTA
   unsigned long long *diag_word = nullptr;      // a word nothing publishes (bounded-wait self-test)
   int32_t *ticket = nullptr;
   void *dummy_pool = nullptr;
@@ -208,6 +209,7 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   add(c->plan.flat_entries, 16);               // flat chunk table
   add(64 * 128, 2);                            // dummy pool (64 rows)
   add(units, 8);                               // look-back words
+  add(16 * units, 8);                          // union and miss offsets by the last CTA (a line per unit)
   add(3, 4);                                   // ticket counters + look-back epoch
   add(1, 8);                                   // self-test word
   if (cudaMalloc(&c->ws, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
@@ -229,6 +231,7 @@ dd_status dd_create(const dd_dims *dims, int64_t max_misses, int64_t hot_slots, 
   c->flat = carve<int4>(cur, c->plan.flat_entries);
   c->dummy_pool = carve<uint16_t>(cur, 64 * 128);
   c->lb_word = carve<unsigned long long>(cur, units);
+  c->lb_pref = carve<unsigned long long>(cur, 16 * units);
   c->ticket = carve<int32_t>(cur, 3);
   c->diag_word = carve<unsigned long long>(cur, 1);
   if (cudaMemset(c->ws, 0, bytes) != cudaSuccess) return fail(DD_ERR_CUDA);
@@ -573,6 +576,7 @@ dd_status dd_step(dd_ctx *c, const dd_step_args *a, dd_stream_t stream) {
     o.chunk_off = c->chunk_off;
     o.flat = c->flat;
     o.lb_word = c->lb_word;
+    o.lb_pref = c->lb_pref;   // the launch drops it when the units cannot all be resident
     o.ticket = c->ticket;
     o.units = c->units;
     o.Hq = d.Hq;

@@ -314,6 +314,11 @@ struct SelectOut {
   int4 *flat;                     // attention plan: [units * umax]
   unsigned long long *lb_word;    // look-back: [units] {epoch:30, union count:17, miss count:17}
   int32_t *ticket;                // [3] next unit, CTAs done, look-back epoch of the next launch (never 0)
+  // [16 * units] every unit's union and miss offsets {epoch:32, offset:32}
+  // (words 16u and 16u + 1), written by the last CTA to arrive when all of
+  // the launch's CTAs are resident at once; null: the look-back over the
+  // earlier units instead
+  unsigned long long *lb_pref;
   int units, Hq, Hkv, C, k, umax, cs;
   int64_t hot_slots, max_misses;
   int32_t *status;

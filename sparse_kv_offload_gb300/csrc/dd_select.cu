@@ -6,6 +6,7 @@
 // the rest), so a chunk wanted by several queries crosses the host link a
 // single time; attention still uses each query's own top-k.
 #include <algorithm>
+#include <mutex>
 
 #include "dd_tc.cuh"
 
@@ -456,6 +457,16 @@ cudaError_t launch_union(const int32_t *sel, const int32_t *resident_slot, int32
 constexpr int kFusedThreads = 512;
 
 constexpr int kLookBatch = 8;   // look-back words per lane in flight (256 units per round)
+constexpr int kPrefStride = 16;  // 64-bit words between two units' offset pairs: a 128-byte line each
+
+// fetch-and-add at GPU scope with no ordering: the words it counts carry
+// their launch's epoch, so a reader re-polls a word it sees too early instead
+// of every writer paying for a GPU-wide fence
+__device__ __forceinline__ int atom_add_relaxed(int32_t *p, int v) {
+  int r;
+  asm volatile("atom.relaxed.gpu.global.add.s32 %0, [%1], %2;" : "=r"(r) : "l"(p), "r"(v) : "memory");
+  return r;
+}
 
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
@@ -694,7 +705,7 @@ __global__ void __launch_bounds__(kFusedThreads, kScore ? 1 : 2)
   extern __shared__ __align__(128) unsigned char fsm_raw[];
   __shared__ int hist[NQ][256];
   __shared__ int scratch[33];
-  __shared__ int s_unit, s_uoff, s_moff;
+  __shared__ int s_unit, s_uoff, s_moff, s_last;
   __shared__ uint32_t s_epoch;
   __shared__ __align__(8) uint64_t s_bars[2 * kFsMaxStages + 5];   // scoring folded in: full, empty, acc full/empty, done
   __shared__ uint32_t s_tmem;
@@ -996,16 +1007,101 @@ __global__ void __launch_bounds__(kFusedThreads, kScore ? 1 : 2)
   }
   const int U = tot >> 16, M = tot & 0xFFFF;
 
-  // look-back over the earlier units: every unit publishes one 64-bit word
-  // {epoch:30, union count:17, miss count:17} as soon as it has its counts
-  // (counts never exceed C <= 16384, and a single aligned 64-bit store is
-  // seen whole, so the word is its own message), and sums all of its
-  // predecessors' counts: each lane loads its strided share of their words
-  // at once and re-polls only those not yet published; one round trip
-  // after the slowest predecessor, no chain
-  if (warp == 0) {
+  // Every unit publishes one 64-bit word {epoch:30, union count:17, miss
+  // count:17} as soon as it has its counts (counts never exceed C <= 16384,
+  // and a single aligned 64-bit store is seen whole, so the word is its own
+  // message).
+  const unsigned long long my_word =
+      ((unsigned long long)epoch << 34) | ((unsigned long long)U << 17) | (unsigned long long)M;
+  if (o.lb_pref) {
+    // Every unit's CTA is resident at once (the host checked the occupancy),
+    // so each may wait for all of them: a CTA publishes its word and counts
+    // itself in; the CTA that arrives last reads every word (re-polling one
+    // not yet seen with this launch's epoch), sums the counts in unit order,
+    // publishes every unit's union and miss offsets as words {epoch:32,
+    // offset:32}, each unit's pair on a cache line of its own, and resets
+    // the counters for the next launch; the others wait for their own pair.
+    // One round trip per CTA on the shared lines, instead of a look-back load
+    // of every earlier word by every CTA, which queued at the few L2 lines
+    // holding the words.
+    if (tid == 0) {
+      st_relaxed_u64(&o.lb_word[unit], my_word);
+      s_last = atom_add_relaxed(o.ticket + 1, 1) == o.units - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+      if (warp == 0) {
+        const unsigned long long tag = (unsigned long long)epoch << 32;
+        bool ok = true;
+        const uint64_t t0 = globaltimer_ns();
+        int carry_u = 0, carry_m = 0;   // counts of the units before this round
+        for (int base = 0; base < o.units; base += 32 * kLookBatch) {
+          unsigned long long w8[kLookBatch];
+          int su = 0, sm = 0;
+#pragma unroll
+          for (int t = 0; t < kLookBatch; ++t) {   // lane l: units base + 8l .. base + 8l + 7
+            const int idx = base + lane * kLookBatch + t;
+            w8[t] = idx < o.units ? ld_relaxed_u64(&o.lb_word[idx]) : (unsigned long long)epoch << 34;
+          }
+#pragma unroll
+          for (int t = 0; t < kLookBatch; ++t) {
+            const int idx = base + lane * kLookBatch + t;
+            if ((w8[t] >> 34) != epoch) w8[t] = wait_published(&o.lb_word[idx], epoch, t0, &ok);
+            su += (int)((w8[t] >> 17) & 0x1FFFFull);
+            sm += (int)(w8[t] & 0x1FFFFull);
+          }
+          if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) set_status(o.status, DD_ERR_TIMEOUT);
+            break;
+          }
+          const int iu = warp_incl_scan(su), im = warp_incl_scan(sm);
+          int eu = carry_u + iu - su, em = carry_m + im - sm;
+#pragma unroll
+          for (int t = 0; t < kLookBatch; ++t) {
+            const int idx = base + lane * kLookBatch + t;
+            if (idx < o.units) {
+              st_relaxed_u64(&o.lb_pref[(int64_t)idx * kPrefStride], tag | (uint32_t)eu);
+              st_relaxed_u64(&o.lb_pref[(int64_t)idx * kPrefStride + 1], tag | (uint32_t)em);
+              if (idx == unit) {
+                s_uoff = eu;
+                s_moff = em;
+              }
+            }
+            eu += (int)((w8[t] >> 17) & 0x1FFFFull);
+            em += (int)(w8[t] & 0x1FFFFull);
+          }
+          carry_u += __shfl_sync(0xffffffffu, iu, 31);
+          carry_m += __shfl_sync(0xffffffffu, im, 31);
+        }
+        if (lane == 0) {   // every CTA has taken its ticket, read the epoch and arrived
+          const uint32_t next = (epoch + 1u) & 0x3FFFFFFFu;
+          o.ticket[0] = 0;
+          o.ticket[1] = 0;
+          o.ticket[2] = (int32_t)(next == 0u ? 1u : next);
+        }
+      }
+    } else if (tid == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      unsigned long long wu = 0, wm = 0;
+      for (uint32_t it = 0;; ++it) {
+        wu = ld_relaxed_u64(&o.lb_pref[(int64_t)unit * kPrefStride]);
+        wm = ld_relaxed_u64(&o.lb_pref[(int64_t)unit * kPrefStride + 1]);
+        if ((wu >> 32) == epoch && (wm >> 32) == epoch) break;
+        if ((it & 63u) == 63u && globaltimer_ns() - t0 > 2000000000ull) {
+          set_status(o.status, DD_ERR_TIMEOUT);
+          break;
+        }
+      }
+      s_uoff = (int)(uint32_t)wu;
+      s_moff = (int)(uint32_t)wm;
+    }
+  } else if (warp == 0) {
+    // look-back over the earlier units: sum all of the predecessors'
+    // counts: each lane loads its strided share of their words at once and
+    // re-polls only those not yet published; one round trip after the
+    // slowest predecessor, no chain
     const unsigned long long ep = (unsigned long long)epoch << 34;
-    if (lane == 0) st_relaxed_u64(&o.lb_word[unit], ep | ((unsigned long long)U << 17) | (unsigned long long)M);
+    if (lane == 0) st_relaxed_u64(&o.lb_word[unit], my_word);
     int su = 0, sm = 0;
     bool ok = true;
     const uint64_t t0 = globaltimer_ns();
@@ -1036,11 +1132,43 @@ __global__ void __launch_bounds__(kFusedThreads, kScore ? 1 : 2)
       s_moff = sm;
     }
   }
+  // the lists that need no offset, while warp 0 finds the offsets: the
+  // union's chunks and query masks, the resident chunks' slots
+  const int64_t ubase = (int64_t)unit * o.umax;
+  if (warp > 0) {
+    for (int wi = tid - 32; wi < W; wi += kFusedThreads - 32) {
+      uint32_t rest = ubw[wi];
+      const uint32_t mb = mbw[wi];
+      int up = upre[wi];
+      while (rest) {
+        const int bit = __ffs(rest) - 1;
+        rest &= rest - 1;
+        const int c = wi * 32 + bit;
+        uint32_t qm = 0;
+        for (int j = 0; j < NQ; ++j) qm |= ((qbits[j * W + wi] >> bit) & 1u) << j;
+        o.union_idx[ubase + up] = c;
+        o.union_qmask[ubase + up] = (uint8_t)qm;
+        if (!((mb >> bit) & 1u)) o.union_slot[ubase + up] = rs_s[c];
+        ++up;
+      }
+    }
+    if (o.attn_slot) {
+      for (int i = tid - 32; i < NQ * k; i += kFusedThreads - 32) {
+        const int j = i / k, r = i - j * k, c = sel_s[i];
+        const bool miss = c >= 0 && c < C && ((mbw[c >> 5] >> (c & 31)) & 1u);
+        if (!miss) o.attn_slot[((int64_t)(b * NQ + j) * Hkv + g) * k + r] = c >= 0 && c < C ? rs_s[c] : INT32_MIN;
+      }
+    }
+    if (tid == 32) {
+      o.union_cnt[unit] = U;
+      o.unit_miss[unit] = M;
+      o.chunk_off[o.units + 1 + unit] = 0;   // arrival counter of the attention's fix-up
+    }
+  }
   __syncthreads();
   const int uoff = s_uoff, moff = s_moff;
 
-  // union lists with global slots, miss list, attention plan entries
-  const int64_t ubase = (int64_t)unit * o.umax;
+  // the attention plan's entries and the misses' slots and list
   if (tid < W) {
     uint32_t rest = ubw[tid];
     const uint32_t mb = mbw[tid];
@@ -1051,8 +1179,6 @@ __global__ void __launch_bounds__(kFusedThreads, kScore ? 1 : 2)
       const int c = tid * 32 + bit;
       uint32_t qm = 0;
       for (int j = 0; j < NQ; ++j) qm |= ((qbits[j * W + tid] >> bit) & 1u) << j;
-      o.union_idx[ubase + up] = c;
-      o.union_qmask[ubase + up] = (uint8_t)qm;
       int32_t row, host = -1;
       if ((mb >> bit) & 1u) {
         const int64_t m = (int64_t)moff + mp++;
@@ -1066,32 +1192,25 @@ __global__ void __launch_bounds__(kFusedThreads, kScore ? 1 : 2)
           qm = 0;
         }
       } else {
-        const int32_t rs = rs_s[c];
-        o.union_slot[ubase + up] = rs;
-        row = rs * o.cs;
+        row = rs_s[c] * o.cs;
       }
       o.flat[uoff + up] = make_int4(row, (int)qm, host, 0);
       ++up;
     }
   }
-  if (o.attn_slot) {
+  if (o.attn_slot && M > 0) {
     for (int i = tid; i < NQ * k; i += kFusedThreads) {
       const int j = i / k, r = i - j * k, c = sel_s[i];
-      int32_t val = INT32_MIN;
-      if (c >= 0 && c < C) {
+      if (c >= 0 && c < C && ((mbw[c >> 5] >> (c & 31)) & 1u)) {
         const int w = c >> 5;
         const uint32_t low = (1u << (c & 31)) - 1u;
-        if ((mbw[w] >> (c & 31)) & 1u) val = -(int32_t)((int64_t)moff + mpre[w] + __popc(mbw[w] & low) + 1);
-        else val = rs_s[c];
+        o.attn_slot[((int64_t)(b * NQ + j) * Hkv + g) * k + r] =
+            -(int32_t)((int64_t)moff + mpre[w] + __popc(mbw[w] & low) + 1);
       }
-      o.attn_slot[((int64_t)(b * NQ + j) * Hkv + g) * k + r] = val;
     }
   }
   if (tid == 0) {
-    o.union_cnt[unit] = U;
-    o.unit_miss[unit] = M;
     o.chunk_off[unit] = uoff;
-    o.chunk_off[o.units + 1 + unit] = 0;   // arrival counter of the attention's fix-up
     if (unit == o.units - 1) {
       o.chunk_off[o.units] = uoff + U;
       *o.miss_count = moff + M;
@@ -1100,20 +1219,50 @@ __global__ void __launch_bounds__(kFusedThreads, kScore ? 1 : 2)
     // the last CTA to finish resets the ticket counters and advances the
     // epoch (30 bits, never 0: zeroed words carry epoch 0) for the next launch;
     // every CTA of this launch has read the epoch by then.  Kept on the device,
-    // so replaying a captured step in a CUDA graph stays correct.
-    __threadfence();
-    if (atomicAdd(o.ticket + 1, 1) == o.units - 1) {
-      uint32_t next = (epoch + 1u) & 0x3FFFFFFFu;
-      o.ticket[0] = 0;
-      o.ticket[1] = 0;
-      o.ticket[2] = (int32_t)(next == 0u ? 1u : next);
+    // so replaying a captured step in a CUDA graph stays correct.  (With
+    // every CTA resident, the last to arrive at the offsets did it.)
+    if (!o.lb_pref) {
       __threadfence();
+      if (atomicAdd(o.ticket + 1, 1) == o.units - 1) {
+        uint32_t next = (epoch + 1u) & 0x3FFFFFFFu;
+        o.ticket[0] = 0;
+        o.ticket[1] = 0;
+        o.ticket[2] = (int32_t)(next == 0u ? 1u : next);
+        __threadfence();
+      }
     }
   }
   if (o.trace) {
     __syncthreads();
     if (tid == 0) trace_end(o.trace);
   }
+}
+
+// Whether a grid of `units` CTAs of the kernel fits on the device at once
+// (blocks per SM at this shared memory x SMs), cached per kernel and size.
+static bool all_resident(const void *func, size_t smem, int units, int sm_count) {
+  struct Entry {
+    const void *func;
+    size_t smem;
+    int dev, per_sm;
+  };
+  static Entry cache[32];
+  static int n_cache = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  int per_sm = -1;
+  for (int i = 0; i < n_cache; ++i)
+    if (cache[i].func == func && cache[i].smem == smem && cache[i].dev == dev) per_sm = cache[i].per_sm;
+  if (per_sm < 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, kFusedThreads, smem) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    if (n_cache < 32) cache[n_cache++] = Entry{func, smem, dev, per_sm};
+  }
+  return (int64_t)units <= (int64_t)per_sm * sm_count;
 }
 
 cudaError_t launch_select_fused(const SelectOut &o, int n_q, cudaStream_t s) {
@@ -1128,7 +1277,9 @@ cudaError_t launch_select_fused(const SelectOut &o, int n_q, cudaStream_t s) {
   case N: {                                                                                                    \
     cudaError_t e = set_dyn_smem((const void *)k_select_fused<N, false>, smem);                               \
     if (e != cudaSuccess) return e;                                                                            \
-    return launch_k(k_select_fused<N, false>, dim3(o.units), dim3(kFusedThreads), smem, s, o, 0);             \
+    SelectOut oo = o;                                                                                          \
+    if (!all_resident((const void *)k_select_fused<N, false>, smem, o.units, o.sm_count)) oo.lb_pref = nullptr; \
+    return launch_k(k_select_fused<N, false>, dim3(o.units), dim3(kFusedThreads), smem, s, oo, 0);            \
   }
     DD_FUSED_CASE(1) DD_FUSED_CASE(2) DD_FUSED_CASE(3) DD_FUSED_CASE(4)
     DD_FUSED_CASE(5) DD_FUSED_CASE(6) DD_FUSED_CASE(7) DD_FUSED_CASE(8)
@@ -1159,7 +1310,9 @@ cudaError_t launch_score_select(const SelectOut &o, int n_q, int stages, cudaStr
   case N: {                                                                                                    \
     cudaError_t e = set_dyn_smem((const void *)k_select_fused<N, true>, smem);                                \
     if (e != cudaSuccess) return e;                                                                            \
-    return launch_k(k_select_fused<N, true>, dim3(o.units), dim3(kFusedThreads), smem, s, o, stages);         \
+    SelectOut oo = o;                                                                                          \
+    if (!all_resident((const void *)k_select_fused<N, true>, smem, o.units, o.sm_count)) oo.lb_pref = nullptr; \
+    return launch_k(k_select_fused<N, true>, dim3(o.units), dim3(kFusedThreads), smem, s, oo, stages);        \
   }
     DD_SS_CASE(1) DD_SS_CASE(2) DD_SS_CASE(3) DD_SS_CASE(4)
     DD_SS_CASE(5) DD_SS_CASE(6) DD_SS_CASE(7) DD_SS_CASE(8)

@@ -42,7 +42,12 @@ V_FOLD5 = Workload("fold_nq5", B=16, Hq=64, Hkv=8, d=128, L=4096, cs=16, k=24, n
                    spec_scale=(0.0, 0.2, 0.4, 0.6, 0.8), seed=92)
 V_FOLD8 = Workload("fold_nq8", B=16, Hq=32, Hkv=8, d=128, L=2048, cs=16, k=8, n_q=8,
                    spec_scale=(0.0,) + (0.1,) * 7, seed=93, residency="uniform", resident_frac=0.5)
-STEP_CASES = [TINY, V_HOT, V_CARRY, V_5Q, V_ZIPF, V_NQ64, V_ALL, V_ONEQ, V_ODD, V_FOLD2, V_FOLD5, V_FOLD8]
+# 384 units: more selection CTAs than fit on the device at once (two per SM),
+# so the selection sums the earlier units' counts by its look-back instead of
+# leaving them to the last CTA to arrive
+V_WAVES = Workload("two_waves", B=48, Hq=16, Hkv=8, d=128, L=512, cs=16, k=4, n_q=2, spec_scale=(0.0, 0.3),
+                   seed=94, residency="uniform", resident_frac=0.5)
+STEP_CASES = [TINY, V_HOT, V_CARRY, V_5Q, V_ZIPF, V_NQ64, V_ALL, V_ONEQ, V_ODD, V_FOLD2, V_FOLD5, V_FOLD8, V_WAVES]
 
 
 @pytest.fixture(scope="module")
