@@ -1034,7 +1034,7 @@ __global__ void __launch_bounds__(kFusedThreads, kScore ? 1 : 2)
         const unsigned long long tag = (unsigned long long)epoch << 32;
         bool ok = true;
         const uint64_t t0 = globaltimer_ns();
-        int carry_u = 0, carry_m = 0;   // counts of the units before this round
+        int carry_u = 0, carry_m = 0;   // counts of the units before this batch of words
         for (int base = 0; base < o.units; base += 32 * kLookBatch) {
           unsigned long long w8[kLookBatch];
           int su = 0, sm = 0;
