@@ -291,7 +291,15 @@ typedef struct {
  * host that a replay would repeat wrongly.  While the stream is capturing, the
  * release events of the staging buffers are left alone -- the graph orders
  * its own steps -- so a caller that replays such a graph and also runs steps
- * on another stream orders the two itself. */
+ * on another stream orders the two itself.
+ *
+ * When all of the step's selection CTAs (one per (request, KV head) unit)
+ * fit on the device at once, the last to finish its counts hands every unit
+ * its union and miss offsets and the others wait for it, so all of them must
+ * be able to start: under MPS with an SM limit below the device's SM count,
+ * or beside a kernel on another stream that holds SMs and waits for this
+ * step, some may not, and the bounded wait then ends the step with
+ * DD_ERR_TIMEOUT in the status word instead of hanging. */
 dd_status dd_step(dd_ctx *ctx, const dd_step_args *args, dd_stream_t stream);
 
 /* Whether dd_step scores the landmarks inside its selection kernel, for a
